@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark of one QUOKA chunked-prefill step on GB300.
+
+A step is one chunk through the whole hot path: query subselection, cosine
+scoring of the history, top-B per KV head, gather, and attention over the kept
+history plus the causal chunk.  The workload is the Llama-3-8B-shaped GQA
+attention layer: H_q=32, H_kv=8, d=128, one chunk of C=2048 queries over
+T=32768 cached keys, N_q=64, B=2048, bf16, synthetic seeded inputs (the
+massive-activation recipe of workloads.py).  The metric is chunk tokens per
+second (C / step time).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.  Under torchrun every rank runs
+its own replica of the workload (the path has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_attention_chunked_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "chunk tokens/sec for QUOKA select+attend at 32K/128K history; % HBM/TC roofline"
+WORKLOADS = {"gqa32k": wl.GQA_32K_BF16, "gqa128k": wl.GQA_128K_BF16}
+FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flop x max SM clock
+L2_FLUSH_BYTES = 512 << 20                              # > 3x the 129 MB L2
+
+
+# ---------------------------------------------------------------- multi-rank plumbing
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(backend: str):
+    rank, world, _ = dist_env()
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+# ---------------------------------------------------------------- algorithmic work per stage
+
+def stage_work(cfg: wl.ChunkConfig, gqa: str) -> dict:
+    """Bytes / flops each stage must move or compute (what the method needs, not what the kernels do)."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    n = min(cfg.N_q, cfg.C)
+    B_e = min(cfg.B, cfg.T)
+    R = cfg.G * n if gqa == "max" else n
+    return {
+        "select": {"bytes": cfg.H_q * cfg.C * cfg.d * e},                               # read Q once
+        "score": {"bytes": cfg.H_kv * cfg.T * cfg.d * e + cfg.H_kv * cfg.T * 4,         # read K, write scores
+                  "flops": 2 * cfg.H_kv * R * cfg.T * cfg.d},
+        "topk": {"bytes": cfg.H_kv * cfg.T * 4 + cfg.H_kv * B_e * 4},
+        "gather": {"bytes": 2 * 2 * cfg.H_kv * B_e * cfg.d * e},                        # read + write K and V rows
+        "attend": {"flops": 4 * cfg.H_q * cfg.d * (cfg.C * B_e + cfg.C * (cfg.C + 1) // 2),
+                   "bytes": 2 * cfg.H_q * cfg.C * cfg.d * e + 2 * cfg.H_kv * (B_e + cfg.C) * cfg.d * e},
+    }
+
+
+def dense_flops(cfg: wl.ChunkConfig) -> int:
+    return 4 * cfg.H_q * cfg.d * (cfg.C * cfg.T + cfg.C * (cfg.C + 1) // 2)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks during the timed region
+
+class ClockSampler:
+    """Samples nvidia-smi every 200 ms in the background (SM clock, max clock, throttle reasons)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        self.dev = device_index
+
+    def _target(self):
+        try:
+            props = torch.cuda.get_device_properties(self.dev)
+            return "GPU-" + str(props.uuid)
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            return vis.split(",")[self.dev] if vis else str(self.dev)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", self._target()],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        time.sleep(0.05)
+        rows = [r for r in self.rows if r[0].replace(".", "").isdigit()]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[0]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+def run_quoka(args, rank, world, local_rank):
+    from sparse_attention_chunked_gb300 import build as qbuild
+    from sparse_attention_chunked_gb300 import quoka as q
+
+    qbuild.build()
+    q.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = WORKLOADS[args.workload]
+    x = wl.make_chunk(cfg, args.seed)
+    Q, Kh, Vh = x.Q.to(dev), x.K_hist.to(dev), x.V_hist.to(dev)
+    Kc, Vc = x.K_chunk.to(dev), x.V_chunk.to(dev)
+    shape = q.shape_of(Q, Kh)
+    params = q.params_of(args.gqa, args.engine)
+    ws = q.make_workspace(shape, cfg.N_q, cfg.B, params, device=dev)
+    n = min(cfg.N_q, cfg.C)
+    H_sel = cfg.H_q if args.gqa == "max" else cfg.H_kv
+    B_e = min(cfg.B, cfg.T)
+    q_idx = torch.empty((H_sel, n), dtype=torch.int32, device=dev)
+    scores = torch.empty((cfg.H_kv, cfg.T), dtype=torch.float32, device=dev)
+    sel = torch.empty((cfg.H_kv, B_e), dtype=torch.int32, device=dev)
+    Ks = torch.empty((cfg.H_kv, B_e, cfg.d), dtype=Q.dtype, device=dev)
+    Vs = torch.empty_like(Ks)
+    O = torch.empty_like(Q)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ["select", "score", "topk", "gather", "attend"]
+
+    def step(evs):
+        evs[0].record(stream)
+        q.quoka_select_queries(shape, Q, cfg.N_q, params, q_idx, ws, stream)
+        evs[1].record(stream)
+        q.quoka_score_keys(shape, Q, q_idx, cfg.N_q, Kh, params, scores, ws, stream)
+        evs[2].record(stream)
+        q.quoka_topk(shape, scores, cfg.B, sel, ws, stream)
+        evs[3].record(stream)
+        q.quoka_gather(shape, Kh, Vh, sel, B_e, Ks, Vs, stream)
+        evs[4].record(stream)
+        q.quoka_sparse_attend(shape, Q, Ks, Vs, B_e, Kc, Vc, params, O, None, ws, stream)
+        evs[5].record(stream)
+
+    def new_events(k):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(new_events(6))
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = q.quoka_launch_count()
+    wall0 = time.perf_counter()
+    all_evs = []
+    for _ in range(args.steps):
+        flush.zero_()                       # L2 flushed between timed steps (outside the events)
+        evs = new_events(6)
+        step(evs)
+        all_evs.append(evs)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - wall0
+    launches = q.quoka_launch_count() - launches0
+    assert q.quoka_get_last_device_error(ws, stream) == 0
+    stage_ms = {nm: [e[i].elapsed_time(e[i + 1]) for e in all_evs] for i, nm in enumerate(names)}
+    step_ms_list = [e[0].elapsed_time(e[5]) for e in all_evs]
+    step_ms = max_over_ranks(statistics.mean(step_ms_list), dev)
+
+    # dense full-history attention on the same chunk: the speedup reference
+    dense_ms = None
+    if not args.no_dense:
+        Od = torch.empty_like(Q)
+        dsteps = max(3, args.steps // 4)
+        for _ in range(2):
+            q.quoka_dense_attend(shape, Q, Kh, Vh, Kc, Vc, params, Od, None, ws, stream)
+        ts = []
+        for _ in range(dsteps):
+            flush.zero_()
+            e = new_events(2)
+            e[0].record(stream)
+            q.quoka_dense_attend(shape, Q, Kh, Vh, Kc, Vc, params, Od, None, ws, stream)
+            e[1].record(stream)
+            ts.append(e)
+        torch.cuda.synchronize(dev)
+        dense_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ts), dev)
+
+    # end to end through quoka_chunk_attend: the chunk's Q, K, V come from pinned host
+    # memory and O goes back to it inside the timed region; the history stays resident.
+    Qh, Kch, Vch = x.Q.pin_memory(), x.K_chunk.pin_memory(), x.V_chunk.pin_memory()
+    Oh = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    Qd, Kcd, Vcd, Od2 = torch.empty_like(Q), torch.empty_like(Kc), torch.empty_like(Vc), torch.empty_like(O)
+    h2d = Qh.numel() * Qh.element_size() + 2 * Kch.numel() * Kch.element_size()
+    d2h = Oh.numel() * Oh.element_size()
+
+    def e2e_step():
+        Qd.copy_(Qh, non_blocking=True)
+        Kcd.copy_(Kch, non_blocking=True)
+        Vcd.copy_(Vch, non_blocking=True)
+        q.quoka_chunk_attend(shape, Qd, Kh, Vh, Kcd, Vcd, cfg.N_q, cfg.B, params, Od2, None, None, ws, stream)
+        Oh.copy_(Od2, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    ets = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e = new_events(2)
+        e[0].record(stream)
+        e2e_step()
+        e[1].record(stream)
+        ets.append(e)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ets), dev)
+    clocks = sampler.stop()
+    assert torch.equal(Od2, O), "chunk_attend and the stage calls disagree"
+
+    if rank != 0:
+        return None
+    work = stage_work(cfg, args.gqa)
+    peaks = load_peaks()
+    att_ms = statistics.mean(stage_ms["attend"])
+    tc_engine = q.uses_tensor_cores("attend", shape, params)
+    if tc_engine:
+        peak, bound = peaks["bf16_tflops"], "tensor"
+    else:
+        peak, bound = FP32_FMA_PEAK_TFLOPS, "alu"
+    achieved = work["attend"]["flops"] / (att_ms * 1e-3) / 1e12
+    stages = {}
+    for nm in names:
+        ms = statistics.mean(stage_ms[nm])
+        st = {"ms": round(ms, 5)}
+        if "bytes" in work[nm]:
+            st["GBps"] = round(work[nm]["bytes"] / (ms * 1e-3) / 1e9, 1)
+            st["hbm_frac"] = round(st["GBps"] / peaks["hbm_gbs"], 4)
+        if "flops" in work[nm]:
+            st["TFLOPs"] = round(work[nm]["flops"] / (ms * 1e-3) / 1e12, 2)
+        stages[nm] = st
+    value = cfg.C * world / (step_ms * 1e-3)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded massive-activation recipe: biased key channels, shared query direction, "
+                "5% outlier queries, planted needles)",
+        "config": {"workload": cfg.name, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "d": cfg.d, "C": cfg.C, "T": cfg.T,
+                   "N_q": cfg.N_q, "B": cfg.B, "gqa_pool": args.gqa, "engine": args.engine,
+                   "l2": "flushed between steps (512 MB write)", "parallelism": f"replicas x{world}"},
+        "impl": "quoka",
+        "gpu_launches": int(launches),
+        "wall_s_timed_region": round(wall, 4),
+        "roofline": {"kernel": "attend", "bound": bound, "achieved": round(achieved, 2),
+                     "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": peaks["source"] if tc_engine else "derived: 152 SM x 128 FP32 x 2 x 2.07 GHz",
+                     "traffic": None},
+        "stages": stages,
+        "dense": None if dense_ms is None else {
+            "ms_per_step": round(dense_ms, 4), "speedup": round(dense_ms / step_ms, 2),
+            "TFLOPs": round(dense_flops(cfg) / (dense_ms * 1e-3) / 1e12, 2)},
+        "e2e": {"value": round(cfg.C * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(cfg, x, args.gqa)
+    return res
+
+
+# ---------------------------------------------------------------- the CPU oracle
+
+def _blas_threads():
+    """Threads of the BLAS numpy uses (OpenBLAS query when it is the loaded library), else the CPU count."""
+    try:
+        import ctypes
+        with open("/proc/self/maps") as f:
+            libs = {line.split()[-1] for line in f if "openblas" in line.lower() and line.strip().endswith(".so")
+                    or "openblas" in line.lower()}
+        for path in libs:
+            if os.path.exists(path):
+                lib = ctypes.CDLL(path)
+                for sym in ("openblas_get_num_threads64_", "openblas_get_num_threads", "scipy_openblas_get_num_threads64_"):
+                    if hasattr(lib, sym):
+                        return int(getattr(lib, sym)())
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def _oracle_inputs(x, g, G):
+    f = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    return (f(x.Q[g * G:(g + 1) * G]), f(x.K_hist[g:g + 1]), f(x.V_hist[g:g + 1]), f(x.K_chunk[g:g + 1]),
+            f(x.V_chunk[g:g + 1]))
+
+
+def cpu_baseline(cfg, x, gqa, groups=None):
+    """The oracle as it stands on this host's cores, on KV groups of the same chunk (each group is an
+    independent 1/H_kv share of the chunk's work); reported as the equivalent chunk tokens/s."""
+    from oracle import quoka_oracle as qo
+    groups = list(range(cfg.H_kv)) if groups is None else groups
+    t = 0.0
+    for g in groups:
+        args = _oracle_inputs(x, g, cfg.G)
+        t0 = time.perf_counter()
+        qo.chunk_attend(*args, cfg.N_q, cfg.B, gqa)
+        t += time.perf_counter() - t0
+    per_chunk = t * cfg.H_kv / len(groups)
+    return {"value": round(cfg.C / per_chunk, 2), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"numpy float64 oracle, {len(groups)} of {cfg.H_kv} KV groups of one chunk "
+                      f"({cfg.G} query heads each), {t:.1f} s measured, scaled to a whole chunk"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    cfg = WORKLOADS[args.workload]
+    x = wl.make_chunk(cfg, args.seed)
+    from oracle import quoka_oracle as qo
+    times = []
+    for k in range(args.warmup + args.steps):
+        g = k % cfg.H_kv
+        a = _oracle_inputs(x, g, cfg.G)
+        t0 = time.perf_counter()
+        qo.chunk_attend(*a, cfg.N_q, cfg.B, args.gqa)
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            times.append(dt)
+    per_chunk = statistics.mean(times) * cfg.H_kv
+    value = round(cfg.C / per_chunk, 2)
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(per_chunk * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "d": cfg.d, "C": cfg.C, "T": cfg.T,
+                   "N_q": cfg.N_q, "B": cfg.B, "gqa_pool": args.gqa, "parallelism": "host cores"},
+        "impl": "reference",
+        "gpu_launches": 0,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+                         "sample": f"each step: one of {cfg.H_kv} KV groups of the chunk through the numpy "
+                                   f"float64 oracle, scaled x{cfg.H_kv} to a whole chunk"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["quoka", "reference"], default="quoka")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa32k")
+    ap.add_argument("--gqa", choices=["max", "mean"], default="max")
+    ap.add_argument("--engine", choices=["auto", "simt", "tensor"], default="auto")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)     # rank 0 alone; other ranks exit without work
+    else:
+        dist_init("nccl")
+        res = run_quoka(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * quoka.h -- C ABI of libquoka.so: QUOKA per-chunk KV selection plus sparse
+ * attention for chunked prefill, on GB300 (sm_103a).
+ *
+ * Method sources (page title, section):
+ *   [P1] "QUOKA: Query-Oriented KV Selection For Efficient LLM Prefill"
+ *        (paper summary): "Transformers and Attention", "Chunked prefill",
+ *        "Attention Sparsity and Sparse Attention", "QUOKA Method",
+ *        "Query Subselection", "Scoring via Cosine Similarity",
+ *        "Aggregation Across Queries and KV Groups", "Chunked Prefill with QUOKA".
+ *   [P2] "QUOKA Explained: Choosing Which KV History Attention Should Read":
+ *        "Pick the queries that disagree with the crowd", "Letting those
+ *        queries score the history", "Why take the maximum", "From scores to
+ *        a smaller KV set", "A wrinkle: grouped-query attention", "MEAN and
+ *        MAX do different jobs".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Tensors are row-major and contiguous unless a stride says otherwise:
+ *   Q        [H_q,  C, d]   chunk queries
+ *   K_hist   [H_kv, T, d]   cached history keys; consecutive KV heads are
+ *   V_hist   [H_kv, T, d]   kv_head_stride elements apart (>= T*d, so a
+ *                           preallocated cache can grow in place)
+ *   K_chunk  [H_kv, C, d]   the chunk's own keys / values
+ *   V_chunk  [H_kv, C, d]
+ *   O        [H_q,  C, d]   output, same element type as Q
+ * Query head h reads KV head h / (H_q / H_kv).  The element type of every
+ * tensor argument is shape->dtype (bf16 or fp32); scores and lse are fp32;
+ * index arrays are int32.
+ *
+ * Pointers: every tensor pointer is a DEVICE pointer (or managed memory)
+ * owned by the caller and 16-byte aligned; the library never allocates,
+ * frees or synchronises on these paths.  `stream` is a cudaStream_t (NULL is
+ * the legacy default stream); every call only enqueues work on it and
+ * returns.  Results are valid once the stream reaches that point.
+ *
+ * Workspace: calls that take (ws, ws_bytes) use caller-owned device scratch of
+ * at least quoka_workspace_size() bytes, 256-byte aligned.  Its first word is
+ * the sticky device error status (see quoka_get_last_device_error); zero it
+ * once (cudaMemset) before first use.  Calls sharing one workspace must be
+ * ordered on one stream.
+ *
+ * Errors: every function returns a quoka_status.  Argument checks happen on
+ * the host before anything is enqueued; a non-OK return means nothing was
+ * enqueued, except QUOKA_ERR_CUDA (a launch failed).  Errors found by the GPU
+ * (an expired bounded wait) are recorded in the workspace error word.
+ */
+#ifndef QUOKA_H_
+#define QUOKA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QUOKA_OK = 0,
+  QUOKA_ERR_INVALID_ARG = 1,   /* a size, pointer or mode is out of range */
+  QUOKA_ERR_UNSUPPORTED = 2,   /* valid, but outside what the kernels handle (e.g. d not 64/128) */
+  QUOKA_ERR_WORKSPACE = 3,     /* ws is NULL, misaligned or smaller than required */
+  QUOKA_ERR_ALIGNMENT = 4,     /* a tensor pointer is not 16-byte aligned */
+  QUOKA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+  QUOKA_ERR_TIMEOUT = 6,       /* device side: a bounded wait expired (kernel exited early) */
+  QUOKA_ERR_DEVICE = 7         /* device side: an internal consistency check failed */
+} quoka_status;
+
+typedef enum { QUOKA_DTYPE_BF16 = 0, QUOKA_DTYPE_FP32 = 1 } quoka_dtype;
+
+/* How scores of the query heads of one KV group are pooled
+ * ([P1] "Aggregation Across Queries and KV Groups"; [P2] "A wrinkle:
+ * grouped-query attention", "MEAN and MAX do different jobs").
+ *  MEAN_PREAGG: one selected token set per KV group (the group's per-head
+ *    cosines to their mean queries are averaged before the N_q least
+ *    similar tokens are kept); the normalised query heads of each kept token
+ *    are averaged (not re-normalised) and that one row scores the keys, so
+ *    a key's score is the maximum over tokens of the head-averaged cosine.
+ *  MAX: one selected token set per query head; every selected row of every
+ *    head of the group scores the keys and the maximum is taken over all
+ *    of them. */
+typedef enum { QUOKA_GQA_MEAN_PREAGG = 0, QUOKA_GQA_MAX = 1 } quoka_gqa_pool;
+
+/* Which kernel family runs the scoring and attention stages.  AUTO picks the
+ * tensor-core (tcgen05) kernels for bf16 where they exist and the CUDA-core
+ * kernels otherwise; SIMT forces the CUDA-core kernels (fp32 always uses them). */
+typedef enum { QUOKA_ENGINE_AUTO = 0, QUOKA_ENGINE_SIMT = 1, QUOKA_ENGINE_TENSOR = 2 } quoka_engine;
+
+typedef struct {
+  int64_t kv_head_stride;  /* elements between KV heads of K_hist / V_hist; 0 means T*d */
+  int32_t H_q;             /* query heads, >= 1, multiple of H_kv */
+  int32_t H_kv;            /* KV heads, >= 1 */
+  int32_t C;               /* chunk length (queries), 1 .. 8192 */
+  int32_t T;               /* history length (cached keys), >= 0 */
+  int32_t d;               /* head dim, 64 or 128 */
+  int32_t dtype;           /* quoka_dtype */
+} quoka_shape;
+
+typedef struct {
+  int32_t gqa_pool;        /* quoka_gqa_pool */
+  int32_t engine;          /* quoka_engine */
+  float softmax_scale;     /* <= 0 means 1/sqrt(d) */
+  int32_t reserved;        /* must be 0 */
+} quoka_params;
+
+/* Human-readable name of a status code (static storage). */
+const char* quoka_status_string(int status);
+
+/* Bytes of workspace that quoka_chunk_attend needs for this problem; the
+ * same size also covers every single-stage call on the same shape.
+ * N_q and B as for quoka_chunk_attend.  Writes *bytes; host only. */
+int quoka_workspace_size(const quoka_shape* shape, int N_q, int B, const quoka_params* params,
+                         size_t* bytes);
+
+/* Query subselection ([P1] "Query Subselection"; [P2] "Pick the queries that
+ * disagree with the crowd").  Per query head the mean query M_q of the
+ * chunk's C raw queries is formed and every query's cosine to it computed
+ * (norms clamped at 1e-12); the N_q' = min(N_q, C) queries with the smallest
+ * cosine (largest -CosSim) are kept, ties to the lower position.
+ * q_idx: int32 [H_sel, N_q'] written in ascending order, where H_sel = H_q
+ * for QUOKA_GQA_MAX (per head) and H_kv for QUOKA_GQA_MEAN_PREAGG (per group,
+ * on the cosine averaged over the group's heads).  Uses ws. */
+int quoka_select_queries(const quoka_shape* shape, const void* Q, int N_q, const quoka_params* params,
+                         int32_t* q_idx, void* ws, size_t ws_bytes, void* stream);
+
+/* Cosine scoring plus aggregation ([P1] "Scoring via Cosine Similarity",
+ * "Aggregation Across Queries and KV Groups"; [P2] "Letting those queries
+ * score the history", "Why take the maximum").  For every KV group g and
+ * history key t < T:
+ *   scores[g, t] = max over the group's scoring rows r of  r . k_t / |k_t|
+ * where the rows are the normalised selected queries of every head of g
+ * (MAX) or their head average per selected token (MEAN_PREAGG).  Products
+ * are accumulated in fp32.  q_idx as written by quoka_select_queries with the
+ * same N_q and pooling.  scores: fp32 [H_kv, T].  Uses ws. */
+int quoka_score_keys(const quoka_shape* shape, const void* Q, const int32_t* q_idx, int N_q,
+                     const void* K_hist, const quoka_params* params, float* scores,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* Top-B history keys per KV head ([P2] "From scores to a smaller KV set").
+ * Reads scores fp32 [H_kv, T] (shape->H_kv, shape->T); writes sel int32
+ * [H_kv, B_e], B_e = min(B, T), the positions of the B_e largest scores in
+ * ascending position order, ties to the lower position (-0.0 equals 0.0).
+ * Scores must not be NaN.  Uses ws. */
+int quoka_topk(const quoka_shape* shape, const float* scores, int B, int32_t* sel,
+               void* ws, size_t ws_bytes, void* stream);
+
+/* Gather the selected rows: K_sel[g, j] = K_hist[g, sel[g, j]], same for V
+ * ([P2] "From scores to a smaller KV set": the value comes with its key).
+ * sel int32 [H_kv, B_e], every entry in [0, T); K_sel, V_sel [H_kv, B_e, d]
+ * contiguous, dtype of the shape. */
+int quoka_gather(const quoka_shape* shape, const void* K_hist, const void* V_hist, const int32_t* sel,
+                 int B_e, void* K_sel, void* V_sel, void* stream);
+
+/* Attention over the reduced set ([P1] "Transformers and Attention",
+ * "Chunked prefill", "QUOKA Method"; [P2] "MEAN and MAX do different jobs":
+ * the original query heads attend).  For query head h, chunk row c:
+ *   O[h, c] = softmax_j(scale * Q[h, c] . k_j) v_j over the keys
+ *   k = [K_sel[g, 0..B_e) ; K_chunk[g, 0..c]]   (causal within the chunk)
+ * K_sel, V_sel [H_kv, B_e, d] contiguous (B_e may be 0).  lse, if not NULL,
+ * receives fp32 [H_q, C] natural-log softmax denominators of the scaled
+ * logits.  Uses ws (error word only). */
+int quoka_sparse_attend(const quoka_shape* shape, const void* Q, const void* K_sel, const void* V_sel,
+                        int B_e, const void* K_chunk, const void* V_chunk, const quoka_params* params,
+                        void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* One chunk of QUOKA chunked prefill end to end ([P1] "QUOKA Method",
+ * "Chunked Prefill with QUOKA"): select queries, score the history, keep the
+ * top-B keys per KV head, attend to them plus the causal chunk.  T = 0 or
+ * B >= T skips selection and attends to the whole history.  sel_out, if not
+ * NULL, receives int32 [H_kv, min(B, T)] (ascending); lse as above. */
+int quoka_chunk_attend(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
+                       const void* K_chunk, const void* V_chunk, int N_q, int B,
+                       const quoka_params* params, void* O, float* lse, int32_t* sel_out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Dense chunked-prefill attention over every history key plus the causal
+ * chunk ([P1] "Chunked prefill"): the reference QUOKA is measured against.
+ * Arguments as quoka_chunk_attend without the selection. */
+int quoka_dense_attend(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
+                       const void* K_chunk, const void* V_chunk, const quoka_params* params,
+                       void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Append the chunk's keys and values to the cache ([P2] "MEAN and MAX do
+ * different jobs": nothing is evicted): K_hist[g, T + c] = K_chunk[g, c] and
+ * likewise V, for c < C.  Requires kv_head_stride >= (T + C) * d. */
+int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const void* K_chunk,
+                    const void* V_chunk, void* stream);
+
+/* Which kernel family a stage runs for this shape and params:
+ * QUOKA_ENGINE_TENSOR (tcgen05 tensor cores) or QUOKA_ENGINE_SIMT (CUDA
+ * cores).  stage: 0 = key scoring, 1 = attention.  Returns a negative
+ * quoka_status if the shape, params or stage are invalid.  Host only. */
+int quoka_stage_engine(const quoka_shape* shape, const quoka_params* params, int stage);
+
+/* Number of CUDA kernels this library has enqueued in this process so far
+ * (diagnostics: lets a caller count the launches of a timed region). */
+uint64_t quoka_launch_count(void);
+
+/* Synchronises `stream`, returns the device error recorded in ws (QUOKA_OK
+ * if none) and clears it.  Returns QUOKA_ERR_CUDA if the synchronisation or
+ * the read fails. */
+int quoka_get_last_device_error(void* ws, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* QUOKA_H_ */

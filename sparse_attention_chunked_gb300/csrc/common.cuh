@@ -1,0 +1,83 @@
+// Device helpers shared by the QUOKA kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace quoka {
+
+constexpr float kNormEps = 1e-12f;   // norms below this are clamped (a zero vector scores 0)
+
+// Sticky device-side error word at the start of every workspace.
+struct WsHeader {
+  unsigned int err;      // first quoka_status recorded by a kernel (0 = none)
+  unsigned int where;    // kernel-specific detail (which wait expired)
+  unsigned int pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header keeps the workspace 256-byte aligned");
+
+__device__ __forceinline__ void record_error(WsHeader* hdr, unsigned int code, unsigned int where) {
+  if (hdr != nullptr && atomicCAS(&hdr->err, 0u, code) == 0u) hdr->where = where;
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Monotone map of a float to uint32: a < b as floats  <=>  key(a) < key(b).
+// -0.0 is folded onto +0.0 so that equal floats get equal keys.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  if (f == 0.0f) f = 0.0f;
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix sum over a block of exactly blockDim.x threads (a multiple
+// of 32, at most 1024).  `scratch` holds 32 ints.  Returns the exclusive
+// prefix of `v`; *total receives the block sum.  Contains __syncthreads().
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarp ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    scratch[lane] = w;   // inclusive prefix over warps
+  }
+  __syncthreads();
+  int warp_base = warp > 0 ? scratch[warp - 1] : 0;
+  *total = scratch[nwarp - 1];
+  int res = warp_base + x - v;
+  __syncthreads();
+  return res;
+}
+
+}  // namespace quoka

@@ -1,0 +1,72 @@
+// Row gather of the selected history keys/values (QUOKA Explained, "From
+// scores to a smaller KV set": the value comes with its key) and the cache
+// append of a processed chunk (QUOKA Explained, "MEAN and MAX do different
+// jobs": nothing is evicted).  Both are 16-byte vector copies, one vector per
+// thread, grid-stride.
+#include "common.cuh"
+#include "launch.h"
+
+namespace quoka {
+
+// K_sel[g, j] = K_hist[g, sel[g, j]] and likewise V; row = vec_per_row uint4.
+__global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restrict__ V, int64_t head_stride_vec,
+                              const int32_t* __restrict__ sel, int H_kv, int B_e, int vec_per_row,
+                              uint4* __restrict__ Ks, uint4* __restrict__ Vs) {
+  const size_t per_mat = (size_t)H_kv * B_e * vec_per_row;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * per_mat;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const bool is_v = i >= per_mat;
+    const size_t w = is_v ? i - per_mat : i;
+    const int v = (int)(w % vec_per_row);
+    const size_t row = w / vec_per_row;              // g * B_e + j
+    const int g = (int)(row / B_e);
+    const int t = sel[row];
+    const uint4* src = (is_v ? V : K) + (size_t)g * head_stride_vec + (size_t)t * vec_per_row + v;
+    (is_v ? Vs : Ks)[w] = *src;
+  }
+}
+
+// K_hist[g, T + c] = K_chunk[g, c] and likewise V.
+__global__ void k_append_rows(uint4* __restrict__ K, uint4* __restrict__ V, int64_t head_stride_vec, int T_len,
+                              const uint4* __restrict__ Kc, const uint4* __restrict__ Vc, int H_kv, int C,
+                              int vec_per_row) {
+  const size_t per_mat = (size_t)H_kv * C * vec_per_row;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * per_mat;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const bool is_v = i >= per_mat;
+    const size_t w = is_v ? i - per_mat : i;
+    const int v = (int)(w % vec_per_row);
+    const size_t row = w / vec_per_row;              // g * C + c
+    const int g = (int)(row / C), c = (int)(row % C);
+    uint4* dst = (is_v ? V : K) + (size_t)g * head_stride_vec + (size_t)(T_len + c) * vec_per_row + v;
+    *dst = (is_v ? Vc : Kc)[w];
+  }
+}
+
+static int grid_for(size_t work) {
+  size_t b = (work + 255) / 256;
+  return (int)(b < 152 * 16 ? (b == 0 ? 1 : b) : 152 * 16);
+}
+
+cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, int64_t head_stride, const int32_t* sel,
+                          int H_kv, int B_e, void* Ks, void* Vs, cudaStream_t st) {
+  if (B_e == 0) return cudaSuccess;
+  const int vpr = d * elt_bytes / 16;
+  const int64_t hsv = head_stride * elt_bytes / 16;
+  k_gather_rows<<<grid_for((size_t)2 * H_kv * B_e * vpr), 256, 0, st>>>(
+      (const uint4*)K, (const uint4*)V, hsv, sel, H_kv, B_e, vpr, (uint4*)Ks, (uint4*)Vs);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(int elt_bytes, int d, void* K, void* V, int64_t head_stride, int T_len, const void* Kc,
+                          const void* Vc, int H_kv, int C, cudaStream_t st) {
+  const int vpr = d * elt_bytes / 16;
+  const int64_t hsv = head_stride * elt_bytes / 16;
+  k_append_rows<<<grid_for((size_t)2 * H_kv * C * vpr), 256, 0, st>>>(
+      (uint4*)K, (uint4*)V, hsv, T_len, (const uint4*)Kc, (const uint4*)Vc, H_kv, C, vpr);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace quoka

@@ -1,0 +1,331 @@
+// C ABI of libquoka.so: argument checks, workspace layout and the launch
+// sequence of each entry point.  Declarations and their contracts are in
+// include/quoka.h.
+#include <math.h>
+#include <string.h>
+
+#include "../../include/quoka.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+using namespace quoka;
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int elt_bytes(int dtype) { return dtype == QUOKA_DTYPE_FP32 ? 4 : 2; }
+
+int64_t head_stride(const quoka_shape* s) {
+  return s->kv_head_stride ? s->kv_head_stride : (int64_t)s->T * s->d;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_shape(const quoka_shape* s) {
+  if (s == nullptr) return QUOKA_ERR_INVALID_ARG;
+  if (s->H_q < 1 || s->H_kv < 1 || s->H_q % s->H_kv != 0) return QUOKA_ERR_INVALID_ARG;
+  if (s->C < 1 || s->T < 0) return QUOKA_ERR_INVALID_ARG;
+  if (s->dtype != QUOKA_DTYPE_BF16 && s->dtype != QUOKA_DTYPE_FP32) return QUOKA_ERR_INVALID_ARG;
+  if (s->kv_head_stride < 0 || head_stride(s) < (int64_t)s->T * s->d) return QUOKA_ERR_INVALID_ARG;
+  if (s->d != 64 && s->d != 128) return QUOKA_ERR_UNSUPPORTED;
+  if (s->C > 8192) return QUOKA_ERR_UNSUPPORTED;
+  if ((head_stride(s) * elt_bytes(s->dtype)) % 16 != 0) return QUOKA_ERR_ALIGNMENT;
+  return QUOKA_OK;
+}
+
+struct Params {
+  int gqa;        // quoka_gqa_pool
+  int engine;     // quoka_engine
+  float scale;
+};
+
+int read_params(const quoka_params* p, const quoka_shape* s, Params* out) {
+  out->gqa = QUOKA_GQA_MEAN_PREAGG;
+  out->engine = QUOKA_ENGINE_AUTO;
+  out->scale = 1.0f / sqrtf((float)s->d);
+  if (p == nullptr) return QUOKA_OK;
+  if (p->gqa_pool != QUOKA_GQA_MEAN_PREAGG && p->gqa_pool != QUOKA_GQA_MAX) return QUOKA_ERR_INVALID_ARG;
+  if (p->engine < QUOKA_ENGINE_AUTO || p->engine > QUOKA_ENGINE_TENSOR) return QUOKA_ERR_INVALID_ARG;
+  if (p->reserved != 0) return QUOKA_ERR_INVALID_ARG;
+  if (!(p->softmax_scale == p->softmax_scale)) return QUOKA_ERR_INVALID_ARG;   // NaN
+  out->gqa = p->gqa_pool;
+  out->engine = p->engine;
+  if (p->softmax_scale > 0.f) out->scale = p->softmax_scale;
+  return QUOKA_OK;
+}
+
+// Which kernels run (stage 0 = scoring, 1 = attention).  Tensor-core kernels are bf16 only.
+bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage) {
+  (void)p;
+  (void)s;
+  (void)stage;
+  return false;
+}
+
+// Workspace regions, in order; each stage only touches the prefix it needs:
+//   [header][select scratch][score scratch][chunk intermediates]
+struct Layout {
+  size_t qnorm, qpart, qcos, select_end;
+  size_t op_f32, op_bf, op_scale, score_end;
+  size_t q_idx, scores, sel, ksel, vsel, total;
+};
+
+int n_sel_of(const quoka_shape* s, int N_q) { return N_q < s->C ? N_q : s->C; }
+
+int score_rows(const quoka_shape* s, int N_q, int gqa) {
+  const int n = n_sel_of(s, N_q), G = s->H_q / s->H_kv;
+  return gqa == QUOKA_GQA_MAX ? G * n : n;
+}
+
+Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa) {
+  Layout L;
+  const size_t H_q = s->H_q, H_kv = s->H_kv, C = s->C, d = s->d, T = s->T;
+  const size_t nblk = (C + 63) / 64;
+  size_t o = sizeof(WsHeader);
+  L.qnorm = o;  o = align_up(o + H_q * C * 4);
+  L.qpart = o;  o = align_up(o + H_q * nblk * d * 4);
+  L.qcos = o;   o = align_up(o + H_q * C * 4);
+  L.select_end = o;
+  const size_t R = (size_t)score_rows(s, N_q > 0 ? N_q : 1, gqa);
+  L.op_f32 = o;   o = align_up(o + H_kv * R * d * 4);
+  L.op_bf = o;    o = align_up(o + H_kv * 2 * R * d * 2);
+  L.op_scale = o; o = align_up(o + H_kv * 2 * R * 4);
+  L.score_end = o;
+  const size_t n = (size_t)n_sel_of(s, N_q > 0 ? N_q : 1);
+  const size_t B_e = (size_t)(B < s->T ? B : s->T);
+  L.q_idx = o;  o = align_up(o + H_q * n * 4);
+  L.scores = o; o = align_up(o + H_kv * T * 4);
+  L.sel = o;    o = align_up(o + H_kv * B_e * 4);
+  L.ksel = o;   o = align_up(o + H_kv * B_e * d * elt_bytes(s->dtype));
+  L.vsel = o;   o = align_up(o + H_kv * B_e * d * elt_bytes(s->dtype));
+  L.total = o;
+  return L;
+}
+
+int check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr || ((uintptr_t)ws % kAlign) != 0 || ws_bytes < need) return QUOKA_ERR_WORKSPACE;
+  return QUOKA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? QUOKA_OK : QUOKA_ERR_CUDA; }
+
+template <typename P> P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<char*>(ws) + off); }
+
+#define QUOKA_TRY(x)                 \
+  do {                               \
+    int _rc = (x);                   \
+    if (_rc != QUOKA_OK) return _rc; \
+  } while (0)
+
+#define QUOKA_CUDA(x) QUOKA_TRY(cuda_status(x))
+
+int run_select(const quoka_shape* s, const void* Q, int n, const Params& p, int32_t* q_idx, void* ws,
+               const Layout& L, cudaStream_t st) {
+  const int G = s->H_q / s->H_kv;
+  const int G_avg = p.gqa == QUOKA_GQA_MAX ? 1 : G;
+  return cuda_status(launch_select_queries(s->dtype, s->d, Q, s->H_q, G_avg, s->C, n, q_idx, at<float>(ws, L.qnorm),
+                                           at<float>(ws, L.qpart), at<float>(ws, L.qcos), st));
+}
+
+int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, const void* K_hist,
+              const Params& p, float* scores, void* ws, const Layout& L, cudaStream_t st) {
+  const int G = s->H_q / s->H_kv;
+  const int mode = p.gqa == QUOKA_GQA_MAX ? 1 : 0;
+  const int R = score_rows(s, n, p.gqa);
+  const bool tc = use_tensor_cores(p, s, 0);
+  QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, mode, at<float>(ws, L.op_f32),
+                                  tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr, at<float>(ws, L.op_scale), st));
+  return cuda_status(launch_score_simt(s->dtype, s->d, K_hist, head_stride(s), s->H_kv, s->T,
+                                       at<float>(ws, L.op_f32), R, scores, st));
+}
+
+int run_attend(const quoka_shape* s, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
+               const void* Kc, const void* Vc, const Params& p, void* O, float* lse, void* ws, cudaStream_t st) {
+  (void)ws;
+  const int G = s->H_q / s->H_kv;
+  return cuda_status(launch_attend_simt(s->dtype, s->d, Q, Kh, Vh, h_stride, n_hist, Kc, Vc, s->H_q, s->C, G,
+                                        p.scale, O, lse, st));
+}
+
+}  // namespace
+
+namespace quoka {
+std::atomic<unsigned long long> g_launch_count{0};
+}
+
+extern "C" {
+
+int quoka_stage_engine(const quoka_shape* shape, const quoka_params* params, int stage) {
+  const int rc = check_shape(shape);
+  if (rc != QUOKA_OK) return -rc;
+  Params p;
+  const int rp = read_params(params, shape, &p);
+  if (rp != QUOKA_OK) return -rp;
+  if (stage != 0 && stage != 1) return -QUOKA_ERR_INVALID_ARG;
+  return use_tensor_cores(p, shape, stage) ? QUOKA_ENGINE_TENSOR : QUOKA_ENGINE_SIMT;
+}
+
+uint64_t quoka_launch_count(void) { return quoka::g_launch_count.load(std::memory_order_relaxed); }
+
+const char* quoka_status_string(int status) {
+  switch (status) {
+    case QUOKA_OK: return "QUOKA_OK";
+    case QUOKA_ERR_INVALID_ARG: return "QUOKA_ERR_INVALID_ARG";
+    case QUOKA_ERR_UNSUPPORTED: return "QUOKA_ERR_UNSUPPORTED";
+    case QUOKA_ERR_WORKSPACE: return "QUOKA_ERR_WORKSPACE";
+    case QUOKA_ERR_ALIGNMENT: return "QUOKA_ERR_ALIGNMENT";
+    case QUOKA_ERR_CUDA: return "QUOKA_ERR_CUDA";
+    case QUOKA_ERR_TIMEOUT: return "QUOKA_ERR_TIMEOUT";
+    case QUOKA_ERR_DEVICE: return "QUOKA_ERR_DEVICE";
+    default: return "QUOKA_ERR_UNKNOWN";
+  }
+}
+
+int quoka_workspace_size(const quoka_shape* shape, int N_q, int B, const quoka_params* params, size_t* bytes) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  if (N_q < 1 || B < 1 || bytes == nullptr) return QUOKA_ERR_INVALID_ARG;
+  *bytes = make_layout(shape, N_q, B, p.gqa).total;
+  return QUOKA_OK;
+}
+
+int quoka_select_queries(const quoka_shape* shape, const void* Q, int N_q, const quoka_params* params,
+                         int32_t* q_idx, void* ws, size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  if (N_q < 1 || Q == nullptr || q_idx == nullptr) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(q_idx)) return QUOKA_ERR_ALIGNMENT;
+  const Layout L = make_layout(shape, N_q, 1, p.gqa);
+  QUOKA_TRY(check_ws(ws, ws_bytes, L.select_end));
+  return run_select(shape, Q, n_sel_of(shape, N_q), p, q_idx, ws, L, (cudaStream_t)stream);
+}
+
+int quoka_score_keys(const quoka_shape* shape, const void* Q, const int32_t* q_idx, int N_q, const void* K_hist,
+                     const quoka_params* params, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  if (N_q < 1 || Q == nullptr || q_idx == nullptr || K_hist == nullptr || scores == nullptr)
+    return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(q_idx) || !aligned16(K_hist) || !aligned16(scores)) return QUOKA_ERR_ALIGNMENT;
+  const Layout L = make_layout(shape, N_q, 1, p.gqa);
+  QUOKA_TRY(check_ws(ws, ws_bytes, L.score_end));
+  if (shape->T == 0) return QUOKA_OK;
+  return run_score(shape, Q, q_idx, n_sel_of(shape, N_q), K_hist, p, scores, ws, L, (cudaStream_t)stream);
+}
+
+int quoka_topk(const quoka_shape* shape, const float* scores, int B, int32_t* sel, void* ws, size_t ws_bytes,
+               void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  if (B < 1 || scores == nullptr || sel == nullptr) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(scores) || !aligned16(sel)) return QUOKA_ERR_ALIGNMENT;
+  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
+  const int B_e = B < shape->T ? B : shape->T;
+  return cuda_status(launch_topk(scores, shape->H_kv, shape->T, B_e, sel, (cudaStream_t)stream));
+}
+
+int quoka_gather(const quoka_shape* shape, const void* K_hist, const void* V_hist, const int32_t* sel, int B_e,
+                 void* K_sel, void* V_sel, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  if (B_e < 0 || B_e > shape->T) return QUOKA_ERR_INVALID_ARG;
+  if (B_e == 0) return QUOKA_OK;
+  if (!K_hist || !V_hist || !sel || !K_sel || !V_sel) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(K_hist) || !aligned16(V_hist) || !aligned16(sel) || !aligned16(K_sel) || !aligned16(V_sel))
+    return QUOKA_ERR_ALIGNMENT;
+  return cuda_status(launch_gather(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), sel,
+                                   shape->H_kv, B_e, K_sel, V_sel, (cudaStream_t)stream));
+}
+
+int quoka_sparse_attend(const quoka_shape* shape, const void* Q, const void* K_sel, const void* V_sel, int B_e,
+                        const void* K_chunk, const void* V_chunk, const quoka_params* params, void* O, float* lse,
+                        void* ws, size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  if (B_e < 0 || Q == nullptr || K_chunk == nullptr || V_chunk == nullptr || O == nullptr) return QUOKA_ERR_INVALID_ARG;
+  if (B_e > 0 && (K_sel == nullptr || V_sel == nullptr)) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K_sel) || !aligned16(V_sel) || !aligned16(K_chunk) || !aligned16(V_chunk) ||
+      !aligned16(O) || !aligned16(lse))
+    return QUOKA_ERR_ALIGNMENT;
+  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
+  return run_attend(shape, Q, K_sel, V_sel, (int64_t)B_e * shape->d, B_e, K_chunk, V_chunk, p, O, lse, ws,
+                    (cudaStream_t)stream);
+}
+
+int quoka_dense_attend(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
+                       const void* K_chunk, const void* V_chunk, const quoka_params* params, void* O, float* lse,
+                       void* ws, size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  if (Q == nullptr || K_chunk == nullptr || V_chunk == nullptr || O == nullptr) return QUOKA_ERR_INVALID_ARG;
+  if (shape->T > 0 && (K_hist == nullptr || V_hist == nullptr)) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K_hist) || !aligned16(V_hist) || !aligned16(K_chunk) || !aligned16(V_chunk) ||
+      !aligned16(O) || !aligned16(lse))
+    return QUOKA_ERR_ALIGNMENT;
+  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
+  return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), shape->T, K_chunk, V_chunk, p, O, lse, ws,
+                    (cudaStream_t)stream);
+}
+
+int quoka_chunk_attend(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
+                       const void* K_chunk, const void* V_chunk, int N_q, int B, const quoka_params* params,
+                       void* O, float* lse, int32_t* sel_out, void* ws, size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  if (N_q < 1 || B < 1 || Q == nullptr || K_chunk == nullptr || V_chunk == nullptr || O == nullptr)
+    return QUOKA_ERR_INVALID_ARG;
+  if (shape->T > 0 && (K_hist == nullptr || V_hist == nullptr)) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K_hist) || !aligned16(V_hist) || !aligned16(K_chunk) || !aligned16(V_chunk) ||
+      !aligned16(O) || !aligned16(lse) || !aligned16(sel_out))
+    return QUOKA_ERR_ALIGNMENT;
+  const Layout L = make_layout(shape, N_q, B, p.gqa);
+  QUOKA_TRY(check_ws(ws, ws_bytes, L.total));
+  cudaStream_t st = (cudaStream_t)stream;
+  const int T = shape->T;
+  if (T == 0 || B >= T) {   // every history key is kept: dense chunked-prefill attention
+    if (sel_out != nullptr && T > 0) QUOKA_CUDA(launch_topk(nullptr, shape->H_kv, T, T, sel_out, st));
+    return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), T, K_chunk, V_chunk, p, O, lse, ws, st);
+  }
+  const int n = n_sel_of(shape, N_q);
+  int32_t* q_idx = at<int32_t>(ws, L.q_idx);
+  float* scores = at<float>(ws, L.scores);
+  int32_t* sel = sel_out != nullptr ? sel_out : at<int32_t>(ws, L.sel);
+  QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
+  QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st));
+  QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st));
+  void* ksel = at<void>(ws, L.ksel);
+  void* vsel = at<void>(ws, L.vsel);
+  QUOKA_CUDA(launch_gather(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), sel, shape->H_kv, B,
+                           ksel, vsel, st));
+  return run_attend(shape, Q, ksel, vsel, (int64_t)B * shape->d, B, K_chunk, V_chunk, p, O, lse, ws, st);
+}
+
+int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const void* K_chunk, const void* V_chunk,
+                    void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  if (!K_hist || !V_hist || !K_chunk || !V_chunk) return QUOKA_ERR_INVALID_ARG;
+  if (head_stride(shape) < (int64_t)(shape->T + (int64_t)shape->C) * shape->d) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(K_hist) || !aligned16(V_hist) || !aligned16(K_chunk) || !aligned16(V_chunk))
+    return QUOKA_ERR_ALIGNMENT;
+  return cuda_status(launch_append(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), shape->T,
+                                   K_chunk, V_chunk, shape->H_kv, shape->C, (cudaStream_t)stream));
+}
+
+int quoka_get_last_device_error(void* ws, void* stream) {
+  if (ws == nullptr) return QUOKA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  WsHeader h;
+  if (cudaMemcpyAsync(&h, ws, 8, cudaMemcpyDeviceToHost, st) != cudaSuccess) return QUOKA_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return QUOKA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QUOKA_ERR_CUDA;
+  return (int)h.err;
+}
+
+}  // extern "C"

@@ -1,0 +1,161 @@
+// Scoring operand and the CUDA-core scoring kernel.
+// Method: QUOKA paper summary, "Scoring via Cosine Similarity" and
+// "Aggregation Across Queries and KV Groups"; QUOKA Explained, "Letting those
+// queries score the history", "Why take the maximum", "A wrinkle:
+// grouped-query attention".
+#include "common.cuh"
+#include "launch.h"
+
+namespace quoka {
+
+// One warp per scoring row.  Row r of KV group g:
+//   MAX : r = k * n + i  -> query head h = g*G + k, position q_idx[h, i];
+//         fp32 row q / |q|; tensor-core copy: the raw row and scale 1/|q|.
+//   MEAN: r = i          -> position q_idx[g, i];
+//         fp32 row (1/G) sum_k q_k / |q_k| over the group's heads (not
+//         re-normalised); tensor-core copy: hi = bf16(row), lo = bf16(row - hi)
+//         as rows r and R + r, scale 1.
+template <typename T, int D>
+__global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, const int32_t* __restrict__ q_idx,
+                                                      int C, int G, int n, int mode, float* __restrict__ op_f32,
+                                                      __nv_bfloat16* __restrict__ op_bf, float* __restrict__ op_scale) {
+  constexpr int E = D / 32;
+  const int g = blockIdx.y, r = blockIdx.x, R = gridDim.x, lane = threadIdx.x;
+  float acc[E];
+  if (mode == 1) {  // MAX
+    const int k = r / n, i = r % n, h = g * G + k;
+    const int c = q_idx[(size_t)h * n + i];
+    const T* q = Q + ((size_t)h * C + c) * D;
+    float x[E], ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      x[j] = to_f32(q[lane + 32 * j]);
+      ss = fmaf(x[j], x[j], ss);
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / fmaxf(sqrtf(ss), kNormEps);
+#pragma unroll
+    for (int j = 0; j < E; ++j) acc[j] = x[j] * inv;
+    if (op_bf != nullptr) {
+#pragma unroll
+      for (int j = 0; j < E; ++j) op_bf[((size_t)g * R + r) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
+      if (lane == 0) op_scale[(size_t)g * R + r] = inv;
+    }
+  } else {  // MEAN (pre-aggregation)
+    const int c = q_idx[(size_t)g * n + r];
+#pragma unroll
+    for (int j = 0; j < E; ++j) acc[j] = 0.f;
+    for (int k = 0; k < G; ++k) {
+      const T* q = Q + ((size_t)(g * G + k) * C + c) * D;
+      float x[E], ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        x[j] = to_f32(q[lane + 32 * j]);
+        ss = fmaf(x[j], x[j], ss);
+      }
+      ss = warp_sum(ss);
+      const float inv = 1.0f / fmaxf(sqrtf(ss), kNormEps);
+#pragma unroll
+      for (int j = 0; j < E; ++j) acc[j] = fmaf(x[j], inv, acc[j]);
+    }
+    const float invG = 1.0f / (float)G;
+#pragma unroll
+    for (int j = 0; j < E; ++j) acc[j] *= invG;
+    if (op_bf != nullptr) {
+#pragma unroll
+      for (int j = 0; j < E; ++j) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(acc[j]);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(acc[j] - __bfloat162float(hi));
+        op_bf[((size_t)g * 2 * R + r) * D + lane + 32 * j] = hi;
+        op_bf[((size_t)g * 2 * R + R + r) * D + lane + 32 * j] = lo;
+      }
+      if (lane == 0) {
+        op_scale[(size_t)g * 2 * R + r] = 1.0f;
+        op_scale[(size_t)g * 2 * R + R + r] = 1.0f;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < E; ++j) op_f32[((size_t)g * R + r) * D + lane + 32 * j] = acc[j];
+}
+
+// One thread per history key: its row is held in registers, the scoring rows
+// stream through shared memory 32 at a time; score = max_r(r . k) / |k|.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int64_t head_stride, int T_len,
+                                                    const float* __restrict__ op_f32, int R,
+                                                    float* __restrict__ scores) {
+  const int g = blockIdx.y;
+  const int t = blockIdx.x * 128 + threadIdx.x;
+  __shared__ float rows[32][D];
+  float k[D];
+  float ss = 0.f;
+  if (t < T_len) {
+    const T* kp = K + (size_t)g * head_stride + (size_t)t * D;
+#pragma unroll
+    for (int e = 0; e < D; ++e) {
+      k[e] = to_f32(kp[e]);
+      ss = fmaf(k[e], k[e], ss);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < D; ++e) k[e] = 0.f;
+  }
+  const float rk = 1.0f / fmaxf(sqrtf(ss), kNormEps);
+  float best = -INFINITY;
+  const float* opg = op_f32 + (size_t)g * R * D;
+  for (int r0 = 0; r0 < R; r0 += 32) {
+    const int nr = min(32, R - r0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nr * D; i += 128) rows[i / D][i % D] = opg[(size_t)r0 * D + i];
+    __syncthreads();
+    for (int rr = 0; rr < nr; ++rr) {
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < D; ++e) dot = fmaf(k[e], rows[rr][e], dot);
+      best = fmaxf(best, dot);
+    }
+  }
+  if (t < T_len) scores[(size_t)g * T_len + t] = best * rk;
+}
+
+cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
+                                 int n, int mode, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
+                                 cudaStream_t st) {
+  const int R = mode == 1 ? G * n : n;
+  dim3 grid(R, H_kv);
+  if (dtype == 0) {
+    if (d == 64)
+      k_build_operand<__nv_bfloat16, 64><<<grid, 32, 0, st>>>((const __nv_bfloat16*)Q, q_idx, C, G, n, mode, op_f32, op_bf, op_scale);
+    else
+      k_build_operand<__nv_bfloat16, 128><<<grid, 32, 0, st>>>((const __nv_bfloat16*)Q, q_idx, C, G, n, mode, op_f32, op_bf, op_scale);
+  } else {
+    if (d == 64)
+      k_build_operand<float, 64><<<grid, 32, 0, st>>>((const float*)Q, q_idx, C, G, n, mode, op_f32, op_bf, op_scale);
+    else
+      k_build_operand<float, 128><<<grid, 32, 0, st>>>((const float*)Q, q_idx, C, G, n, mode, op_f32, op_bf, op_scale);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
+                              const float* op_f32, int R, float* scores, cudaStream_t st) {
+  if (T_len == 0) return cudaSuccess;
+  dim3 grid((T_len + 127) / 128, H_kv);
+  if (dtype == 0) {
+    if (d == 64)
+      k_score_simt<__nv_bfloat16, 64><<<grid, 128, 0, st>>>((const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, scores);
+    else
+      k_score_simt<__nv_bfloat16, 128><<<grid, 128, 0, st>>>((const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, scores);
+  } else {
+    if (d == 64)
+      k_score_simt<float, 64><<<grid, 128, 0, st>>>((const float*)K, head_stride, T_len, op_f32, R, scores);
+    else
+      k_score_simt<float, 128><<<grid, 128, 0, st>>>((const float*)K, head_stride, T_len, op_f32, R, scores);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace quoka

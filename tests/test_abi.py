@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports what include/quoka.h declares,
+and rejects bad arguments on the host before anything is enqueued."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "quoka.h"
+
+# A fake, 256-byte aligned device address: every call below fails its host-side
+# checks before any pointer is used, so the address is never dereferenced.
+FAKE = 1 << 20
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(quoka_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_stage_entry_points():
+    names = declared_functions()
+    for fn in ("quoka_select_queries", "quoka_score_keys", "quoka_topk", "quoka_gather", "quoka_sparse_attend",
+               "quoka_chunk_attend", "quoka_dense_attend", "quoka_append_kv", "quoka_workspace_size",
+               "quoka_get_last_device_error", "quoka_status_string"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(quoka):
+    lib = ctypes.CDLL(str(quoka.lib_path()))
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_missing_library_fails_loudly(quoka, tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        quoka.load(tmp_path / "nope.so")
+
+
+def _shape(q, **kw):
+    base = dict(kv_head_stride=0, H_q=8, H_kv=2, C=128, T=1000, d=128, dtype=0)
+    base.update(kw)
+    return q.Shape(**base)
+
+
+def test_status_strings(quoka):
+    assert quoka.status_string(0) == "QUOKA_OK"
+    assert quoka.status_string(3) == "QUOKA_ERR_WORKSPACE"
+    assert quoka.status_string(99) == "QUOKA_ERR_UNKNOWN"
+
+
+def test_workspace_size_grows_with_problem(quoka):
+    p = quoka.params_of("max")
+    small = quoka.workspace_size(_shape(quoka), 16, 64, p)
+    big = quoka.workspace_size(_shape(quoka, T=100000), 16, 4096, p)
+    assert 256 < small < big
+    assert small % 256 == 0 and big % 256 == 0
+    # mean pooling scores with fewer rows than max pooling
+    assert quoka.workspace_size(_shape(quoka), 16, 64, quoka.params_of("mean")) < small
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H_q=6, H_kv=4), 1),          # H_q not a multiple of H_kv
+    (dict(H_kv=0), 1),
+    (dict(C=0), 1),
+    (dict(T=-1), 1),
+    (dict(dtype=7), 1),
+    (dict(d=96), 2),                   # head dim outside 64/128
+    (dict(C=9000), 2),
+    (dict(kv_head_stride=1000 * 128 - 1), 1),   # stride below T*d
+    (dict(kv_head_stride=1001 * 128 + 4), 4),   # stride not a multiple of 16 bytes
+])
+def test_shape_checks(quoka, kw, code):
+    n = ctypes.c_size_t(0)
+    rc = quoka.load().quoka_workspace_size(ctypes.byref(_shape(quoka, **kw)), 4, 16,
+                                           ctypes.byref(quoka.params_of()), ctypes.byref(n))
+    assert rc == code, quoka.status_string(rc)
+
+
+def _chunk_call(q, shape, N_q=4, B=16, ws=FAKE, ws_bytes=None, params=None, Q=FAKE, O=FAKE, sel=None):
+    p = params or q.params_of("max")
+    if ws_bytes is None:
+        ws_bytes = 1 << 30
+    P = ctypes.c_void_p
+    return q.load().quoka_chunk_attend(ctypes.byref(shape), P(Q), P(FAKE), P(FAKE), P(FAKE), P(FAKE), N_q, B,
+                                       ctypes.byref(p), P(O), None, P(sel) if sel else None, P(ws), ws_bytes, None)
+
+
+def test_chunk_attend_argument_errors(quoka):
+    q = quoka
+    s = _shape(q)
+    assert _chunk_call(q, s, N_q=0) == 1
+    assert _chunk_call(q, s, B=0) == 1
+    assert _chunk_call(q, s, Q=0) == 1                       # NULL query
+    assert _chunk_call(q, s, Q=FAKE + 8) == 4                # misaligned query
+    assert _chunk_call(q, s, sel=FAKE + 4) == 4              # misaligned sel_out
+    assert _chunk_call(q, s, ws=0) == 3                      # no workspace
+    assert _chunk_call(q, s, ws=FAKE + 16) == 3              # workspace not 256-byte aligned
+    need = q.workspace_size(s, 4, 16, q.params_of("max"))
+    assert _chunk_call(q, s, ws_bytes=need - 1) == 3         # workspace too small
+    assert _chunk_call(q, s, params=q.Params(5, 0, 0.0, 0)) == 1     # unknown pooling
+    assert _chunk_call(q, s, params=q.Params(0, 9, 0.0, 0)) == 1     # unknown engine
+    assert _chunk_call(q, s, params=q.Params(0, 0, 0.0, 1)) == 1     # reserved field set
+    assert _chunk_call(q, s, params=q.Params(0, 0, float("nan"), 0)) == 1
+
+
+def test_stage_argument_errors(quoka):
+    q = quoka
+    lib = q.load()
+    s = _shape(q)
+    P = ctypes.c_void_p
+    p = q.params_of("max")
+    assert lib.quoka_select_queries(ctypes.byref(s), P(FAKE), 0, ctypes.byref(p), P(FAKE), P(FAKE), 1 << 30, None) == 1
+    assert lib.quoka_select_queries(ctypes.byref(s), P(FAKE), 4, ctypes.byref(p), P(FAKE), P(FAKE), 16, None) == 3
+    assert lib.quoka_score_keys(ctypes.byref(s), P(FAKE), P(FAKE), 4, P(FAKE + 2), ctypes.byref(p), P(FAKE), P(FAKE),
+                                1 << 30, None) == 4
+    assert lib.quoka_topk(ctypes.byref(s), P(FAKE), 0, P(FAKE), P(FAKE), 1 << 30, None) == 1
+    assert lib.quoka_topk(ctypes.byref(s), P(FAKE), 8, P(FAKE), P(0), 1 << 30, None) == 3
+    assert lib.quoka_gather(ctypes.byref(s), P(FAKE), P(FAKE), P(FAKE), 1001, P(FAKE), P(FAKE), None) == 1
+    assert lib.quoka_gather(ctypes.byref(s), P(FAKE), P(FAKE), P(FAKE), -1, P(FAKE), P(FAKE), None) == 1
+    assert lib.quoka_sparse_attend(ctypes.byref(s), P(FAKE), P(0), P(0), 5, P(FAKE), P(FAKE), ctypes.byref(p), P(FAKE),
+                                   None, P(FAKE), 1 << 30, None) == 1
+    # appending needs room for T + C rows per head
+    assert lib.quoka_append_kv(ctypes.byref(s), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None) == 1
+    assert lib.quoka_get_last_device_error(None, None) == 3
