@@ -1,0 +1,257 @@
+// Tensor-core key scoring (bf16 keys, tcgen05 + TMA).
+// Method: QUOKA paper summary, "Scoring via Cosine Similarity" and
+// "Aggregation Across Queries and KV Groups"; QUOKA Explained, "Letting those
+// queries score the history", "Why take the maximum".
+//
+// One pass over the history keys, each read from HBM once.  A CTA owns a
+// contiguous range of 128-key tiles of one KV head.  Per tile:
+//   D[128 keys x N rows] = K_tile[128 x d] . OP[N x d]^T   (tcgen05, fp32 in TMEM)
+// with the keys on the TMEM lanes, so the epilogue thread of a key reduces the
+// maximum over the scoring rows from its own lane with no cross-thread step:
+//   score[t] = max_r (D[t, r] * scale[r]) / |k_t|.
+// OP is the scoring operand built by k_build_operand: for max pooling the raw
+// bf16 query rows (exact) with scale 1/|q|; for mean pooling the fp32
+// pre-aggregated rows split as hi + lo bf16, both accumulated into the same
+// TMEM columns (two MMA passes, scale 1).  |k_t| comes from the same shared
+// memory tile, in fp32.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads (operand once, then a ring
+// of key tiles), warp 1 owns TMEM and issues the MMAs, warps 2-5 are the
+// epilogue (one key per thread).  Every wait is bounded; on a timeout the
+// CTA records QUOKA_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees
+// TMEM and exits.
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace quoka {
+
+namespace {
+
+constexpr int kTileKeys = 128;
+constexpr int kScoreThreads = 192;
+
+struct ScoreSmem {
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t op_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    k_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
+               const float* __restrict__ op_scale, int T_len, int R, int N_pad, int passes, int nst, int nacc,
+               uint32_t tmem_cols, float* __restrict__ scores, WsHeader* hdr) {
+  constexpr int HALVES = D / 64;
+  constexpr uint32_t kHalfBytes = kTileKeys * 128;            // one 64-column half of a key tile
+  constexpr uint32_t kStageBytes = HALVES * kHalfBytes;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t op_bytes = (uint32_t)passes * HALVES * N_pad * 128;
+  uint8_t* op_s = smem;                                         // [passes][HALVES][N_pad][128 B]
+  uint8_t* ktiles = smem + op_bytes;                            // [nst][HALVES][128][128 B]
+  float* scale_s = reinterpret_cast<float*>(ktiles + (size_t)nst * kStageBytes);
+  ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(scale_s + N_pad);
+
+  const int g = blockIdx.y;
+  const int tiles_head = (T_len + kTileKeys - 1) / kTileKeys;
+  const int per = (tiles_head + gridDim.x - 1) / gridDim.x;
+  const int tile0 = blockIdx.x * per;
+  const int ntiles = max(0, min(tiles_head, tile0 + per) - tile0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nst; ++s) {
+      tc::mbar_init(&sm->kv_full[s], 1);
+      tc::mbar_init(&sm->kv_empty[s], 1 + 4);
+    }
+    for (int a = 0; a < nacc; ++a) {
+      tc::mbar_init(&sm->acc_full[a], 1);
+      tc::mbar_init(&sm->acc_empty[a], 4);
+    }
+    tc::mbar_init(&sm->op_full, 1);
+    tc::mbar_init(&sm->drain, 1);
+    sm->abort = 0;
+    tc::fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < N_pad; i += blockDim.x) scale_s[i] = op_scale[(size_t)g * N_pad + i];
+  if (warp == 1) {
+    tc::tmem_alloc(&sm->tmem_base, tmem_cols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int* abort = &sm->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && ntiles > 0) {
+      tc::tma_prefetch_desc(&kmap);
+      tc::tma_prefetch_desc(&omap);
+      tc::mbar_arrive_expect_tx(&sm->op_full, op_bytes);
+      const int nb = N_pad < 256 ? N_pad : 256;
+      for (int p = 0; p < passes; ++p)
+        for (int hf = 0; hf < HALVES; ++hf)
+          for (int rb = 0; rb < N_pad; rb += nb)
+            tc::tma_load_3d(op_s + ((size_t)(p * HALVES + hf) * N_pad + rb) * 128, &omap, &sm->op_full, hf * 64,
+                            p * N_pad + rb, g);
+      int issued = 0;
+      for (int it = 0; it < ntiles; ++it) {
+        const int s = it % nst;
+        if (it >= nst && !tc::mbar_wait(&sm->kv_empty[s], ((it / nst) - 1) & 1, abort, hdr, 0x101)) break;
+        tc::mbar_arrive_expect_tx(&sm->kv_full[s], kStageBytes);
+        for (int hf = 0; hf < HALVES; ++hf)
+          tc::tma_load_3d(ktiles + (size_t)s * kStageBytes + hf * kHalfBytes, &kmap, &sm->kv_full[s], hf * 64,
+                          (tile0 + it) * kTileKeys, g);
+        ++issued;
+      }
+      if (*abort) {   // let every copy already issued land before the CTA can exit
+        tc::mbar_drain(&sm->op_full, 0);
+        for (int it = issued - nst < 0 ? 0 : issued - nst; it < issued; ++it)
+          tc::mbar_drain(&sm->kv_full[it % nst], (it / nst) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      bool ok = tc::mbar_wait(&sm->op_full, 0, abort, hdr, 0x102);
+      tc::tc_fence_after();
+      const uint32_t idesc_full = tc::idesc_bf16_f32(128, N_pad < 256 ? N_pad : 256, false);
+      for (int it = 0; ok && it < ntiles; ++it) {
+        const int s = it % nst, a = it % nacc;
+        if (!tc::mbar_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x103)) break;
+        if (it >= nacc && !tc::mbar_wait(&sm->acc_empty[a], ((it / nacc) - 1) & 1, abort, hdr, 0x104)) break;
+        tc::tc_fence_after();
+        const uint32_t a_base = tc::smem_u32(ktiles + (size_t)s * kStageBytes);
+        const uint32_t b_base = tc::smem_u32(op_s);
+        for (int nc = 0; nc < N_pad; nc += 256) {
+          const int n_this = N_pad - nc < 256 ? N_pad - nc : 256;
+          const uint32_t idesc = n_this == 256 || n_this == N_pad ? idesc_full : tc::idesc_bf16_f32(128, n_this, false);
+          for (int p = 0; p < passes; ++p) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int hf = kk >> 2, kin = kk & 3;
+              const uint64_t adesc = tc::sw128_desc(a_base + hf * kHalfBytes + kin * 32, 16, 1024);
+              const uint64_t bdesc =
+                  tc::sw128_desc(b_base + ((uint32_t)(p * HALVES + hf) * N_pad + nc) * 128 + kin * 32, 16, 1024);
+              tc::mma_ss(tmem + (uint32_t)(a * N_pad + nc), adesc, bdesc, idesc, (p > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+        }
+        tc::mma_commit(&sm->kv_empty[s]);
+        tc::mma_commit(&sm->acc_full[a]);
+      }
+      tc::mma_commit(&sm->drain);        // completes once every MMA above has finished
+      tc::mbar_drain(&sm->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue: one key per thread
+    const int quad = warp & 3;                      // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;               // key within the tile
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    for (int it = 0; it < ntiles; ++it) {
+      const int s = it % nst, a = it % nacc;
+      if (!tc::mbar_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105)) break;
+      // |k| from the swizzled tile: 16-byte chunk c of row r sits at chunk c ^ (r & 7)
+      float ss = 0.f;
+      const uint8_t* tile = ktiles + (size_t)s * kStageBytes;
+#pragma unroll
+      for (int hf = 0; hf < HALVES; ++hf) {
+        const uint8_t* rp = tile + hf * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & 7)) << 4));
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h2[j]);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+          }
+        }
+      }
+      const float rk = 1.0f / fmaxf(sqrtf(ss), kNormEps);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm->kv_empty[s]);
+      if (!tc::mbar_wait(&sm->acc_full[a], (it / nacc) & 1, abort, hdr, 0x106)) break;
+      tc::tc_fence_after();
+      float best = -INFINITY;
+      for (int c0 = 0; c0 < R; c0 += 32) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + lane_addr + (uint32_t)(a * N_pad + c0), v);
+        tc::tmem_wait_ld();
+        const int nvalid = R - c0 < 32 ? R - c0 : 32;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) best = fmaxf(best, __uint_as_float(v[j]) * scale_s[c0 + j]);
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm->acc_empty[a]);
+      const int t = (tile0 + it) * kTileKeys + row;
+      if (t < T_len) scores[(size_t)g * T_len + t] = best * rk;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+}  // namespace
+
+int score_tc_pad_rows(int R) { return (R + 15) / 16 * 16; }
+
+size_t score_tc_smem(int d, int N_pad, int passes, int nst) {
+  return 1024 + (size_t)passes * (d / 64) * N_pad * 128 + (size_t)nst * (d / 64) * kTileKeys * 128 +
+         (size_t)N_pad * 4 + sizeof(ScoreSmem);
+}
+
+cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
+                            const float* op_scale, int R, int passes, float* scores, WsHeader* hdr, int num_sms,
+                            cudaStream_t st) {
+  if (T_len == 0) return cudaSuccess;
+  const int N_pad = score_tc_pad_rows(R);
+  if (N_pad > 512) return cudaErrorInvalidValue;
+  const size_t budget = 227 * 1024;
+  int nst = 6;
+  while (nst > 2 && score_tc_smem(d, N_pad, passes, nst) > budget) --nst;
+  const size_t smem = score_tc_smem(d, N_pad, passes, nst);
+  if (smem > budget) return cudaErrorInvalidValue;
+  const int nacc = 2 * N_pad <= 512 ? 2 : 1;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(nacc * N_pad)) cols <<= 1;
+  CUtensorMap kmap, omap;
+  cudaError_t e = make_tmap_bf16_3d(&kmap, K, d, T_len, H_kv, (uint64_t)d * 2, (uint64_t)head_stride * 2, 64, 128);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_bf16_3d(&omap, op_bf, d, (uint64_t)passes * N_pad, H_kv, (uint64_t)d * 2,
+                        (uint64_t)passes * N_pad * d * 2, 64, N_pad < 256 ? N_pad : 256);
+  if (e != cudaSuccess) return e;
+  const int tiles_head = (T_len + kTileKeys - 1) / kTileKeys;
+  int per_head = (num_sms + H_kv - 1) / H_kv;
+  if (per_head > tiles_head) per_head = tiles_head;
+  dim3 grid(per_head, H_kv);
+  if (d == 64) {
+    e = cudaFuncSetAttribute(k_score_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_score_tc<64><<<grid, kScoreThreads, smem, st>>>(kmap, omap, op_scale, T_len, R, N_pad, passes, nst, nacc, cols,
+                                                      scores, hdr);
+  } else {
+    e = cudaFuncSetAttribute(k_score_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_score_tc<128><<<grid, kScoreThreads, smem, st>>>(kmap, omap, op_scale, T_len, R, N_pad, passes, nst, nacc,
+                                                       cols, scores, hdr);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace quoka
