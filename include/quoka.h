@@ -196,6 +196,13 @@ int quoka_stage_engine(const quoka_shape* shape, const quoka_params* params, int
  * (diagnostics: lets a caller count the launches of a timed region). */
 uint64_t quoka_launch_count(void);
 
+/* Self-test of device-side failure detection: enqueues a kernel whose one
+ * wait can never be satisfied; the wait gives up after `cycles` SM clock
+ * cycles, records QUOKA_ERR_TIMEOUT in the workspace error word and the
+ * kernel returns normally (no fault, no hang; the context stays usable).
+ * Read the result with quoka_get_last_device_error. */
+int quoka_selftest_expire_wait(void* ws, size_t ws_bytes, long long cycles, void* stream);
+
 /* Synchronises `stream`, returns the device error recorded in ws (QUOKA_OK
  * if none) and clears it.  Returns QUOKA_ERR_CUDA if the synchronisation or
  * the read fails. */

@@ -1,0 +1,342 @@
+// Tensor-core flash attention over [history rows ; causal chunk] (bf16, tcgen05 + TMA).
+// Method: QUOKA paper summary, "Transformers and Attention" (softmax attention,
+// causal mask), "Chunked prefill" (a chunk attends to the earlier keys plus
+// itself, causally), "QUOKA Method" (the reduced key set feeds a dense
+// attention kernel); QUOKA Explained, "MEAN and MAX do different jobs" (the
+// original query heads attend).
+//
+// A CTA owns two 128-row query tiles ("slots") of two query heads of the same
+// KV group over the same chunk rows, so both share every K/V tile and the same
+// causal structure.  Keys are the history rows (selected or all) followed by
+// the chunk's own rows; the history part is unmasked except past n_hist, the
+// chunk part is causal.
+//   S_s = Q_s K_j^T        tcgen05, A = Q (smem), B = K tile (smem), fp32 in TMEM
+//   P_s = exp2(S_s - m)    softmax warpgroup of the slot, one query row per
+//                          thread, written back to TMEM as bf16 over S_s
+//   O_s += P_s V_j         tcgen05, A = P (TMEM), B = V tile (smem, MN-major)
+// The running maximum is only moved (and O rescaled in TMEM) when it grows by
+// more than 2^8, so most blocks never touch O.
+//
+// Warps (320 threads): 0 = TMA producer, 1 = TMEM owner + MMA issuer,
+// 2-5 = softmax of slot 0, 6-9 = softmax of slot 1.  Every wait is bounded;
+// on a timeout the CTA records QUOKA_ERR_TIMEOUT, drains what it has in
+// flight, frees TMEM and exits.
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace quoka {
+
+namespace {
+
+constexpr int kAttThreads = 320;
+constexpr int kKvStages = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+struct AttSmem {
+  uint64_t q_full;
+  uint64_t kv_full[kKvStages];
+  uint64_t kv_empty[kKvStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, WsHeader* hdr,
+                                          unsigned where) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, abort, hdr, where);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttThreads, 1)
+    k_attend_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap khmap,
+                const __grid_constant__ CUtensorMap vhmap, const __grid_constant__ CUtensorMap kcmap,
+                const __grid_constant__ CUtensorMap vcmap, int n_hist, int C, int G, float scale_log2,
+                __nv_bfloat16* __restrict__ O, float* __restrict__ lse, WsHeader* hdr) {
+  constexpr int HALVES = D / 64;
+  constexpr uint32_t kHalfBytes = 128 * 128;            // 128 rows x 128 bytes
+  constexpr uint32_t kTileBytes = HALVES * kHalfBytes;  // one Q, K or V tile of 128 rows
+  constexpr uint32_t kSlotCols = 256;                   // S (128 cols) then O (D cols)
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem;                                  // [2][HALVES][128][128 B]
+  uint8_t* kv_s = smem + 2 * kTileBytes;                // [kKvStages][HALVES][128][128 B]
+  AttSmem* sm = reinterpret_cast<AttSmem*>(kv_s + kKvStages * kTileBytes);
+
+  // ---- work item: longest (last query tile) first
+  const int pairs = (G + 1) / 2;
+  const int n_qt = (C + 127) / 128;
+  const int H_kv_pairs = gridDim.x / n_qt;              // H_kv * pairs
+  const int qt = n_qt - 1 - (int)blockIdx.x / H_kv_pairs;
+  const int rem = (int)blockIdx.x % H_kv_pairs;
+  const int g = rem / pairs, hp = rem % pairs;
+  const int h0 = g * G + 2 * hp;
+  const int n_slots = (2 * hp + 1 < G) ? 2 : 1;
+  const int nh = (n_hist + 127) / 128;
+  const int n_blocks = nh + qt + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&sm->q_full, 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      tc::mbar_init(&sm->kv_full[s], 1);
+      tc::mbar_init(&sm->kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&sm->s_full[s], 1);
+      tc::mbar_init(&sm->p_full[s], 4);
+      tc::mbar_init(&sm->o_done[s], 1);
+    }
+    tc::mbar_init(&sm->drain, 1);
+    sm->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&sm->tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  volatile int* abort = &sm->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&qmap);
+      tc::tma_prefetch_desc(&kcmap);
+      tc::tma_prefetch_desc(&vcmap);
+      if (nh > 0) {
+        tc::tma_prefetch_desc(&khmap);
+        tc::tma_prefetch_desc(&vhmap);
+      }
+      tc::mbar_arrive_expect_tx(&sm->q_full, n_slots * kTileBytes);
+      for (int s = 0; s < n_slots; ++s)
+        for (int hf = 0; hf < HALVES; ++hf)
+          tc::tma_load_3d(q_s + s * kTileBytes + hf * kHalfBytes, &qmap, &sm->q_full, hf * 64, qt * 128, h0 + s);
+      int k = 0;
+      bool ok = true;
+      for (int jb = 0; ok && jb < n_blocks; ++jb) {
+        const bool hist = jb < nh;
+        const int row = hist ? jb * 128 : (jb - nh) * 128;
+        for (int which = 0; which < 2; ++which, ++k) {
+          const int s = k % kKvStages;
+          if (k >= kKvStages && !tc::mbar_wait(&sm->kv_empty[s], ((k / kKvStages) - 1) & 1, abort, hdr, 0x201)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = hist ? (which == 0 ? &khmap : &vhmap) : (which == 0 ? &kcmap : &vcmap);
+          tc::mbar_arrive_expect_tx(&sm->kv_full[s], kTileBytes);
+          for (int hf = 0; hf < HALVES; ++hf)
+            tc::tma_load_3d(kv_s + s * kTileBytes + hf * kHalfBytes, map, &sm->kv_full[s], hf * 64, row, g);
+        }
+      }
+      if (*abort) {   // let issued copies land before exiting
+        tc::mbar_drain(&sm->q_full, 0);
+        for (int kk = k - kKvStages < 0 ? 0 : k - kKvStages; kk < k; ++kk)
+          tc::mbar_drain(&sm->kv_full[kk % kKvStages], (kk / kKvStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
+      bool ok = tc::mbar_wait(&sm->q_full, 0, abort, hdr, 0x202);
+      tc::tc_fence_after();
+      int k = 0;
+      for (int jb = 0; ok && jb < n_blocks; ++jb) {
+        // S_s = Q_s K^T
+        const int sk = k % kKvStages;
+        if (!(ok = tc::mbar_wait(&sm->kv_full[sk], (k / kKvStages) & 1, abort, hdr, 0x203))) break;
+        ++k;
+        tc::tc_fence_after();
+        const uint32_t kb = tc::smem_u32(kv_s + sk * kTileBytes);
+        for (int s = 0; s < n_slots; ++s) {
+          if (jb > 0 && !(ok = tc::mbar_wait(&sm->o_done[s], (jb - 1) & 1, abort, hdr, 0x204))) break;
+          tc::tc_fence_after();
+          const uint32_t qb = tc::smem_u32(q_s + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int hf = kk >> 2, kin = kk & 3;
+            tc::mma_ss(tmem + s * kSlotCols, tc::sw128_desc(qb + hf * kHalfBytes + kin * 32, 16, 1024),
+                       tc::sw128_desc(kb + hf * kHalfBytes + kin * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&sm->s_full[s]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&sm->kv_empty[sk]);
+        // O_s += P_s V
+        const int sv = k % kKvStages;
+        if (!(ok = tc::mbar_wait(&sm->kv_full[sv], (k / kKvStages) & 1, abort, hdr, 0x205))) break;
+        ++k;
+        const uint32_t vb = tc::smem_u32(kv_s + sv * kTileBytes);
+        for (int s = 0; s < n_slots; ++s) {
+          if (!(ok = tc::mbar_wait(&sm->p_full[s], jb & 1, abort, hdr, 0x206))) break;
+          tc::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)    // 16 keys per MMA; P holds 2 keys per TMEM column
+            tc::mma_ts(tmem + s * kSlotCols + 128, tmem + s * kSlotCols + kk * 8,
+                       tc::sw128_desc(vb + kk * 16 * 128, kHalfBytes, 1024), idesc_o, (jb > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(&sm->o_done[s]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&sm->kv_empty[sv]);
+      }
+      tc::mma_commit(&sm->drain);
+      tc::mbar_drain(&sm->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue, one row per thread
+    const int s = (warp - 2) >> 2;                 // slot
+    const int quad = warp & 3;                     // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;                // row within the query tile
+    const int c = qt * 128 + r;                    // chunk position of the row
+    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + s * kSlotCols;
+    const uint32_t o_addr = s_addr + 128;
+    if (s < n_slots) {
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int jb = 0; jb < n_blocks; ++jb) {
+        if (!(ok = warp_wait(&sm->s_full[s], jb & 1, abort, hdr, 0x207))) break;
+        tc::tc_fence_after();
+        uint32_t sv[128];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(s_addr + q4 * 32, sv + q4 * 32);
+        tc::tmem_wait_ld();
+        const bool hist = jb < nh;
+        // keys of this block visible to row c: [0, lim)
+        const int lim = hist ? min(128, n_hist - jb * 128) : min(128, c - (jb - nh) * 128 + 1);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const float x = i < lim ? __uint_as_float(sv[i]) * scale_log2 : -INFINITY;
+          sv[i] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m_used, mx);
+        const bool rescale = m_new > m_used + kRescaleThreshold;
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = exp2f(m_used - m_new);           // 0 on the first visible block
+          m_used = m_new;
+        }
+        float sum = 0.f;
+        uint32_t pv[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float p0 = exp2f(__uint_as_float(sv[2 * i]) - m_used);
+          const float p1 = exp2f(__uint_as_float(sv[2 * i + 1]) - m_used);
+          sum += p0 + p1;
+          pv[i] = pack_bf16x2(p0, p1);
+        }
+        l = l * alpha + sum;
+        if (jb > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O of the previous blocks must be complete before it is rescaled in place
+          if (!(ok = warp_wait(&sm->o_done[s], (jb - 1) & 1, abort, hdr, 0x208))) break;
+          tc::tc_fence_after();
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            uint32_t ov[32];
+            tc::tmem_ld32(o_addr + q4 * 32, ov);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tc::tmem_st32(o_addr + q4 * 32, ov);
+          }
+        }
+        tc::tmem_st32(s_addr, pv);
+        tc::tmem_st32(s_addr + 32, pv + 32);
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm->p_full[s]);
+      }
+      // epilogue: O / l
+      if (ok && warp_wait(&sm->o_done[s], (n_blocks - 1) & 1, abort, hdr, 0x209)) {
+        tc::tc_fence_after();
+        const int h = h0 + s;
+        const float inv = 1.f / l;
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t ov[32];
+          tc::tmem_ld32(o_addr + q4 * 32, ov);
+          tc::tmem_wait_ld();
+          if (c < C) {
+            uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)h * C + c) * D + q4 * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv, __uint_as_float(ov[8 * v + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv, __uint_as_float(ov[8 * v + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv, __uint_as_float(ov[8 * v + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv, __uint_as_float(ov[8 * v + 7]) * inv);
+              dst[v] = w;
+            }
+          }
+        }
+        if (lse != nullptr && c < C) lse[(size_t)h * C + c] = (m_used + log2f(l)) * 0.69314718055994531f;
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t attend_tc_smem(int d) {
+  return 1024 + (size_t)(2 + kKvStages) * (d / 64) * 128 * 128 + sizeof(AttSmem);
+}
+
+cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
+                             const void* Kc, const void* Vc, int H_q, int H_kv, int C, float scale, void* O,
+                             float* lse, WsHeader* hdr, cudaStream_t st) {
+  const int G = H_q / H_kv;
+  CUtensorMap qmap, khmap, vhmap, kcmap, vcmap;
+  cudaError_t e;
+  if ((e = make_tmap_bf16_3d(&qmap, Q, d, C, H_q, (uint64_t)d * 2, (uint64_t)C * d * 2, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_3d(&kcmap, Kc, d, C, H_kv, (uint64_t)d * 2, (uint64_t)C * d * 2, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_3d(&vcmap, Vc, d, C, H_kv, (uint64_t)d * 2, (uint64_t)C * d * 2, 64, 128)) != cudaSuccess) return e;
+  if (n_hist > 0) {
+    if ((e = make_tmap_bf16_3d(&khmap, Kh, d, n_hist, H_kv, (uint64_t)d * 2, (uint64_t)h_stride * 2, 64, 128)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16_3d(&vhmap, Vh, d, n_hist, H_kv, (uint64_t)d * 2, (uint64_t)h_stride * 2, 64, 128)) != cudaSuccess) return e;
+  } else {   // never read: no history blocks
+    khmap = kcmap;
+    vhmap = vcmap;
+  }
+  const int n_qt = (C + 127) / 128;
+  const int pairs = (G + 1) / 2;
+  dim3 grid(n_qt * H_kv * pairs);
+  const size_t smem = attend_tc_smem(d);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  if (d == 64) {
+    if ((e = cudaFuncSetAttribute(k_attend_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    k_attend_tc<64><<<grid, kAttThreads, smem, st>>>(qmap, khmap, vhmap, kcmap, vcmap, n_hist, C, G, scale_log2,
+                                                     (__nv_bfloat16*)O, lse, hdr);
+  } else {
+    if ((e = cudaFuncSetAttribute(k_attend_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    k_attend_tc<128><<<grid, kAttThreads, smem, st>>>(qmap, khmap, vhmap, kcmap, vcmap, n_hist, C, G, scale_log2,
+                                                      (__nv_bfloat16*)O, lse, hdr);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace quoka

@@ -3,6 +3,7 @@
 // and returns the launch status.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -18,12 +19,38 @@ inline void count_launches(unsigned n) { g_launch_count.fetch_add(n, std::memory
 cudaError_t launch_select_queries(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel,
                                   int32_t* q_idx, float* qnorm, float* qpart, float* qcos, cudaStream_t st);
 
+// op_bf may be NULL (CUDA-core scoring only needs op_f32); otherwise N_pad
+// (a multiple of 16, >= the row count) rows per pass are written.
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
-                                 int n, int mode, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
+                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
                                  cudaStream_t st);
 
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
                               const float* op_f32, int R, float* scores, cudaStream_t st);
+
+// Tensor-core scoring (bf16 keys).  op_bf / op_scale as written by
+// launch_build_operand with N_pad = score_tc_pad_rows(R); passes = 1 (max
+// pooling) or 2 (mean pooling hi/lo).
+int score_tc_pad_rows(int R);
+size_t score_tc_smem(int d, int N_pad, int passes, int nst);
+struct WsHeader;
+cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
+                            const float* op_scale, int R, int passes, float* scores, WsHeader* hdr, int num_sms,
+                            cudaStream_t st);
+
+// TMA descriptor of a bf16 3-D tensor (see tmaps.cu).
+cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1);
+
+// Tensor-core attention (bf16): history rows [H_kv, n_hist, d] with head
+// stride h_stride elements, then the causal chunk.
+size_t attend_tc_smem(int d);
+cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
+                             const void* Kc, const void* Vc, int H_q, int H_kv, int C, float scale, void* O,
+                             float* lse, WsHeader* hdr, cudaStream_t st);
+
+// Bounded-wait self-test (see selftest.cu).
+cudaError_t launch_expire_wait(WsHeader* hdr, long long limit, cudaStream_t st);
 
 cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st);
 

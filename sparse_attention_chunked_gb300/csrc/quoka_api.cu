@@ -57,12 +57,35 @@ int read_params(const quoka_params* p, const quoka_shape* s, Params* out) {
   return QUOKA_OK;
 }
 
+int n_sel_of(const quoka_shape* s, int N_q) { return N_q < s->C ? N_q : s->C; }
+
+int score_rows(const quoka_shape* s, int N_q, int gqa) {
+  const int n = n_sel_of(s, N_q), G = s->H_q / s->H_kv;
+  return gqa == QUOKA_GQA_MAX ? G * n : n;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 148;
+  return n;
+}
+
+// Whether the scoring stage can run on the tensor cores: bf16 keys, at most
+// 512 scoring rows (the TMEM width) and an operand that fits shared memory
+// next to two key stages.
+bool score_tc_fits(const quoka_shape* s, int N_q, int gqa) {
+  if (s->dtype != QUOKA_DTYPE_BF16) return false;
+  const int N_pad = score_tc_pad_rows(score_rows(s, N_q, gqa));
+  const int passes = gqa == QUOKA_GQA_MAX ? 1 : 2;
+  return N_pad <= 512 && score_tc_smem(s->d, N_pad, passes, 2) <= 227 * 1024;
+}
+
 // Which kernels run (stage 0 = scoring, 1 = attention).  Tensor-core kernels are bf16 only.
-bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage) {
-  (void)p;
-  (void)s;
-  (void)stage;
-  return false;
+bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage, int N_q = 1) {
+  if (p.engine == QUOKA_ENGINE_SIMT || s->dtype != QUOKA_DTYPE_BF16) return false;
+  if (stage == 0) return score_tc_fits(s, N_q, p.gqa);
+  return attend_tc_smem(s->d) <= 227 * 1024;
 }
 
 // Workspace regions, in order; each stage only touches the prefix it needs:
@@ -72,13 +95,6 @@ struct Layout {
   size_t op_f32, op_bf, op_scale, score_end;
   size_t q_idx, scores, sel, ksel, vsel, total;
 };
-
-int n_sel_of(const quoka_shape* s, int N_q) { return N_q < s->C ? N_q : s->C; }
-
-int score_rows(const quoka_shape* s, int N_q, int gqa) {
-  const int n = n_sel_of(s, N_q), G = s->H_q / s->H_kv;
-  return gqa == QUOKA_GQA_MAX ? G * n : n;
-}
 
 Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa) {
   Layout L;
@@ -90,9 +106,10 @@ Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa) {
   L.qcos = o;   o = align_up(o + H_q * C * 4);
   L.select_end = o;
   const size_t R = (size_t)score_rows(s, N_q > 0 ? N_q : 1, gqa);
+  const size_t N_pad = (size_t)score_tc_pad_rows((int)R);
   L.op_f32 = o;   o = align_up(o + H_kv * R * d * 4);
-  L.op_bf = o;    o = align_up(o + H_kv * 2 * R * d * 2);
-  L.op_scale = o; o = align_up(o + H_kv * 2 * R * 4);
+  L.op_bf = o;    o = align_up(o + H_kv * 2 * N_pad * d * 2);
+  L.op_scale = o; o = align_up(o + H_kv * N_pad * 4);
   L.score_end = o;
   const size_t n = (size_t)n_sel_of(s, N_q > 0 ? N_q : 1);
   const size_t B_e = (size_t)(B < s->T ? B : s->T);
@@ -135,17 +152,27 @@ int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, 
   const int G = s->H_q / s->H_kv;
   const int mode = p.gqa == QUOKA_GQA_MAX ? 1 : 0;
   const int R = score_rows(s, n, p.gqa);
-  const bool tc = use_tensor_cores(p, s, 0);
-  QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, mode, at<float>(ws, L.op_f32),
+  const int N_pad = score_tc_pad_rows(R);
+  const bool tc = use_tensor_cores(p, s, 0, n);
+  if (p.engine == QUOKA_ENGINE_TENSOR && !tc) return QUOKA_ERR_UNSUPPORTED;
+  QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, mode, N_pad, at<float>(ws, L.op_f32),
                                   tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr, at<float>(ws, L.op_scale), st));
+  if (tc)
+    return cuda_status(launch_score_tc(s->d, K_hist, head_stride(s), s->H_kv, s->T, at<__nv_bfloat16>(ws, L.op_bf),
+                                       at<float>(ws, L.op_scale), R, mode == 1 ? 1 : 2, scores, at<WsHeader>(ws, 0),
+                                       num_sms(), st));
   return cuda_status(launch_score_simt(s->dtype, s->d, K_hist, head_stride(s), s->H_kv, s->T,
                                        at<float>(ws, L.op_f32), R, scores, st));
 }
 
 int run_attend(const quoka_shape* s, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
                const void* Kc, const void* Vc, const Params& p, void* O, float* lse, void* ws, cudaStream_t st) {
-  (void)ws;
   const int G = s->H_q / s->H_kv;
+  const bool tc = use_tensor_cores(p, s, 1);
+  if (p.engine == QUOKA_ENGINE_TENSOR && !tc) return QUOKA_ERR_UNSUPPORTED;
+  if (tc)
+    return cuda_status(launch_attend_tc(s->d, Q, Kh, Vh, h_stride, n_hist, Kc, Vc, s->H_q, s->H_kv, s->C, p.scale, O,
+                                        lse, at<WsHeader>(ws, 0), st));
   return cuda_status(launch_attend_simt(s->dtype, s->d, Q, Kh, Vh, h_stride, n_hist, Kc, Vc, s->H_q, s->C, G,
                                         p.scale, O, lse, st));
 }
@@ -165,7 +192,7 @@ int quoka_stage_engine(const quoka_shape* shape, const quoka_params* params, int
   const int rp = read_params(params, shape, &p);
   if (rp != QUOKA_OK) return -rp;
   if (stage != 0 && stage != 1) return -QUOKA_ERR_INVALID_ARG;
-  return use_tensor_cores(p, shape, stage) ? QUOKA_ENGINE_TENSOR : QUOKA_ENGINE_SIMT;
+  return use_tensor_cores(p, shape, stage, 1) ? QUOKA_ENGINE_TENSOR : QUOKA_ENGINE_SIMT;
 }
 
 uint64_t quoka_launch_count(void) { return quoka::g_launch_count.load(std::memory_order_relaxed); }
@@ -316,6 +343,12 @@ int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const 
     return QUOKA_ERR_ALIGNMENT;
   return cuda_status(launch_append(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), shape->T,
                                    K_chunk, V_chunk, shape->H_kv, shape->C, (cudaStream_t)stream));
+}
+
+int quoka_selftest_expire_wait(void* ws, size_t ws_bytes, long long cycles, void* stream) {
+  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
+  if (cycles < 1) return QUOKA_ERR_INVALID_ARG;
+  return cuda_status(launch_expire_wait(at<WsHeader>(ws, 0), cycles, (cudaStream_t)stream));
 }
 
 int quoka_get_last_device_error(void* ws, void* stream) {

@@ -8,19 +8,33 @@
 
 namespace quoka {
 
-// One warp per scoring row.  Row r of KV group g:
+// One warp per scoring row; grid.x covers N_pad >= R rows (padding rows are
+// zero in the tensor-core copy and never read by the epilogue).  Row r of
+// KV group g:
 //   MAX : r = k * n + i  -> query head h = g*G + k, position q_idx[h, i];
 //         fp32 row q / |q|; tensor-core copy: the raw row and scale 1/|q|.
 //   MEAN: r = i          -> position q_idx[g, i];
 //         fp32 row (1/G) sum_k q_k / |q_k| over the group's heads (not
-//         re-normalised); tensor-core copy: hi = bf16(row), lo = bf16(row - hi)
-//         as rows r and R + r, scale 1.
+//         re-normalised); tensor-core copy: hi = bf16(row) in pass 0 and
+//         lo = bf16(row - hi) in pass 1, scale 1.
+// Layouts: op_f32 [H_kv, R, D]; op_bf [H_kv, passes, N_pad, D]; op_scale [H_kv, N_pad].
 template <typename T, int D>
 __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, const int32_t* __restrict__ q_idx,
-                                                      int C, int G, int n, int mode, float* __restrict__ op_f32,
+                                                      int C, int G, int n, int mode, int R, float* __restrict__ op_f32,
                                                       __nv_bfloat16* __restrict__ op_bf, float* __restrict__ op_scale) {
   constexpr int E = D / 32;
-  const int g = blockIdx.y, r = blockIdx.x, R = gridDim.x, lane = threadIdx.x;
+  const int g = blockIdx.y, r = blockIdx.x, N_pad = gridDim.x, lane = threadIdx.x;
+  const int passes = mode == 1 ? 1 : 2;
+  if (r >= R) {   // padding row of the tensor-core operand
+    if (op_bf != nullptr) {
+      for (int p = 0; p < passes; ++p)
+#pragma unroll
+        for (int j = 0; j < E; ++j)
+          op_bf[(((size_t)g * passes + p) * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(0.f);
+      if (lane == 0) op_scale[(size_t)g * N_pad + r] = 0.f;
+    }
+    return;
+  }
   float acc[E];
   if (mode == 1) {  // MAX
     const int k = r / n, i = r % n, h = g * G + k;
@@ -38,8 +52,8 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
     for (int j = 0; j < E; ++j) acc[j] = x[j] * inv;
     if (op_bf != nullptr) {
 #pragma unroll
-      for (int j = 0; j < E; ++j) op_bf[((size_t)g * R + r) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
-      if (lane == 0) op_scale[(size_t)g * R + r] = inv;
+      for (int j = 0; j < E; ++j) op_bf[((size_t)g * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
+      if (lane == 0) op_scale[(size_t)g * N_pad + r] = inv;
     }
   } else {  // MEAN (pre-aggregation)
     const int c = q_idx[(size_t)g * n + r];
@@ -66,13 +80,10 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
       for (int j = 0; j < E; ++j) {
         const __nv_bfloat16 hi = __float2bfloat16_rn(acc[j]);
         const __nv_bfloat16 lo = __float2bfloat16_rn(acc[j] - __bfloat162float(hi));
-        op_bf[((size_t)g * 2 * R + r) * D + lane + 32 * j] = hi;
-        op_bf[((size_t)g * 2 * R + R + r) * D + lane + 32 * j] = lo;
+        op_bf[(((size_t)g * 2 + 0) * N_pad + r) * D + lane + 32 * j] = hi;
+        op_bf[(((size_t)g * 2 + 1) * N_pad + r) * D + lane + 32 * j] = lo;
       }
-      if (lane == 0) {
-        op_scale[(size_t)g * 2 * R + r] = 1.0f;
-        op_scale[(size_t)g * 2 * R + R + r] = 1.0f;
-      }
+      if (lane == 0) op_scale[(size_t)g * N_pad + r] = 1.0f;
     }
   }
 #pragma unroll
@@ -120,20 +131,20 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
 }
 
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
-                                 int n, int mode, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
+                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
                                  cudaStream_t st) {
   const int R = mode == 1 ? G * n : n;
-  dim3 grid(R, H_kv);
+  dim3 grid(op_bf != nullptr ? N_pad : R, H_kv);
   if (dtype == 0) {
     if (d == 64)
-      k_build_operand<__nv_bfloat16, 64><<<grid, 32, 0, st>>>((const __nv_bfloat16*)Q, q_idx, C, G, n, mode, op_f32, op_bf, op_scale);
+      k_build_operand<__nv_bfloat16, 64><<<grid, 32, 0, st>>>((const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
     else
-      k_build_operand<__nv_bfloat16, 128><<<grid, 32, 0, st>>>((const __nv_bfloat16*)Q, q_idx, C, G, n, mode, op_f32, op_bf, op_scale);
+      k_build_operand<__nv_bfloat16, 128><<<grid, 32, 0, st>>>((const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
   } else {
     if (d == 64)
-      k_build_operand<float, 64><<<grid, 32, 0, st>>>((const float*)Q, q_idx, C, G, n, mode, op_f32, op_bf, op_scale);
+      k_build_operand<float, 64><<<grid, 32, 0, st>>>((const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
     else
-      k_build_operand<float, 128><<<grid, 32, 0, st>>>((const float*)Q, q_idx, C, G, n, mode, op_f32, op_bf, op_scale);
+      k_build_operand<float, 128><<<grid, 32, 0, st>>>((const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
   }
   count_launches(1);
   return cudaGetLastError();

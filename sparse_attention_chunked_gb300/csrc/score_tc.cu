@@ -30,6 +30,17 @@ namespace {
 constexpr int kTileKeys = 128;
 constexpr int kScoreThreads = 192;
 
+// Rows of one operand TMA box: it must divide N_pad (<= 512) and be <= 256.
+__host__ __device__ inline int op_box_rows(int N_pad) { return N_pad <= 256 ? N_pad : N_pad / 2; }
+
+// Bounded wait done by lane 0 only, result broadcast, so the warp stays converged.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, WsHeader* hdr,
+                                          unsigned where) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(bar, parity, abort, hdr, where);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 struct ScoreSmem {
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
@@ -95,7 +106,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc::tma_prefetch_desc(&kmap);
       tc::tma_prefetch_desc(&omap);
       tc::mbar_arrive_expect_tx(&sm->op_full, op_bytes);
-      const int nb = N_pad < 256 ? N_pad : 256;
+      const int nb = op_box_rows(N_pad);
       for (int p = 0; p < passes; ++p)
         for (int hf = 0; hf < HALVES; ++hf)
           for (int rb = 0; rb < N_pad; rb += nb)
@@ -157,7 +168,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     for (int it = 0; it < ntiles; ++it) {
       const int s = it % nst, a = it % nacc;
-      if (!tc::mbar_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105)) break;
+      if (!warp_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105)) break;
       // |k| from the swizzled tile: 16-byte chunk c of row r sits at chunk c ^ (r & 7)
       float ss = 0.f;
       const uint8_t* tile = ktiles + (size_t)s * kStageBytes;
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       const float rk = 1.0f / fmaxf(sqrtf(ss), kNormEps);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->kv_empty[s]);
-      if (!tc::mbar_wait(&sm->acc_full[a], (it / nacc) & 1, abort, hdr, 0x106)) break;
+      if (!warp_wait(&sm->acc_full[a], (it / nacc) & 1, abort, hdr, 0x106)) break;
       tc::tc_fence_after();
       float best = -INFINITY;
       for (int c0 = 0; c0 < R; c0 += 32) {
@@ -208,7 +219,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
 }  // namespace
 
-int score_tc_pad_rows(int R) { return (R + 15) / 16 * 16; }
+// Scoring rows padded to a multiple of 32: MMA N must be a multiple of 16 and
+// the epilogue reads TMEM 32 columns at a time without crossing N_pad.
+int score_tc_pad_rows(int R) { return (R + 31) / 32 * 32; }
 
 size_t score_tc_smem(int d, int N_pad, int passes, int nst) {
   return 1024 + (size_t)passes * (d / 64) * N_pad * 128 + (size_t)nst * (d / 64) * kTileKeys * 128 +
@@ -233,7 +246,7 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
   cudaError_t e = make_tmap_bf16_3d(&kmap, K, d, T_len, H_kv, (uint64_t)d * 2, (uint64_t)head_stride * 2, 64, 128);
   if (e != cudaSuccess) return e;
   e = make_tmap_bf16_3d(&omap, op_bf, d, (uint64_t)passes * N_pad, H_kv, (uint64_t)d * 2,
-                        (uint64_t)passes * N_pad * d * 2, 64, N_pad < 256 ? N_pad : 256);
+                        (uint64_t)passes * N_pad * d * 2, 64, op_box_rows(N_pad));
   if (e != cudaSuccess) return e;
   const int tiles_head = (T_len + kTileKeys - 1) / kTileKeys;
   int per_head = (num_sms + H_kv - 1) / H_kv;

@@ -62,6 +62,7 @@ _SIG = {
     "quoka_append_kv": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
     "quoka_get_last_device_error": (ctypes.c_int, [_P, _P]),
     "quoka_launch_count": (ctypes.c_uint64, []),
+    "quoka_selftest_expire_wait": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_longlong, _P]),
     "quoka_stage_engine": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_int]),
 }
 
@@ -195,6 +196,11 @@ def quoka_stage_engine(shape, params, stage: int) -> int:
 def uses_tensor_cores(stage: str, shape, params) -> bool:
     """True if the library runs `stage` ("score" or "attend") on tcgen05 tensor cores for this problem."""
     return quoka_stage_engine(shape, params, {"score": 0, "attend": 1}[stage]) == ENGINE["tensor"]
+
+
+def quoka_selftest_expire_wait(ws, cycles: int, stream=None):
+    _check("quoka_selftest_expire_wait", load().quoka_selftest_expire_wait(_ptr(ws), ws.numel(), cycles,
+                                                                           _stream(stream)))
 
 
 def quoka_launch_count() -> int:
