@@ -52,6 +52,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// 2^x on the SFU (MUFU.EX2): the hardware's approximate exponential, flushing
+// subnormals; ex2(-inf) = 0.  P is rounded to bf16 afterwards.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -207,42 +215,49 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const uint32_t s_addr = tmem + lane_addr + s * kSlotCols;
     const uint32_t o_addr = s_addr + 128;
     if (s < n_slots) {
-      float m_used = -INFINITY, l = 0.f;
+      float m_used = -INFINITY, l = 0.f;            // running max of the raw logits, softmax denominator
       bool ok = true;
       for (int jb = 0; jb < n_blocks; ++jb) {
         if (!(ok = warp_wait(&sm->s_full[s], jb & 1, abort, hdr, 0x207))) break;
         tc::tc_fence_after();
         uint32_t sv[128];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(s_addr + q4 * 32, sv + q4 * 32);
-        tc::tmem_wait_ld();
+        tc::tmem_ld128(s_addr, sv);
         const bool hist = jb < nh;
-        // keys of this block visible to row c: [0, lim)
-        const int lim = hist ? min(128, n_hist - jb * 128) : min(128, c - (jb - nh) * 128 + 1);
+        // only the last history block (if partial) and the diagonal chunk block have masked keys
+        const bool need_mask = hist ? (jb == nh - 1 && (n_hist & 127) != 0) : (jb - nh == qt);
         float mx = -INFINITY;
+        if (need_mask) {
+          // keys of this block visible to row c: [0, lim)
+          const int lim = hist ? n_hist - jb * 128 : c - (jb - nh) * 128 + 1;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          const float x = i < lim ? __uint_as_float(sv[i]) * scale_log2 : -INFINITY;
-          sv[i] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          for (int i = 0; i < 128; ++i) {
+            const float x = i < lim ? __uint_as_float(sv[i]) : -INFINITY;
+            sv[i] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
         }
         const float m_new = fmaxf(m_used, mx);
-        const bool rescale = m_new > m_used + kRescaleThreshold;
+        const bool rescale = (m_new - m_used) * scale_log2 > kRescaleThreshold;   // true on the first block
         float alpha = 1.f;
         if (rescale) {
-          alpha = exp2f(m_used - m_new);           // 0 on the first visible block
+          alpha = ex2_approx((m_used - m_new) * scale_log2);   // 0 on the first block
           m_used = m_new;
         }
-        float sum = 0.f;
+        const float neg_m = -m_used * scale_log2;
+        float sum0 = 0.f, sum1 = 0.f;
         uint32_t pv[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          const float p0 = exp2f(__uint_as_float(sv[2 * i]) - m_used);
-          const float p1 = exp2f(__uint_as_float(sv[2 * i + 1]) - m_used);
-          sum += p0 + p1;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), scale_log2, neg_m));
+          sum0 += p0;
+          sum1 += p1;
           pv[i] = pack_bf16x2(p0, p1);
         }
-        l = l * alpha + sum;
+        l = l * alpha + (sum0 + sum1);
         if (jb > 0 && __any_sync(0xffffffffu, rescale)) {
           // O of the previous blocks must be complete before it is rescaled in place
           if (!(ok = warp_wait(&sm->o_done[s], (jb - 1) & 1, abort, hdr, 0x208))) break;
@@ -251,14 +266,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           for (int q4 = 0; q4 < D / 32; ++q4) {
             uint32_t ov[32];
             tc::tmem_ld32(o_addr + q4 * 32, ov);
-            tc::tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
             tc::tmem_st32(o_addr + q4 * 32, ov);
           }
         }
-        tc::tmem_st32(s_addr, pv);
-        tc::tmem_st32(s_addr + 32, pv + 32);
+        tc::tmem_st64(s_addr, pv);
         tc::tmem_wait_st();
         tc::tc_fence_before();
         __syncwarp();
@@ -287,7 +300,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             }
           }
         }
-        if (lse != nullptr && c < C) lse[(size_t)h * C + c] = (m_used + log2f(l)) * 0.69314718055994531f;
+        if (lse != nullptr && c < C) lse[(size_t)h * C + c] = m_used * scale_log2 * 0.69314718055994531f + logf(l);
       }
     }
   }

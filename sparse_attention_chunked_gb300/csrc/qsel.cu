@@ -8,10 +8,12 @@
 //   k_qcos   : per (head, 64-row block) M_q from the partials (fixed order,
 //              deterministic), then cos(q, M_q) for the block's rows
 //   k_qselect: per selection row (query head, or KV group with the cosine
-//              averaged over the group's heads) a shared-memory bitonic sort of
-//              (key(cos), position) pairs; the first N_q are re-sorted by position.
+//              averaged over the group's heads) an exact block radix select of
+//              the N_q smallest cosines (keys = inverted order-mapped cosines,
+//              so ties go to the lower position), written in position order.
 #include "common.cuh"
 #include "launch.h"
+#include "radix_select.cuh"
 
 namespace quoka {
 
@@ -86,51 +88,24 @@ __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, co
   }
 }
 
-// Ascending bitonic sort of n (a power of two) 64-bit keys in shared memory.
-__device__ void bitonic_sort_u64(uint64_t* a, int n) {
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const bool up = (i & k) == 0;
-          const uint64_t x = a[i], y = a[ixj];
-          if ((x > y) == up) {
-            a[i] = y;
-            a[ixj] = x;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
 __global__ void __launch_bounds__(1024) k_qselect(const float* __restrict__ qcos, int C, int G_avg, int n_sel,
-                                                  int npow2, int32_t* __restrict__ q_idx) {
-  extern __shared__ uint64_t keys[];
+                                                  int32_t* __restrict__ q_idx) {
+  extern __shared__ uint32_t keys_s[];
+  __shared__ RadixSelectShared rs;
   const int row = blockIdx.x;
-  for (int c = threadIdx.x; c < npow2; c += blockDim.x) {
-    uint64_t key = ~0ull;
-    if (c < C) {
-      float u;
-      if (G_avg == 1) {
-        u = qcos[(size_t)row * C + c];
-      } else {
-        float s = 0.f;
-        for (int k = 0; k < G_avg; ++k) s += qcos[((size_t)row * G_avg + k) * C + c];
-        u = s / (float)G_avg;
-      }
-      key = ((uint64_t)order_key(u) << 32) | (uint32_t)c;   // smallest cosine first, then lowest position
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    float u;
+    if (G_avg == 1) {
+      u = qcos[(size_t)row * C + c];
+    } else {
+      float s = 0.f;
+      for (int k = 0; k < G_avg; ++k) s += qcos[((size_t)row * G_avg + k) * C + c];
+      u = s / (float)G_avg;
     }
-    keys[c] = key;
+    keys_s[c] = ~order_key(u);   // the largest key is the smallest cosine
   }
   __syncthreads();
-  bitonic_sort_u64(keys, npow2);
-  for (int i = threadIdx.x; i < npow2; i += blockDim.x) keys[i] = (i < n_sel) ? (keys[i] & 0xffffffffull) : ~0ull;
-  __syncthreads();
-  bitonic_sort_u64(keys, npow2);
-  for (int i = threadIdx.x; i < n_sel; i += blockDim.x) q_idx[(size_t)row * n_sel + i] = (int32_t)keys[i];
+  block_radix_topk([&](int i) { return keys_s[i]; }, C, n_sel, q_idx + (size_t)row * n_sel, rs);
 }
 
 template <typename T, int D>
@@ -140,15 +115,9 @@ static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel
   dim3 grid(nblk, H_q);
   k_qstats<T, D><<<grid, 256, 0, st>>>((const T*)Q, C, qnorm, qpart);
   k_qcos<T, D><<<grid, 256, 0, st>>>((const T*)Q, C, qpart, qnorm, qcos);
-  int npow2 = 32;
-  while (npow2 < C) npow2 <<= 1;
-  const size_t smem = (size_t)npow2 * sizeof(uint64_t);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_qselect, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  const size_t smem = (size_t)C * sizeof(uint32_t);   // C <= 8192: at most 32 KB
   const int rows = H_q / G_avg;
-  k_qselect<<<rows, 1024, smem, st>>>(qcos, C, G_avg, n_sel, npow2, q_idx);
+  k_qselect<<<rows, 1024, smem, st>>>(qcos, C, G_avg, n_sel, q_idx);
   count_launches(3);
   return cudaGetLastError();
 }

@@ -15,9 +15,11 @@
 // TMEM columns (two MMA passes, scale 1).  |k_t| comes from the same shared
 // memory tile, in fp32.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads (operand once, then a ring
-// of key tiles), warp 1 owns TMEM and issues the MMAs, warps 2-5 are the
-// epilogue (one key per thread).  Every wait is bounded; on a timeout the
+// Warp roles (320 threads): warp 0 issues TMA loads (operand once, then a ring
+// of key tiles), warp 1 owns TMEM and issues the MMAs, warps 2-9 are the
+// epilogue: two warps per TMEM lane quadrant, each reducing half of the
+// scoring columns and half of the key's squared norm; the halves meet in
+// shared memory behind a named barrier of the 256 epilogue threads.  Every wait is bounded; on a timeout the
 // CTA records QUOKA_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees
 // TMEM and exits.
 #include "launch.h"
@@ -28,7 +30,8 @@ namespace quoka {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kScoreThreads = 192;
+constexpr int kScoreThreads = 320;
+constexpr int kEpiWarps = 8;
 
 // Rows of one operand TMA box: it must divide N_pad (<= 512) and be <= 256.
 __host__ __device__ inline int op_box_rows(int N_pad) { return N_pad <= 256 ? N_pad : N_pad / 2; }
@@ -42,6 +45,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 struct ScoreSmem {
+  float red_max[2][2][128];   // [tile parity][column half][key]
+  float red_ss[2][2][128];
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t acc_full[2];
@@ -78,11 +83,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
       tc::mbar_init(&sm->kv_full[s], 1);
-      tc::mbar_init(&sm->kv_empty[s], 1 + 4);
+      tc::mbar_init(&sm->kv_empty[s], 1 + kEpiWarps);
     }
     for (int a = 0; a < nacc; ++a) {
       tc::mbar_init(&sm->acc_full[a], 1);
-      tc::mbar_init(&sm->acc_empty[a], 4);
+      tc::mbar_init(&sm->acc_empty[a], kEpiWarps);
     }
     tc::mbar_init(&sm->op_full, 1);
     tc::mbar_init(&sm->drain, 1);
@@ -162,51 +167,67 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc::mbar_drain(&sm->drain, 0);
     }
   } else {
-    // ------------------------------------------------------------ epilogue: one key per thread
+    // ------------------------------------------------------------ epilogue: one key per thread pair
     const int quad = warp & 3;                      // TMEM lane quadrant this warp may access
+    const int part = (warp - 2) >> 2;               // which half of the columns / of d
     const int row = quad * 32 + lane;               // key within the tile
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+    const int half_cols = ((N_pad >> 1) + 31) & ~31;
+    const int c_begin = part * half_cols, c_end = min(R, part == 0 ? half_cols : N_pad);
+    bool alive = true;                              // false once a wait gave up (warp-uniform)
     for (int it = 0; it < ntiles; ++it) {
-      const int s = it % nst, a = it % nacc;
-      if (!warp_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105)) break;
-      // |k| from the swizzled tile: 16-byte chunk c of row r sits at chunk c ^ (r & 7)
+      const int s = it % nst, a = it % nacc, buf = it & 1;
+      if (alive) alive = warp_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105);
       float ss = 0.f;
-      const uint8_t* tile = ktiles + (size_t)s * kStageBytes;
+      if (alive) {
+        // |k|^2 over this part's 64-column halves of d; 16-byte chunk c of row r sits at c ^ (r & 7)
+        const uint8_t* tile = ktiles + (size_t)s * kStageBytes;
 #pragma unroll
-      for (int hf = 0; hf < HALVES; ++hf) {
-        const uint8_t* rp = tile + hf * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
+        for (int hf = 0; hf < HALVES; ++hf) {
+          if ((hf & 1) != part) continue;
+          const uint8_t* rp = tile + hf * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & 7)) << 4));
-          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & 7)) << 4));
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __bfloat1622float2(h2[j]);
-            ss = fmaf(f.x, f.x, ss);
-            ss = fmaf(f.y, f.y, ss);
+            for (int j = 0; j < 4; ++j) {
+              const float2 f = __bfloat1622float2(h2[j]);
+              ss = fmaf(f.x, f.x, ss);
+              ss = fmaf(f.y, f.y, ss);
+            }
           }
         }
       }
-      const float rk = 1.0f / fmaxf(sqrtf(ss), kNormEps);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->kv_empty[s]);
-      if (!warp_wait(&sm->acc_full[a], (it / nacc) & 1, abort, hdr, 0x106)) break;
-      tc::tc_fence_after();
+      if (alive) alive = warp_wait(&sm->acc_full[a], (it / nacc) & 1, abort, hdr, 0x106);
       float best = -INFINITY;
-      for (int c0 = 0; c0 < R; c0 += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + lane_addr + (uint32_t)(a * N_pad + c0), v);
-        tc::tmem_wait_ld();
-        const int nvalid = R - c0 < 32 ? R - c0 : 32;
+      if (alive) {
+        tc::tc_fence_after();
+        for (int c0 = c_begin; c0 < c_end; c0 += 64) {
+          uint32_t v[64];
+          const bool two = c0 + 32 < c_end;         // both 32-column groups hold valid rows
+          if (two) tc::tmem_ld64(tmem + lane_addr + (uint32_t)(a * N_pad + c0), v);
+          else tc::tmem_ld32(tmem + lane_addr + (uint32_t)(a * N_pad + c0), v);
+          const int nvalid = c_end - c0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nvalid) best = fmaxf(best, __uint_as_float(v[j]) * scale_s[c0 + j]);
+          for (int j = 0; j < 64; ++j)
+            if (j < nvalid && (j < 32 || two)) best = fmaxf(best, __uint_as_float(v[j]) * scale_s[c0 + j]);
+        }
+        tc::tc_fence_before();
       }
-      tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->acc_empty[a]);
-      const int t = (tile0 + it) * kTileKeys + row;
-      if (t < T_len) scores[(size_t)g * T_len + t] = best * rk;
+      sm->red_max[buf][part][row] = best;
+      sm->red_ss[buf][part][row] = ss;
+      asm volatile("bar.sync 1, 256;" ::: "memory");   // the 8 epilogue warps
+      if (part == 0 && alive) {
+        const float mx = fmaxf(sm->red_max[buf][0][row], sm->red_max[buf][1][row]);
+        const float rk = 1.0f / fmaxf(sqrtf(sm->red_ss[buf][0][row] + sm->red_ss[buf][1][row]), kNormEps);
+        const int t = (tile0 + it) * kTileKeys + row;
+        if (t < T_len) scores[(size_t)g * T_len + t] = mx * rk;
+      }
     }
   }
   tc::tc_fence_before();

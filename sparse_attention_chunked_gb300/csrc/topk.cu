@@ -1,80 +1,34 @@
 // Top-B history keys per KV head (QUOKA Explained, "From scores to a smaller
 // KV set"; QUOKA paper summary, "Chunked Prefill with QUOKA").
 //
-// One CTA per KV head.  Scores are mapped to order-preserving 32-bit keys and
-// an MSB-first radix select (4 digits of 8 bits, shared-memory histograms)
-// finds the exact B-th largest key theta and how many keys equal to theta
-// still have to be taken.  A final pass in position order writes every key
-// above theta plus the lowest-position keys equal to theta, so the output is
-// ascending and ties go to the lower position.
+// One CTA (1024 threads) per KV head runs an exact block radix select
+// (radix_select.cuh) on the order-preserving 32-bit keys of the scores; when
+// the head's keys fit in shared memory (T <= 48K) they are loaded once and all
+// passes run from shared memory, otherwise every pass re-reads the scores
+// from global memory (they are L2-resident right after the scoring kernel).
+// The output is ascending and ties go to the lower position.
 #include "common.cuh"
 #include "launch.h"
+#include "radix_select.cuh"
 
 namespace quoka {
 
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkSmemKeys = 48 * 1024;   // keys cached in shared memory (192 KB)
 
 __global__ void __launch_bounds__(kTopkThreads) k_topk_radix(const float* __restrict__ scores, int T_len, int B_e,
-                                                             int32_t* __restrict__ sel) {
+                                                             int32_t* __restrict__ sel, int cache) {
+  extern __shared__ uint32_t keys_s[];
+  __shared__ RadixSelectShared rs;
   const int g = blockIdx.x;
   const float* s = scores + (size_t)g * T_len;
   int32_t* out = sel + (size_t)g * B_e;
-  __shared__ unsigned int hist[256];
-  __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_need;
-  __shared__ int scan_scratch[32];
-  if (threadIdx.x == 0) {
-    s_prefix = 0;
-    s_mask = 0;
-    s_need = B_e;
-  }
-  __syncthreads();
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (threadIdx.x < 256) hist[threadIdx.x] = 0;
+  if (cache) {
+    for (int i = threadIdx.x; i < T_len; i += blockDim.x) keys_s[i] = order_key(s[i]);
     __syncthreads();
-    const uint32_t prefix = s_prefix, mask = s_mask;
-    for (int t = threadIdx.x; t < T_len; t += blockDim.x) {
-      const uint32_t k = order_key(s[t]);
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int need = s_need, cum = 0, b = 255;
-      for (; b > 0; --b) {
-        if (cum + (int)hist[b] >= need) break;
-        cum += (int)hist[b];
-      }
-      s_need = need - cum;
-      s_prefix = prefix | ((uint32_t)b << shift);
-      s_mask = mask | (255u << shift);
-    }
-    __syncthreads();
-  }
-  const uint32_t theta = s_prefix;
-  const int r = s_need;   // keys equal to theta still to take, lowest positions first
-  // Position-ordered compaction over contiguous per-thread ranges.
-  const int per = (T_len + blockDim.x - 1) / blockDim.x;
-  const int t0 = min(T_len, (int)threadIdx.x * per), t1 = min(T_len, t0 + per);
-  int n_gt = 0, n_eq = 0;
-  for (int t = t0; t < t1; ++t) {
-    const uint32_t k = order_key(s[t]);
-    n_gt += k > theta;
-    n_eq += k == theta;
-  }
-  int total;
-  const int eq_base = block_exclusive_scan(n_eq, scan_scratch, &total);
-  const int take_eq = max(0, min(n_eq, r - eq_base));
-  const int out_base = block_exclusive_scan(n_gt + take_eq, scan_scratch, &total);
-  int o = out_base, eq_seen = 0;
-  for (int t = t0; t < t1 && o < B_e; ++t) {     // o < B_e always holds; the test only guards the store
-    const uint32_t k = order_key(s[t]);
-    if (k > theta) {
-      out[o++] = t;
-    } else if (k == theta) {
-      if (eq_seen < take_eq) out[o++] = t;
-      ++eq_seen;
-    }
+    block_radix_topk([&](int i) { return keys_s[i]; }, T_len, B_e, out, rs);
+  } else {
+    block_radix_topk([&](int i) { return order_key(s[i]); }, T_len, B_e, out, rs);
   }
 }
 
@@ -94,7 +48,13 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
     count_launches(1);
     return cudaGetLastError();
   }
-  k_topk_radix<<<H_kv, kTopkThreads, 0, st>>>(scores, T_len, B_e, sel);
+  const int cache = T_len <= kTopkSmemKeys ? 1 : 0;
+  const size_t smem = cache ? (size_t)T_len * 4 : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_topk_radix, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k_topk_radix<<<H_kv, kTopkThreads, smem, st>>>(scores, T_len, B_e, sel, cache);
   count_launches(1);
   return cudaGetLastError();
 }
