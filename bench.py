@@ -181,45 +181,67 @@ def run_quoka(args, rank, world, local_rank):
     Vs = torch.empty_like(Ks)
     O = torch.empty_like(Q)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)
     names = ["select", "score", "topk", "gather", "attend"]
-
-    def step(evs):
-        evs[0].record(stream)
-        q.quoka_select_queries(shape, Q, cfg.N_q, params, q_idx, ws, stream)
-        evs[1].record(stream)
-        q.quoka_score_keys(shape, Q, q_idx, cfg.N_q, Kh, params, scores, ws, stream)
-        evs[2].record(stream)
-        q.quoka_topk(shape, scores, cfg.B, sel, ws, stream)
-        evs[3].record(stream)
-        q.quoka_gather(shape, Kh, Vh, sel, B_e, Ks, Vs, stream)
-        evs[4].record(stream)
-        q.quoka_sparse_attend(shape, Q, Ks, Vs, B_e, Kc, Vc, params, O, None, ws, stream)
-        evs[5].record(stream)
+    stage_fns = [
+        lambda: q.quoka_select_queries(shape, Q, cfg.N_q, params, q_idx, ws, stream),
+        lambda: q.quoka_score_keys(shape, Q, q_idx, cfg.N_q, Kh, params, scores, ws, stream),
+        lambda: q.quoka_topk(shape, scores, cfg.B, sel, ws, stream),
+        lambda: q.quoka_gather(shape, Kh, Vh, sel, B_e, Ks, Vs, stream),
+        lambda: q.quoka_sparse_attend(shape, Q, Ks, Vs, B_e, Kc, Vc, params, O, None, ws, stream),
+    ]
 
     def new_events(k):
         return [torch.cuda.Event(enable_timing=True) for _ in range(k)]
 
+    # Each stage is captured once into its own CUDA graph (the library only
+    # enqueues kernels, so a captured call replays the identical launches); a
+    # step replays the five graphs back to back with events between them.
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for fn in stage_fns:
+                fn()
+    torch.cuda.synchronize(dev)
+    graphs = []
+    launches_before = q.quoka_launch_count()
+    for fn in stage_fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs.append(g)
+    launches_per_step = q.quoka_launch_count() - launches_before
+
+    def step(evs):
+        evs[0].record(stream)
+        for i, g in enumerate(graphs):
+            g.replay()
+            evs[i + 1].record(stream)
+
     sampler = ClockSampler(local_rank)
     sampler.start()
-    for _ in range(args.warmup):
-        flush.zero_()
-        step(new_events(6))
-    torch.cuda.synchronize(dev)
-    barrier()
-    torch.cuda.synchronize(dev)
-    launches0 = q.quoka_launch_count()
-    wall0 = time.perf_counter()
-    all_evs = []
-    for _ in range(args.steps):
-        flush.zero_()                       # L2 flushed between timed steps (outside the events)
-        evs = new_events(6)
-        step(evs)
-        all_evs.append(evs)
-    torch.cuda.synchronize(dev)
-    barrier()
-    wall = time.perf_counter() - wall0
-    launches = q.quoka_launch_count() - launches0
+    with torch.cuda.stream(stream):
+        t_w = time.perf_counter()
+        done = 0
+        while done < args.warmup or time.perf_counter() - t_w < 0.5:   # also gives the clock sampler a lead-in
+            flush.zero_()
+            step(new_events(6))
+            done += 1
+            if done % 50 == 0:
+                torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        all_evs = []
+        for _ in range(args.steps):
+            flush.zero_()                   # L2 flushed between timed steps (outside the events)
+            evs = new_events(6)
+            step(evs)
+            all_evs.append(evs)
+        torch.cuda.synchronize(dev)
+        barrier()
+        wall = time.perf_counter() - wall0
+    launches = launches_per_step * args.steps
     assert q.quoka_get_last_device_error(ws, stream) == 0
     stage_ms = {nm: [e[i].elapsed_time(e[i + 1]) for e in all_evs] for i, nm in enumerate(names)}
     step_ms_list = [e[0].elapsed_time(e[5]) for e in all_evs]
@@ -230,16 +252,17 @@ def run_quoka(args, rank, world, local_rank):
     if not args.no_dense:
         Od = torch.empty_like(Q)
         dsteps = max(3, args.steps // 4)
-        for _ in range(2):
-            q.quoka_dense_attend(shape, Q, Kh, Vh, Kc, Vc, params, Od, None, ws, stream)
-        ts = []
-        for _ in range(dsteps):
-            flush.zero_()
-            e = new_events(2)
-            e[0].record(stream)
-            q.quoka_dense_attend(shape, Q, Kh, Vh, Kc, Vc, params, Od, None, ws, stream)
-            e[1].record(stream)
-            ts.append(e)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                q.quoka_dense_attend(shape, Q, Kh, Vh, Kc, Vc, params, Od, None, ws, stream)
+            ts = []
+            for _ in range(dsteps):
+                flush.zero_()
+                e = new_events(2)
+                e[0].record(stream)
+                q.quoka_dense_attend(shape, Q, Kh, Vh, Kc, Vc, params, Od, None, ws, stream)
+                e[1].record(stream)
+                ts.append(e)
         torch.cuda.synchronize(dev)
         dense_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ts), dev)
 
@@ -258,17 +281,18 @@ def run_quoka(args, rank, world, local_rank):
         q.quoka_chunk_attend(shape, Qd, Kh, Vh, Kcd, Vcd, cfg.N_q, cfg.B, params, Od2, None, None, ws, stream)
         Oh.copy_(Od2, non_blocking=True)
 
-    for _ in range(args.warmup):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    ets = []
-    for _ in range(args.steps):
-        flush.zero_()
-        e = new_events(2)
-        e[0].record(stream)
-        e2e_step()
-        e[1].record(stream)
-        ets.append(e)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        ets = []
+        for _ in range(args.steps):
+            flush.zero_()
+            e = new_events(2)
+            e[0].record(stream)
+            e2e_step()
+            e[1].record(stream)
+            ets.append(e)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ets), dev)
     clocks = sampler.stop()
@@ -312,7 +336,9 @@ def run_quoka(args, rank, world, local_rank):
                 "5% outlier queries, planted needles)",
         "config": {"workload": cfg.name, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "d": cfg.d, "C": cfg.C, "T": cfg.T,
                    "N_q": cfg.N_q, "B": cfg.B, "gqa_pool": args.gqa, "engine": args.engine,
-                   "l2": "flushed between steps (512 MB write)", "parallelism": f"replicas x{world}"},
+                   "l2": "flushed between steps (512 MB write)",
+                   "timing": "each stage captured as a CUDA graph; CUDA events between stages",
+                   "parallelism": f"replicas x{world}"},
         "impl": "quoka",
         "gpu_launches": int(launches),
         "wall_s_timed_region": round(wall, 4),

@@ -192,6 +192,10 @@ int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const 
  * quoka_status if the shape, params or stage are invalid.  Host only. */
 int quoka_stage_engine(const quoka_shape* shape, const quoka_params* params, int stage);
 
+/* Description of the CUDA error behind the calling thread's most recent
+ * QUOKA_ERR_CUDA ("no error" if there was none).  Static storage. */
+const char* quoka_last_cuda_error_string(void);
+
 /* Number of CUDA kernels this library has enqueued in this process so far
  * (diagnostics: lets a caller count the launches of a timed region). */
 uint64_t quoka_launch_count(void);

@@ -109,7 +109,7 @@ static cudaError_t attend_impl(const void* Q, const void* Kh, const void* Vh, in
                                const void* Kc, const void* Vc, int H_q, int C, int G, float scale, void* O,
                                float* lse, cudaStream_t st) {
   const size_t smem = sizeof(float) * (kAttRows * D + kAttKeys * (D + 1) + kAttKeys * D);
-  cudaError_t e = cudaFuncSetAttribute(k_attend_simt<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem((const void*)k_attend_simt<T, D>, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((C + kAttRows - 1) / kAttRows, H_q);
   const float scale_log2 = scale * 1.4426950408889634f;

@@ -12,9 +12,12 @@
 // chunk part is causal.
 //   S_s = Q_s K_j^T        tcgen05, A = Q (smem), B = K tile (smem), fp32 in TMEM
 //   P_s = exp2(S_s - m)    softmax warpgroup of the slot, one query row per
-//                          thread, written back to TMEM as bf16 over S_s
-//   O_s += P_s V_j         tcgen05, A = P (TMEM), B = V tile (smem, MN-major)
-// The running maximum is only moved (and O rescaled in TMEM) when it grows by
+//                          thread, written to shared memory as bf16 in the
+//                          128-byte-swizzled K-major layout of an MMA operand
+//   O_s += P_s V_j         tcgen05, A = P (smem), B = V tile (smem, MN-major)
+// The softmax releases S_s as soon as it has loaded it, so the MMA warp
+// computes S_s for block j+1 while the softmax of block j is still running;
+// the running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8, so most blocks never touch O.
 //
 // Warps (320 threads): 0 = TMA producer, 1 = TMEM owner + MMA issuer,
@@ -29,17 +32,19 @@ namespace quoka {
 namespace {
 
 constexpr int kAttThreads = 320;
-constexpr int kKvStages = 4;
+constexpr int kKvStages = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr uint32_t kPBytes = 128 * 128 * 2;   // one slot's P tile: 128 rows x 128 keys, bf16
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 struct AttSmem {
   uint64_t q_full;
   uint64_t kv_full[kKvStages];
   uint64_t kv_empty[kKvStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_done[2];
+  uint64_t s_full[2];    // S_s of the current block is in TMEM
+  uint64_t s_free[2];    // the softmax has loaded S_s (TMEM free for the next block)
+  uint64_t p_full[2];    // P_s is in shared memory
+  uint64_t o_done[2];    // PV_s of the current block has completed
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -78,7 +83,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem;                                  // [2][HALVES][128][128 B]
-  uint8_t* kv_s = smem + 2 * kTileBytes;                // [kKvStages][HALVES][128][128 B]
+  uint8_t* p_s = q_s + 2 * kTileBytes;                  // [2][2 halves of 64 keys][128][128 B]
+  uint8_t* kv_s = p_s + 2 * kPBytes;                    // [kKvStages][HALVES][128][128 B]
   AttSmem* sm = reinterpret_cast<AttSmem*>(kv_s + kKvStages * kTileBytes);
 
   // ---- work item: longest (last query tile) first
@@ -102,6 +108,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&sm->s_full[s], 1);
+      tc::mbar_init(&sm->s_free[s], 4);
       tc::mbar_init(&sm->p_full[s], 4);
       tc::mbar_init(&sm->o_done[s], 1);
     }
@@ -120,7 +127,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   volatile int* abort = &sm->abort;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer: Q once, then K_j, V_j, ...
     if (lane == 0) {
       tc::tma_prefetch_desc(&qmap);
       tc::tma_prefetch_desc(&kcmap);
@@ -133,22 +140,27 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       for (int s = 0; s < n_slots; ++s)
         for (int hf = 0; hf < HALVES; ++hf)
           tc::tma_load_3d(q_s + s * kTileBytes + hf * kHalfBytes, &qmap, &sm->q_full, hf * 64, qt * 128, h0 + s);
+      // Ring items in the order the MMA warp consumes them: K_0, then for every
+      // block j: K_{j+1} (used early, by S of the next block) and V_j (used late).
       int k = 0;
       bool ok = true;
-      for (int jb = 0; ok && jb < n_blocks; ++jb) {
+      auto load = [&](int jb, int which) {      // which: 0 = K, 1 = V
+        const int s = k % kKvStages;
+        if (k >= kKvStages && !tc::mbar_wait(&sm->kv_empty[s], ((k / kKvStages) - 1) & 1, abort, hdr, 0x201))
+          return false;
         const bool hist = jb < nh;
         const int row = hist ? jb * 128 : (jb - nh) * 128;
-        for (int which = 0; which < 2; ++which, ++k) {
-          const int s = k % kKvStages;
-          if (k >= kKvStages && !tc::mbar_wait(&sm->kv_empty[s], ((k / kKvStages) - 1) & 1, abort, hdr, 0x201)) {
-            ok = false;
-            break;
-          }
-          const CUtensorMap* map = hist ? (which == 0 ? &khmap : &vhmap) : (which == 0 ? &kcmap : &vcmap);
-          tc::mbar_arrive_expect_tx(&sm->kv_full[s], kTileBytes);
-          for (int hf = 0; hf < HALVES; ++hf)
-            tc::tma_load_3d(kv_s + s * kTileBytes + hf * kHalfBytes, map, &sm->kv_full[s], hf * 64, row, g);
-        }
+        const CUtensorMap* map = hist ? (which == 0 ? &khmap : &vhmap) : (which == 0 ? &kcmap : &vcmap);
+        tc::mbar_arrive_expect_tx(&sm->kv_full[s], kTileBytes);
+        for (int hf = 0; hf < HALVES; ++hf)
+          tc::tma_load_3d(kv_s + s * kTileBytes + hf * kHalfBytes, map, &sm->kv_full[s], hf * 64, row, g);
+        ++k;
+        return true;
+      };
+      ok = load(0, 0);
+      for (int jb = 0; ok && jb < n_blocks; ++jb) {
+        if (jb + 1 < n_blocks) ok = load(jb + 1, 0);
+        if (ok) ok = load(jb, 1);
       }
       if (*abort) {   // let issued copies land before exiting
         tc::mbar_drain(&sm->q_full, 0);
@@ -158,49 +170,62 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Order per block j: S_s(j+1) for each slot as soon as its softmax has
+    // loaded S_s(j); then PV_s(j) as soon as P_s(j) is in shared memory.
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
-      bool ok = tc::mbar_wait(&sm->q_full, 0, abort, hdr, 0x202);
-      tc::tc_fence_after();
-      int k = 0;
-      for (int jb = 0; ok && jb < n_blocks; ++jb) {
-        // S_s = Q_s K^T
-        const int sk = k % kKvStages;
-        if (!(ok = tc::mbar_wait(&sm->kv_full[sk], (k / kKvStages) & 1, abort, hdr, 0x203))) break;
-        ++k;
-        tc::tc_fence_after();
-        const uint32_t kb = tc::smem_u32(kv_s + sk * kTileBytes);
-        for (int s = 0; s < n_slots; ++s) {
-          if (jb > 0 && !(ok = tc::mbar_wait(&sm->o_done[s], (jb - 1) & 1, abort, hdr, 0x204))) break;
-          tc::tc_fence_after();
-          const uint32_t qb = tc::smem_u32(q_s + s * kTileBytes);
+      const uint32_t kvb = tc::smem_u32(kv_s), qb0 = tc::smem_u32(q_s), pb0 = tc::smem_u32(p_s);
+      auto issue_s = [&](int s, int stage) {   // S_s = Q_s K^T, K in `stage`
+        const uint32_t qb = qb0 + s * kTileBytes, kb = kvb + stage * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int hf = kk >> 2, kin = kk & 3;
-            tc::mma_ss(tmem + s * kSlotCols, tc::sw128_desc(qb + hf * kHalfBytes + kin * 32, 16, 1024),
-                       tc::sw128_desc(kb + hf * kHalfBytes + kin * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(&sm->s_full[s]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int hf = kk >> 2, kin = kk & 3;
+          tc::mma_ss(tmem + s * kSlotCols, tc::sw128_desc(qb + hf * kHalfBytes + kin * 32, 16, 1024),
+                     tc::sw128_desc(kb + hf * kHalfBytes + kin * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
-        if (!ok) break;
-        tc::mma_commit(&sm->kv_empty[sk]);
-        // O_s += P_s V
-        const int sv = k % kKvStages;
-        if (!(ok = tc::mbar_wait(&sm->kv_full[sv], (k / kKvStages) & 1, abort, hdr, 0x205))) break;
-        ++k;
-        const uint32_t vb = tc::smem_u32(kv_s + sv * kTileBytes);
+        tc::mma_commit(&sm->s_full[s]);
+      };
+      bool ok = tc::mbar_wait(&sm->q_full, 0, abort, hdr, 0x202);
+      int item = 0;                              // ring item: K_0, then K_{j+1}, V_j per block
+      ok = ok && tc::mbar_wait(&sm->kv_full[0], 0, abort, hdr, 0x203);
+      tc::tc_fence_after();
+      if (ok) {
+        for (int s = 0; s < n_slots; ++s) issue_s(s, 0);
+        tc::mma_commit(&sm->kv_empty[0]);
+        item = 1;
+      }
+      for (int jb = 0; ok && jb < n_blocks; ++jb) {
+        if (jb + 1 < n_blocks) {
+          const int st = item % kKvStages;
+          if (!(ok = tc::mbar_wait(&sm->kv_full[st], (item / kKvStages) & 1, abort, hdr, 0x204))) break;
+          for (int s = 0; s < n_slots; ++s) {
+            if (!(ok = tc::mbar_wait(&sm->s_free[s], jb & 1, abort, hdr, 0x205))) break;
+            tc::tc_fence_after();
+            issue_s(s, st);
+          }
+          if (!ok) break;
+          tc::mma_commit(&sm->kv_empty[st]);
+          ++item;
+        }
+        const int sv = item % kKvStages;
+        if (!(ok = tc::mbar_wait(&sm->kv_full[sv], (item / kKvStages) & 1, abort, hdr, 0x206))) break;
+        const uint32_t vb = kvb + sv * kTileBytes;
         for (int s = 0; s < n_slots; ++s) {
-          if (!(ok = tc::mbar_wait(&sm->p_full[s], jb & 1, abort, hdr, 0x206))) break;
+          if (!(ok = tc::mbar_wait(&sm->p_full[s], jb & 1, abort, hdr, 0x207))) break;
           tc::tc_fence_after();
+          const uint32_t pb = pb0 + s * kPBytes;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)    // 16 keys per MMA; P holds 2 keys per TMEM column
-            tc::mma_ts(tmem + s * kSlotCols + 128, tmem + s * kSlotCols + kk * 8,
+          for (int kk = 0; kk < 8; ++kk) {      // 16 keys per MMA
+            const int hf = kk >> 2, kin = kk & 3;
+            tc::mma_ss(tmem + s * kSlotCols + 128, tc::sw128_desc(pb + hf * kHalfBytes + kin * 32, 16, 1024),
                        tc::sw128_desc(vb + kk * 16 * 128, kHalfBytes, 1024), idesc_o, (jb > 0 || kk > 0) ? 1u : 0u);
+          }
           tc::mma_commit(&sm->o_done[s]);
         }
         if (!ok) break;
         tc::mma_commit(&sm->kv_empty[sv]);
+        ++item;
       }
       tc::mma_commit(&sm->drain);
       tc::mbar_drain(&sm->drain, 0);
@@ -214,31 +239,37 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + s * kSlotCols;
     const uint32_t o_addr = s_addr + 128;
+    // this row of P in the swizzled operand layout: chunk q of half h at
+    // p_row + h * kHalfBytes + ((q ^ (r & 7)) << 4)
+    uint8_t* p_row = p_s + s * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
     if (s < n_slots) {
       float m_used = -INFINITY, l = 0.f;            // running max of the raw logits, softmax denominator
       bool ok = true;
       for (int jb = 0; jb < n_blocks; ++jb) {
-        if (!(ok = warp_wait(&sm->s_full[s], jb & 1, abort, hdr, 0x207))) break;
+        if (!(ok = warp_wait(&sm->s_full[s], jb & 1, abort, hdr, 0x208))) break;
         tc::tc_fence_after();
         uint32_t sv[128];
         tc::tmem_ld128(s_addr, sv);
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm->s_free[s]);   // the MMA may now write S_s of the next block
         const bool hist = jb < nh;
         // only the last history block (if partial) and the diagonal chunk block have masked keys
         const bool need_mask = hist ? (jb == nh - 1 && (n_hist & 127) != 0) : (jb - nh == qt);
-        float mx = -INFINITY;
         if (need_mask) {
           // keys of this block visible to row c: [0, lim)
           const int lim = hist ? n_hist - jb * 128 : c - (jb - nh) * 128 + 1;
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            const float x = i < lim ? __uint_as_float(sv[i]) : -INFINITY;
-            sv[i] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) sv[i] = __float_as_uint(-INFINITY);
         }
+        float mx8[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx8[t] = __uint_as_float(sv[t]);
+#pragma unroll
+        for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_used, mx);
         const bool rescale = (m_new - m_used) * scale_log2 > kRescaleThreshold;   // true on the first block
         float alpha = 1.f;
@@ -247,20 +278,28 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           m_used = m_new;
         }
         const float neg_m = -m_used * scale_log2;
-        float sum0 = 0.f, sum1 = 0.f;
-        uint32_t pv[64];
+        // PV_s of the previous block must be done before P_s is overwritten and before O is rescaled
+        if (jb > 0 && !(ok = warp_wait(&sm->o_done[s], (jb - 1) & 1, abort, hdr, 0x209))) break;
+        float sum8[8];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), scale_log2, neg_m));
-          sum0 += p0;
-          sum1 += p1;
-          pv[i] = pack_bf16x2(p0, p1);
+        for (int t = 0; t < 8; ++t) sum8[t] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {             // 8 keys = one 16-byte chunk of P at a time
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = 8 * q + 2 * j;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), scale_log2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), scale_log2, neg_m));
+            sum8[(2 * j) & 7] += p0;
+            sum8[(2 * j + 1) & 7] += p1;
+            w[j] = pack_bf16x2(p0, p1);
+          }
+          const int hf = q >> 3, ch = q & 7;
+          *reinterpret_cast<uint4*>(p_row + hf * kHalfBytes + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l = l * alpha + (sum0 + sum1);
-        if (jb > 0 && __any_sync(0xffffffffu, rescale)) {
-          // O of the previous blocks must be complete before it is rescaled in place
-          if (!(ok = warp_wait(&sm->o_done[s], (jb - 1) & 1, abort, hdr, 0x208))) break;
+        l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+        if (jb > 0 && __any_sync(0xffffffffu, rescale)) {   // O *= alpha in TMEM (rows without a rescale: alpha = 1)
           tc::tc_fence_after();
 #pragma unroll
           for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -270,9 +309,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
             tc::tmem_st32(o_addr + q4 * 32, ov);
           }
+          tc::tmem_wait_st();
         }
-        tc::tmem_st64(s_addr, pv);
-        tc::tmem_wait_st();
+        tc::fence_proxy_async_smem();              // P visible to the tensor core
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm->p_full[s]);
@@ -315,7 +354,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 }  // namespace
 
 size_t attend_tc_smem(int d) {
-  return 1024 + (size_t)(2 + kKvStages) * (d / 64) * 128 * 128 + sizeof(AttSmem);
+  return 1024 + (size_t)(2 + kKvStages) * (d / 64) * 128 * 128 + 2 * (size_t)kPBytes + sizeof(AttSmem);
 }
 
 cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
@@ -340,11 +379,11 @@ cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* V
   const size_t smem = attend_tc_smem(d);
   const float scale_log2 = scale * 1.4426950408889634f;
   if (d == 64) {
-    if ((e = cudaFuncSetAttribute(k_attend_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    if ((e = ensure_smem((const void*)k_attend_tc<64>, smem)) != cudaSuccess) return e;
     k_attend_tc<64><<<grid, kAttThreads, smem, st>>>(qmap, khmap, vhmap, kcmap, vcmap, n_hist, C, G, scale_log2,
                                                      (__nv_bfloat16*)O, lse, hdr);
   } else {
-    if ((e = cudaFuncSetAttribute(k_attend_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    if ((e = ensure_smem((const void*)k_attend_tc<128>, smem)) != cudaSuccess) return e;
     k_attend_tc<128><<<grid, kAttThreads, smem, st>>>(qmap, khmap, vhmap, kcmap, vcmap, n_hist, C, G, scale_log2,
                                                       (__nv_bfloat16*)O, lse, hdr);
   }

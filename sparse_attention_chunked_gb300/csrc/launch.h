@@ -38,6 +38,9 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
                             const float* op_scale, int R, int passes, float* scores, WsHeader* hdr, int num_sms,
                             cudaStream_t st);
 
+// Raises `func`'s dynamic shared-memory limit to `bytes` on the current device (cached).
+cudaError_t ensure_smem(const void* func, size_t bytes);
+
 // TMA descriptor of a bf16 3-D tensor (see tmaps.cu).
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                               uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1);

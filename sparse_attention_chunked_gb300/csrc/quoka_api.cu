@@ -4,7 +4,7 @@
 #include <math.h>
 #include <string.h>
 
-#include "../../include/quoka.h"
+#include "quoka.h"
 #include "common.cuh"
 #include "launch.h"
 
@@ -72,13 +72,13 @@ int num_sms() {
 }
 
 // Whether the scoring stage can run on the tensor cores: bf16 keys, at most
-// 512 scoring rows (the TMEM width) and an operand that fits shared memory
-// next to two key stages.
+// 512 operand rows (the TMEM width; mean pooling needs its rows twice, hi and
+// lo) and an operand that fits shared memory next to two key stages.
 bool score_tc_fits(const quoka_shape* s, int N_q, int gqa) {
   if (s->dtype != QUOKA_DTYPE_BF16) return false;
   const int N_pad = score_tc_pad_rows(score_rows(s, N_q, gqa));
   const int passes = gqa == QUOKA_GQA_MAX ? 1 : 2;
-  return N_pad <= 512 && score_tc_smem(s->d, N_pad, passes, 2) <= 227 * 1024;
+  return passes * N_pad <= 512 && score_tc_smem(s->d, N_pad, passes, 2) <= 227 * 1024;
 }
 
 // Which kernels run (stage 0 = scoring, 1 = attention).  Tensor-core kernels are bf16 only.
@@ -127,7 +127,13 @@ int check_ws(const void* ws, size_t ws_bytes, size_t need) {
   return QUOKA_OK;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? QUOKA_OK : QUOKA_ERR_CUDA; }
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return QUOKA_OK;
+  t_last_cuda_error = e;
+  return QUOKA_ERR_CUDA;
+}
 
 template <typename P> P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<char*>(ws) + off); }
 
@@ -194,6 +200,8 @@ int quoka_stage_engine(const quoka_shape* shape, const quoka_params* params, int
   if (stage != 0 && stage != 1) return -QUOKA_ERR_INVALID_ARG;
   return use_tensor_cores(p, shape, stage, 1) ? QUOKA_ENGINE_TENSOR : QUOKA_ENGINE_SIMT;
 }
+
+const char* quoka_last_cuda_error_string(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 uint64_t quoka_launch_count(void) { return quoka::g_launch_count.load(std::memory_order_relaxed); }
 

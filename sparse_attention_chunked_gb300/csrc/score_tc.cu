@@ -57,6 +57,36 @@ struct ScoreSmem {
   int abort;
 };
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a.x * b.x, a.y * b.y) and (a.x + b.x, a.y + b.y) as single packed instructions.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long pa, pb, pc;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+  asm("mul.f32x2 %0, %1, %2;" : "=l"(pc) : "l"(pa), "l"(pb));
+  float2 c;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c.x), "=f"(c.y) : "l"(pc));
+  return c;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long pa, pb, pc;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+  asm("add.f32x2 %0, %1, %2;" : "=l"(pc) : "l"(pa), "l"(pb));
+  float2 c;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c.x), "=f"(c.y) : "l"(pc));
+  return c;
+}
+
+// Operand rows in shared memory: [HALVES][NT][128 B], NT = passes * N_pad, so
+// that one MMA with N = NT (in chunks of 256) covers every pass; pass p of row
+// r is B row p * N_pad + r and lands in TMEM column p * N_pad + r.
 template <int D>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     k_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
@@ -67,8 +97,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   constexpr uint32_t kStageBytes = HALVES * kHalfBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t op_bytes = (uint32_t)passes * HALVES * N_pad * 128;
-  uint8_t* op_s = smem;                                         // [passes][HALVES][N_pad][128 B]
+  const int NT = passes * N_pad;
+  const uint32_t op_bytes = (uint32_t)HALVES * NT * 128;
+  uint8_t* op_s = smem;                                         // [HALVES][NT][128 B]
   uint8_t* ktiles = smem + op_bytes;                            // [nst][HALVES][128][128 B]
   float* scale_s = reinterpret_cast<float*>(ktiles + (size_t)nst * kStageBytes);
   ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(scale_s + N_pad);
@@ -111,12 +142,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc::tma_prefetch_desc(&kmap);
       tc::tma_prefetch_desc(&omap);
       tc::mbar_arrive_expect_tx(&sm->op_full, op_bytes);
-      const int nb = op_box_rows(N_pad);
-      for (int p = 0; p < passes; ++p)
-        for (int hf = 0; hf < HALVES; ++hf)
-          for (int rb = 0; rb < N_pad; rb += nb)
-            tc::tma_load_3d(op_s + ((size_t)(p * HALVES + hf) * N_pad + rb) * 128, &omap, &sm->op_full, hf * 64,
-                            p * N_pad + rb, g);
+      const int nb = op_box_rows(NT);
+      for (int hf = 0; hf < HALVES; ++hf)
+        for (int rb = 0; rb < NT; rb += nb)
+          tc::tma_load_3d(op_s + ((size_t)hf * NT + rb) * 128, &omap, &sm->op_full, hf * 64, rb, g);
       int issued = 0;
       for (int it = 0; it < ntiles; ++it) {
         const int s = it % nst;
@@ -138,26 +167,22 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (lane == 0 && ntiles > 0) {
       bool ok = tc::mbar_wait(&sm->op_full, 0, abort, hdr, 0x102);
       tc::tc_fence_after();
-      const uint32_t idesc_full = tc::idesc_bf16_f32(128, N_pad < 256 ? N_pad : 256, false);
+      const uint32_t b_base = tc::smem_u32(op_s);
       for (int it = 0; ok && it < ntiles; ++it) {
         const int s = it % nst, a = it % nacc;
         if (!tc::mbar_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x103)) break;
         if (it >= nacc && !tc::mbar_wait(&sm->acc_empty[a], ((it / nacc) - 1) & 1, abort, hdr, 0x104)) break;
         tc::tc_fence_after();
         const uint32_t a_base = tc::smem_u32(ktiles + (size_t)s * kStageBytes);
-        const uint32_t b_base = tc::smem_u32(op_s);
-        for (int nc = 0; nc < N_pad; nc += 256) {
-          const int n_this = N_pad - nc < 256 ? N_pad - nc : 256;
-          const uint32_t idesc = n_this == 256 || n_this == N_pad ? idesc_full : tc::idesc_bf16_f32(128, n_this, false);
-          for (int p = 0; p < passes; ++p) {
+        for (int nc = 0; nc < NT; nc += 256) {
+          const int n_this = NT - nc < 256 ? NT - nc : 256;
+          const uint32_t idesc = tc::idesc_bf16_f32(128, n_this, false);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const int hf = kk >> 2, kin = kk & 3;
-              const uint64_t adesc = tc::sw128_desc(a_base + hf * kHalfBytes + kin * 32, 16, 1024);
-              const uint64_t bdesc =
-                  tc::sw128_desc(b_base + ((uint32_t)(p * HALVES + hf) * N_pad + nc) * 128 + kin * 32, 16, 1024);
-              tc::mma_ss(tmem + (uint32_t)(a * N_pad + nc), adesc, bdesc, idesc, (p > 0 || kk > 0) ? 1u : 0u);
-            }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int hf = kk >> 2, kin = kk & 3;
+            const uint64_t adesc = tc::sw128_desc(a_base + hf * kHalfBytes + kin * 32, 16, 1024);
+            const uint64_t bdesc = tc::sw128_desc(b_base + ((uint32_t)hf * NT + nc) * 128 + kin * 32, 16, 1024);
+            tc::mma_ss(tmem + (uint32_t)(a * NT + nc), adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
           }
         }
         tc::mma_commit(&sm->kv_empty[s]);
@@ -169,11 +194,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue: one key per thread pair
     const int quad = warp & 3;                      // TMEM lane quadrant this warp may access
-    const int part = (warp - 2) >> 2;               // which half of the columns / of d
+    const int part = (warp - 2) >> 2;               // which half of the rows / of d
     const int row = quad * 32 + lane;               // key within the tile
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    const int half_cols = ((N_pad >> 1) + 31) & ~31;
-    const int c_begin = part * half_cols, c_end = min(R, part == 0 ? half_cols : N_pad);
+    const int half_rows = ((N_pad >> 1) + 31) & ~31;
+    const int r_begin = part * half_rows, r_end = min(R, part == 0 ? half_rows : N_pad);
+    const bool mean_mode = passes == 2;
     bool alive = true;                              // false once a wait gave up (warp-uniform)
     for (int it = 0; it < ntiles; ++it) {
       const int s = it % nst, a = it % nacc, buf = it & 1;
@@ -182,6 +208,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (alive) {
         // |k|^2 over this part's 64-column halves of d; 16-byte chunk c of row r sits at c ^ (r & 7)
         const uint8_t* tile = ktiles + (size_t)s * kStageBytes;
+        float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
         for (int hf = 0; hf < HALVES; ++hf) {
           if ((hf & 1) != part) continue;
@@ -189,34 +216,63 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & 7)) << 4));
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 f = __bfloat1622float2(h2[j]);
-              ss = fmaf(f.x, f.x, ss);
-              ss = fmaf(f.y, f.y, ss);
+            for (int j = 0; j < 4; ++j) {           // bf16 pair -> two fp32 (exact: shift into the high half)
+              const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+              ss0 = fmaf(lo, lo, ss0);
+              ss1 = fmaf(hi, hi, ss1);
             }
           }
         }
+        ss = ss0 + ss1;
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->kv_empty[s]);
       if (alive) alive = warp_wait(&sm->acc_full[a], (it / nacc) & 1, abort, hdr, 0x106);
-      float best = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (alive) {
         tc::tc_fence_after();
-        for (int c0 = c_begin; c0 < c_end; c0 += 64) {
-          uint32_t v[64];
-          const bool two = c0 + 32 < c_end;         // both 32-column groups hold valid rows
-          if (two) tc::tmem_ld64(tmem + lane_addr + (uint32_t)(a * N_pad + c0), v);
-          else tc::tmem_ld32(tmem + lane_addr + (uint32_t)(a * N_pad + c0), v);
-          const int nvalid = c_end - c0;
+        for (int c0 = r_begin; c0 < r_end; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(tmem + lane_addr + (uint32_t)(a * NT + c0), v);
+          if (mean_mode) {                           // hi + lo of the pre-aggregated row
+            uint32_t w[32];
+            tc::tmem_ld32(tmem + lane_addr + (uint32_t)(a * NT + N_pad + c0), w);
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (j < nvalid && (j < 32 || two)) best = fmaxf(best, __uint_as_float(v[j]) * scale_s[c0 + j]);
+            for (int j = 0; j < 16; ++j) {
+              const float2 s2 = add2(make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])),
+                                     make_float2(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1])));
+              v[2 * j] = __float_as_uint(s2.x);
+              v[2 * j + 1] = __float_as_uint(s2.y);
+            }
+          } else {                                   // x 1/|q| of the raw query row
+            const float4* sc = reinterpret_cast<const float4*>(scale_s + c0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 q = sc[j];
+              const float2 p0 = mul2(make_float2(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1])),
+                                     make_float2(q.x, q.y));
+              const float2 p1 = mul2(make_float2(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])),
+                                     make_float2(q.z, q.w));
+              v[4 * j] = __float_as_uint(p0.x);
+              v[4 * j + 1] = __float_as_uint(p0.y);
+              v[4 * j + 2] = __float_as_uint(p1.x);
+              v[4 * j + 3] = __float_as_uint(p1.y);
+            }
+          }
+          if (c0 + 32 > r_end) {                     // padding rows of the last chunk never win
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j >= r_end) v[j] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            m4[j & 3] = fmax3(m4[j & 3], __uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
         }
         tc::tc_fence_before();
       }
+      const float best = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->acc_empty[a]);
       sm->red_max[buf][part][row] = best;
@@ -260,26 +316,28 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
   while (nst > 2 && score_tc_smem(d, N_pad, passes, nst) > budget) --nst;
   const size_t smem = score_tc_smem(d, N_pad, passes, nst);
   if (smem > budget) return cudaErrorInvalidValue;
-  const int nacc = 2 * N_pad <= 512 ? 2 : 1;
+  const int NT = passes * N_pad;
+  if (NT > 512) return cudaErrorInvalidValue;
+  const int nacc = 2 * NT <= 512 ? 2 : 1;
   uint32_t cols = 32;
-  while (cols < (uint32_t)(nacc * N_pad)) cols <<= 1;
+  while (cols < (uint32_t)(nacc * NT)) cols <<= 1;
   CUtensorMap kmap, omap;
   cudaError_t e = make_tmap_bf16_3d(&kmap, K, d, T_len, H_kv, (uint64_t)d * 2, (uint64_t)head_stride * 2, 64, 128);
   if (e != cudaSuccess) return e;
   e = make_tmap_bf16_3d(&omap, op_bf, d, (uint64_t)passes * N_pad, H_kv, (uint64_t)d * 2,
-                        (uint64_t)passes * N_pad * d * 2, 64, op_box_rows(N_pad));
+                        (uint64_t)passes * N_pad * d * 2, 64, op_box_rows(NT));
   if (e != cudaSuccess) return e;
   const int tiles_head = (T_len + kTileKeys - 1) / kTileKeys;
   int per_head = (num_sms + H_kv - 1) / H_kv;
   if (per_head > tiles_head) per_head = tiles_head;
   dim3 grid(per_head, H_kv);
   if (d == 64) {
-    e = cudaFuncSetAttribute(k_score_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_smem((const void*)k_score_tc<64>, smem);
     if (e != cudaSuccess) return e;
     k_score_tc<64><<<grid, kScoreThreads, smem, st>>>(kmap, omap, op_scale, T_len, R, N_pad, passes, nst, nacc, cols,
                                                       scores, hdr);
   } else {
-    e = cudaFuncSetAttribute(k_score_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_smem((const void*)k_score_tc<128>, smem);
     if (e != cudaSuccess) return e;
     k_score_tc<128><<<grid, kScoreThreads, smem, st>>>(kmap, omap, op_scale, T_len, R, N_pad, passes, nst, nacc,
                                                        cols, scores, hdr);

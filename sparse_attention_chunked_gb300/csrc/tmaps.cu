@@ -37,4 +37,33 @@ cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, u
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Raises a kernel's dynamic shared-memory limit on the current device, once
+// per (kernel, device) unless a larger size is asked for later.
+cudaError_t ensure_smem(const void* func, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  struct Entry {
+    const void* func;
+    int dev;
+    size_t bytes;
+  };
+  static Entry table[64];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].func == func && table[i].dev == dev && table[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < used; ++i)
+    if (table[i].func == func && table[i].dev == dev) {
+      table[i].bytes = bytes;
+      return cudaSuccess;
+    }
+  if (used < 64) table[used++] = Entry{func, dev, bytes};
+  return cudaSuccess;
+}
+
 }  // namespace quoka

@@ -62,6 +62,7 @@ _SIG = {
     "quoka_append_kv": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
     "quoka_get_last_device_error": (ctypes.c_int, [_P, _P]),
     "quoka_launch_count": (ctypes.c_uint64, []),
+    "quoka_last_cuda_error_string": (ctypes.c_char_p, []),
     "quoka_selftest_expire_wait": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_longlong, _P]),
     "quoka_stage_engine": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.c_int]),
 }
@@ -91,7 +92,10 @@ def load(path: str | os.PathLike | None = None):
 
 def _check(fn, rc):
     if rc != QUOKA_OK:
-        raise QuokaError(fn, rc)
+        err = QuokaError(fn, rc)
+        if rc == 5:   # QUOKA_ERR_CUDA: say which CUDA error
+            err.args = (f"{err.args[0]} ({load().quoka_last_cuda_error_string().decode()})",)
+        raise err
 
 
 def _ptr(t):

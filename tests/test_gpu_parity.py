@@ -276,3 +276,19 @@ def test_ragged_batch(quoka, gqa):
         r = run_stages(quoka, sub, x, gqa)
         if s in (0, 3, 7):
             check_stages(sub, x, gqa, r)
+
+
+@pytest.mark.parametrize("T,B", [(400_000, 5000), (70_000, 4096), (9, 8)])
+def test_topk_sizes_and_slices(quoka, T, B):
+    """Slices that do and do not fit in shared memory, and tiny rows, with frequent exact ties."""
+    H_kv = 2
+    rng = np.random.default_rng(T)
+    s = (rng.integers(-200, 200, (H_kv, T)) * 0.01).astype(np.float32)
+    scores = torch.from_numpy(s).to(DEV)
+    shape = quoka.Shape(0, H_kv, H_kv, 4, T, 64, 1)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    sel = torch.empty((H_kv, B), dtype=torch.int32, device=DEV)
+    quoka.quoka_topk(shape, scores, B, sel, ws)
+    got = sel.cpu().numpy()
+    for g in range(H_kv):
+        assert np.array_equal(got[g], qo.top_b(s[g].astype(np.float64), B))
