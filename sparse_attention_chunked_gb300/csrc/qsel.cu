@@ -88,9 +88,9 @@ __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, co
   }
 }
 
-__global__ void __launch_bounds__(1024) k_qselect(const float* __restrict__ qcos, int C, int G_avg, int n_sel,
+__global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos, int C, int G_avg, int n_sel,
                                                   int32_t* __restrict__ q_idx) {
-  extern __shared__ uint32_t keys_s[];
+  extern __shared__ __align__(16) uint32_t keys_s[];
   __shared__ RadixSelectShared rs;
   const int row = blockIdx.x;
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(1024) k_qselect(const float* __restrict__ qcos
     keys_s[c] = ~order_key(u);   // the largest key is the smallest cosine
   }
   __syncthreads();
-  block_radix_topk([&](int i) { return keys_s[i]; }, C, n_sel, q_idx + (size_t)row * n_sel, rs);
+  block_radix_topk4(reinterpret_cast<const uint4*>(keys_s), C, n_sel, q_idx + (size_t)row * n_sel, rs);
 }
 
 template <typename T, int D>
@@ -115,9 +115,9 @@ static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel
   dim3 grid(nblk, H_q);
   k_qstats<T, D><<<grid, 256, 0, st>>>((const T*)Q, C, qnorm, qpart);
   k_qcos<T, D><<<grid, 256, 0, st>>>((const T*)Q, C, qpart, qnorm, qcos);
-  const size_t smem = (size_t)C * sizeof(uint32_t);   // C <= 8192: at most 32 KB
+  const size_t smem = (size_t)((C + 3) & ~3) * sizeof(uint32_t);   // C <= 8192: at most 32 KB
   const int rows = H_q / G_avg;
-  k_qselect<<<rows, 1024, smem, st>>>(qcos, C, G_avg, n_sel, q_idx);
+  k_qselect<<<rows, 256, smem, st>>>(qcos, C, G_avg, n_sel, q_idx);
   count_launches(3);
   return cudaGetLastError();
 }

@@ -31,6 +31,10 @@ __device__ __forceinline__ void radix_zero(unsigned int* h, int count) {
 }
 
 // Histogram of digit (key >> shift) & 255 over keys i < n with (key & mask) == prefix.
+// Keys of neighbouring positions usually share the digit (in the first pass
+// nearly all keys do) or do not match the prefix at all, so each warp adds
+// the lanes that share the first matching lane's digit with one atomic (a
+// ballot) and only the remaining lanes add one by one.
 template <typename KeyAt>
 __device__ __forceinline__ void radix_hist(const KeyAt& key_at, int n, uint32_t prefix, uint32_t mask, int shift,
                                            unsigned int (*sub)[256]) {
@@ -43,8 +47,14 @@ __device__ __forceinline__ void radix_hist(const KeyAt& key_at, int n, uint32_t 
       const uint32_t u = key_at(i);
       if ((u & mask) == prefix) bin = (u >> shift) & 255u;
     }
-    const unsigned grp = __match_any_sync(0xffffffffu, bin);
-    if (bin != 0xFFFFFFFFu && lane == __ffs(grp) - 1) atomicAdd(&my_hist[bin], (unsigned)__popc(grp));
+    const unsigned valid = __ballot_sync(0xffffffffu, bin != 0xFFFFFFFFu);
+    if (valid != 0u) {
+      const int leader = __ffs(valid) - 1;
+      const uint32_t lb = __shfl_sync(0xffffffffu, bin, leader);
+      const unsigned same = __ballot_sync(0xffffffffu, bin == lb);
+      if (lane == leader) atomicAdd(&my_hist[lb], (unsigned)__popc(same));
+      else if (bin != 0xFFFFFFFFu && bin != lb) atomicAdd(&my_hist[bin], 1u);
+    }
   }
 }
 
@@ -121,6 +131,82 @@ __device__ __forceinline__ void radix_compact(const KeyAt& key_at, int n, uint32
   }
 }
 
+// ---- variants over keys cached in shared memory as uint4 (4 keys per
+// thread per step, which gives each warp four independent chains).  keys4
+// holds ceil(n / 4) vectors; entries at index >= n are ignored.
+
+__device__ __forceinline__ void radix_hist_one(uint32_t bin, int lane, unsigned int* my_hist) {
+  const unsigned valid = __ballot_sync(0xffffffffu, bin != 0xFFFFFFFFu);
+  if (valid != 0u) {
+    const int leader = __ffs(valid) - 1;
+    const uint32_t lb = __shfl_sync(0xffffffffu, bin, leader);
+    const unsigned same = __ballot_sync(0xffffffffu, bin == lb);
+    if (lane == leader) atomicAdd(&my_hist[lb], (unsigned)__popc(same));
+    else if (bin != 0xFFFFFFFFu && bin != lb) atomicAdd(&my_hist[bin], 1u);
+  }
+}
+
+__device__ __forceinline__ void radix_hist4(const uint4* __restrict__ keys4, int n, uint32_t prefix, uint32_t mask,
+                                            int shift, unsigned int (*sub)[256]) {
+  const int lane = threadIdx.x & 31;
+  unsigned int* my_hist = sub[(threadIdx.x >> 5) & (kRadixSubHists - 1)];
+  const int nv = (n + 3) >> 2;
+  for (int base = 0; base < nv; base += blockDim.x) {
+    const int v = base + threadIdx.x;
+    uint32_t b[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+    if (v < nv) {
+      const uint4 q = keys4[v];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (4 * v + j < n && (u[j] & mask) == prefix) b[j] = (u[j] >> shift) & 255u;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) radix_hist_one(b[j], lane, my_hist);
+  }
+}
+
+// Index-ordered compaction (see radix_compact) with 4 consecutive keys per thread.
+__device__ __forceinline__ void radix_compact4(const uint4* __restrict__ keys4, int n, uint32_t theta, int r,
+                                               int taken0, int ties0, int k, int index_base,
+                                               int32_t* __restrict__ out, int* scan) {
+  const int lane = threadIdx.x & 31;
+  const int nv = (n + 3) >> 2;
+  int taken = taken0, ties = ties0;   // block-uniform running totals
+  for (int base = 0; base < nv && taken < k; base += blockDim.x) {
+    const int v = base + threadIdx.x;
+    bool gt[4] = {false, false, false, false}, eq[4] = {false, false, false, false};
+    if (v < nv) {
+      const uint4 q = keys4[v];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gt[j] = 4 * v + j < n && u[j] > theta;
+        eq[j] = 4 * v + j < n && u[j] == theta;
+      }
+    }
+    const int my_gt = gt[0] + gt[1] + gt[2] + gt[3], my_eq = eq[0] + eq[1] + eq[2] + eq[3];
+    int total;
+    const int excl = block_exclusive_scan((my_gt << 16) | my_eq, scan, &total);  // per-thread, in index order
+    const int gt_before = excl >> 16, eq_before = excl & 0xFFFF;
+    int pos = taken + gt_before + min(eq_before, max(0, r - ties));
+    int tie_rank = ties + eq_before;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (gt[j]) {
+        out[pos++] = index_base + 4 * v + j;
+      } else if (eq[j]) {
+        if (tie_rank < r) out[pos++] = index_base + 4 * v + j;
+        ++tie_rank;
+      }
+    }
+    const int gt_tot = total >> 16, eq_tot = total & 0xFFFF;
+    taken += gt_tot + min(eq_tot, max(0, r - ties));
+    ties += eq_tot;
+  }
+  (void)lane;
+}
+
 struct RadixSelectShared {
   unsigned int sub[kRadixSubHists][256];
   unsigned int hist[256];
@@ -156,6 +242,34 @@ __device__ void block_radix_topk(const KeyAt& key_at, int n, int k, int32_t* __r
     __syncthreads();
   }
   radix_compact(key_at, n, prefix, need, 0, 0, k, 0, out, sm.scan);
+}
+
+// Whole-block top-k over keys cached in shared memory as uint4 (4 per thread per step).
+__device__ inline void block_radix_topk4(const uint4* __restrict__ keys4, int n, int k, int32_t* __restrict__ out,
+                                  RadixSelectShared& sm) {
+  uint32_t prefix = 0, mask = 0;
+  int need = k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    radix_zero(&sm.sub[0][0], kRadixSubHists * 256);
+    __syncthreads();
+    radix_hist4(keys4, n, prefix, mask, shift, sm.sub);
+    __syncthreads();
+    radix_reduce(sm.sub, sm.hist);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      unsigned c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = sm.hist[255 - 8 * threadIdx.x - j];
+      radix_find_digit(c, need, &sm.bin, &sm.need);
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm.bin << shift;
+    mask |= 255u << shift;
+    need = sm.need;
+    __syncthreads();
+  }
+  radix_compact4(keys4, n, prefix, need, 0, 0, k, 0, out, sm.scan);
 }
 
 }  // namespace quoka

@@ -29,6 +29,7 @@ constexpr int kTopkSliceCap = 40 * 1024;   // keys per CTA cached in shared memo
 struct TopkClusterShared {
   unsigned int sub[kRadixSubHists][256];
   unsigned int hist[2][256];   // this CTA's digit histogram by pass parity, read by the whole cluster
+  unsigned int merged[256];    // the cluster's histogram of the current pass
   int counts[2];               // this CTA's keys above / equal to the threshold
   int scan[32];
   int bin, need, gt_base, eq_base;
@@ -37,7 +38,7 @@ struct TopkClusterShared {
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
     k_topk_cluster(const float* __restrict__ scores, int T_len, int B_e, int32_t* __restrict__ sel, int per,
                    int cache) {
-  extern __shared__ uint32_t keys_s[];
+  extern __shared__ __align__(16) uint32_t keys_s[];
   __shared__ TopkClusterShared sm;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -46,10 +47,24 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   const int n = min(T_len, t0 + per) - t0;
   const float* s = scores + (size_t)g * T_len + t0;
   if (cache) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) keys_s[i] = order_key(s[i]);
+    // batched loads: 4 independent scores per thread in flight
+    for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
+      float f[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + j * blockDim.x;
+        f[j] = i < n ? s[i] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + j * blockDim.x;
+        if (i < n) keys_s[i] = order_key(f[j]);
+      }
+    }
     __syncthreads();
   }
   auto key_at = [&](int i) -> uint32_t { return cache ? keys_s[i] : order_key(s[i]); };
+  const uint4* keys4 = reinterpret_cast<const uint4*>(keys_s);
 
   uint32_t prefix = 0, mask = 0;
   int need = B_e;
@@ -57,19 +72,22 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     const int shift = 24 - 8 * pass, buf = pass & 1;
     radix_zero(&sm.sub[0][0], kRadixSubHists * 256);
     __syncthreads();
-    radix_hist(key_at, n, prefix, mask, shift, sm.sub);
+    if (cache) radix_hist4(keys4, n, prefix, mask, shift, sm.sub);
+    else radix_hist(key_at, n, prefix, mask, shift, sm.sub);
     __syncthreads();
     radix_reduce(sm.sub, sm.hist[buf]);
     cluster.sync();                       // every CTA's histogram of this pass is ready
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) {   // merge bin b across the cluster
+      unsigned t = 0;
+#pragma unroll
+      for (int q = 0; q < kTopkCluster; ++q) t += cluster.map_shared_rank(&sm.hist[buf][0], q)[b];
+      sm.merged[b] = t;
+    }
+    __syncthreads();
     if (threadIdx.x < 32) {
       unsigned c[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = 0;
-      for (int q = 0; q < kTopkCluster; ++q) {
-        const unsigned int* rh = cluster.map_shared_rank(&sm.hist[buf][0], q);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) c[j] += rh[255 - 8 * threadIdx.x - j];
-      }
+      for (int j = 0; j < 8; ++j) c[j] = sm.merged[255 - 8 * threadIdx.x - j];
       radix_find_digit(c, need, &sm.bin, &sm.need);
     }
     __syncthreads();
@@ -107,7 +125,10 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   }
   __syncthreads();
   const int gt_base = sm.gt_base, eq_base = sm.eq_base;
-  radix_compact(key_at, n, theta, r, gt_base + min(eq_base, r), eq_base, B_e, t0, sel + (size_t)g * B_e, sm.scan);
+  if (cache)
+    radix_compact4(keys4, n, theta, r, gt_base + min(eq_base, r), eq_base, B_e, t0, sel + (size_t)g * B_e, sm.scan);
+  else
+    radix_compact(key_at, n, theta, r, gt_base + min(eq_base, r), eq_base, B_e, t0, sel + (size_t)g * B_e, sm.scan);
   cluster.sync();                         // keep this CTA's shared memory alive for remote readers
 }
 
@@ -127,9 +148,9 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
     count_launches(1);
     return cudaGetLastError();
   }
-  const int per = (T_len + kTopkCluster - 1) / kTopkCluster;
+  const int per = ((T_len + kTopkCluster - 1) / kTopkCluster + 3) & ~3;
   const int cache = per <= kTopkSliceCap ? 1 : 0;
-  const size_t smem = cache ? (size_t)per * 4 : 0;
+  const size_t smem = cache ? (size_t)per * 4 + 16 : 0;
   cudaError_t e = ensure_smem((const void*)k_topk_cluster, smem);
   if (e != cudaSuccess) return e;
   k_topk_cluster<<<dim3(kTopkCluster, H_kv), kTopkThreads, smem, st>>>(scores, T_len, B_e, sel, per, cache);
