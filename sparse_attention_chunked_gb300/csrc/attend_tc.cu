@@ -65,6 +65,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (x0 * s + b, x1 * s + b) as one packed f32x2 FMA.
+__device__ __forceinline__ void fma2(float& x0, float& x1, float s, float b) {
+  unsigned long long px, ps, pb;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(px) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(ps) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(pb) : "f"(b));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(px) : "l"(px), "l"(ps), "l"(pb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(px));
+}
+
+// (a0 + b0, a1 + b1) as one packed f32x2 add.
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  unsigned long long pa, pb;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b0), "f"(b1));
+  asm("add.f32x2 %0, %1, %2;" : "=l"(pa) : "l"(pa), "l"(pb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(pa));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -263,13 +288,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           for (int i = 0; i < 128; ++i)
             if (i >= lim) sv[i] = __float_as_uint(-INFINITY);
         }
-        float mx8[8];
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int t = 0; t < 8; ++t) mx8[t] = __uint_as_float(sv[t]);
-#pragma unroll
-        for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sv[i]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int i = 0; i < 64; ++i)
+          mx4[i & 3] = fmax3(mx4[i & 3], __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_new = fmaxf(m_used, mx);
         const bool rescale = (m_new - m_used) * scale_log2 > kRescaleThreshold;   // true on the first block
         float alpha = 1.f;
@@ -280,25 +303,24 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const float neg_m = -m_used * scale_log2;
         // PV_s of the previous block must be done before P_s is overwritten and before O is rescaled
         if (jb > 0 && !(ok = warp_wait(&sm->o_done[s], (jb - 1) & 1, abort, hdr, 0x209))) break;
-        float sum8[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) sum8[t] = 0.f;
+        float sa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q = 0; q < 16; ++q) {             // 8 keys = one 16-byte chunk of P at a time
           uint32_t w[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int i = 8 * q + 2 * j;
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), scale_log2, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), scale_log2, neg_m));
-            sum8[(2 * j) & 7] += p0;
-            sum8[(2 * j + 1) & 7] += p1;
+            float x0 = __uint_as_float(sv[i]), x1 = __uint_as_float(sv[i + 1]);
+            fma2(x0, x1, scale_log2, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (j & 1) add2(sa[2], sa[3], p0, p1);
+            else add2(sa[0], sa[1], p0, p1);
             w[j] = pack_bf16x2(p0, p1);
           }
           const int hf = q >> 3, ch = q & 7;
           *reinterpret_cast<uint4*>(p_row + hf * kHalfBytes + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+        l = l * alpha + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
         if (jb > 0 && __any_sync(0xffffffffu, rescale)) {   // O *= alpha in TMEM (rows without a rescale: alpha = 1)
           tc::tc_fence_after();
 #pragma unroll

@@ -18,6 +18,31 @@
 namespace quoka {
 
 constexpr int kRowsPerBlock = 64;
+constexpr int kRowsPerWarp = kRowsPerBlock / 8;
+
+// E consecutive elements of a row per lane, loaded as one vector.
+template <typename T, int E>
+struct alignas(sizeof(T) * E) RowSlice {
+  T v[E];
+};
+
+// Loads the warp's kRowsPerWarp rows (lane holds elements lane*E .. lane*E+E-1),
+// all loads issued before any use; rows at or beyond C read as zero.
+template <typename T, int D>
+__device__ __forceinline__ void load_rows(const T* __restrict__ Q, int h, int C, int c0, float (*x)[D / 32]) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  RowSlice<T, E> raw[kRowsPerWarp];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int c = c0 + r;
+    if (c < C) raw[r] = *reinterpret_cast<const RowSlice<T, E>*>(Q + ((size_t)h * C + c) * D + lane * E);
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+    for (int j = 0; j < E; ++j) x[r][j] = (c0 + r < C) ? to_f32(raw[r].v[j]) : 0.f;
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_qstats(const T* __restrict__ Q, int C, float* __restrict__ qnorm,
@@ -25,26 +50,34 @@ __global__ void __launch_bounds__(256) k_qstats(const T* __restrict__ Q, int C, 
   constexpr int E = D / 32;
   const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float part[E];
+  const int c0 = blk * kRowsPerBlock + warp * kRowsPerWarp;
+  float x[kRowsPerWarp][E];
+  load_rows<T, D>(Q, h, C, c0, x);
+  float part[E], ss[kRowsPerWarp];
 #pragma unroll
   for (int j = 0; j < E; ++j) part[j] = 0.f;
-  for (int r = warp; r < kRowsPerBlock; r += 8) {
-    const int c = blk * kRowsPerBlock + r;
-    if (c >= C) break;
-    const T* q = Q + ((size_t)h * C + c) * D;
-    float ss = 0.f;
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    ss[r] = 0.f;
 #pragma unroll
     for (int j = 0; j < E; ++j) {
-      float x = to_f32(q[lane + 32 * j]);
-      part[j] += x;
-      ss = fmaf(x, x, ss);
+      part[j] += x[r][j];
+      ss[r] = fmaf(x[r][j], x[r][j], ss[r]);
     }
-    ss = warp_sum(ss);
-    if (lane == 0) qnorm[(size_t)h * C + c] = sqrtf(ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
+  if (lane < kRowsPerWarp) {
+    float v = ss[0];
+#pragma unroll
+    for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? ss[r] : v;
+    if (c0 + lane < C) qnorm[(size_t)h * C + c0 + lane] = sqrtf(v);
   }
   __shared__ float sp[8][D];
 #pragma unroll
-  for (int j = 0; j < E; ++j) sp[warp][lane + 32 * j] = part[j];
+  for (int j = 0; j < E; ++j) sp[warp][lane * E + j] = part[j];
   __syncthreads();
   if (threadIdx.x < D) {
     float s = 0.f;
@@ -60,6 +93,9 @@ __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, co
   constexpr int E = D / 32;
   const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c0 = blk * kRowsPerBlock + warp * kRowsPerWarp;
+  float x[kRowsPerWarp][E];
+  load_rows<T, D>(Q, h, C, c0, x);                 // issued before the mean is ready
   __shared__ float M[D];
   __shared__ float mnorm;
   if (threadIdx.x < D) {
@@ -76,15 +112,26 @@ __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, co
     if (lane == 0) mnorm = fmaxf(sqrtf(ss), kNormEps);
   }
   __syncthreads();
-  for (int r = warp; r < kRowsPerBlock; r += 8) {
-    const int c = blk * kRowsPerBlock + r;
-    if (c >= C) break;
-    const T* q = Q + ((size_t)h * C + c) * D;
-    float dot = 0.f;
+  float m[E];
 #pragma unroll
-    for (int j = 0; j < E; ++j) dot = fmaf(to_f32(q[lane + 32 * j]), M[lane + 32 * j], dot);
-    dot = warp_sum(dot);
-    if (lane == 0) qcos[(size_t)h * C + c] = dot / (fmaxf(qnorm[(size_t)h * C + c], kNormEps) * mnorm);
+  for (int j = 0; j < E; ++j) m[j] = M[lane * E + j];
+  float dot[kRowsPerWarp];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    dot[r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < E; ++j) dot[r] = fmaf(x[r][j], m[j], dot[r]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+  if (lane < kRowsPerWarp && c0 + lane < C) {
+    float v = dot[0];
+#pragma unroll
+    for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? dot[r] : v;
+    const int c = c0 + lane;
+    qcos[(size_t)h * C + c] = v / (fmaxf(qnorm[(size_t)h * C + c], kNormEps) * mnorm);
   }
 }
 
