@@ -123,6 +123,23 @@ int quoka_workspace_size(const quoka_shape* shape, int N_q, int B, const quoka_p
 int quoka_select_queries(const quoka_shape* shape, const void* Q, int N_q, const quoka_params* params,
                          int32_t* q_idx, void* ws, size_t ws_bytes, void* stream);
 
+/* quoka_select_queries without a workspace (the paper has no counterpart: this
+ * is a calling convention, not a step of the method).  For callers that
+ * cannot provide device scratch memory at all -- inference-engine plugins
+ * whose enqueue path may not allocate, and runtimes that plan every byte of
+ * device memory ahead of time -- the scratch of the query-selection kernels
+ * lives in a 4 MiB device array owned by the library, which every GPU that
+ * loads libquoka.so holds until the process exits.  Same arguments, layout and
+ * results as quoka_select_queries, minus (ws, ws_bytes).
+ * Limit: 8*H_q*C + 4*H_q*ceil(C/64)*d bytes (each region rounded up to 256)
+ * must fit in 4 MiB, e.g. 64 heads x 4096 queries at d = 128; larger problems
+ * return QUOKA_ERR_UNSUPPORTED.  The first call on a device looks up the
+ * array's device address (make that first call before any stream capture).
+ * Every call shares the one array: calls that overlap on the GPU (different
+ * streams or host threads) race and must be serialised by the caller. */
+int quoka_select_queries_noalloc(const quoka_shape* shape, const void* Q, int N_q, const quoka_params* params,
+                                 int32_t* q_idx, void* stream);
+
 /* Cosine scoring plus aggregation ([P1] "Scoring via Cosine Similarity",
  * "Aggregation Across Queries and KV Groups"; [P2] "Letting those queries
  * score the history", "Why take the maximum").  For every KV group g and

@@ -49,6 +49,8 @@ _SIG = {
                                             ctypes.POINTER(Params), ctypes.POINTER(ctypes.c_size_t)]),
     "quoka_select_queries": (ctypes.c_int, [ctypes.POINTER(Shape), _P, ctypes.c_int, ctypes.POINTER(Params), _P,
                                             _P, ctypes.c_size_t, _P]),
+    "quoka_select_queries_noalloc": (ctypes.c_int, [ctypes.POINTER(Shape), _P, ctypes.c_int, ctypes.POINTER(Params),
+                                                    _P, _P]),
     "quoka_score_keys": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, ctypes.c_int, _P, ctypes.POINTER(Params), _P,
                                         _P, ctypes.c_size_t, _P]),
     "quoka_topk": (ctypes.c_int, [ctypes.POINTER(Shape), _P, ctypes.c_int, _P, _P, ctypes.c_size_t, _P]),
@@ -148,6 +150,11 @@ def status_string(status: int) -> str:
 def quoka_select_queries(shape, Q, N_q, params, q_idx, ws, stream=None):
     _check("quoka_select_queries", load().quoka_select_queries(
         ctypes.byref(shape), _ptr(Q), N_q, ctypes.byref(params), _ptr(q_idx), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def quoka_select_queries_noalloc(shape, Q, N_q, params, q_idx, stream=None):
+    _check("quoka_select_queries_noalloc", load().quoka_select_queries_noalloc(
+        ctypes.byref(shape), _ptr(Q), N_q, ctypes.byref(params), _ptr(q_idx), _stream(stream)))
 
 
 def quoka_score_keys(shape, Q, q_idx, N_q, K_hist, params, scores, ws, stream=None):
