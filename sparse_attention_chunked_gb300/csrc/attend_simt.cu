@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(128) k_attend_simt(const T* __restrict__ Q, co
                                                      const T* __restrict__ Kc, const T* __restrict__ Vc, int C,
                                                      int G, float scale_log2, T* __restrict__ O,
                                                      float* __restrict__ lse) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int E = D / 32;
   constexpr int RPW = kAttRows / 4;   // rows per warp
   extern __shared__ float smem[];
@@ -113,10 +115,10 @@ static cudaError_t attend_impl(const void* Q, const void* Kh, const void* Vh, in
   if (e != cudaSuccess) return e;
   dim3 grid((C + kAttRows - 1) / kAttRows, H_q);
   const float scale_log2 = scale * 1.4426950408889634f;
-  k_attend_simt<T, D><<<grid, 128, smem, st>>>((const T*)Q, (const T*)Kh, (const T*)Vh, h_stride, n_hist,
-                                                (const T*)Kc, (const T*)Vc, C, G, scale_log2, (T*)O, lse);
+  e = launch_pdl(k_attend_simt<T, D>, grid, dim3(128), smem, st, (const T*)Q, (const T*)Kh, (const T*)Vh, h_stride,
+                 n_hist, (const T*)Kc, (const T*)Vc, C, G, scale_log2, (T*)O, lse);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_attend_simt(int dtype, int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,

@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     tc::tmem_alloc(&sm->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
+  pdl_launch_dependents();
+  pdl_wait();                                   // inputs may come from the previous kernel
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -402,12 +404,14 @@ cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* V
   const float scale_log2 = scale * 1.4426950408889634f;
   if (d == 64) {
     if ((e = ensure_smem((const void*)k_attend_tc<64>, smem)) != cudaSuccess) return e;
-    k_attend_tc<64><<<grid, kAttThreads, smem, st>>>(qmap, khmap, vhmap, kcmap, vcmap, n_hist, C, G, scale_log2,
-                                                     (__nv_bfloat16*)O, lse, hdr);
+    if ((e = launch_pdl(k_attend_tc<64>, grid, dim3(kAttThreads), smem, st, qmap, khmap, vhmap, kcmap, vcmap, n_hist, C,
+                        G, scale_log2, (__nv_bfloat16*)O, lse, hdr)) != cudaSuccess)
+      return e;
   } else {
     if ((e = ensure_smem((const void*)k_attend_tc<128>, smem)) != cudaSuccess) return e;
-    k_attend_tc<128><<<grid, kAttThreads, smem, st>>>(qmap, khmap, vhmap, kcmap, vcmap, n_hist, C, G, scale_log2,
-                                                      (__nv_bfloat16*)O, lse, hdr);
+    if ((e = launch_pdl(k_attend_tc<128>, grid, dim3(kAttThreads), smem, st, qmap, khmap, vhmap, kcmap, vcmap, n_hist,
+                        C, G, scale_log2, (__nv_bfloat16*)O, lse, hdr)) != cudaSuccess)
+      return e;
   }
   count_launches(1);
   return cudaGetLastError();

@@ -21,6 +21,15 @@ __device__ __forceinline__ void record_error(WsHeader* hdr, unsigned int code, u
   if (hdr != nullptr && atomicCAS(&hdr->err, 0u, code) == 0u) hdr->where = where;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation: it lets the next kernel in the stream
+// start launching right away and, before touching global memory, waits until
+// the kernels before it have completed (a no-op without the launch attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 

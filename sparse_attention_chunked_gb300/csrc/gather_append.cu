@@ -12,6 +12,8 @@ namespace quoka {
 __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restrict__ V, int64_t head_stride_vec,
                               const int32_t* __restrict__ sel, int H_kv, int B_e, int vec_per_row,
                               uint4* __restrict__ Ks, uint4* __restrict__ Vs) {
+  pdl_launch_dependents();
+  pdl_wait();
   const size_t per_mat = (size_t)H_kv * B_e * vec_per_row;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * per_mat;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -30,6 +32,8 @@ __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restri
 __global__ void k_append_rows(uint4* __restrict__ K, uint4* __restrict__ V, int64_t head_stride_vec, int T_len,
                               const uint4* __restrict__ Kc, const uint4* __restrict__ Vc, int H_kv, int C,
                               int vec_per_row) {
+  pdl_launch_dependents();
+  pdl_wait();
   const size_t per_mat = (size_t)H_kv * C * vec_per_row;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * per_mat;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -53,20 +57,20 @@ cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, in
   if (B_e == 0) return cudaSuccess;
   const int vpr = d * elt_bytes / 16;
   const int64_t hsv = head_stride * elt_bytes / 16;
-  k_gather_rows<<<grid_for((size_t)2 * H_kv * B_e * vpr), 256, 0, st>>>(
-      (const uint4*)K, (const uint4*)V, hsv, sel, H_kv, B_e, vpr, (uint4*)Ks, (uint4*)Vs);
+  cudaError_t e = launch_pdl(k_gather_rows, dim3(grid_for((size_t)2 * H_kv * B_e * vpr)), dim3(256), 0, st,
+                             (const uint4*)K, (const uint4*)V, hsv, sel, H_kv, B_e, vpr, (uint4*)Ks, (uint4*)Vs);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_append(int elt_bytes, int d, void* K, void* V, int64_t head_stride, int T_len, const void* Kc,
                           const void* Vc, int H_kv, int C, cudaStream_t st) {
   const int vpr = d * elt_bytes / 16;
   const int64_t hsv = head_stride * elt_bytes / 16;
-  k_append_rows<<<grid_for((size_t)2 * H_kv * C * vpr), 256, 0, st>>>(
-      (uint4*)K, (uint4*)V, hsv, T_len, (const uint4*)Kc, (const uint4*)Vc, H_kv, C, vpr);
+  cudaError_t e = launch_pdl(k_append_rows, dim3(grid_for((size_t)2 * H_kv * C * vpr)), dim3(256), 0, st, (uint4*)K,
+                             (uint4*)V, hsv, T_len, (const uint4*)Kc, (const uint4*)Vc, H_kv, C, vpr);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace quoka

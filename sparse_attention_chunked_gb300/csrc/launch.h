@@ -9,8 +9,28 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 namespace quoka {
+
+// Launches `kernel` on `st` with programmatic stream serialisation, so its
+// launch and prologue overlap the tail of the previous kernel (each kernel
+// waits with griddepcontrol.wait before reading what that kernel wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Kernels enqueued by this library in this process (read by quoka_launch_count).
 extern std::atomic<unsigned long long> g_launch_count;

@@ -47,6 +47,8 @@ __device__ __forceinline__ void load_rows(const T* __restrict__ Q, int h, int C,
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_qstats(const T* __restrict__ Q, int C, float* __restrict__ qnorm,
                                                 float* __restrict__ qpart) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int E = D / 32;
   const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(256) k_qstats(const T* __restrict__ Q, int C, 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, const float* __restrict__ qpart,
                                               const float* __restrict__ qnorm, float* __restrict__ qcos) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int E = D / 32;
   const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -137,6 +141,8 @@ __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, co
 
 __global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos, int C, int G_avg, int n_sel,
                                                   int32_t* __restrict__ q_idx) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ __align__(16) uint32_t keys_s[];
   __shared__ RadixSelectShared rs;
   const int row = blockIdx.x;
@@ -160,11 +166,14 @@ static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel
                              float* qnorm, float* qpart, float* qcos, cudaStream_t st) {
   const int nblk = (C + kRowsPerBlock - 1) / kRowsPerBlock;
   dim3 grid(nblk, H_q);
-  k_qstats<T, D><<<grid, 256, 0, st>>>((const T*)Q, C, qnorm, qpart);
-  k_qcos<T, D><<<grid, 256, 0, st>>>((const T*)Q, C, qpart, qnorm, qcos);
+  cudaError_t e = launch_pdl(k_qstats<T, D>, grid, dim3(256), 0, st, (const T*)Q, C, qnorm, qpart);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(k_qcos<T, D>, grid, dim3(256), 0, st, (const T*)Q, C, (const float*)qpart, (const float*)qnorm, qcos);
+  if (e != cudaSuccess) return e;
   const size_t smem = (size_t)((C + 3) & ~3) * sizeof(uint32_t);   // C <= 8192: at most 32 KB
   const int rows = H_q / G_avg;
-  k_qselect<<<rows, 256, smem, st>>>(qcos, C, G_avg, n_sel, q_idx);
+  e = launch_pdl(k_qselect, dim3(rows), dim3(256), smem, st, (const float*)qcos, C, G_avg, n_sel, q_idx);
+  if (e != cudaSuccess) return e;
   count_launches(3);
   return cudaGetLastError();
 }

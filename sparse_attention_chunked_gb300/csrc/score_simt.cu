@@ -22,6 +22,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, const int32_t* __restrict__ q_idx,
                                                       int C, int G, int n, int mode, int R, float* __restrict__ op_f32,
                                                       __nv_bfloat16* __restrict__ op_bf, float* __restrict__ op_scale) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int E = D / 32;
   const int g = blockIdx.y, r = blockIdx.x, N_pad = gridDim.x, lane = threadIdx.x;
   const int passes = mode == 1 ? 1 : 2;
@@ -96,6 +98,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int64_t head_stride, int T_len,
                                                     const float* __restrict__ op_f32, int R,
                                                     float* __restrict__ scores) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int g = blockIdx.y;
   const int t = blockIdx.x * 128 + threadIdx.x;
   __shared__ float rows[32][D];
@@ -135,38 +139,40 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
                                  cudaStream_t st) {
   const int R = mode == 1 ? G * n : n;
   dim3 grid(op_bf != nullptr ? N_pad : R, H_kv);
+  cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      k_build_operand<__nv_bfloat16, 64><<<grid, 32, 0, st>>>((const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
+      e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
     else
-      k_build_operand<__nv_bfloat16, 128><<<grid, 32, 0, st>>>((const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
+      e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
   } else {
     if (d == 64)
-      k_build_operand<float, 64><<<grid, 32, 0, st>>>((const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
+      e = launch_pdl(k_build_operand<float, 64>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
     else
-      k_build_operand<float, 128><<<grid, 32, 0, st>>>((const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
+      e = launch_pdl(k_build_operand<float, 128>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
   }
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
                               const float* op_f32, int R, float* scores, cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
   dim3 grid((T_len + 127) / 128, H_kv);
+  cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      k_score_simt<__nv_bfloat16, 64><<<grid, 128, 0, st>>>((const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, scores);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, scores);
     else
-      k_score_simt<__nv_bfloat16, 128><<<grid, 128, 0, st>>>((const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, scores);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, scores);
   } else {
     if (d == 64)
-      k_score_simt<float, 64><<<grid, 128, 0, st>>>((const float*)K, head_stride, T_len, op_f32, R, scores);
+      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, scores);
     else
-      k_score_simt<float, 128><<<grid, 128, 0, st>>>((const float*)K, head_stride, T_len, op_f32, R, scores);
+      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, scores);
   }
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace quoka

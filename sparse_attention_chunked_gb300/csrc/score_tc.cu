@@ -15,11 +15,11 @@
 // TMEM columns (two MMA passes, scale 1).  |k_t| comes from the same shared
 // memory tile, in fp32.
 //
-// Warp roles (320 threads): warp 0 issues TMA loads (operand once, then a ring
-// of key tiles), warp 1 owns TMEM and issues the MMAs, warps 2-9 are the
-// epilogue: two warps per TMEM lane quadrant, each reducing half of the
-// scoring columns and half of the key's squared norm; the halves meet in
-// shared memory behind a named barrier of the 256 epilogue threads.  Every wait is bounded; on a timeout the
+// Warp roles (576 threads): warp 0 issues TMA loads (operand once, then a ring
+// of key tiles), warp 1 owns TMEM and issues the MMAs, warps 2-17 are the
+// epilogue: four warps per TMEM lane quadrant, each reducing a quarter of the
+// scoring rows and a quarter of the key's squared norm; the quarters meet in
+// shared memory behind a named barrier of the 512 epilogue threads.  Every wait is bounded; on a timeout the
 // CTA records QUOKA_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees
 // TMEM and exits.
 #include "launch.h"
@@ -30,8 +30,9 @@ namespace quoka {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kScoreThreads = 320;
-constexpr int kEpiWarps = 8;
+constexpr int kScoreThreads = 576;
+constexpr int kEpiWarps = 16;
+constexpr int kEpiParts = 4;
 
 // Rows of one operand TMA box: it must divide N_pad (<= 512) and be <= 256.
 __host__ __device__ inline int op_box_rows(int N_pad) { return N_pad <= 256 ? N_pad : N_pad / 2; }
@@ -45,8 +46,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 struct ScoreSmem {
-  float red_max[2][2][128];   // [tile parity][column half][key]
-  float red_ss[2][2][128];
+  float red_max[2][kEpiParts][128];   // [tile parity][row quarter][key]
+  float red_ss[2][kEpiParts][128];
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t acc_full[2];
@@ -88,7 +89,7 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
 // that one MMA with N = NT (in chunks of 256) covers every pass; pass p of row
 // r is B row p * N_pad + r and lands in TMEM column p * N_pad + r.
 template <int D>
-__global__ void __launch_bounds__(kScoreThreads, 1)
+__global__ void __maxnreg__(96)
     k_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
                const float* __restrict__ op_scale, int T_len, int R, int N_pad, int passes, int nst, int nacc,
                uint32_t tmem_cols, float* __restrict__ scores, WsHeader* hdr) {
@@ -125,11 +126,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     sm->abort = 0;
     tc::fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < N_pad; i += blockDim.x) scale_s[i] = op_scale[(size_t)g * N_pad + i];
   if (warp == 1) {
     tc::tmem_alloc(&sm->tmem_base, tmem_cols);
     tc::tmem_relinquish();
   }
+  pdl_launch_dependents();
+  pdl_wait();                                   // the operand and its scales come from the previous kernel
+  for (int i = threadIdx.x; i < N_pad; i += blockDim.x) scale_s[i] = op_scale[(size_t)g * N_pad + i];
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -192,13 +195,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc::mbar_drain(&sm->drain, 0);
     }
   } else {
-    // ------------------------------------------------------------ epilogue: one key per thread pair
+    // ------------------------------------------------------------ epilogue: one key per four threads
     const int quad = warp & 3;                      // TMEM lane quadrant this warp may access
-    const int part = (warp - 2) >> 2;               // which half of the rows / of d
+    const int part = (warp - 2) >> 2;               // which quarter of the rows / of d
     const int row = quad * 32 + lane;               // key within the tile
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    const int half_rows = ((N_pad >> 1) + 31) & ~31;
-    const int r_begin = part * half_rows, r_end = min(R, part == 0 ? half_rows : N_pad);
+    const int quarter = ((N_pad >> 2) + 31) & ~31;
+    const int r_begin = min(N_pad, part * quarter), r_end = min(R, part == kEpiParts - 1 ? N_pad : (part + 1) * quarter);
     const bool mean_mode = passes == 2;
     bool alive = true;                              // false once a wait gave up (warp-uniform)
     for (int it = 0; it < ntiles; ++it) {
@@ -206,15 +209,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (alive) alive = warp_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105);
       float ss = 0.f;
       if (alive) {
-        // |k|^2 over this part's 64-column halves of d; 16-byte chunk c of row r sits at c ^ (r & 7)
+        // |k|^2 over this part's quarter of d (16-byte chunks); chunk c of row r sits at c ^ (r & 7)
         const uint8_t* tile = ktiles + (size_t)s * kStageBytes;
         float ss0 = 0.f, ss1 = 0.f;
+        constexpr int kChunks = HALVES * 8 / kEpiParts;   // 16-byte chunks of the row per part
 #pragma unroll
-        for (int hf = 0; hf < HALVES; ++hf) {
-          if ((hf & 1) != part) continue;
+        for (int cc = 0; cc < kChunks; ++cc) {
+          const int chunk = part * kChunks + cc, hf = chunk >> 3, c = chunk & 7;
           const uint8_t* rp = tile + hf * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          {
             const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & 7)) << 4));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -277,10 +280,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (lane == 0) tc::mbar_arrive(&sm->acc_empty[a]);
       sm->red_max[buf][part][row] = best;
       sm->red_ss[buf][part][row] = ss;
-      asm volatile("bar.sync 1, 256;" ::: "memory");   // the 8 epilogue warps
+      asm volatile("bar.sync 1, 512;" ::: "memory");   // the 16 epilogue warps
       if (part == 0 && alive) {
-        const float mx = fmaxf(sm->red_max[buf][0][row], sm->red_max[buf][1][row]);
-        const float rk = 1.0f / fmaxf(sqrtf(sm->red_ss[buf][0][row] + sm->red_ss[buf][1][row]), kNormEps);
+        const float mx = fmaxf(fmaxf(sm->red_max[buf][0][row], sm->red_max[buf][1][row]),
+                               fmaxf(sm->red_max[buf][2][row], sm->red_max[buf][3][row]));
+        const float rk = 1.0f / fmaxf(sqrtf((sm->red_ss[buf][0][row] + sm->red_ss[buf][1][row]) +
+                                            (sm->red_ss[buf][2][row] + sm->red_ss[buf][3][row])), kNormEps);
         const int t = (tile0 + it) * kTileKeys + row;
         if (t < T_len) scores[(size_t)g * T_len + t] = mx * rk;
       }
@@ -334,13 +339,15 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
   if (d == 64) {
     e = ensure_smem((const void*)k_score_tc<64>, smem);
     if (e != cudaSuccess) return e;
-    k_score_tc<64><<<grid, kScoreThreads, smem, st>>>(kmap, omap, op_scale, T_len, R, N_pad, passes, nst, nacc, cols,
-                                                      scores, hdr);
+    e = launch_pdl(k_score_tc<64>, grid, dim3(kScoreThreads), smem, st, kmap, omap, op_scale, T_len, R, N_pad, passes,
+                   nst, nacc, cols, scores, hdr);
+    if (e != cudaSuccess) return e;
   } else {
     e = ensure_smem((const void*)k_score_tc<128>, smem);
     if (e != cudaSuccess) return e;
-    k_score_tc<128><<<grid, kScoreThreads, smem, st>>>(kmap, omap, op_scale, T_len, R, N_pad, passes, nst, nacc,
-                                                       cols, scores, hdr);
+    e = launch_pdl(k_score_tc<128>, grid, dim3(kScoreThreads), smem, st, kmap, omap, op_scale, T_len, R, N_pad, passes,
+                   nst, nacc, cols, scores, hdr);
+    if (e != cudaSuccess) return e;
   }
   count_launches(1);
   return cudaGetLastError();

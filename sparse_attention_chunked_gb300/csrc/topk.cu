@@ -38,6 +38,8 @@ struct TopkClusterShared {
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
     k_topk_cluster(const float* __restrict__ scores, int T_len, int B_e, int32_t* __restrict__ sel, int per,
                    int cache) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ __align__(16) uint32_t keys_s[];
   __shared__ TopkClusterShared sm;
   cg::cluster_group cluster = cg::this_cluster();
@@ -133,6 +135,8 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
 }
 
 __global__ void k_iota_rows(int32_t* __restrict__ sel, int rows, int n) {
+  pdl_launch_dependents();
+  pdl_wait();
   const size_t total = (size_t)rows * n;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x)
     sel[i] = (int32_t)(i % n);
@@ -144,18 +148,19 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
     const size_t total = (size_t)H_kv * T_len;
     const size_t nb = (total + 255) / 256;
     const int blocks = (int)(nb < 4096 ? (nb == 0 ? 1 : nb) : 4096);
-    k_iota_rows<<<blocks, 256, 0, st>>>(sel, H_kv, T_len);
+    cudaError_t e = launch_pdl(k_iota_rows, dim3(blocks), dim3(256), 0, st, sel, H_kv, T_len);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
   }
   const int per = ((T_len + kTopkCluster - 1) / kTopkCluster + 3) & ~3;
   const int cache = per <= kTopkSliceCap ? 1 : 0;
   const size_t smem = cache ? (size_t)per * 4 + 16 : 0;
   cudaError_t e = ensure_smem((const void*)k_topk_cluster, smem);
   if (e != cudaSuccess) return e;
-  k_topk_cluster<<<dim3(kTopkCluster, H_kv), kTopkThreads, smem, st>>>(scores, T_len, B_e, sel, per, cache);
+  e = launch_pdl(k_topk_cluster, dim3(kTopkCluster, H_kv), dim3(kTopkThreads), smem, st, scores, T_len, B_e, sel, per,
+                 cache);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace quoka
