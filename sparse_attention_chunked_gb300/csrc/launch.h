@@ -42,21 +42,18 @@ cudaError_t launch_select_queries(int dtype, int d, const void* Q, int H_q, int 
 // op_bf may be NULL (CUDA-core scoring only needs op_f32); otherwise N_pad
 // (a multiple of 16, >= the row count) rows per pass are written.
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
-                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
-                                 cudaStream_t st);
+                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, cudaStream_t st);
 
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
                               const float* op_f32, int R, float* scores, cudaStream_t st);
 
-// Tensor-core scoring (bf16 keys).  op_bf / op_scale as written by
-// launch_build_operand with N_pad = score_tc_pad_rows(R); passes = 1 (max
-// pooling) or 2 (mean pooling hi/lo).
+// Tensor-core scoring (bf16 keys).  op_bf (hi/lo rows) as written by
+// launch_build_operand with N_pad = score_tc_pad_rows(R).
 int score_tc_pad_rows(int R);
-size_t score_tc_smem(int d, int N_pad, int passes, int nst);
+size_t score_tc_smem(int d, int N_pad, int nst);
 struct WsHeader;
 cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
-                            const float* op_scale, int R, int passes, float* scores, WsHeader* hdr, int num_sms,
-                            cudaStream_t st);
+                            int R, float* scores, WsHeader* hdr, int num_sms, cudaStream_t st);
 
 // Raises `func`'s dynamic shared-memory limit to `bytes` on the current device (cached).
 cudaError_t ensure_smem(const void* func, size_t bytes);

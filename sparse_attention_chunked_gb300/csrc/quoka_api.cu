@@ -72,13 +72,12 @@ int num_sms() {
 }
 
 // Whether the scoring stage can run on the tensor cores: bf16 keys, at most
-// 512 operand rows (the TMEM width; mean pooling needs its rows twice, hi and
-// lo) and an operand that fits shared memory next to two key stages.
+// 512 scoring rows (the TMEM width) and an operand (every row twice, hi and
+// lo) that fits shared memory next to two key stages.
 bool score_tc_fits(const quoka_shape* s, int N_q, int gqa) {
   if (s->dtype != QUOKA_DTYPE_BF16) return false;
   const int N_pad = score_tc_pad_rows(score_rows(s, N_q, gqa));
-  const int passes = gqa == QUOKA_GQA_MAX ? 1 : 2;
-  return passes * N_pad <= 512 && score_tc_smem(s->d, N_pad, passes, 2) <= 227 * 1024;
+  return N_pad <= 512 && score_tc_smem(s->d, N_pad, 2) <= 227 * 1024;
 }
 
 // Which kernels run (stage 0 = scoring, 1 = attention).  Tensor-core kernels are bf16 only.
@@ -92,7 +91,7 @@ bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage, int N_q 
 //   [header][select scratch][score scratch][chunk intermediates]
 struct Layout {
   size_t qnorm, qpart, qcos, select_end;
-  size_t op_f32, op_bf, op_scale, score_end;
+  size_t op_f32, op_bf, score_end;
   size_t q_idx, scores, sel, ksel, vsel, total;
 };
 
@@ -109,7 +108,6 @@ Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa) {
   const size_t N_pad = (size_t)score_tc_pad_rows((int)R);
   L.op_f32 = o;   o = align_up(o + H_kv * R * d * 4);
   L.op_bf = o;    o = align_up(o + H_kv * 2 * N_pad * d * 2);
-  L.op_scale = o; o = align_up(o + H_kv * N_pad * 4);
   L.score_end = o;
   const size_t n = (size_t)n_sel_of(s, N_q > 0 ? N_q : 1);
   const size_t B_e = (size_t)(B < s->T ? B : s->T);
@@ -162,11 +160,10 @@ int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, 
   const bool tc = use_tensor_cores(p, s, 0, n);
   if (p.engine == QUOKA_ENGINE_TENSOR && !tc) return QUOKA_ERR_UNSUPPORTED;
   QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, mode, N_pad, at<float>(ws, L.op_f32),
-                                  tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr, at<float>(ws, L.op_scale), st));
+                                  tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr, st));
   if (tc)
     return cuda_status(launch_score_tc(s->d, K_hist, head_stride(s), s->H_kv, s->T, at<__nv_bfloat16>(ws, L.op_bf),
-                                       at<float>(ws, L.op_scale), R, mode == 1 ? 1 : 2, scores, at<WsHeader>(ws, 0),
-                                       num_sms(), st));
+                                       R, scores, at<WsHeader>(ws, 0), num_sms(), st));
   return cuda_status(launch_score_simt(s->dtype, s->d, K_hist, head_stride(s), s->H_kv, s->T,
                                        at<float>(ws, L.op_f32), R, scores, st));
 }

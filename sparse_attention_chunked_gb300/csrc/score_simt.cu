@@ -12,28 +12,27 @@ namespace quoka {
 // zero in the tensor-core copy and never read by the epilogue).  Row r of
 // KV group g:
 //   MAX : r = k * n + i  -> query head h = g*G + k, position q_idx[h, i];
-//         fp32 row q / |q|; tensor-core copy: the raw row and scale 1/|q|.
+//         fp32 row q / |q|.
 //   MEAN: r = i          -> position q_idx[g, i];
 //         fp32 row (1/G) sum_k q_k / |q_k| over the group's heads (not
-//         re-normalised); tensor-core copy: hi = bf16(row) in pass 0 and
-//         lo = bf16(row - hi) in pass 1, scale 1.
-// Layouts: op_f32 [H_kv, R, D]; op_bf [H_kv, passes, N_pad, D]; op_scale [H_kv, N_pad].
+//         re-normalised).
+// Tensor-core copy of either: hi = bf16(row) in pass 0 and lo = bf16(row - hi)
+// in pass 1 (hi + lo carries the fp32 row to about 2^-16 relative).
+// Layouts: op_f32 [H_kv, R, D]; op_bf [H_kv, 2, N_pad, D].
 template <typename T, int D>
 __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, const int32_t* __restrict__ q_idx,
                                                       int C, int G, int n, int mode, int R, float* __restrict__ op_f32,
-                                                      __nv_bfloat16* __restrict__ op_bf, float* __restrict__ op_scale) {
+                                                      __nv_bfloat16* __restrict__ op_bf) {
   pdl_launch_dependents();
   pdl_wait();
   constexpr int E = D / 32;
   const int g = blockIdx.y, r = blockIdx.x, N_pad = gridDim.x, lane = threadIdx.x;
-  const int passes = mode == 1 ? 1 : 2;
   if (r >= R) {   // padding row of the tensor-core operand
     if (op_bf != nullptr) {
-      for (int p = 0; p < passes; ++p)
+      for (int p = 0; p < 2; ++p)
 #pragma unroll
         for (int j = 0; j < E; ++j)
-          op_bf[(((size_t)g * passes + p) * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(0.f);
-      if (lane == 0) op_scale[(size_t)g * N_pad + r] = 0.f;
+          op_bf[(((size_t)g * 2 + p) * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(0.f);
     }
     return;
   }
@@ -52,11 +51,6 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
     const float inv = 1.0f / fmaxf(sqrtf(ss), kNormEps);
 #pragma unroll
     for (int j = 0; j < E; ++j) acc[j] = x[j] * inv;
-    if (op_bf != nullptr) {
-#pragma unroll
-      for (int j = 0; j < E; ++j) op_bf[((size_t)g * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
-      if (lane == 0) op_scale[(size_t)g * N_pad + r] = inv;
-    }
   } else {  // MEAN (pre-aggregation)
     const int c = q_idx[(size_t)g * n + r];
 #pragma unroll
@@ -77,15 +71,14 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
     const float invG = 1.0f / (float)G;
 #pragma unroll
     for (int j = 0; j < E; ++j) acc[j] *= invG;
-    if (op_bf != nullptr) {
+  }
+  if (op_bf != nullptr) {
 #pragma unroll
-      for (int j = 0; j < E; ++j) {
-        const __nv_bfloat16 hi = __float2bfloat16_rn(acc[j]);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(acc[j] - __bfloat162float(hi));
-        op_bf[(((size_t)g * 2 + 0) * N_pad + r) * D + lane + 32 * j] = hi;
-        op_bf[(((size_t)g * 2 + 1) * N_pad + r) * D + lane + 32 * j] = lo;
-      }
-      if (lane == 0) op_scale[(size_t)g * N_pad + r] = 1.0f;
+    for (int j = 0; j < E; ++j) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(acc[j]);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(acc[j] - __bfloat162float(hi));
+      op_bf[(((size_t)g * 2 + 0) * N_pad + r) * D + lane + 32 * j] = hi;
+      op_bf[(((size_t)g * 2 + 1) * N_pad + r) * D + lane + 32 * j] = lo;
     }
   }
 #pragma unroll
@@ -135,21 +128,20 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
 }
 
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
-                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
-                                 cudaStream_t st) {
+                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, cudaStream_t st) {
   const int R = mode == 1 ? G * n : n;
   dim3 grid(op_bf != nullptr ? N_pad : R, H_kv);
   cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
+      e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf);
     else
-      e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
+      e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf);
   } else {
     if (d == 64)
-      e = launch_pdl(k_build_operand<float, 64>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
+      e = launch_pdl(k_build_operand<float, 64>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf);
     else
-      e = launch_pdl(k_build_operand<float, 128>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf, op_scale);
+      e = launch_pdl(k_build_operand<float, 128>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf);
   }
   count_launches(1);
   return e;
