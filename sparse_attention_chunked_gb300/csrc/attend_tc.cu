@@ -20,8 +20,12 @@
 // the running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8, so most blocks never touch O.
 //
-// Warps (320 threads): 0 = TMA producer, 1 = TMEM owner + MMA issuer,
-// 2-5 = softmax of slot 0, 6-9 = softmax of slot 1.  Every wait is bounded;
+// Warps (352 threads): 0 = TMA producer, 1 = TMEM owner + issuer of the S
+// MMAs, 2-5 = softmax of slot 0, 6-9 = softmax of slot 1, 10 = issuer of the
+// PV MMAs.  With one issuer, every wait between MMA groups (key tile, S
+// released, P written, value tile) leaves the tensor pipe with only the few
+// MMAs it has queued; two issuers each wait only for their own operands while
+// the other keeps the pipe fed.  Every wait is bounded;
 // on a timeout the CTA records QUOKA_ERR_TIMEOUT, drains what it has in
 // flight, frees TMEM and exits.
 #include "launch.h"
@@ -31,7 +35,7 @@ namespace quoka {
 
 namespace {
 
-constexpr int kAttThreads = 320;
+constexpr int kAttThreads = 352;
 constexpr int kKvStages = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPBytes = 128 * 128 * 2;   // one slot's P tile: 128 rows x 128 keys, bf16
@@ -45,7 +49,7 @@ struct AttSmem {
   uint64_t s_free[2];    // the softmax has loaded S_s (TMEM free for the next block)
   uint64_t p_full[2];    // P_s is in shared memory
   uint64_t o_done[2];    // PV_s of the current block has completed
-  uint64_t drain;
+  uint64_t drain[2];    // one per MMA issuer: its last MMAs have completed
   uint32_t tmem_base;
   int abort;
 };
@@ -137,7 +141,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       tc::mbar_init(&sm->p_full[s], 4);
       tc::mbar_init(&sm->o_done[s], 1);
     }
-    tc::mbar_init(&sm->drain, 1);
+    tc::mbar_init(&sm->drain[0], 1);
+    tc::mbar_init(&sm->drain[1], 1);
     sm->abort = 0;
     tc::fence_mbar_init();
   }
@@ -195,35 +200,37 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           tc::mbar_drain(&sm->kv_full[kk % kKvStages], (kk / kKvStages) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Order per block j: S_s(j+1) for each slot as soon as its softmax has
-    // loaded S_s(j); then PV_s(j) as soon as P_s(j) is in shared memory.
+  } else if (warp == 1 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // Ring items: K_0, then per block j: K_{j+1} (if any), V_j.  Warp 1 issues
+    // S_s(j+1) for each slot as soon as the key tile is in and the softmax has
+    // loaded S_s(j); warp 10 issues PV_s(j) as soon as the value tile is in and
+    // P_s(j) is in shared memory.  Each issuer releases the ring stages it read.
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
       const uint32_t kvb = tc::smem_u32(kv_s), qb0 = tc::smem_u32(q_s), pb0 = tc::smem_u32(p_s);
-      auto issue_s = [&](int s, int stage) {   // S_s = Q_s K^T, K in `stage`
-        const uint32_t qb = qb0 + s * kTileBytes, kb = kvb + stage * kTileBytes;
+      const bool s_issuer = warp == 1;
+      bool ok = true;
+      int item = 1;
+      if (s_issuer) {
+        auto issue_s = [&](int s, int stage) {   // S_s = Q_s K^T, K in `stage`
+          const uint32_t qb = qb0 + s * kTileBytes, kb = kvb + stage * kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int hf = kk >> 2, kin = kk & 3;
-          tc::mma_ss(tmem + s * kSlotCols, tc::sw128_desc(qb + hf * kHalfBytes + kin * 32, 16, 1024),
-                     tc::sw128_desc(kb + hf * kHalfBytes + kin * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int hf = kk >> 2, kin = kk & 3;
+            tc::mma_ss(tmem + s * kSlotCols, tc::sw128_desc(qb + hf * kHalfBytes + kin * 32, 16, 1024),
+                       tc::sw128_desc(kb + hf * kHalfBytes + kin * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&sm->s_full[s]);
+        };
+        ok = tc::mbar_wait(&sm->q_full, 0, abort, hdr, 0x202) && tc::mbar_wait(&sm->kv_full[0], 0, abort, hdr, 0x203);
+        tc::tc_fence_after();
+        if (ok) {
+          for (int s = 0; s < n_slots; ++s) issue_s(s, 0);
+          tc::mma_commit(&sm->kv_empty[0]);
         }
-        tc::mma_commit(&sm->s_full[s]);
-      };
-      bool ok = tc::mbar_wait(&sm->q_full, 0, abort, hdr, 0x202);
-      int item = 0;                              // ring item: K_0, then K_{j+1}, V_j per block
-      ok = ok && tc::mbar_wait(&sm->kv_full[0], 0, abort, hdr, 0x203);
-      tc::tc_fence_after();
-      if (ok) {
-        for (int s = 0; s < n_slots; ++s) issue_s(s, 0);
-        tc::mma_commit(&sm->kv_empty[0]);
-        item = 1;
-      }
-      for (int jb = 0; ok && jb < n_blocks; ++jb) {
-        if (jb + 1 < n_blocks) {
+        for (int jb = 0; ok && jb + 1 < n_blocks; ++jb) {
           const int st = item % kKvStages;
           if (!(ok = tc::mbar_wait(&sm->kv_full[st], (item / kKvStages) & 1, abort, hdr, 0x204))) break;
           for (int s = 0; s < n_slots; ++s) {
@@ -233,31 +240,36 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           }
           if (!ok) break;
           tc::mma_commit(&sm->kv_empty[st]);
+          item += 2;                             // K_{j+1}, then V_j (the other issuer's)
+        }
+      } else {
+        for (int jb = 0; ok && jb < n_blocks; ++jb) {
+          if (jb + 1 < n_blocks) ++item;         // K_{j+1} (the other issuer's)
+          const int sv = item % kKvStages;
+          if (!(ok = tc::mbar_wait(&sm->kv_full[sv], (item / kKvStages) & 1, abort, hdr, 0x206))) break;
+          const uint32_t vb = kvb + sv * kTileBytes;
+          for (int s = 0; s < n_slots; ++s) {
+            if (!(ok = tc::mbar_wait(&sm->p_full[s], jb & 1, abort, hdr, 0x207))) break;
+            tc::tc_fence_after();
+            const uint32_t pb = pb0 + s * kPBytes;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {      // 16 keys per MMA
+              const int hf = kk >> 2, kin = kk & 3;
+              tc::mma_ss(tmem + s * kSlotCols + 128, tc::sw128_desc(pb + hf * kHalfBytes + kin * 32, 16, 1024),
+                         tc::sw128_desc(vb + kk * 16 * 128, kHalfBytes, 1024), idesc_o, (jb > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(&sm->o_done[s]);
+          }
+          if (!ok) break;
+          tc::mma_commit(&sm->kv_empty[sv]);
           ++item;
         }
-        const int sv = item % kKvStages;
-        if (!(ok = tc::mbar_wait(&sm->kv_full[sv], (item / kKvStages) & 1, abort, hdr, 0x206))) break;
-        const uint32_t vb = kvb + sv * kTileBytes;
-        for (int s = 0; s < n_slots; ++s) {
-          if (!(ok = tc::mbar_wait(&sm->p_full[s], jb & 1, abort, hdr, 0x207))) break;
-          tc::tc_fence_after();
-          const uint32_t pb = pb0 + s * kPBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {      // 16 keys per MMA
-            const int hf = kk >> 2, kin = kk & 3;
-            tc::mma_ss(tmem + s * kSlotCols + 128, tc::sw128_desc(pb + hf * kHalfBytes + kin * 32, 16, 1024),
-                       tc::sw128_desc(vb + kk * 16 * 128, kHalfBytes, 1024), idesc_o, (jb > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc::mma_commit(&sm->o_done[s]);
-        }
-        if (!ok) break;
-        tc::mma_commit(&sm->kv_empty[sv]);
-        ++item;
       }
-      tc::mma_commit(&sm->drain);
-      tc::mbar_drain(&sm->drain, 0);
+      uint64_t* dr = &sm->drain[s_issuer ? 0 : 1];
+      tc::mma_commit(dr);                        // completes once every MMA this thread issued has finished
+      tc::mbar_drain(dr, 0);
     }
-  } else {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ softmax + epilogue, one row per thread
     const int s = (warp - 2) >> 2;                 // slot
     const int quad = warp & 3;                     // TMEM lane quadrant of this warp
