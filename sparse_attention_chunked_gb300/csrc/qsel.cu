@@ -2,18 +2,36 @@
 // Method: QUOKA paper summary, "Query Subselection"; QUOKA Explained, "Pick
 // the queries that disagree with the crowd".
 //
-// Three small launches (the stage reads Q about twice, ~2 x 17 MB at a
-// 32-head 2048-token chunk, and is not on the critical byte path):
+// A selection row is a query head, or a KV group with the cosine averaged
+// over the group's heads.  Its N_q smallest cosines are taken by an exact
+// radix select (keys = inverted order-mapped cosines, so ties go to the lower
+// position), written in position order.
+//
+// One launch, k_qselect_fused: a cluster of 8 CTAs per selection row, CTA r
+// owning the r-th eighth of the chunk positions.  Each CTA streams its rows
+// once for the row norms |q| and the column sums of its slice; the cluster
+// adds the slices' sums through distributed shared memory in rank order
+// (deterministic) for M_q; each CTA then computes cos(q, M_q) for its rows
+// (re-read, now from L2) into shared-memory keys.  For N_q <= 256 the
+// selection is a bitonic network (warp_topk.cuh): each warp keeps the top
+// L >= N_q of its keys, warp 0 merges its CTA's lists, CTA 0 merges the
+// cluster's lists through distributed shared memory and writes the winners'
+// positions in ascending order; larger N_q take the cluster radix select of
+// cluster_topk.cuh.  Shapes whose per-CTA shared memory would
+// not fit (very large groups) take three launches instead:
 //   k_qstats : per (head, 64-row block) row norms |q| and partial column sums
-//   k_qcos   : per (head, 64-row block) M_q from the partials (fixed order,
-//              deterministic), then cos(q, M_q) for the block's rows
-//   k_qselect: per selection row (query head, or KV group with the cosine
-//              averaged over the group's heads) an exact block radix select of
-//              the N_q smallest cosines (keys = inverted order-mapped cosines,
-//              so ties go to the lower position), written in position order.
+//   k_qcos   : per (head, 64-row block) M_q from the partials (fixed order),
+//              then cos(q, M_q) for the block's rows
+//   k_qselect: per selection row, a block radix select over the cosines.
 #include "common.cuh"
 #include "launch.h"
+#include <cooperative_groups.h>
+
+#include "cluster_topk.cuh"
 #include "radix_select.cuh"
+#include "warp_topk.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace quoka {
 
@@ -42,6 +60,227 @@ __device__ __forceinline__ void load_rows(const T* __restrict__ Q, int h, int C,
   for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
     for (int j = 0; j < E; ++j) x[r][j] = (c0 + r < C) ? to_f32(raw[r].v[j]) : 0.f;
+}
+
+// Rows c0 .. c0 + kRowsPerWarp - 1 of `base` (row stride D), zero at or beyond n.
+template <typename T, int D>
+__device__ __forceinline__ void load_rows_n(const T* __restrict__ base, int n, int c0, float (*x)[D / 32]) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  RowSlice<T, E> raw[kRowsPerWarp];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r)
+    if (c0 + r < n) raw[r] = *reinterpret_cast<const RowSlice<T, E>*>(base + (size_t)(c0 + r) * D + lane * E);
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+    for (int j = 0; j < E; ++j) x[r][j] = (c0 + r < n) ? to_f32(raw[r].v[j]) : 0.f;
+}
+
+constexpr int kSelCluster = 8;
+constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+
+// Offset (in floats) of the selection lists in k_qselect_fused's dynamic shared memory, and its size in bytes.
+__host__ __device__ inline size_t qselect_lists_offset(int per, int G_avg, int D) {
+  return ((size_t)per + (size_t)G_avg * per + 2 * (size_t)G_avg * D + (size_t)G_avg + 1) & ~(size_t)1;
+}
+static size_t qselect_fused_smem(int per, int G_avg, int D, int sel_p) {
+  return qselect_lists_offset(per, G_avg, D) * sizeof(float) + (size_t)(kSelWarps + 1) * 32 * sel_p * sizeof(uint64_t);
+}
+
+// Top n_sel (<= 32 * P) of the row's keys, split over the cluster as in
+// k_qselect_fused; out receives their positions in ascending order.  lists:
+// (kSelWarps + 1) * 32 * P composites of shared memory.  Ends with a cluster
+// barrier.
+template <int P>
+__device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* keys_s, int n, int t0, int n_sel,
+                                  uint64_t* lists, int32_t* __restrict__ out) {
+  constexpr int L = 32 * P;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t run[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) run[p] = 0ull;
+  for (int seg = warp; seg * L < n; seg += kSelWarps) {
+    uint64_t v[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const int i = seg * L + p * 32 + lane;
+      v[p] = i < n ? (((uint64_t)keys_s[i] << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)(t0 + i))) : 0ull;
+    }
+    warp_sort_desc<P>(v);
+    warp_merge_desc<P>(run, v);
+  }
+#pragma unroll
+  for (int p = 0; p < P; ++p) lists[warp * L + p * 32 + lane] = run[p];
+  __syncthreads();
+  if (warp == 0) {
+    for (int w = 1; w < kSelWarps; ++w) {
+      uint64_t b[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) b[p] = lists[w * L + p * 32 + lane];
+      warp_merge_desc<P>(run, b);
+    }
+#pragma unroll
+    for (int p = 0; p < P; ++p) lists[kSelWarps * L + p * 32 + lane] = run[p];   // this CTA's top L
+  }
+  cluster.sync();
+  if (cluster.block_rank() == 0 && warp == 0) {
+    for (int q = 1; q < kSelCluster; ++q) {
+      const uint64_t* rl = cluster.map_shared_rank(lists + kSelWarps * L, q);
+      uint64_t b[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) b[p] = rl[p * 32 + lane];
+      warp_merge_desc<P>(run, b);
+    }
+    // the first n_sel winners, by ascending position (0xFFFFFFFF - position, descending)
+#pragma unroll
+    for (int p = 0; p < P; ++p) run[p] = p * 32 + lane < n_sel ? (uint64_t)(uint32_t)run[p] : 0ull;
+    warp_sort_desc<P>(run);
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+      if (p * 32 + lane < n_sel) out[p * 32 + lane] = (int32_t)(0xFFFFFFFFu - (uint32_t)run[p]);
+  }
+  cluster.sync();   // every CTA's list stays alive until CTA 0 has read it
+}
+
+template <typename T, int D>
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
+    k_qselect_fused(const T* __restrict__ Q, int C, int G_avg, int n_sel, int per, int sel_p,
+                    int32_t* __restrict__ q_idx) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int E = D / 32;
+  extern __shared__ __align__(16) float dyn[];
+  uint32_t* keys_s = reinterpret_cast<uint32_t*>(dyn);   // [per], per % 4 == 0
+  float* norm_s = dyn + per;                             // [G_avg][per]
+  float* part_s = norm_s + (size_t)G_avg * per;          // [G_avg][D] column sums of this slice (read cluster-wide)
+  float* mean_s = part_s + (size_t)G_avg * D;            // [G_avg][D]
+  float* mnorm_s = mean_s + (size_t)G_avg * D;           // [G_avg]
+  uint64_t* lists = reinterpret_cast<uint64_t*>(dyn + qselect_lists_offset(per, G_avg, D));
+  __shared__ float sp[kSelWarps][D];
+  __shared__ ClusterTopkShared tk;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.y;
+  const int t0 = min(C, rank * per), n = min(C, t0 + per) - t0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // 1. row norms and column sums of this slice, head by head
+  for (int k = 0; k < G_avg; ++k) {
+    const T* base = Q + ((size_t)(row * G_avg + k) * C + t0) * D;
+    float part[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) part[j] = 0.f;
+    for (int c0 = warp * kRowsPerWarp; c0 < n; c0 += kSelWarps * kRowsPerWarp) {
+      float x[kRowsPerWarp][E];
+      load_rows_n<T, D>(base, n, c0, x);
+      float ss[kRowsPerWarp];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        ss[r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          part[j] += x[r][j];
+          ss[r] = fmaf(x[r][j], x[r][j], ss[r]);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
+      if (lane < kRowsPerWarp && c0 + lane < n) {
+        float v = ss[0];
+#pragma unroll
+        for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? ss[r] : v;
+        norm_s[(size_t)k * per + c0 + lane] = sqrtf(v);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < E; ++j) sp[warp][lane * E + j] = part[j];
+    __syncthreads();
+    for (int t = threadIdx.x; t < D; t += blockDim.x) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSelWarps; ++w) acc += sp[w][t];
+      part_s[(size_t)k * D + t] = acc;
+    }
+    __syncthreads();
+  }
+  cluster.sync();
+
+  // 2. M_q of every head of the row: the slices' sums in rank order, / C
+  for (int i = threadIdx.x; i < G_avg * D; i += blockDim.x) {
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < kSelCluster; ++q) acc += cluster.map_shared_rank(part_s, q)[i];
+    mean_s[i] = acc / (float)C;
+  }
+  __syncthreads();
+  for (int k = warp; k < G_avg; k += kSelWarps) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < E; ++j) ss = fmaf(mean_s[k * D + lane + 32 * j], mean_s[k * D + lane + 32 * j], ss);
+    ss = warp_sum(ss);
+    if (lane == 0) mnorm_s[k] = fmaxf(sqrtf(ss), kNormEps);
+  }
+  __syncthreads();
+
+  // 3. cos(q, M_q) (averaged over the row's heads) -> keys
+  for (int c0 = warp * kRowsPerWarp; c0 < n; c0 += kSelWarps * kRowsPerWarp) {
+    float u[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) u[r] = 0.f;
+    for (int k = 0; k < G_avg; ++k) {
+      float x[kRowsPerWarp][E];
+      load_rows_n<T, D>(Q + ((size_t)(row * G_avg + k) * C + t0) * D, n, c0, x);
+      float m[E];
+#pragma unroll
+      for (int j = 0; j < E; ++j) m[j] = mean_s[k * D + lane * E + j];
+      float dot[kRowsPerWarp];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        dot[r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < E; ++j) dot[r] = fmaf(x[r][j], m[j], dot[r]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+      const float mn = mnorm_s[k];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r)
+        if (c0 + r < n) u[r] += dot[r] / (fmaxf(norm_s[(size_t)k * per + c0 + r], kNormEps) * mn);
+    }
+    if (lane < kRowsPerWarp && c0 + lane < n) {
+      float v = u[0];
+#pragma unroll
+      for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? u[r] : v;
+      if (G_avg > 1) v = v / (float)G_avg;
+      keys_s[c0 + lane] = ~order_key(v);   // the largest key is the smallest cosine
+    }
+  }
+  __syncthreads();
+
+  // 4. the n_sel least similar positions of the row
+  int32_t* out = q_idx + (size_t)row * n_sel;
+  if (n_sel >= C) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) out[t0 + i] = t0 + i;
+    cluster.sync();   // keep part_s alive until every CTA has read it
+    return;
+  }
+  switch (sel_p) {
+    case 1: cluster_warp_topk<1>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 2: cluster_warp_topk<2>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 4: cluster_warp_topk<4>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 8: cluster_warp_topk<8>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    default: {
+      auto key_at = [&](int i) -> uint32_t { return keys_s[i]; };
+      cluster_radix_topk<kSelCluster>(cluster, true, reinterpret_cast<const uint4*>(keys_s), key_at, n, t0, n_sel, out,
+                                      tk);
+    }
+  }
 }
 
 template <typename T, int D>
@@ -164,6 +403,19 @@ __global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos,
 template <typename T, int D>
 static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel, int32_t* q_idx,
                              float* qnorm, float* qpart, float* qcos, cudaStream_t st) {
+  const int rows = H_q / G_avg;
+  const int per = ((C + kSelCluster - 1) / kSelCluster + 3) & ~3;
+  // the network's list length L = 32 * sel_p >= n_sel (0: radix select)
+  const int sel_p = n_sel <= 32 ? 1 : n_sel <= 64 ? 2 : n_sel <= 128 ? 4 : n_sel <= 256 ? 8 : 0;
+  const size_t fsmem = qselect_fused_smem(per, G_avg, D, sel_p);
+  if (fsmem <= 160 * 1024) {
+    cudaError_t e = ensure_smem((const void*)k_qselect_fused<T, D>, fsmem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(k_qselect_fused<T, D>, dim3(kSelCluster, rows), dim3(kSelThreads), fsmem, st, (const T*)Q, C, G_avg,
+                   n_sel, per, sel_p, q_idx);
+    count_launches(1);
+    return e;
+  }
   const int nblk = (C + kRowsPerBlock - 1) / kRowsPerBlock;
   dim3 grid(nblk, H_q);
   cudaError_t e = launch_pdl(k_qstats<T, D>, grid, dim3(256), 0, st, (const T*)Q, C, qnorm, qpart);
@@ -171,7 +423,6 @@ static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel
   e = launch_pdl(k_qcos<T, D>, grid, dim3(256), 0, st, (const T*)Q, C, (const float*)qpart, (const float*)qnorm, qcos);
   if (e != cudaSuccess) return e;
   const size_t smem = (size_t)((C + 3) & ~3) * sizeof(uint32_t);   // C <= 8192: at most 32 KB
-  const int rows = H_q / G_avg;
   e = launch_pdl(k_qselect, dim3(rows), dim3(256), smem, st, (const float*)qcos, C, G_avg, n_sel, q_idx);
   if (e != cudaSuccess) return e;
   count_launches(3);

@@ -1,22 +1,17 @@
 // Top-B history keys per KV head (QUOKA Explained, "From scores to a smaller
 // KV set"; QUOKA paper summary, "Chunked Prefill with QUOKA").
 //
-// A thread-block cluster of 8 CTAs per KV head runs an exact radix select
-// (radix_select.cuh) on the order-preserving 32-bit keys of the scores.  CTA
+// A thread-block cluster of 8 CTAs per KV head runs the cluster radix select
+// of cluster_topk.cuh on the order-preserving 32-bit keys of the scores.  CTA
 // r of the cluster owns the r-th contiguous eighth of the head's keys and
 // caches them in shared memory (up to 40K keys per CTA; larger slices are
 // re-read from global memory, where they are L2-resident right after the
-// scoring kernel).  Each digit pass builds per-CTA histograms; warp 0 of every
-// CTA sums the 8 histograms through distributed shared memory and finds the
-// digit.  At the end each CTA counts its keys above / equal to the threshold,
-// reads the counts of the lower-ranked CTAs, and writes its selected positions
-// at the right offsets, so the output is ascending and ties go to the lower
-// position.
+// scoring kernel).
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "launch.h"
-#include "radix_select.cuh"
+#include "cluster_topk.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -26,22 +21,13 @@ constexpr int kTopkCluster = 8;
 constexpr int kTopkThreads = 512;
 constexpr int kTopkSliceCap = 40 * 1024;   // keys per CTA cached in shared memory (160 KB)
 
-struct TopkClusterShared {
-  unsigned int sub[kRadixSubHists][256];
-  unsigned int hist[2][256];   // this CTA's digit histogram by pass parity, read by the whole cluster
-  unsigned int merged[256];    // the cluster's histogram of the current pass
-  int counts[2];               // this CTA's keys above / equal to the threshold
-  int scan[32];
-  int bin, need, gt_base, eq_base;
-};
-
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
     k_topk_cluster(const float* __restrict__ scores, int T_len, int B_e, int32_t* __restrict__ sel, int per,
                    int cache) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ __align__(16) uint32_t keys_s[];
-  __shared__ TopkClusterShared sm;
+  __shared__ ClusterTopkShared sm;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int g = blockIdx.y;
@@ -68,70 +54,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   auto key_at = [&](int i) -> uint32_t { return cache ? keys_s[i] : order_key(s[i]); };
   const uint4* keys4 = reinterpret_cast<const uint4*>(keys_s);
 
-  uint32_t prefix = 0, mask = 0;
-  int need = B_e;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass, buf = pass & 1;
-    radix_zero(&sm.sub[0][0], kRadixSubHists * 256);
-    __syncthreads();
-    if (cache) radix_hist4(keys4, n, prefix, mask, shift, sm.sub);
-    else radix_hist(key_at, n, prefix, mask, shift, sm.sub);
-    __syncthreads();
-    radix_reduce(sm.sub, sm.hist[buf]);
-    cluster.sync();                       // every CTA's histogram of this pass is ready
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) {   // merge bin b across the cluster
-      unsigned t = 0;
-#pragma unroll
-      for (int q = 0; q < kTopkCluster; ++q) t += cluster.map_shared_rank(&sm.hist[buf][0], q)[b];
-      sm.merged[b] = t;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      unsigned c[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = sm.merged[255 - 8 * threadIdx.x - j];
-      radix_find_digit(c, need, &sm.bin, &sm.need);
-    }
-    __syncthreads();
-    prefix |= (uint32_t)sm.bin << shift;
-    mask |= 255u << shift;
-    need = sm.need;
-    // hist[buf] is next written two passes later, after a cluster barrier every CTA
-    // reaches only once it has finished reading this pass's histograms.
-  }
-  const uint32_t theta = prefix;
-  const int r = need;
-  int n_gt = 0, n_eq = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint32_t u = key_at(i);
-    n_gt += u > theta;
-    n_eq += u == theta;
-  }
-  int tot_gt, tot_eq;
-  block_exclusive_scan(n_gt, sm.scan, &tot_gt);
-  block_exclusive_scan(n_eq, sm.scan, &tot_eq);
-  if (threadIdx.x == 0) {
-    sm.counts[0] = tot_gt;
-    sm.counts[1] = tot_eq;
-  }
-  cluster.sync();
-  if (threadIdx.x == 0) {
-    int gb = 0, eb = 0;
-    for (int q = 0; q < rank; ++q) {
-      const int* rc = cluster.map_shared_rank(&sm.counts[0], q);
-      gb += rc[0];
-      eb += rc[1];
-    }
-    sm.gt_base = gb;
-    sm.eq_base = eb;
-  }
-  __syncthreads();
-  const int gt_base = sm.gt_base, eq_base = sm.eq_base;
-  if (cache)
-    radix_compact4(keys4, n, theta, r, gt_base + min(eq_base, r), eq_base, B_e, t0, sel + (size_t)g * B_e, sm.scan);
-  else
-    radix_compact(key_at, n, theta, r, gt_base + min(eq_base, r), eq_base, B_e, t0, sel + (size_t)g * B_e, sm.scan);
-  cluster.sync();                         // keep this CTA's shared memory alive for remote readers
+  cluster_radix_topk<kTopkCluster>(cluster, cache != 0, keys4, key_at, n, t0, B_e, sel + (size_t)g * B_e, sm);
 }
 
 __global__ void k_iota_rows(int32_t* __restrict__ sel, int rows, int n) {
