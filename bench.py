@@ -35,7 +35,8 @@ if ROOT not in sys.path:
 from sparse_attention_chunked_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "chunk tokens/sec for QUOKA select+attend at 32K/128K history; % HBM/TC roofline"
-WORKLOADS = {"gqa32k": wl.GQA_32K_BF16, "gqa128k": wl.GQA_128K_BF16}
+WORKLOADS = {"gqa32k": wl.GQA_32K_BF16, "gqa128k": wl.GQA_128K_BF16,
+             "tiny": wl.TINY_MHA_FP32}   # tiny: the small parity case, for quick checks of the harness
 FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flop x max SM clock
 L2_FLUSH_BYTES = 512 << 20                              # > 3x the 129 MB L2
 
@@ -56,6 +57,11 @@ def dist_init(backend: str):
 def barrier():
     if torch.distributed.is_available() and torch.distributed.is_initialized():
         torch.distributed.barrier()
+
+
+def job_throughput(tokens_per_rank_step: int, world: int, step_ms_max: float) -> float:
+    """Whole-job tokens/s: every rank processes its own chunk per step; the slowest rank's step time counts."""
+    return tokens_per_rank_step * world / (step_ms_max * 1e-3)
 
 
 def max_over_ranks(x: float, device="cpu") -> float:
@@ -334,7 +340,7 @@ def run_quoka(args, rank, world, local_rank):
         if "flops" in work[nm]:
             st["TFLOPs"] = round(work[nm]["flops"] / (ms * 1e-3) / 1e12, 2)
         stages[nm] = st
-    value = cfg.C * world / (step_ms * 1e-3)
+    value = job_throughput(cfg.C, world, step_ms)
     res = {
         "metric": METRIC,
         "value": round(value, 1),
