@@ -38,6 +38,28 @@ METRIC = "chunk tokens/sec for QUOKA select+attend at 32K/128K history; % HBM/TC
 WORKLOADS = {"gqa32k": wl.GQA_32K_BF16, "gqa128k": wl.GQA_128K_BF16,
              "tiny": wl.TINY_MHA_FP32}   # tiny: the small parity case, for quick checks of the harness
 FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flop x max SM clock
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one tensor-core attention launch per
+# workload, from one ncu capture, and a digest of the kernel sources that capture ran on: once the
+# sources change the figure no longer describes the kernel and the bench reports null.
+ATTEND_TRAFFIC = {"gqa32k": 33_616_896}
+ATTEND_TRAFFIC_SOURCES = ("attend_tc.cu", "tc_common.cuh", "common.cuh", "launch.h")
+ATTEND_TRAFFIC_SHA256 = "f94f9cb397112b792290eb0444c3ea39d62455bd143ed0b3e50182a184bff11a"
+
+
+def attend_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ATTEND_TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "sparse_attention_chunked_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def attend_traffic(workload: str):
+    if workload not in ATTEND_TRAFFIC or attend_sources_sha256() != ATTEND_TRAFFIC_SHA256:
+        return None
+    return ATTEND_TRAFFIC[workload]
 L2_FLUSH_BYTES = 512 << 20                              # > 3x the 129 MB L2
 INPUT_SETS = 3    # timed steps rotate over this many copies of the inputs (> 3x L2 together at 32K history)
 
@@ -400,7 +422,8 @@ def run_quoka(args, rank, world, local_rank):
         "roofline": {"kernel": "attend", "bound": bound, "achieved": round(achieved, 2),
                      "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": peaks["source"] if tc_engine else "derived: 152 SM x 128 FP32 x 2 x 2.07 GHz",
-                     "traffic": None},
+                     "traffic": attend_traffic(args.workload) if tc_engine else None,
+                     "traffic_unit": "bytes/launch"},
         "stages": stages,
         "staged_ms_per_step": round(staged_ms, 5),
         "l2_write_flush": {"ms_per_step": round(flush_step_ms, 5),
