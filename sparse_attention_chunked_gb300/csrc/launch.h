@@ -36,8 +36,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 extern std::atomic<unsigned long long> g_launch_count;
 inline void count_launches(unsigned n) { g_launch_count.fetch_add(n, std::memory_order_relaxed); }
 
+struct WsHeader;
+// hdr: where device-side errors (an expired wait) are recorded; may be NULL.
 cudaError_t launch_select_queries(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel,
-                                  int32_t* q_idx, float* qnorm, float* qpart, float* qcos, cudaStream_t st);
+                                  int32_t* q_idx, float* qnorm, float* qpart, float* qcos, WsHeader* hdr,
+                                  cudaStream_t st);
 
 // op_bf may be NULL (CUDA-core scoring only needs op_f32); otherwise N_pad
 // (a multiple of 16, >= the row count) rows per pass are written.

@@ -82,6 +82,6 @@ extern "C" int quoka_select_queries_noalloc(const quoka_shape* s, const void* Q,
   const int G_avg = gqa == QUOKA_GQA_MAX ? 1 : s->H_q / s->H_kv;
   const cudaError_t e = launch_select_queries(s->dtype, s->d, Q, s->H_q, G_avg, s->C, n, q_idx,
                                               reinterpret_cast<float*>(b + off_norm), reinterpret_cast<float*>(b + off_part),
-                                              reinterpret_cast<float*>(b + off_cos), (cudaStream_t)stream);
+                                              reinterpret_cast<float*>(b + off_cos), nullptr, (cudaStream_t)stream);
   return e == cudaSuccess ? QUOKA_OK : QUOKA_ERR_CUDA;
 }

@@ -8,11 +8,14 @@
 // position), written in position order.
 //
 // One launch, k_qselect_fused: a cluster of 8 CTAs per selection row, CTA r
-// owning the r-th eighth of the chunk positions.  Each CTA streams its rows
-// once for the row norms |q| and the column sums of its slice; the cluster
-// adds the slices' sums through distributed shared memory in rank order
-// (deterministic) for M_q; each CTA then computes cos(q, M_q) for its rows
-// (re-read, now from L2) into shared-memory keys.  For N_q <= 256 the
+// owning the r-th eighth of the chunk positions.  Each CTA copies its slice
+// of Q into shared memory with bulk copies (64-row chunks, each on its own
+// mbarrier, so the arithmetic starts as the first chunk lands), takes the row
+// norms |q| and the column sums; the cluster adds the slices' sums through
+// distributed shared memory in rank order (deterministic) for M_q; each CTA
+// then computes cos(q, M_q) for its rows from shared memory (a slice larger
+// than the 64 KB staging buffer, or a group of several heads, is staged again
+// piece by piece, from L2) into shared-memory keys.  For N_q <= 256 the
 // selection is a bitonic network (warp_topk.cuh): each warp keeps the top
 // L >= N_q of its keys, warp 0 merges its CTA's lists, CTA 0 merges the
 // cluster's lists through distributed shared memory and writes the winners'
@@ -28,6 +31,7 @@
 #include <cooperative_groups.h>
 
 #include "cluster_topk.cuh"
+#include "tc_common.cuh"
 #include "radix_select.cuh"
 #include "warp_topk.cuh"
 
@@ -81,12 +85,22 @@ constexpr int kSelCluster = 8;
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 
-// Offset (in floats) of the selection lists in k_qselect_fused's dynamic shared memory, and its size in bytes.
+constexpr int kSelChunkRows = 64;                   // rows per bulk copy / mbarrier
+constexpr size_t kSelStageBytes = 64 * 1024;          // shared-memory staging of Q rows
+constexpr int kSelMaxChunks = 16;
+
+// Rows of one staged piece of a slice (a multiple of kSelChunkRows).
+__host__ __device__ inline int qselect_piece_rows(int D, int elt) {
+  return (int)(kSelStageBytes / ((size_t)D * elt)) / kSelChunkRows * kSelChunkRows;
+}
+// Offset (in floats, after the staging buffer) of the selection lists in
+// k_qselect_fused's dynamic shared memory, and the total size in bytes.
 __host__ __device__ inline size_t qselect_lists_offset(int per, int G_avg, int D) {
-  return ((size_t)per + (size_t)G_avg * per + 2 * (size_t)G_avg * D + (size_t)G_avg + 1) & ~(size_t)1;
+  return ((size_t)per + (size_t)per + (size_t)G_avg * per + 2 * (size_t)G_avg * D + (size_t)G_avg + 1) & ~(size_t)1;
 }
 static size_t qselect_fused_smem(int per, int G_avg, int D, int sel_p) {
-  return qselect_lists_offset(per, G_avg, D) * sizeof(float) + (size_t)(kSelWarps + 1) * 32 * sel_p * sizeof(uint64_t);
+  return kSelStageBytes + qselect_lists_offset(per, G_avg, D) * sizeof(float) +
+         (size_t)(kSelWarps + 1) * 32 * sel_p * sizeof(uint64_t);
 }
 
 // Top n_sel (<= 32 * P) of the row's keys, split over the cluster as in
@@ -147,53 +161,105 @@ __device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* ke
 template <typename T, int D>
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
     k_qselect_fused(const T* __restrict__ Q, int C, int G_avg, int n_sel, int per, int sel_p,
-                    int32_t* __restrict__ q_idx) {
+                    int32_t* __restrict__ q_idx, WsHeader* hdr) {
   pdl_launch_dependents();
-  pdl_wait();
   constexpr int E = D / 32;
-  extern __shared__ __align__(16) float dyn[];
+  extern __shared__ __align__(1024) uint8_t dsm_raw[];
+  T* rows_s = reinterpret_cast<T*>(dsm_raw);                                 // staged rows of a piece
+  float* dyn = reinterpret_cast<float*>(dsm_raw + kSelStageBytes);
   uint32_t* keys_s = reinterpret_cast<uint32_t*>(dyn);   // [per], per % 4 == 0
-  float* norm_s = dyn + per;                             // [G_avg][per]
+  float* u_s = dyn + per;                                // [per] cosine summed over the row's heads
+  float* norm_s = u_s + per;                             // [G_avg][per]
   float* part_s = norm_s + (size_t)G_avg * per;          // [G_avg][D] column sums of this slice (read cluster-wide)
   float* mean_s = part_s + (size_t)G_avg * D;            // [G_avg][D]
   float* mnorm_s = mean_s + (size_t)G_avg * D;           // [G_avg]
   uint64_t* lists = reinterpret_cast<uint64_t*>(dyn + qselect_lists_offset(per, G_avg, D));
   __shared__ float sp[kSelWarps][D];
   __shared__ ClusterTopkShared tk;
+  __shared__ uint64_t rbar[kSelMaxChunks];
+  __shared__ int abort_flag;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
   const int t0 = min(C, rank * per), n = min(C, t0 + per) - t0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int piece = qselect_piece_rows(D, (int)sizeof(T));
+  const int npieces = (n + piece - 1) / piece;
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < kSelMaxChunks; ++c) tc::mbar_init(&rbar[c], 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < per; i += blockDim.x) u_s[i] = 0.f;
+  __syncthreads();
+  volatile int* abort = &abort_flag;
+  pdl_wait();                                     // Q may come from the previous kernel
+
+  // Stage rows [p0, p0 + pn) of head k's slice; every thread calls it (it syncs), thread 0 issues.
+  int round = 0;                                  // staging rounds so far: chunk barriers' phase
+  int last_pn = 0;                                // rows of the last staged piece
+  auto stage = [&](int k, int p0, int pn) {
+    __syncthreads();                              // the previous piece is no longer read
+    if (threadIdx.x == 0) {
+      tc::fence_proxy_async_smem();               // generic reads of the buffer before the async writes
+      const T* src = Q + ((size_t)(row * G_avg + k) * C + t0 + p0) * D;
+      for (int c = 0; c * kSelChunkRows < pn; ++c) {
+        const uint32_t bytes = (uint32_t)(min(kSelChunkRows, pn - c * kSelChunkRows) * D * (int)sizeof(T));
+        tc::mbar_arrive_expect_tx(&rbar[c], bytes);
+        tc::bulk_load(rows_s + (size_t)c * kSelChunkRows * D, src + (size_t)c * kSelChunkRows * D, bytes, &rbar[c]);
+      }
+    }
+    ++round;
+    last_pn = pn;
+  };
+  // the rows c0 .. c0+7 of the staged piece (pn rows), waiting for their chunk; false once a wait gave up
+  auto rows_ready = [&](int c0) -> bool {
+    bool ok = true;
+    if (lane == 0) ok = tc::mbar_wait(&rbar[c0 / kSelChunkRows], (round - 1) & 1, abort, hdr, 0x301);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  };
+  auto read_rows = [&](int c0, int pn, float (*x)[E]) {
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      RowSlice<T, E> raw;
+      if (c0 + r < pn) raw = *reinterpret_cast<const RowSlice<T, E>*>(rows_s + (size_t)(c0 + r) * D + lane * E);
+#pragma unroll
+      for (int j = 0; j < E; ++j) x[r][j] = (c0 + r < pn) ? to_f32(raw.v[j]) : 0.f;
+    }
+  };
 
   // 1. row norms and column sums of this slice, head by head
   for (int k = 0; k < G_avg; ++k) {
-    const T* base = Q + ((size_t)(row * G_avg + k) * C + t0) * D;
     float part[E];
 #pragma unroll
     for (int j = 0; j < E; ++j) part[j] = 0.f;
-    for (int c0 = warp * kRowsPerWarp; c0 < n; c0 += kSelWarps * kRowsPerWarp) {
-      float x[kRowsPerWarp][E];
-      load_rows_n<T, D>(base, n, c0, x);
-      float ss[kRowsPerWarp];
+    for (int pi = 0; pi < npieces; ++pi) {
+      const int p0 = pi * piece, pn = min(piece, n - p0);
+      stage(k, p0, pn);
+      for (int c0 = warp * kRowsPerWarp; c0 < pn; c0 += kSelWarps * kRowsPerWarp) {
+        if (!rows_ready(c0)) break;
+        float x[kRowsPerWarp][E];
+        read_rows(c0, pn, x);
+        float ss[kRowsPerWarp];
 #pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        ss[r] = 0.f;
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+          ss[r] = 0.f;
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-          part[j] += x[r][j];
-          ss[r] = fmaf(x[r][j], x[r][j], ss[r]);
+          for (int j = 0; j < E; ++j) {
+            part[j] += x[r][j];
+            ss[r] = fmaf(x[r][j], x[r][j], ss[r]);
+          }
         }
-      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
+        for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
-      if (lane < kRowsPerWarp && c0 + lane < n) {
-        float v = ss[0];
+          for (int r = 0; r < kRowsPerWarp; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
+        if (lane < kRowsPerWarp && c0 + lane < pn) {
+          float v = ss[0];
 #pragma unroll
-        for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? ss[r] : v;
-        norm_s[(size_t)k * per + c0 + lane] = sqrtf(v);
+          for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? ss[r] : v;
+          norm_s[(size_t)k * per + p0 + c0 + lane] = sqrtf(v);
+        }
       }
     }
 #pragma unroll
@@ -226,40 +292,49 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   }
   __syncthreads();
 
-  // 3. cos(q, M_q) (averaged over the row's heads) -> keys
-  for (int c0 = warp * kRowsPerWarp; c0 < n; c0 += kSelWarps * kRowsPerWarp) {
-    float u[kRowsPerWarp];
+  // 3. cos(q, M_q), summed over the row's heads in head order; the last staged
+  //    piece is still in shared memory when the row has one head and one piece
+  const bool resident = G_avg == 1 && npieces == 1;
+  for (int k = 0; k < G_avg; ++k) {
+    float m[E];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) u[r] = 0.f;
-    for (int k = 0; k < G_avg; ++k) {
-      float x[kRowsPerWarp][E];
-      load_rows_n<T, D>(Q + ((size_t)(row * G_avg + k) * C + t0) * D, n, c0, x);
-      float m[E];
+    for (int j = 0; j < E; ++j) m[j] = mean_s[k * D + lane * E + j];
+    const float mn = mnorm_s[k];
+    for (int pi = 0; pi < npieces; ++pi) {
+      const int p0 = pi * piece, pn = min(piece, n - p0);
+      if (!resident) stage(k, p0, pn);
+      for (int c0 = warp * kRowsPerWarp; c0 < pn; c0 += kSelWarps * kRowsPerWarp) {
+        if (!resident && !rows_ready(c0)) break;
+        float x[kRowsPerWarp][E];
+        read_rows(c0, pn, x);
+        float dot[kRowsPerWarp];
 #pragma unroll
-      for (int j = 0; j < E; ++j) m[j] = mean_s[k * D + lane * E + j];
-      float dot[kRowsPerWarp];
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+          dot[r] = 0.f;
 #pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        dot[r] = 0.f;
+          for (int j = 0; j < E; ++j) dot[r] = fmaf(x[r][j], m[j], dot[r]);
+        }
 #pragma unroll
-        for (int j = 0; j < E; ++j) dot[r] = fmaf(x[r][j], m[j], dot[r]);
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int r = 0; r < kRowsPerWarp; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+        if (lane < kRowsPerWarp && c0 + lane < pn) {
+          float v = dot[0];
+#pragma unroll
+          for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? dot[r] : v;
+          const int i = p0 + c0 + lane;
+          u_s[i] += v / (fmaxf(norm_s[(size_t)k * per + i], kNormEps) * mn);
+        }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
-      const float mn = mnorm_s[k];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r)
-        if (c0 + r < n) u[r] += dot[r] / (fmaxf(norm_s[(size_t)k * per + c0 + r], kNormEps) * mn);
     }
-    if (lane < kRowsPerWarp && c0 + lane < n) {
-      float v = u[0];
-#pragma unroll
-      for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? u[r] : v;
-      if (G_avg > 1) v = v / (float)G_avg;
-      keys_s[c0 + lane] = ~order_key(v);   // the largest key is the smallest cosine
-    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float v = G_avg > 1 ? u_s[i] / (float)G_avg : u_s[i];
+    keys_s[i] = ~order_key(v);   // the largest key is the smallest cosine
+  }
+  if (threadIdx.x == 0 && *abort && round > 0) {   // let the last staged copies land before the CTA can exit
+    for (int c = 0; c * kSelChunkRows < last_pn; ++c) tc::mbar_drain(&rbar[c], (round - 1) & 1);
   }
   __syncthreads();
 
@@ -402,17 +477,17 @@ __global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos,
 
 template <typename T, int D>
 static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel, int32_t* q_idx,
-                             float* qnorm, float* qpart, float* qcos, cudaStream_t st) {
+                             float* qnorm, float* qpart, float* qcos, WsHeader* hdr, cudaStream_t st) {
   const int rows = H_q / G_avg;
   const int per = ((C + kSelCluster - 1) / kSelCluster + 3) & ~3;
   // the network's list length L = 32 * sel_p >= n_sel (0: radix select)
   const int sel_p = n_sel <= 32 ? 1 : n_sel <= 64 ? 2 : n_sel <= 128 ? 4 : n_sel <= 256 ? 8 : 0;
   const size_t fsmem = qselect_fused_smem(per, G_avg, D, sel_p);
-  if (fsmem <= 160 * 1024) {
+  if (fsmem <= 160 * 1024 && ((uintptr_t)Q & 15u) == 0) {   // bulk copies want 16-byte aligned rows
     cudaError_t e = ensure_smem((const void*)k_qselect_fused<T, D>, fsmem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(k_qselect_fused<T, D>, dim3(kSelCluster, rows), dim3(kSelThreads), fsmem, st, (const T*)Q, C, G_avg,
-                   n_sel, per, sel_p, q_idx);
+                   n_sel, per, sel_p, q_idx, hdr);
     count_launches(1);
     return e;
   }
@@ -430,13 +505,14 @@ static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel
 }
 
 cudaError_t launch_select_queries(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel,
-                                  int32_t* q_idx, float* qnorm, float* qpart, float* qcos, cudaStream_t st) {
+                                  int32_t* q_idx, float* qnorm, float* qpart, float* qcos, WsHeader* hdr,
+                                  cudaStream_t st) {
   if (dtype == 0) {
-    return d == 64 ? qsel_impl<__nv_bfloat16, 64>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, st)
-                   : qsel_impl<__nv_bfloat16, 128>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, st);
+    return d == 64 ? qsel_impl<__nv_bfloat16, 64>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, hdr, st)
+                   : qsel_impl<__nv_bfloat16, 128>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, hdr, st);
   }
-  return d == 64 ? qsel_impl<float, 64>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, st)
-                 : qsel_impl<float, 128>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, st);
+  return d == 64 ? qsel_impl<float, 64>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, hdr, st)
+                 : qsel_impl<float, 128>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, hdr, st);
 }
 
 }  // namespace quoka

@@ -148,7 +148,7 @@ int run_select(const quoka_shape* s, const void* Q, int n, const Params& p, int3
   const int G = s->H_q / s->H_kv;
   const int G_avg = p.gqa == QUOKA_GQA_MAX ? 1 : G;
   return cuda_status(launch_select_queries(s->dtype, s->d, Q, s->H_q, G_avg, s->C, n, q_idx, at<float>(ws, L.qnorm),
-                                           at<float>(ws, L.qpart), at<float>(ws, L.qcos), st));
+                                           at<float>(ws, L.qpart), at<float>(ws, L.qcos), at<WsHeader>(ws, 0), st));
 }
 
 int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, const void* K_hist,
