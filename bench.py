@@ -230,13 +230,10 @@ def run_quoka(args, rank, world, local_rank):
     set_bytes = sum(t.numel() * t.element_size() for t in sets[0])
 
     def step_fns(Qx, Khx, Vhx, Kcx, Vcx):
-        return [
-            lambda: q.quoka_select_queries(shape, Qx, cfg.N_q, params, q_idx, ws, stream),
-            lambda: q.quoka_score_keys(shape, Qx, q_idx, cfg.N_q, Khx, params, scores, ws, stream),
-            lambda: q.quoka_topk(shape, scores, cfg.B, sel, ws, stream),
-            lambda: q.quoka_gather(shape, Khx, Vhx, sel, B_e, Ks, Vs, stream),
-            lambda: q.quoka_sparse_attend(shape, Qx, Ks, Vs, B_e, Kcx, Vcx, params, O, None, ws, stream),
-        ]
+        # the step: one quoka_chunk_attend (every stage of the path; top-B and the
+        # gather share one launch there)
+        return [lambda: q.quoka_chunk_attend(shape, Qx, Khx, Vhx, Kcx, Vcx, cfg.N_q, cfg.B, params, O, None, None, ws,
+                                             stream)]
 
     # Each stage is captured once into its own CUDA graph (the library only
     # enqueues kernels, so a captured call replays the identical launches); a
@@ -413,8 +410,8 @@ def run_quoka(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2: the timed steps rotate over {INPUT_SETS} copies of the inputs "
                          f"({INPUT_SETS * set_bytes / 2**20:.0f} MB), no flush; l2_write_flush: the same step after "
                          f"a {L2_FLUSH_BYTES >> 20} MB write",
-                   "timing": "step = one CUDA graph of the five stage calls, K steps timed back to back; stages "
-                             "also replayed one graph each (after a flush) for the breakdown",
+                   "timing": "step = one CUDA graph of one quoka_chunk_attend call, K steps timed back to back; "
+                             "the five stage calls replayed one graph each (after a flush) for the breakdown",
                    "parallelism": f"replicas x{world}"},
         "impl": "quoka",
         "gpu_launches": int(launches),
