@@ -5,9 +5,12 @@
 // attention kernel); QUOKA Explained, "MEAN and MAX do different jobs" (the
 // original query heads attend).
 //
-// A CTA owns two 128-row query tiles ("slots") of two query heads of the same
-// KV group over the same chunk rows, so both share every K/V tile and the same
-// causal structure.  Keys are the history rows (selected or all) followed by
+// A work item is two 128-row query tiles ("slots") of two query heads of the
+// same KV group over the same chunk rows, so both share every K/V tile and the
+// same causal structure.  The kernel is persistent: one CTA per SM runs a
+// fixed serpentine share of the longest-first item list, keeping its TMEM and
+// barriers, so one item's tail (last PV, epilogue) overlaps the next item's
+// Q and first K/V loads.  Keys are the history rows (selected or all) followed by
 // the chunk's own rows; the history part is unmasked except past n_hist, the
 // chunk part is causal.
 //   S_s = Q_s K_j^T        tcgen05, A = Q (smem), B = K tile (smem), fp32 in TMEM
@@ -43,6 +46,8 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 struct AttSmem {
   uint64_t q_full;
+  uint64_t q_free;       // every S MMA of the work item has completed: Q may be replaced
+  uint64_t o_free[2];    // the epilogue has read O_s: the next item's first PV may overwrite it
   uint64_t kv_full[kKvStages];
   uint64_t kv_empty[kKvStages];
   uint64_t s_full[2];    // S_s of the current block is in TMEM
@@ -99,11 +104,148 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Work item i (0 = most key blocks): query tile qt = n_qt - 1 - i / (H_kv * pairs)
+// of KV group g and head pair hp.  CTA c of P runs items c, 2P - 1 - c, 2P + c,
+// 4P - 1 - c, ...: a serpentine over the longest-first list, so the CTAs that
+// drew the longest first items draw the shortest second ones.
+struct AttItem {
+  int qt, g, h0, n_slots, n_blocks;
+};
+
+__device__ __forceinline__ int att_item_index(int c, int round, int P) {
+  return (round & 1) ? (round + 1) * P - 1 - c : round * P + c;
+}
+
+__device__ __forceinline__ AttItem att_item(int i, int n_qt, int H_kv_pairs, int pairs, int G, int nh) {
+  AttItem it;
+  it.qt = n_qt - 1 - i / H_kv_pairs;
+  const int rem = i % H_kv_pairs;
+  it.g = rem / pairs;
+  const int hp = rem % pairs;
+  it.h0 = it.g * G + 2 * hp;
+  it.n_slots = (2 * hp + 1 < G) ? 2 : 1;
+  it.n_blocks = nh + it.qt + 1;
+  return it;
+}
+
+// One work item's softmax, rows of slot s: blocks nb .. nb + n_blocks - 1 of
+// the slot's barrier phases, then the epilogue (O / l to global memory, LSE)
+// and the release of O_s.  Kept out of line: inlined into the kernel's work-item
+// loop its unrolled block body was scheduled about 1.4x slower.  Returns false
+// once a bounded wait gave up.
+template <int D>
+__device__ __noinline__ bool softmax_item(AttSmem* sm, uint8_t* p_row, int s, int lane, int r, uint32_t s_addr, int nb,
+                                          int n_blocks, int nh, int n_hist, int qt, int C, int h, float scale_log2,
+                                          __nv_bfloat16* __restrict__ O, float* __restrict__ lse, WsHeader* hdr) {
+  constexpr uint32_t kHalfBytes = 128 * 128;
+  const uint32_t o_addr = s_addr + 128;
+  volatile int* abort = &sm->abort;
+  const int c = qt * 128 + r;                   // chunk position of the row
+  bool ok = true;
+  float m_used = -INFINITY, l = 0.f;           // running max of the raw logits, softmax denominator
+  for (int jb = 0; jb < n_blocks; ++jb) {
+    if (!(ok = warp_wait(&sm->s_full[s], (nb + jb) & 1, abort, hdr, 0x208))) break;
+    tc::tc_fence_after();
+    uint32_t sv[128];
+    tc::tmem_ld128(s_addr, sv);
+    tc::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&sm->s_free[s]);   // the MMA may now write S_s of the next block
+    const bool hist = jb < nh;
+    // only the last history block (if partial) and the diagonal chunk block have masked keys
+    const bool need_mask = hist ? (jb == nh - 1 && (n_hist & 127) != 0) : (jb - nh == qt);
+    if (need_mask) {
+      // keys of this block visible to row c: [0, lim)
+      const int lim = hist ? n_hist - jb * 128 : c - (jb - nh) * 128 + 1;
+#pragma unroll
+      for (int i2 = 0; i2 < 128; ++i2)
+        if (i2 >= lim) sv[i2] = __float_as_uint(-INFINITY);
+    }
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int i2 = 0; i2 < 64; ++i2)
+      mx4[i2 & 3] = fmax3(mx4[i2 & 3], __uint_as_float(sv[2 * i2]), __uint_as_float(sv[2 * i2 + 1]));
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    const float m_new = fmaxf(m_used, mx);
+    const bool rescale = (m_new - m_used) * scale_log2 > kRescaleThreshold;   // true on the first block
+    float alpha = 1.f;
+    if (rescale) {
+      alpha = ex2_approx((m_used - m_new) * scale_log2);   // 0 on the first block
+      m_used = m_new;
+    }
+    const float neg_m = -m_used * scale_log2;
+    // PV_s of the previous block must be done before P_s is overwritten and before O is rescaled
+    // (for an item's first block the previous item's epilogue already waited for it)
+    if (jb > 0 && !(ok = warp_wait(&sm->o_done[s], (nb + jb - 1) & 1, abort, hdr, 0x209))) break;
+    float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {             // 8 keys = one 16-byte chunk of P at a time
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i2 = 8 * q + 2 * j;
+        float x0 = __uint_as_float(sv[i2]), x1 = __uint_as_float(sv[i2 + 1]);
+        fma2(x0, x1, scale_log2, neg_m);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        if (j & 1) add2(sa[2], sa[3], p0, p1);
+        else add2(sa[0], sa[1], p0, p1);
+        w[j] = pack_bf16x2(p0, p1);
+      }
+      const int hf = q >> 3, ch = q & 7;
+      *reinterpret_cast<uint4*>(p_row + hf * kHalfBytes + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    l = l * alpha + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
+    if (jb > 0 && __any_sync(0xffffffffu, rescale)) {   // O *= alpha in TMEM (rows without a rescale: alpha = 1)
+      tc::tc_fence_after();
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t ov[32];
+        tc::tmem_ld32(o_addr + q4 * 32, ov);
+#pragma unroll
+        for (int i2 = 0; i2 < 32; ++i2) ov[i2] = __float_as_uint(__uint_as_float(ov[i2]) * alpha);
+        tc::tmem_st32(o_addr + q4 * 32, ov);
+      }
+      tc::tmem_wait_st();
+    }
+    tc::fence_proxy_async_smem();              // P visible to the tensor core
+    tc::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&sm->p_full[s]);
+  }
+  if (!ok) return false;
+  // epilogue: O / l, then O_s is free for the next item's PV
+  if (!warp_wait(&sm->o_done[s], (nb + n_blocks - 1) & 1, abort, hdr, 0x209)) return false;
+  tc::tc_fence_after();
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int q4 = 0; q4 < D / 32; ++q4) {
+    uint32_t ov[32];
+    tc::tmem_ld32(o_addr + q4 * 32, ov);
+    if (c < C) {
+      uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)h * C + c) * D + q4 * 32);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv, __uint_as_float(ov[8 * v + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv, __uint_as_float(ov[8 * v + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv, __uint_as_float(ov[8 * v + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv, __uint_as_float(ov[8 * v + 7]) * inv);
+        dst[v] = w;
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive(&sm->o_free[s]);
+  if (lse != nullptr && c < C) lse[(size_t)h * C + c] = m_used * scale_log2 * 0.69314718055994531f + logf(l);
+  return true;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttThreads, 1)
     k_attend_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap khmap,
                 const __grid_constant__ CUtensorMap vhmap, const __grid_constant__ CUtensorMap kcmap,
-                const __grid_constant__ CUtensorMap vcmap, int n_hist, int C, int G, float scale_log2,
+                const __grid_constant__ CUtensorMap vcmap, int n_hist, int C, int G, int H_kv, float scale_log2,
                 __nv_bfloat16* __restrict__ O, float* __restrict__ lse, WsHeader* hdr) {
   constexpr int HALVES = D / 64;
   constexpr uint32_t kHalfBytes = 128 * 128;            // 128 rows x 128 bytes
@@ -116,21 +258,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   uint8_t* kv_s = p_s + 2 * kPBytes;                    // [kKvStages][HALVES][128][128 B]
   AttSmem* sm = reinterpret_cast<AttSmem*>(kv_s + kKvStages * kTileBytes);
 
-  // ---- work item: longest (last query tile) first
   const int pairs = (G + 1) / 2;
   const int n_qt = (C + 127) / 128;
-  const int H_kv_pairs = gridDim.x / n_qt;              // H_kv * pairs
-  const int qt = n_qt - 1 - (int)blockIdx.x / H_kv_pairs;
-  const int rem = (int)blockIdx.x % H_kv_pairs;
-  const int g = rem / pairs, hp = rem % pairs;
-  const int h0 = g * G + 2 * hp;
-  const int n_slots = (2 * hp + 1 < G) ? 2 : 1;
+  const int H_kv_pairs = H_kv * pairs;
+  const int n_items = n_qt * H_kv_pairs;
+  const int P = gridDim.x, cta = blockIdx.x;
   const int nh = (n_hist + 127) / 128;
-  const int n_blocks = nh + qt + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     tc::mbar_init(&sm->q_full, 1);
+    tc::mbar_init(&sm->q_free, 1);
     for (int s = 0; s < kKvStages; ++s) {
       tc::mbar_init(&sm->kv_full[s], 1);
       tc::mbar_init(&sm->kv_empty[s], 1);
@@ -140,6 +278,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       tc::mbar_init(&sm->s_free[s], 4);
       tc::mbar_init(&sm->p_full[s], 4);
       tc::mbar_init(&sm->o_done[s], 1);
+      tc::mbar_init(&sm->o_free[s], 4);
     }
     tc::mbar_init(&sm->drain[0], 1);
     tc::mbar_init(&sm->drain[1], 1);
@@ -159,7 +298,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   volatile int* abort = &sm->abort;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer: Q once, then K_j, V_j, ...
+    // ------------------------------------------------------------ TMA producer: per work item Q, then K_j, V_j, ...
     if (lane == 0) {
       tc::tma_prefetch_desc(&qmap);
       tc::tma_prefetch_desc(&kcmap);
@@ -168,101 +307,125 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         tc::tma_prefetch_desc(&khmap);
         tc::tma_prefetch_desc(&vhmap);
       }
-      tc::mbar_arrive_expect_tx(&sm->q_full, n_slots * kTileBytes);
-      for (int s = 0; s < n_slots; ++s)
-        for (int hf = 0; hf < HALVES; ++hf)
-          tc::tma_load_3d(q_s + s * kTileBytes + hf * kHalfBytes, &qmap, &sm->q_full, hf * 64, qt * 128, h0 + s);
-      // Ring items in the order the MMA warp consumes them: K_0, then for every
-      // block j: K_{j+1} (used early, by S of the next block) and V_j (used late).
-      int k = 0;
+      int k = 0, n_done = 0;                    // ring items issued; work items started
       bool ok = true;
-      auto load = [&](int jb, int which) {      // which: 0 = K, 1 = V
-        const int s = k % kKvStages;
-        if (k >= kKvStages && !tc::mbar_wait(&sm->kv_empty[s], ((k / kKvStages) - 1) & 1, abort, hdr, 0x201))
-          return false;
-        const bool hist = jb < nh;
-        const int row = hist ? jb * 128 : (jb - nh) * 128;
-        const CUtensorMap* map = hist ? (which == 0 ? &khmap : &vhmap) : (which == 0 ? &kcmap : &vcmap);
-        tc::mbar_arrive_expect_tx(&sm->kv_full[s], kTileBytes);
-        for (int hf = 0; hf < HALVES; ++hf)
-          tc::tma_load_3d(kv_s + s * kTileBytes + hf * kHalfBytes, map, &sm->kv_full[s], hf * 64, row, g);
-        ++k;
-        return true;
-      };
-      ok = load(0, 0);
-      for (int jb = 0; ok && jb < n_blocks; ++jb) {
-        if (jb + 1 < n_blocks) ok = load(jb + 1, 0);
-        if (ok) ok = load(jb, 1);
+      for (int round = 0; ok; ++round) {
+        const int i = att_item_index(cta, round, P);
+        if (i >= n_items) break;
+        const AttItem it = att_item(i, n_qt, H_kv_pairs, pairs, G, nh);
+        // Q of this item, once every S MMA of the previous one has read the old Q
+        if (n_done > 0 && !(ok = tc::mbar_wait(&sm->q_free, (n_done - 1) & 1, abort, hdr, 0x20a))) break;
+        tc::mbar_arrive_expect_tx(&sm->q_full, it.n_slots * kTileBytes);
+        for (int s = 0; s < it.n_slots; ++s)
+          for (int hf = 0; hf < HALVES; ++hf)
+            tc::tma_load_3d(q_s + s * kTileBytes + hf * kHalfBytes, &qmap, &sm->q_full, hf * 64, it.qt * 128,
+                            it.h0 + s);
+        ++n_done;
+        // Ring items in the order the MMA warps consume them: K_0, then for every
+        // block j: K_{j+1} (used early, by S of the next block) and V_j (used late).
+        auto load = [&](int jb, int which) {    // which: 0 = K, 1 = V
+          const int s = k % kKvStages;
+          if (k >= kKvStages && !tc::mbar_wait(&sm->kv_empty[s], ((k / kKvStages) - 1) & 1, abort, hdr, 0x201))
+            return false;
+          const bool hist = jb < nh;
+          const int row = hist ? jb * 128 : (jb - nh) * 128;
+          const CUtensorMap* map = hist ? (which == 0 ? &khmap : &vhmap) : (which == 0 ? &kcmap : &vcmap);
+          tc::mbar_arrive_expect_tx(&sm->kv_full[s], kTileBytes);
+          for (int hf = 0; hf < HALVES; ++hf)
+            tc::tma_load_3d(kv_s + s * kTileBytes + hf * kHalfBytes, map, &sm->kv_full[s], hf * 64, row, it.g);
+          ++k;
+          return true;
+        };
+        ok = load(0, 0);
+        for (int jb = 0; ok && jb < it.n_blocks; ++jb) {
+          if (jb + 1 < it.n_blocks) ok = load(jb + 1, 0);
+          if (ok) ok = load(jb, 1);
+        }
       }
       if (*abort) {   // let issued copies land before exiting
-        tc::mbar_drain(&sm->q_full, 0);
+        if (n_done > 0) tc::mbar_drain(&sm->q_full, (n_done - 1) & 1);
         for (int kk = k - kKvStages < 0 ? 0 : k - kKvStages; kk < k; ++kk)
           tc::mbar_drain(&sm->kv_full[kk % kKvStages], (kk / kKvStages) & 1);
       }
     }
   } else if (warp == 1 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers
-    // Ring items: K_0, then per block j: K_{j+1} (if any), V_j.  Warp 1 issues
-    // S_s(j+1) for each slot as soon as the key tile is in and the softmax has
-    // loaded S_s(j); warp 10 issues PV_s(j) as soon as the value tile is in and
-    // P_s(j) is in shared memory.  Each issuer releases the ring stages it read.
+    // Warp 1 issues S_s(j+1) for each slot as soon as the key tile is in and
+    // the softmax has loaded S_s(j); warp 10 issues PV_s(j) as soon as the
+    // value tile is in and P_s(j) is in shared memory.  Each issuer releases
+    // the ring stages it read.  Block and item counts run on across work items
+    // (per slot), and with them the barrier phases.
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, D, true);
       const uint32_t kvb = tc::smem_u32(kv_s), qb0 = tc::smem_u32(q_s), pb0 = tc::smem_u32(p_s);
       const bool s_issuer = warp == 1;
       bool ok = true;
-      int item = 1;
-      if (s_issuer) {
-        auto issue_s = [&](int s, int stage) {   // S_s = Q_s K^T, K in `stage`
-          const uint32_t qb = qb0 + s * kTileBytes, kb = kvb + stage * kTileBytes;
+      int item = 0;                              // ring item counter
+      int nb[2] = {0, 0}, ni[2] = {0, 0};        // blocks / work items per slot so far
+      for (int round = 0, n_done = 0; ok; ++round, ++n_done) {
+        const int i = att_item_index(cta, round, P);
+        if (i >= n_items) break;
+        const AttItem it = att_item(i, n_qt, H_kv_pairs, pairs, G, nh);
+        if (s_issuer) {
+          auto issue_s = [&](int s, int stage) {   // S_s = Q_s K^T, K in `stage`
+            const uint32_t qb = qb0 + s * kTileBytes, kb = kvb + stage * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int hf = kk >> 2, kin = kk & 3;
-            tc::mma_ss(tmem + s * kSlotCols, tc::sw128_desc(qb + hf * kHalfBytes + kin * 32, 16, 1024),
-                       tc::sw128_desc(kb + hf * kHalfBytes + kin * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(&sm->s_full[s]);
-        };
-        ok = tc::mbar_wait(&sm->q_full, 0, abort, hdr, 0x202) && tc::mbar_wait(&sm->kv_full[0], 0, abort, hdr, 0x203);
-        tc::tc_fence_after();
-        if (ok) {
-          for (int s = 0; s < n_slots; ++s) issue_s(s, 0);
-          tc::mma_commit(&sm->kv_empty[0]);
-        }
-        for (int jb = 0; ok && jb + 1 < n_blocks; ++jb) {
-          const int st = item % kKvStages;
-          if (!(ok = tc::mbar_wait(&sm->kv_full[st], (item / kKvStages) & 1, abort, hdr, 0x204))) break;
-          for (int s = 0; s < n_slots; ++s) {
-            if (!(ok = tc::mbar_wait(&sm->s_free[s], jb & 1, abort, hdr, 0x205))) break;
-            tc::tc_fence_after();
-            issue_s(s, st);
-          }
-          if (!ok) break;
-          tc::mma_commit(&sm->kv_empty[st]);
-          item += 2;                             // K_{j+1}, then V_j (the other issuer's)
-        }
-      } else {
-        for (int jb = 0; ok && jb < n_blocks; ++jb) {
-          if (jb + 1 < n_blocks) ++item;         // K_{j+1} (the other issuer's)
-          const int sv = item % kKvStages;
-          if (!(ok = tc::mbar_wait(&sm->kv_full[sv], (item / kKvStages) & 1, abort, hdr, 0x206))) break;
-          const uint32_t vb = kvb + sv * kTileBytes;
-          for (int s = 0; s < n_slots; ++s) {
-            if (!(ok = tc::mbar_wait(&sm->p_full[s], jb & 1, abort, hdr, 0x207))) break;
-            tc::tc_fence_after();
-            const uint32_t pb = pb0 + s * kPBytes;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {      // 16 keys per MMA
+            for (int kk = 0; kk < D / 16; ++kk) {
               const int hf = kk >> 2, kin = kk & 3;
-              tc::mma_ss(tmem + s * kSlotCols + 128, tc::sw128_desc(pb + hf * kHalfBytes + kin * 32, 16, 1024),
-                         tc::sw128_desc(vb + kk * 16 * 128, kHalfBytes, 1024), idesc_o, (jb > 0 || kk > 0) ? 1u : 0u);
+              tc::mma_ss(tmem + s * kSlotCols, tc::sw128_desc(qb + hf * kHalfBytes + kin * 32, 16, 1024),
+                         tc::sw128_desc(kb + hf * kHalfBytes + kin * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
             }
-            tc::mma_commit(&sm->o_done[s]);
+            tc::mma_commit(&sm->s_full[s]);
+          };
+          if (!(ok = tc::mbar_wait(&sm->q_full, n_done & 1, abort, hdr, 0x202))) break;
+          for (int jb = 0; ok && jb < it.n_blocks; ++jb) {   // key tile of block jb: ring item K_0 or K_{jb}
+            const int st = item % kKvStages;
+            if (!(ok = tc::mbar_wait(&sm->kv_full[st], (item / kKvStages) & 1, abort, hdr, 0x204))) break;
+            for (int s = 0; s < it.n_slots; ++s) {
+              const int b = nb[s] + jb;            // the slot's block count over all items
+              if (b > 0 && !(ok = tc::mbar_wait(&sm->s_free[s], (b - 1) & 1, abort, hdr, 0x205))) break;
+              tc::tc_fence_after();
+              issue_s(s, st);
+            }
+            if (!ok) break;
+            tc::mma_commit(&sm->kv_empty[st]);
+            item += jb == 0 ? 1 : 2;             // K_0; later K_{j}, after V_{j-1} (the other issuer's)
           }
           if (!ok) break;
-          tc::mma_commit(&sm->kv_empty[sv]);
-          ++item;
+          item += 1;                             // the item's last V (the other issuer's)
+          tc::mma_commit(&sm->q_free);           // Q no longer read once these MMAs complete
+        } else {
+          item += 1;                             // K_0 (the other issuer's)
+          for (int jb = 0; ok && jb < it.n_blocks; ++jb) {
+            if (jb + 1 < it.n_blocks) ++item;    // K_{j+1} (the other issuer's)
+            const int sv = item % kKvStages;
+            if (!(ok = tc::mbar_wait(&sm->kv_full[sv], (item / kKvStages) & 1, abort, hdr, 0x206))) break;
+            const uint32_t vb = kvb + sv * kTileBytes;
+            for (int s = 0; s < it.n_slots; ++s) {
+              if (!(ok = tc::mbar_wait(&sm->p_full[s], (nb[s] + jb) & 1, abort, hdr, 0x207))) break;
+              // the first PV of an item overwrites O_s: the previous item's epilogue must have read it
+              if (jb == 0 && ni[s] > 0 && !(ok = tc::mbar_wait(&sm->o_free[s], (ni[s] - 1) & 1, abort, hdr, 0x20b)))
+                break;
+              tc::tc_fence_after();
+              const uint32_t pb = pb0 + s * kPBytes;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {    // 16 keys per MMA
+                const int hf = kk >> 2, kin = kk & 3;
+                tc::mma_ss(tmem + s * kSlotCols + 128, tc::sw128_desc(pb + hf * kHalfBytes + kin * 32, 16, 1024),
+                           tc::sw128_desc(vb + kk * 16 * 128, kHalfBytes, 1024), idesc_o,
+                           (jb > 0 || kk > 0) ? 1u : 0u);
+              }
+              tc::mma_commit(&sm->o_done[s]);
+            }
+            if (!ok) break;
+            tc::mma_commit(&sm->kv_empty[sv]);
+            ++item;
+          }
+        }
+        for (int s = 0; s < it.n_slots; ++s) {
+          nb[s] += it.n_blocks;
+          ++ni[s];
         }
       }
       uint64_t* dr = &sm->drain[s_issuer ? 0 : 1];
@@ -274,109 +437,20 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const int s = (warp - 2) >> 2;                 // slot
     const int quad = warp & 3;                     // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;                // row within the query tile
-    const int c = qt * 128 + r;                    // chunk position of the row
-    const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    const uint32_t s_addr = tmem + lane_addr + s * kSlotCols;
-    const uint32_t o_addr = s_addr + 128;
+    const uint32_t s_addr = tmem + ((uint32_t)(quad * 32) << 16) + s * kSlotCols;
     // this row of P in the swizzled operand layout: chunk q of half h at
     // p_row + h * kHalfBytes + ((q ^ (r & 7)) << 4)
     uint8_t* p_row = p_s + s * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
-    if (s < n_slots) {
-      float m_used = -INFINITY, l = 0.f;            // running max of the raw logits, softmax denominator
-      bool ok = true;
-      for (int jb = 0; jb < n_blocks; ++jb) {
-        if (!(ok = warp_wait(&sm->s_full[s], jb & 1, abort, hdr, 0x208))) break;
-        tc::tc_fence_after();
-        uint32_t sv[128];
-        tc::tmem_ld128(s_addr, sv);
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sm->s_free[s]);   // the MMA may now write S_s of the next block
-        const bool hist = jb < nh;
-        // only the last history block (if partial) and the diagonal chunk block have masked keys
-        const bool need_mask = hist ? (jb == nh - 1 && (n_hist & 127) != 0) : (jb - nh == qt);
-        if (need_mask) {
-          // keys of this block visible to row c: [0, lim)
-          const int lim = hist ? n_hist - jb * 128 : c - (jb - nh) * 128 + 1;
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i >= lim) sv[i] = __float_as_uint(-INFINITY);
-        }
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          mx4[i & 3] = fmax3(mx4[i & 3], __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float m_new = fmaxf(m_used, mx);
-        const bool rescale = (m_new - m_used) * scale_log2 > kRescaleThreshold;   // true on the first block
-        float alpha = 1.f;
-        if (rescale) {
-          alpha = ex2_approx((m_used - m_new) * scale_log2);   // 0 on the first block
-          m_used = m_new;
-        }
-        const float neg_m = -m_used * scale_log2;
-        // PV_s of the previous block must be done before P_s is overwritten and before O is rescaled
-        if (jb > 0 && !(ok = warp_wait(&sm->o_done[s], (jb - 1) & 1, abort, hdr, 0x209))) break;
-        float sa[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {             // 8 keys = one 16-byte chunk of P at a time
-          uint32_t w[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i = 8 * q + 2 * j;
-            float x0 = __uint_as_float(sv[i]), x1 = __uint_as_float(sv[i + 1]);
-            fma2(x0, x1, scale_log2, neg_m);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (j & 1) add2(sa[2], sa[3], p0, p1);
-            else add2(sa[0], sa[1], p0, p1);
-            w[j] = pack_bf16x2(p0, p1);
-          }
-          const int hf = q >> 3, ch = q & 7;
-          *reinterpret_cast<uint4*>(p_row + hf * kHalfBytes + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        l = l * alpha + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
-        if (jb > 0 && __any_sync(0xffffffffu, rescale)) {   // O *= alpha in TMEM (rows without a rescale: alpha = 1)
-          tc::tc_fence_after();
-#pragma unroll
-          for (int q4 = 0; q4 < D / 32; ++q4) {
-            uint32_t ov[32];
-            tc::tmem_ld32(o_addr + q4 * 32, ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tc::tmem_st32(o_addr + q4 * 32, ov);
-          }
-          tc::tmem_wait_st();
-        }
-        tc::fence_proxy_async_smem();              // P visible to the tensor core
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sm->p_full[s]);
-      }
-      // epilogue: O / l
-      if (ok && warp_wait(&sm->o_done[s], (n_blocks - 1) & 1, abort, hdr, 0x209)) {
-        tc::tc_fence_after();
-        const int h = h0 + s;
-        const float inv = 1.f / l;
-#pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
-          uint32_t ov[32];
-          tc::tmem_ld32(o_addr + q4 * 32, ov);
-          tc::tmem_wait_ld();
-          if (c < C) {
-            uint4* dst = reinterpret_cast<uint4*>(O + ((size_t)h * C + c) * D + q4 * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv, __uint_as_float(ov[8 * v + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv, __uint_as_float(ov[8 * v + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv, __uint_as_float(ov[8 * v + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv, __uint_as_float(ov[8 * v + 7]) * inv);
-              dst[v] = w;
-            }
-          }
-        }
-        if (lse != nullptr && c < C) lse[(size_t)h * C + c] = m_used * scale_log2 * 0.69314718055994531f + logf(l);
-      }
+    int nb = 0;                                    // blocks of this slot in earlier work items
+    for (int round = 0;; ++round) {
+      const int i = att_item_index(cta, round, P);
+      if (i >= n_items) break;
+      const AttItem it = att_item(i, n_qt, H_kv_pairs, pairs, G, nh);
+      if (s >= it.n_slots) continue;
+      if (!softmax_item<D>(sm, p_row, s, lane, r, s_addr, nb, it.n_blocks, nh, n_hist, it.qt, C, it.h0 + s, scale_log2,
+                           O, lse, hdr))
+        break;
+      nb += it.n_blocks;
     }
   }
   tc::tc_fence_before();
@@ -411,18 +485,22 @@ cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* V
   }
   const int n_qt = (C + 127) / 128;
   const int pairs = (G + 1) / 2;
-  dim3 grid(n_qt * H_kv * pairs);
+  const int n_items = n_qt * H_kv * pairs;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  dim3 grid(n_items < sms ? n_items : sms);     // persistent: one CTA per SM, looping over work items
   const size_t smem = attend_tc_smem(d);
   const float scale_log2 = scale * 1.4426950408889634f;
   if (d == 64) {
     if ((e = ensure_smem((const void*)k_attend_tc<64>, smem)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_attend_tc<64>, grid, dim3(kAttThreads), smem, st, qmap, khmap, vhmap, kcmap, vcmap, n_hist, C,
-                        G, scale_log2, (__nv_bfloat16*)O, lse, hdr)) != cudaSuccess)
+                        G, H_kv, scale_log2, (__nv_bfloat16*)O, lse, hdr)) != cudaSuccess)
       return e;
   } else {
     if ((e = ensure_smem((const void*)k_attend_tc<128>, smem)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_attend_tc<128>, grid, dim3(kAttThreads), smem, st, qmap, khmap, vhmap, kcmap, vcmap, n_hist,
-                        C, G, scale_log2, (__nv_bfloat16*)O, lse, hdr)) != cudaSuccess)
+                        C, G, H_kv, scale_log2, (__nv_bfloat16*)O, lse, hdr)) != cudaSuccess)
       return e;
   }
   count_launches(1);
