@@ -84,6 +84,28 @@ __device__ __forceinline__ void load_rows_n(const T* __restrict__ base, int n, i
 constexpr int kSelCluster = 8;
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
+static_assert(kSelWarps == kSelCluster, "warp q of CTA 0 fetches the list of CTA q");
+static_assert(kRowsPerWarp == 8, "the reduce-scatter below is written for 8 rows");
+
+// Warp sums of 8 rows at once: v[r] is this lane's part of row r; afterwards
+// every lane holds the full sum of row rs_row(lane) (lanes 4k .. 4k+3 share a
+// row).  9 shuffles instead of 8 separate 5-step butterflies.
+__device__ __forceinline__ int rs_row(int lane) { return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1); }
+__device__ __forceinline__ float reduce_scatter8(const float (&v)[8]) {
+  const int lane = threadIdx.x & 31;
+  const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+  float a[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)   // keep rows 4*b4 .. 4*b4+3, send the partner the other four
+    a[j] = (b4 ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, b4 ? v[j] : v[j + 4], 16);
+  float b[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) b[j] = (b3 ? a[j + 2] : a[j]) + __shfl_xor_sync(0xffffffffu, b3 ? a[j] : a[j + 2], 8);
+  float c = (b2 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, b2 ? b[0] : b[1], 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
 
 constexpr int kSelChunkRows = 64;                   // rows per bulk copy / mbarrier
 constexpr size_t kSelStageBytes = 64 * 1024;          // shared-memory staging of Q rows
@@ -105,8 +127,10 @@ static size_t qselect_fused_smem(int per, int G_avg, int D, int sel_p) {
 
 // Top n_sel (<= 32 * P) of the row's keys, split over the cluster as in
 // k_qselect_fused; out receives their positions in ascending order.  lists:
-// (kSelWarps + 1) * 32 * P composites of shared memory.  Ends with a cluster
-// barrier.
+// (kSelWarps + 1) * 32 * P composites of shared memory.  The warps' lists are
+// merged as a tree, then CTA 0's warps fetch the CTAs' lists (one each) and
+// merge those as a tree.  Every CTA passes the same two cluster barriers; CTA
+// 0 alone continues after the second.
 template <int P>
 __device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* keys_s, int n, int t0, int n_sel,
                                   uint64_t* lists, int32_t* __restrict__ out) {
@@ -125,28 +149,39 @@ __device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* ke
     warp_sort_desc<P>(v);
     warp_merge_desc<P>(run, v);
   }
+  // tree merge of the warps' lists: after it list 0 (and warp 0's run) is the CTA's top L
+  auto tree_merge = [&]() {
 #pragma unroll
-  for (int p = 0; p < P; ++p) lists[warp * L + p * 32 + lane] = run[p];
-  __syncthreads();
-  if (warp == 0) {
-    for (int w = 1; w < kSelWarps; ++w) {
-      uint64_t b[P];
+    for (int p = 0; p < P; ++p) lists[warp * L + p * 32 + lane] = run[p];
+    __syncthreads();
+    for (int stride = 1; stride < kSelWarps; stride <<= 1) {
+      if ((warp & (2 * stride - 1)) == 0) {
+        uint64_t b[P];
 #pragma unroll
-      for (int p = 0; p < P; ++p) b[p] = lists[w * L + p * 32 + lane];
-      warp_merge_desc<P>(run, b);
+        for (int p = 0; p < P; ++p) b[p] = lists[(warp + stride) * L + p * 32 + lane];
+        warp_merge_desc<P>(run, b);
+#pragma unroll
+        for (int p = 0; p < P; ++p) lists[warp * L + p * 32 + lane] = run[p];
+      }
+      __syncthreads();
     }
+  };
+  tree_merge();
+  // this CTA's list goes to the spare slot, where CTA 0 reads it
+  if (warp == 0)
 #pragma unroll
-    for (int p = 0; p < P; ++p) lists[kSelWarps * L + p * 32 + lane] = run[p];   // this CTA's top L
+    for (int p = 0; p < P; ++p) lists[kSelWarps * L + p * 32 + lane] = run[p];
+  cluster.sync();                                 // every CTA's list is ready
+  const bool leader = cluster.block_rank() == 0;
+  if (leader) {                                   // warp q of CTA 0 fetches CTA q's list
+    const uint64_t* rl = cluster.map_shared_rank(lists + kSelWarps * L, warp);
+#pragma unroll
+    for (int p = 0; p < P; ++p) run[p] = rl[p * 32 + lane];
   }
-  cluster.sync();
-  if (cluster.block_rank() == 0 && warp == 0) {
-    for (int q = 1; q < kSelCluster; ++q) {
-      const uint64_t* rl = cluster.map_shared_rank(lists + kSelWarps * L, q);
-      uint64_t b[P];
-#pragma unroll
-      for (int p = 0; p < P; ++p) b[p] = rl[p * 32 + lane];
-      warp_merge_desc<P>(run, b);
-    }
+  cluster.sync();                                 // every remote read is done: the other CTAs may finish
+  if (!leader) return;
+  tree_merge();
+  if (warp == 0) {
     // the first n_sel winners, by ascending position (0xFFFFFFFF - position, descending)
 #pragma unroll
     for (int p = 0; p < P; ++p) run[p] = p * 32 + lane < n_sel ? (uint64_t)(uint32_t)run[p] : 0ull;
@@ -155,7 +190,6 @@ __device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* ke
     for (int p = 0; p < P; ++p)
       if (p * 32 + lane < n_sel) out[p * 32 + lane] = (int32_t)(0xFFFFFFFFu - (uint32_t)run[p]);
   }
-  cluster.sync();   // every CTA's list stays alive until CTA 0 has read it
 }
 
 template <typename T, int D>
@@ -250,16 +284,9 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
             ss[r] = fmaf(x[r][j], x[r][j], ss[r]);
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-          for (int r = 0; r < kRowsPerWarp; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
-        if (lane < kRowsPerWarp && c0 + lane < pn) {
-          float v = ss[0];
-#pragma unroll
-          for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? ss[r] : v;
-          norm_s[(size_t)k * per + p0 + c0 + lane] = sqrtf(v);
-        }
+        const float v = reduce_scatter8(ss);
+        const int rr = rs_row(lane);
+        if ((lane & 3) == 0 && c0 + rr < pn) norm_s[(size_t)k * per + p0 + c0 + rr] = sqrtf(v);
       }
     }
 #pragma unroll
@@ -314,15 +341,10 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
 #pragma unroll
           for (int j = 0; j < E; ++j) dot[r] = fmaf(x[r][j], m[j], dot[r]);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-          for (int r = 0; r < kRowsPerWarp; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
-        if (lane < kRowsPerWarp && c0 + lane < pn) {
-          float v = dot[0];
-#pragma unroll
-          for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? dot[r] : v;
-          const int i = p0 + c0 + lane;
+        const float v = reduce_scatter8(dot);
+        const int rr = rs_row(lane);
+        if ((lane & 3) == 0 && c0 + rr < pn) {
+          const int i = p0 + c0 + rr;
           u_s[i] += v / (fmaxf(norm_s[(size_t)k * per + i], kNormEps) * mn);
         }
       }
