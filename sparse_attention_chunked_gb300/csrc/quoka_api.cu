@@ -71,13 +71,24 @@ int num_sms() {
   return n;
 }
 
+// MMA passes of the tensor-core scoring operand.  Mean-pooled rows are fp32
+// and go in as hi + lo bf16 rows (two passes).  Max pooling can score with the
+// bf16 query rows themselves (one pass, a per-row scale in the epilogue), but
+// the scale loads slow the epilogue more than the second pass costs, so the
+// unit rows go in as hi + lo too whenever that operand fits shared memory
+// (up to 256 rows at d = 128); wider operands take the one-pass form.
+int score_npass(const quoka_shape* s, int N_pad, int gqa) {
+  if (gqa != QUOKA_GQA_MAX) return 2;
+  return score_tc_smem(s->d, N_pad, 2, 2) <= 227 * 1024 ? 2 : 1;
+}
+
 // Whether the scoring stage can run on the tensor cores: bf16 keys, at most
-// 512 scoring rows (the TMEM width) and an operand (every row twice, hi and
-// lo) that fits shared memory next to two key stages.
+// 512 scoring rows (the TMEM width) and an operand that fits shared memory
+// next to two key stages.
 bool score_tc_fits(const quoka_shape* s, int N_q, int gqa) {
   if (s->dtype != QUOKA_DTYPE_BF16) return false;
   const int N_pad = score_tc_pad_rows(score_rows(s, N_q, gqa));
-  return N_pad <= 512 && score_tc_smem(s->d, N_pad, 2) <= 227 * 1024;
+  return N_pad <= 512 && score_tc_smem(s->d, N_pad, score_npass(s, N_pad, gqa), 2) <= 227 * 1024;
 }
 
 // Which kernels run (stage 0 = scoring, 1 = attention).  Tensor-core kernels are bf16 only.
@@ -91,7 +102,7 @@ bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage, int N_q 
 //   [header][select scratch][score scratch][chunk intermediates]
 struct Layout {
   size_t qnorm, qpart, qcos, select_end;
-  size_t op_f32, op_bf, score_end;
+  size_t op_f32, op_bf, op_scale, score_end;
   size_t q_idx, scores, sel, ksel, vsel, total;
 };
 
@@ -107,7 +118,8 @@ Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa) {
   const size_t R = (size_t)score_rows(s, N_q > 0 ? N_q : 1, gqa);
   const size_t N_pad = (size_t)score_tc_pad_rows((int)R);
   L.op_f32 = o;   o = align_up(o + H_kv * R * d * 4);
-  L.op_bf = o;    o = align_up(o + H_kv * 2 * N_pad * d * 2);
+  L.op_bf = o;    o = align_up(o + H_kv * (size_t)score_npass(s, (int)N_pad, gqa) * N_pad * d * 2);
+  L.op_scale = o; o = align_up(o + H_kv * N_pad * 4);
   L.score_end = o;
   const size_t n = (size_t)n_sel_of(s, N_q > 0 ? N_q : 1);
   const size_t B_e = (size_t)(B < s->T ? B : s->T);
@@ -159,11 +171,13 @@ int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, 
   const int N_pad = score_tc_pad_rows(R);
   const bool tc = use_tensor_cores(p, s, 0, n);
   if (p.engine == QUOKA_ENGINE_TENSOR && !tc) return QUOKA_ERR_UNSUPPORTED;
-  QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, mode, N_pad, at<float>(ws, L.op_f32),
-                                  tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr, st));
+  float* op_scale = tc && score_npass(s, N_pad, p.gqa) == 1 ? at<float>(ws, L.op_scale) : nullptr;
+  QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, mode, N_pad,
+                                  tc ? nullptr : at<float>(ws, L.op_f32), tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr,
+                                  op_scale, st));
   if (tc)
     return cuda_status(launch_score_tc(s->d, K_hist, head_stride(s), s->H_kv, s->T, at<__nv_bfloat16>(ws, L.op_bf),
-                                       R, scores, at<WsHeader>(ws, 0), num_sms(), st));
+                                       op_scale, R, scores, at<WsHeader>(ws, 0), num_sms(), st));
   return cuda_status(launch_score_simt(s->dtype, s->d, K_hist, head_stride(s), s->H_kv, s->T,
                                        at<float>(ws, L.op_f32), R, scores, st));
 }

@@ -22,17 +22,19 @@ namespace quoka {
 template <typename T, int D>
 __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, const int32_t* __restrict__ q_idx,
                                                       int C, int G, int n, int mode, int R, float* __restrict__ op_f32,
-                                                      __nv_bfloat16* __restrict__ op_bf) {
+                                                      __nv_bfloat16* __restrict__ op_bf, float* __restrict__ op_scale) {
   pdl_launch_dependents();
   pdl_wait();
   constexpr int E = D / 32;
   const int g = blockIdx.y, r = blockIdx.x, N_pad = gridDim.x, lane = threadIdx.x;
+  const int npass = op_scale != nullptr ? 1 : 2;
   if (r >= R) {   // padding row of the tensor-core operand
     if (op_bf != nullptr) {
-      for (int p = 0; p < 2; ++p)
+      for (int p = 0; p < npass; ++p)
 #pragma unroll
         for (int j = 0; j < E; ++j)
-          op_bf[(((size_t)g * 2 + p) * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(0.f);
+          op_bf[(((size_t)g * npass + p) * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(0.f);
+      if (op_scale != nullptr && lane == 0) op_scale[(size_t)g * N_pad + r] = 0.f;
     }
     return;
   }
@@ -49,6 +51,11 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
     }
     ss = warp_sum(ss);
     const float inv = 1.0f / fmaxf(sqrtf(ss), kNormEps);
+    if (op_scale != nullptr) {   // the query row itself (exact in bf16) and its scale
+#pragma unroll
+      for (int j = 0; j < E; ++j) op_bf[((size_t)g * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
+      if (lane == 0) op_scale[(size_t)g * N_pad + r] = inv;
+    }
 #pragma unroll
     for (int j = 0; j < E; ++j) acc[j] = x[j] * inv;
   } else {  // MEAN (pre-aggregation)
@@ -72,7 +79,7 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
 #pragma unroll
     for (int j = 0; j < E; ++j) acc[j] *= invG;
   }
-  if (op_bf != nullptr) {
+  if (op_bf != nullptr && npass == 2) {
 #pragma unroll
     for (int j = 0; j < E; ++j) {
       const __nv_bfloat16 hi = __float2bfloat16_rn(acc[j]);
@@ -81,8 +88,10 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
       op_bf[(((size_t)g * 2 + 1) * N_pad + r) * D + lane + 32 * j] = lo;
     }
   }
+  if (op_f32 != nullptr) {
 #pragma unroll
-  for (int j = 0; j < E; ++j) op_f32[((size_t)g * R + r) * D + lane + 32 * j] = acc[j];
+    for (int j = 0; j < E; ++j) op_f32[((size_t)g * R + r) * D + lane + 32 * j] = acc[j];
+  }
 }
 
 // One thread per history key: its row is held in registers, the scoring rows
@@ -128,20 +137,26 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
 }
 
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
-                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, cudaStream_t st) {
+                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
+                                 cudaStream_t st) {
   const int R = mode == 1 ? G * n : n;
+  if (op_scale != nullptr && (mode != 1 || dtype != 0 || op_bf == nullptr)) return cudaErrorInvalidValue;
   dim3 grid(op_bf != nullptr ? N_pad : R, H_kv);
   cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf);
+      e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n,
+                     mode, R, op_f32, op_bf, op_scale);
     else
-      e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf);
+      e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G,
+                     n, mode, R, op_f32, op_bf, op_scale);
   } else {
     if (d == 64)
-      e = launch_pdl(k_build_operand<float, 64>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf);
+      e = launch_pdl(k_build_operand<float, 64>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R,
+                     op_f32, op_bf, op_scale);
     else
-      e = launch_pdl(k_build_operand<float, 128>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R, op_f32, op_bf);
+      e = launch_pdl(k_build_operand<float, 128>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R,
+                     op_f32, op_bf, op_scale);
   }
   count_launches(1);
   return e;

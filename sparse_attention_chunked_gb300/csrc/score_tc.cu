@@ -5,24 +5,28 @@
 //
 // One pass over the history keys, each read from HBM once.  A CTA owns a
 // contiguous range of 128-key tiles of one KV head.  Per tile:
-//   D[128 keys x N_pad rows] = K_tile[128 x d] . (HI + LO)[N_pad x d]^T
-// (tcgen05, fp32 in TMEM), the keys on the TMEM lanes, so the thread of a key
-// reduces the maximum over the scoring rows from its own lane with no
-// cross-thread step:   score[t] = max_r D[t, r] / |k_t|.
-// HI + LO is the fp32 scoring row (a unit query for max pooling, the
-// pre-aggregated row for mean pooling) split into two bf16 rows by
-// k_build_operand; both MMA passes accumulate into the same TMEM columns, so
-// the epilogue needs no per-row scale.  |k_t| comes from the key tile in
-// shared memory, in fp32.
+//   D[128 keys x N_pad rows] = K_tile[128 x d] . OP[N_pad x d]^T
+// (tcgen05, fp32 in TMEM), the keys on the TMEM lanes, so the threads of a key
+// reduce the maximum over the scoring rows from their own lane:
+//   score[t] = max_r (D[t, r] * s_r) / |k_t|.
+// Two operand forms, both exact to fp32 rounding:
+//  * scaled (max pooling): OP holds the selected query rows as they are
+//    (bf16, exact) and s_r = 1 / |q_r| is applied per column in the epilogue;
+//    one MMA pass.
+//  * hi/lo (mean pooling): the pre-aggregated row is an fp32 vector with no
+//    exact bf16 form, so k_build_operand splits it into hi + lo bf16 rows and
+//    both passes accumulate into the same TMEM columns; s_r = 1.
+// |k_t| comes from the key tile in shared memory, in fp32.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads (operand once, then a ring
-// of key tiles), warp 1 owns TMEM and issues the MMAs, warps 2-5 are the
-// epilogue, one key per thread.  Shared memory is left to the tensor core's
-// operand reads while an accumulator is being drained: the epilogue reads the
-// key tile for |k|^2 before it waits for the accumulator, and between
-// "accumulator full" and "accumulator free" it touches only TMEM and
-// registers.  Every wait is bounded; on a timeout the CTA records
-// QUOKA_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM and exits.
+// Warp roles (320 threads): warp 0 issues TMA loads (operand once, then a ring
+// of key tiles), warp 1 owns TMEM and issues the MMAs, warps 2-9 are the
+// epilogue: the two warps of a TMEM lane quadrant share its 32 keys, each
+// taking half of the columns (and half of |k|^2), and combine through shared
+// memory.  The accumulator is a ring of two TMEM units of up to 256 columns;
+// a tile with more than 256 scoring rows fills both in turn, so the epilogue
+// drains one unit while the tensor core fills the other.  Every wait is
+// bounded; on a timeout the CTA records QUOKA_ERR_TIMEOUT, lets in-flight
+// copies and MMAs land, frees TMEM and exits.
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -31,12 +35,13 @@ namespace quoka {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kScoreThreads = 192;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kScoreThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 8;
+constexpr int kUnitCols = 256;     // widest accumulator unit (one MMA's N)
 
-// Rows of one operand TMA box: it must divide NT = 2 * N_pad (<= 512) and be <= 256.
-__host__ __device__ inline int op_box_rows(int NT) { return NT <= 256 ? NT : NT / 2; }
+// Rows of one operand TMA box: at most 256 and a divisor of NT (a multiple of 64).
+__host__ __device__ inline int op_box_rows(int NT) { return NT % 256 == 0 ? 256 : NT % 128 == 0 ? 128 : 64; }
 
 // Bounded wait done by lane 0 only, result broadcast, so the warp stays converged.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, WsHeader* hdr,
@@ -46,6 +51,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// Barrier of the two epilogue warps of one TMEM lane quadrant (ids 1..4).
+__device__ __forceinline__ void pair_sync(int quad) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+}
+
 struct ScoreSmem {
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];
@@ -53,6 +63,8 @@ struct ScoreSmem {
   uint64_t acc_empty[2];
   uint64_t op_full;
   uint64_t drain;
+  float part_max[2][4][32];     // upper warp of a quadrant -> lower warp, by tile parity
+  float part_ss[2][4][32];
   uint32_t tmem_base;
   int abort;
 };
@@ -63,42 +75,73 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// Maximum over n (32 or 64) TMEM columns of this thread's lane starting at
-// taddr; columns at index >= lim (the operand's padding rows) are skipped.
-template <int N>
-__device__ __forceinline__ float tmem_max(uint32_t taddr, int lim, float m) {
+// (a0, a1) * (b0, b1) elementwise, one packed fp32 multiply.
+__device__ __forceinline__ void fmul2(float& a0, float& a1, float b0, float b1) {
+  uint64_t x, y, z;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(z));
+}
+
+// Maximum over N (32 or 64) TMEM columns of this thread's lane starting at
+// taddr, each multiplied by its row scale sc[j] when SCALED; columns at index
+// >= lim (the operand's padding rows) are skipped.
+template <int N, bool SCALED>
+__device__ __forceinline__ float tmem_max(uint32_t taddr, const float* sc, int lim, float m) {
   uint32_t v[N];
+  float4 s4[SCALED ? N / 4 : 1];
+  if constexpr (SCALED) {
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j) s4[j] = reinterpret_cast<const float4*>(sc)[j];   // same address in every lane
+  }
   if constexpr (N == 64) tc::tmem_ld64(taddr, v); else tc::tmem_ld32(taddr, v);
+  float x[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) x[j] = __uint_as_float(v[j]);
+  if constexpr (SCALED) {
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j) {
+      fmul2(x[4 * j], x[4 * j + 1], s4[j].x, s4[j].y);
+      fmul2(x[4 * j + 2], x[4 * j + 3], s4[j].z, s4[j].w);
+    }
+  }
   if (lim < N) {
 #pragma unroll
     for (int j = 0; j < N; ++j)
-      if (j >= lim) v[j] = __float_as_uint(-INFINITY);
+      if (j >= lim) x[j] = -INFINITY;
   }
   float m0 = m, m1 = -INFINITY;
 #pragma unroll
   for (int j = 0; j < N / 4; ++j) {
-    m0 = fmax3(m0, __uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
-    m1 = fmax3(m1, __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+    m0 = fmax3(m0, x[4 * j], x[4 * j + 1]);
+    m1 = fmax3(m1, x[4 * j + 2], x[4 * j + 3]);
   }
   return fmaxf(m0, m1);
 }
 
-// Operand rows in shared memory: [HALVES][NT = 2 * N_pad][128 B]; row
-// p * N_pad + r is pass p (0 = hi, 1 = lo) of scoring row r.
-template <int D>
+// Operand rows in shared memory: [HALVES][NT = NPASS * N_pad][128 B]; row
+// p * N_pad + r is pass p of scoring row r.  Column chunk c of a tile covers
+// scoring rows [c * cw, c * cw + width) and goes to accumulator unit q & 1,
+// q counting (tile, chunk) pairs.
+template <int D, bool SCALED>
 __global__ void __launch_bounds__(kScoreThreads, 1)
-    k_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap, int T_len, int R,
-               int N_pad, int nst, int nacc, uint32_t tmem_cols, float* __restrict__ scores, WsHeader* hdr) {
+    k_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
+               const float* __restrict__ op_scale, int T_len, int R, int N_pad, int nst, int cw,
+               uint32_t tmem_cols, float* __restrict__ scores, WsHeader* hdr) {
   constexpr int HALVES = D / 64;
+  constexpr int NPASS = SCALED ? 1 : 2;
   constexpr uint32_t kHalfBytes = kTileKeys * 128;            // one 64-column half of a key tile
   constexpr uint32_t kStageBytes = HALVES * kHalfBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int NT = 2 * N_pad;
+  const int NT = NPASS * N_pad;
+  const int nch = (N_pad + cw - 1) / cw;
   const uint32_t op_bytes = (uint32_t)HALVES * NT * 128;
   uint8_t* op_s = smem;                                         // [HALVES][NT][128 B]
   uint8_t* ktiles = smem + op_bytes;                            // [nst][HALVES][128][128 B]
-  ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(ktiles + (size_t)nst * kStageBytes);
+  float* sc_s = reinterpret_cast<float*>(ktiles + (size_t)nst * kStageBytes);   // [N_pad] row scales
+  ScoreSmem* sm = reinterpret_cast<ScoreSmem*>(sc_s + (SCALED ? N_pad : 0));
 
   const int g = blockIdx.y;
   const int tiles_head = (T_len + kTileKeys - 1) / kTileKeys;
@@ -112,7 +155,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       tc::mbar_init(&sm->kv_full[s], 1);
       tc::mbar_init(&sm->kv_empty[s], 1 + kEpiWarps);
     }
-    for (int a = 0; a < nacc; ++a) {
+    for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&sm->acc_full[a], 1);
       tc::mbar_init(&sm->acc_empty[a], kEpiWarps);
     }
@@ -142,11 +185,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       for (int it = 0; it < ntiles && it < nst; ++it)
         for (int hf = 0; hf < HALVES; ++hf) tc::tma_prefetch_l2_3d(&kmap, hf * 64, (tile0 + it) * kTileKeys, g);
       pdl_wait();                               // the operand comes from the previous kernel
-      tc::mbar_arrive_expect_tx(&sm->op_full, op_bytes);
+      tc::mbar_arrive_expect_tx(&sm->op_full, op_bytes + (SCALED ? (uint32_t)N_pad * 4 : 0u));
       const int nb = op_box_rows(NT);
       for (int hf = 0; hf < HALVES; ++hf)
         for (int rb = 0; rb < NT; rb += nb)
-          tc::tma_load_3d(op_s + ((size_t)hf * NT + rb) * 128, &omap, &sm->op_full, hf * 64, rb, g);
+          tc::tma_load_3d(op_s + ((size_t)hf * NT + rb) * 128, &omap, &sm->op_full,
+                          hf * 64, rb, g);
+      if constexpr (SCALED) tc::bulk_load(sc_s, op_scale + (size_t)g * N_pad, (uint32_t)N_pad * 4, &sm->op_full);
       int issued = 0;
       for (int it = 0; it < ntiles; ++it) {
         const int s = it % nst;
@@ -169,48 +214,56 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       bool ok = tc::mbar_wait(&sm->op_full, 0, abort, hdr, 0x102);
       tc::tc_fence_after();
       const uint32_t b_base = tc::smem_u32(op_s);
+      int q = 0;
       for (int it = 0; ok && it < ntiles; ++it) {
-        const int s = it % nst, a = it % nacc;
-        if (!tc::mbar_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x103)) break;
-        if (it >= nacc && !tc::mbar_wait(&sm->acc_empty[a], ((it / nacc) - 1) & 1, abort, hdr, 0x104)) break;
-        tc::tc_fence_after();
+        const int s = it % nst;
+        if (!(ok = tc::mbar_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x103))) break;
         const uint32_t a_base = tc::smem_u32(ktiles + (size_t)s * kStageBytes);
-        for (int nc = 0; nc < N_pad; nc += 256) {
-          const int n_this = N_pad - nc < 256 ? N_pad - nc : 256;
-          const uint32_t idesc = tc::idesc_bf16_f32(128, n_this, false);
+        for (int c = 0; c < nch; ++c, ++q) {
+          const int u = q & 1;
+          if (q >= 2 && !(ok = tc::mbar_wait(&sm->acc_empty[u], ((q >> 1) - 1) & 1, abort, hdr, 0x104))) break;
+          tc::tc_fence_after();
+          const int c0 = c * cw, width = min(cw, N_pad - c0);
+          const uint32_t idesc = tc::idesc_bf16_f32(128, width, false);
 #pragma unroll
-          for (int p = 0; p < 2; ++p)
+          for (int p = 0; p < NPASS; ++p)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const int hf = kk >> 2, kin = kk & 3;
               const uint64_t adesc = tc::sw128_desc(a_base + hf * kHalfBytes + kin * 32, 16, 1024);
               const uint64_t bdesc =
-                  tc::sw128_desc(b_base + ((uint32_t)hf * NT + p * N_pad + nc) * 128 + kin * 32, 16, 1024);
-              tc::mma_ss(tmem + (uint32_t)(a * N_pad + nc), adesc, bdesc, idesc, (p | kk) > 0 ? 1u : 0u);
+                  tc::sw128_desc(b_base + ((uint32_t)hf * NT + p * N_pad + c0) * 128 + kin * 32, 16, 1024);
+              tc::mma_ss(tmem + (uint32_t)(u * cw), adesc, bdesc, idesc, (p | kk) > 0 ? 1u : 0u);
             }
+          if (c == nch - 1) tc::mma_commit(&sm->kv_empty[s]);
+          tc::mma_commit(&sm->acc_full[u]);
         }
-        tc::mma_commit(&sm->kv_empty[s]);
-        tc::mma_commit(&sm->acc_full[a]);
       }
       tc::mma_commit(&sm->drain);        // completes once every MMA above has finished
       tc::mbar_drain(&sm->drain, 0);
     }
   } else {
-    // ------------------------------------------------------------ epilogue: one key per thread
+    // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;                      // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;               // which half of the columns (and of |k|^2)
     const int row = quad * 32 + lane;               // key within the tile
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    bool alive = true;                              // false once a wait gave up (warp-uniform)
+    bool alive = ntiles > 0;                        // false once a wait gave up (warp-uniform)
+    if constexpr (SCALED) {
+      if (alive) alive = warp_wait(&sm->op_full, 0, abort, hdr, 0x107);   // sc_s is in place
+    }
+    int q = 0;
     for (int it = 0; it < ntiles; ++it) {
-      const int s = it % nst, a = it % nacc;
+      const int s = it % nst;
       if (alive) alive = warp_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105);
       float ss = 0.f;
       if (alive) {
-        // |k|^2 from the tile (16-byte chunks; chunk c of row r sits at c ^ (r & 7))
+        // this half's share of |k|^2 (16-byte chunks; chunk c of row r sits at c ^ (r & 7))
         const uint8_t* rp = ktiles + (size_t)s * kStageBytes + (row >> 3) * 1024 + (row & 7) * 128;
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-        for (int chunk = 0; chunk < HALVES * 8; ++chunk) {
+        for (int j = 0; j < HALVES * 4; ++j) {
+          const int chunk = half * HALVES * 4 + j;
           const int hf = chunk >> 3, c = chunk & 7;
           const uint4 v = *reinterpret_cast<const uint4*>(rp + hf * kHalfBytes + ((c ^ (row & 7)) << 4));
           // bf16 pair -> two fp32 (exact: shift into the high half)
@@ -231,20 +284,36 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm->kv_empty[s]);
-      if (alive) alive = warp_wait(&sm->acc_full[a], (it / nacc) & 1, abort, hdr, 0x106);
       float m = -INFINITY;
-      if (alive) {
-        tc::tc_fence_after();
-        const uint32_t base = tmem + lane_addr + (uint32_t)(a * N_pad);
-        int c0 = 0;
-        for (; c0 + 64 <= N_pad; c0 += 64) m = tmem_max<64>(base + c0, R - c0, m);
-        if (c0 < N_pad) m = tmem_max<32>(base + c0, R - c0, m);
-        tc::tc_fence_before();
+      for (int c = 0; c < nch; ++c, ++q) {
+        const int u = q & 1;
+        if (alive) alive = warp_wait(&sm->acc_full[u], (q >> 1) & 1, abort, hdr, 0x106);
+        if (alive) {
+          tc::tc_fence_after();
+          const int c0 = c * cw, hw = min(cw, N_pad - c0) >> 1;   // this warp's columns: a multiple of 32
+          const int col = c0 + half * hw;
+          const uint32_t base = tmem + lane_addr + (uint32_t)(u * cw + half * hw);
+          int j = 0;
+          for (; j + 64 <= hw; j += 64) m = tmem_max<64, SCALED>(base + j, sc_s + col + j, R - (col + j), m);
+          if (j < hw) m = tmem_max<32, SCALED>(base + j, sc_s + col + j, R - (col + j), m);
+          tc::tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm->acc_empty[u]);
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm->acc_empty[a]);
-      const int t = (tile0 + it) * kTileKeys + row;
-      if (alive && t < T_len) scores[(size_t)g * T_len + t] = m * (1.0f / fmaxf(sqrtf(ss), kNormEps));
+      // the quadrant's upper warp hands its half to the lower warp, which writes the score
+      const int buf = it & 1;
+      if (half == 1) {
+        sm->part_max[buf][quad][lane] = m;
+        sm->part_ss[buf][quad][lane] = ss;
+      }
+      pair_sync(quad);
+      if (half == 0) {
+        m = fmaxf(m, sm->part_max[buf][quad][lane]);
+        ss += sm->part_ss[buf][quad][lane];
+        const int t = (tile0 + it) * kTileKeys + row;
+        if (alive && t < T_len) scores[(size_t)g * T_len + t] = m * (1.0f / fmaxf(sqrtf(ss), kNormEps));
+      }
     }
   }
   tc::tc_fence_before();
@@ -255,30 +324,43 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
 }
 
+template <int D, bool SCALED>
+cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t st, const CUtensorMap& kmap, const CUtensorMap& omap,
+                       const float* op_scale, int T_len, int R, int N_pad, int nst, int cw, uint32_t cols,
+                       float* scores, WsHeader* hdr) {
+  cudaError_t e = ensure_smem((const void*)k_score_tc<D, SCALED>, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_score_tc<D, SCALED>, grid, dim3(kScoreThreads), smem, st, kmap, omap, op_scale, T_len, R, N_pad,
+                    nst, cw, cols, scores, hdr);
+}
+
 }  // namespace
 
-// Scoring rows padded to a multiple of 32: MMA N must be a multiple of 16 and
-// the epilogue reads TMEM 32 columns at a time.
-int score_tc_pad_rows(int R) { return (R + 31) / 32 * 32; }
+// Scoring rows padded to a multiple of 64: each epilogue warp then reads its
+// half of a column chunk from TMEM 32 columns at a time.
+int score_tc_pad_rows(int R) { return (R + 63) / 64 * 64; }
 
-size_t score_tc_smem(int d, int N_pad, int nst) {
-  return 1024 + (size_t)2 * (d / 64) * N_pad * 128 + (size_t)nst * (d / 64) * kTileKeys * 128 + sizeof(ScoreSmem);
+size_t score_tc_smem(int d, int N_pad, int npass, int nst) {
+  return 1024 + (size_t)npass * (d / 64) * N_pad * 128 + (size_t)nst * (d / 64) * kTileKeys * 128 +
+         (npass == 1 ? (size_t)N_pad * 4 : 0) + sizeof(ScoreSmem);
 }
 
 cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
-                            int R, float* scores, WsHeader* hdr, int num_sms, cudaStream_t st) {
+                            const float* op_scale, int R, float* scores, WsHeader* hdr, int num_sms,
+                            cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
   const int N_pad = score_tc_pad_rows(R);
+  const int npass = op_scale != nullptr ? 1 : 2;
   if (N_pad > 512) return cudaErrorInvalidValue;
   const size_t budget = 227 * 1024;
   int nst = kMaxStages;
-  while (nst > 2 && score_tc_smem(d, N_pad, nst) > budget) --nst;
-  const size_t smem = score_tc_smem(d, N_pad, nst);
+  while (nst > 2 && score_tc_smem(d, N_pad, npass, nst) > budget) --nst;
+  const size_t smem = score_tc_smem(d, N_pad, npass, nst);
   if (smem > budget) return cudaErrorInvalidValue;
-  const int NT = 2 * N_pad;
-  const int nacc = 2 * N_pad <= 512 ? 2 : 1;
+  const int NT = npass * N_pad;
+  const int cw = N_pad < kUnitCols ? N_pad : kUnitCols;   // accumulator unit width
   uint32_t cols = 32;
-  while (cols < (uint32_t)(nacc * N_pad)) cols <<= 1;
+  while (cols < (uint32_t)(2 * cw)) cols <<= 1;
   CUtensorMap kmap, omap;
   cudaError_t e = make_tmap_bf16_3d(&kmap, K, d, T_len, H_kv, (uint64_t)d * 2, (uint64_t)head_stride * 2, 64, 128);
   if (e != cudaSuccess) return e;
@@ -289,19 +371,13 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
   int per_head = (num_sms + H_kv - 1) / H_kv;
   if (per_head > tiles_head) per_head = tiles_head;
   dim3 grid(per_head, H_kv);
-  if (d == 64) {
-    e = ensure_smem((const void*)k_score_tc<64>, smem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(k_score_tc<64>, grid, dim3(kScoreThreads), smem, st, kmap, omap, T_len, R, N_pad, nst, nacc, cols,
-                   scores, hdr);
-    if (e != cudaSuccess) return e;
-  } else {
-    e = ensure_smem((const void*)k_score_tc<128>, smem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(k_score_tc<128>, grid, dim3(kScoreThreads), smem, st, kmap, omap, T_len, R, N_pad, nst, nacc,
-                   cols, scores, hdr);
-    if (e != cudaSuccess) return e;
-  }
+  if (d == 64)
+    e = npass == 1 ? launch_one<64, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, scores, hdr)
+                   : launch_one<64, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, scores, hdr);
+  else
+    e = npass == 1 ? launch_one<128, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, scores, hdr)
+                   : launch_one<128, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, scores, hdr);
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }

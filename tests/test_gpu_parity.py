@@ -86,6 +86,10 @@ SMALL = [
     ("nq_above_C", dict(H_q=4, H_kv=1, d=64, C=20, T=300, N_q=64, B=31, dtype="fp32")),
     ("single_row_chunk", dict(H_q=4, H_kv=2, d=128, C=1, T=257, N_q=4, B=17, dtype="bf16")),
     ("iid_recipe_bf16", dict(H_q=4, H_kv=4, d=64, C=128, T=1024, N_q=16, B=256, dtype="bf16", recipe="iid_outliers")),
+    # max pooling with 320 scoring rows: two accumulator chunks, the second 64 wide
+    ("gqa5_bf16_320_rows", dict(H_q=10, H_kv=2, d=128, C=256, T=2000, N_q=64, B=300, dtype="bf16")),
+    # max pooling with 576 scoring rows: wider than TMEM, the CUDA-core scorer takes it
+    ("gqa8_bf16_576_rows", dict(H_q=16, H_kv=2, d=64, C=100, T=900, N_q=72, B=111, dtype="bf16")),
 ]
 
 
