@@ -37,6 +37,7 @@ from sparse_attention_chunked_gb300 import workloads as wl  # noqa: E402
 METRIC = "chunk tokens/sec for QUOKA select+attend at 32K/128K history; % HBM/TC roofline"
 WORKLOADS = {"gqa32k": wl.GQA_32K_BF16, "gqa128k": wl.GQA_128K_BF16,
              "tiny": wl.TINY_MHA_FP32}   # tiny: the small parity case, for quick checks of the harness
+RAGGED = {"ragged8": wl.RAGGED_8x_BF16}  # one quoka_chunk_attend_varlen call over a ragged batch
 FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 flop x max SM clock
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one tensor-core attention launch per
@@ -437,6 +438,192 @@ def run_quoka(args, rank, world, local_rank):
     return res
 
 
+def run_quoka_ragged(args, rank, world, local_rank):
+    """The ragged batch: one quoka_chunk_attend_varlen call per step over every sequence's chunk."""
+    from sparse_attention_chunked_gb300 import build as qbuild
+    from sparse_attention_chunked_gb300 import quoka as q
+
+    qbuild.build()
+    q.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = RAGGED[args.workload]
+    seqs = wl.make_ragged(cfg, args.seed)
+    pk = wl.pack_varlen(seqs)
+    cu_T, cu_C = pk["cu_T"], pk["cu_C"]
+    names = ("Q", "K_hist", "V_hist", "K_chunk", "V_chunk")
+    base = tuple(pk[k].to(dev) for k in names)
+    sets = [base] + [tuple(t.clone() for t in base) for _ in range(INPUT_SETS - 1)]
+    set_bytes = sum(t.numel() * t.element_size() for t in base)
+    vshape = q.varlen_shape_of(len(seqs), cfg.H_q, cfg.H_kv, cfg.d, base[0].dtype)
+    params = q.params_of(args.gqa, args.engine)
+    T_max = max(b - a for a, b in zip(cu_T, cu_T[1:]))
+    n_ws = max(q.quoka_workspace_size_varlen(vshape, cu_T, cu_C, cfg.N_q, cfg.B, params),
+               q.quoka_workspace_size_varlen(vshape, cu_T, cu_C, cfg.N_q, T_max, params))
+    ws = torch.zeros(n_ws, dtype=torch.uint8, device=dev)
+    O = torch.empty_like(base[0])
+    B_s = [min(cfg.B, b - a) for a, b in zip(cu_T, cu_T[1:])]
+    sel = torch.empty(cfg.H_kv * sum(B_s), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    new_events = lambda k: [torch.cuda.Event(enable_timing=True) for _ in range(k)]  # noqa: E731
+
+    def call(xs, B, O_out, sel_out=None):
+        q.quoka_chunk_attend_varlen(vshape, cu_T, cu_C, *xs, cfg.N_q, B, params, O_out, None, sel_out, ws, stream)
+
+    with torch.cuda.stream(stream):
+        call(base, cfg.B, O, sel)       # also leaves every sequence's kept set in sel
+        call(base, cfg.B, O)
+    torch.cuda.synchronize(dev)
+    step_graphs = []
+    for si, xs in enumerate(sets):
+        g = torch.cuda.CUDAGraph()
+        before = q.quoka_launch_count()
+        with torch.cuda.graph(g, stream=stream):
+            call(xs, cfg.B, O)
+        if si == 0:
+            launches_per_step = q.quoka_launch_count() - before
+        step_graphs.append(g)
+    # the attention stage alone over the batch (kept rows gathered once up front), for the roofline
+    att_fns, att_flops, off = [], 0, 0
+    for s, x in enumerate(seqs):
+        C, T = cu_C[s + 1] - cu_C[s], cu_T[s + 1] - cu_T[s]
+        sub = wl.ChunkConfig("seq", cfg.H_q, cfg.H_kv, cfg.d, C, T, cfg.N_q, cfg.B, cfg.dtype, "massive_act")
+        sh = q.Shape(0, cfg.H_q, cfg.H_kv, C, T, cfg.d, 0)
+        part = lambda t, h, a, b: t[h * cfg.d * a:h * cfg.d * b]  # noqa: E731
+        Qs = part(base[0], cfg.H_q, cu_C[s], cu_C[s + 1]).view(cfg.H_q, C, cfg.d)
+        Kh = part(base[1], cfg.H_kv, cu_T[s], cu_T[s + 1]).view(cfg.H_kv, T, cfg.d)
+        Vh = part(base[2], cfg.H_kv, cu_T[s], cu_T[s + 1]).view(cfg.H_kv, T, cfg.d)
+        Kc = part(base[3], cfg.H_kv, cu_C[s], cu_C[s + 1]).view(cfg.H_kv, C, cfg.d)
+        Vc = part(base[4], cfg.H_kv, cu_C[s], cu_C[s + 1]).view(cfg.H_kv, C, cfg.d)
+        sl = sel[cfg.H_kv * off:cfg.H_kv * (off + B_s[s])].view(cfg.H_kv, B_s[s])
+        off += B_s[s]
+        Ks = torch.empty((cfg.H_kv, B_s[s], cfg.d), dtype=Qs.dtype, device=dev)
+        Vs = torch.empty_like(Ks)
+        q.quoka_gather(sh, Kh, Vh, sl, B_s[s], Ks, Vs, stream)
+        Os = torch.empty_like(Qs)
+        att_fns.append((sh, Qs, Ks, Vs, B_s[s], Kc, Vc, Os))
+        att_flops += stage_work(sub, args.gqa)["attend"]["flops"]
+    torch.cuda.synchronize(dev)
+    att_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(att_graph, stream=stream):
+        for (sh, Qs, Ks, Vs, b, Kc, Vc, Os) in att_fns:
+            q.quoka_sparse_attend(sh, Qs, Ks, Vs, b, Kc, Vc, params, Os, None, ws, stream)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        t_w = time.perf_counter()
+        done = 0
+        while done < args.warmup or time.perf_counter() - t_w < 0.5:
+            for g in step_graphs:
+                g.replay()
+            att_graph.replay()
+            done += 1
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e_rot = new_events(2)
+        torch.cuda.nvtx.range_push("timed_steps")
+        e_rot[0].record(stream)
+        for k in range(args.steps):
+            step_graphs[k % INPUT_SETS].replay()
+        e_rot[1].record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize(dev)
+        barrier()
+        att = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.zero_()
+            e = new_events(2)
+            e[0].record(stream)
+            att_graph.replay()
+            e[1].record(stream)
+            att.append(e)
+        dense = []
+        Od = torch.empty_like(O)
+        if not args.no_dense:
+            call(base, T_max, Od)      # a budget covering every history: dense chunked attention
+            for _ in range(max(3, args.steps // 4)):
+                flush.zero_()
+                e = new_events(2)
+                e[0].record(stream)
+                call(base, T_max, Od)
+                e[1].record(stream)
+                dense.append(e)
+        torch.cuda.synchronize(dev)
+    assert q.quoka_get_last_device_error(ws, stream) == 0
+    step_ms = max_over_ranks(e_rot[0].elapsed_time(e_rot[1]) / args.steps, dev)
+    att_ms = statistics.mean(a.elapsed_time(b) for a, b in att)
+    dense_ms = statistics.mean(a.elapsed_time(b) for a, b in dense) if dense else None
+
+    # end to end: the packed chunk tensors come from pinned host memory, O goes back
+    host = [pk[k].pin_memory() for k in ("Q", "K_chunk", "V_chunk")]
+    devb = [torch.empty_like(base[i]) for i in (0, 3, 4)]
+    Oh = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    O2 = torch.empty_like(O)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = Oh.numel() * Oh.element_size()
+    with torch.cuda.stream(stream):
+        ets = []
+        for k in range(args.warmup + args.steps):
+            flush.zero_()
+            e = new_events(2)
+            e[0].record(stream)
+            for hd, dv in zip(host, devb):
+                dv.copy_(hd, non_blocking=True)
+            call((devb[0], base[1], base[2], devb[1], devb[2]), cfg.B, O2)
+            Oh.copy_(O2, non_blocking=True)
+            e[1].record(stream)
+            if k >= args.warmup:
+                ets.append(e)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ets), dev)
+    clocks = sampler.stop()
+    assert torch.equal(O2, O), "the end-to-end call and the timed steps disagree"
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    tokens = cu_C[-1]
+    achieved = att_flops / (att_ms * 1e-3) / 1e12
+    res = {
+        "metric": METRIC,
+        "value": round(job_throughput(tokens, world, step_ms), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded massive-activation recipe per sequence, log-uniform history lengths)",
+        "config": {"workload": cfg.name, "nseq": len(seqs), "H_q": cfg.H_q, "H_kv": cfg.H_kv, "d": cfg.d,
+                   "C": cfg.C, "T_per_seq": [b - a for a, b in zip(cu_T, cu_T[1:])], "N_q": cfg.N_q, "B": cfg.B,
+                   "gqa_pool": args.gqa, "engine": args.engine,
+                   "l2": f"inputs larger than L2: the timed steps rotate over {INPUT_SETS} copies of the packed "
+                         f"inputs ({INPUT_SETS * set_bytes / 2**20:.0f} MB), no flush",
+                   "timing": "step = one CUDA graph of one quoka_chunk_attend_varlen call, K steps back to back",
+                   "parallelism": f"replicas x{world}"},
+        "impl": "quoka",
+        "gpu_launches": int(launches_per_step * args.steps),
+        "roofline": {"kernel": "attend (all sequences)", "bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": round(peaks["bf16_tflops"], 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4), "peak_source": peaks["source"],
+                     "traffic": None, "traffic_unit": "bytes/launch"},
+        "attend_ms_per_batch": round(att_ms, 5),
+        "dense": None if dense_ms is None else {"ms_per_step": round(dense_ms, 4),
+                                                "speedup": round(dense_ms / step_ms, 2)},
+        "e2e": {"value": round(tokens * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_ragged(cfg, seqs, args.gqa)
+    return res
+
+
 # ---------------------------------------------------------------- the CPU oracle
 
 def _blas_threads():
@@ -480,7 +667,57 @@ def cpu_baseline(cfg, x, gqa, groups=None):
                       f"({cfg.G} query heads each), {t:.1f} s measured, scaled to a whole chunk"}
 
 
+def cpu_baseline_ragged(cfg, seqs, gqa):
+    """The oracle on one KV group of every sequence, scaled by H_kv to the whole batch."""
+    from oracle import quoka_oracle as qo
+    t = 0.0
+    for x in seqs:
+        args = _oracle_inputs(x, 0, cfg.G)
+        t0 = time.perf_counter()
+        qo.chunk_attend(*args, cfg.N_q, cfg.B, gqa)
+        t += time.perf_counter() - t0
+    tokens = sum(x.Q.shape[1] for x in seqs)
+    return {"value": round(tokens / (t * cfg.H_kv), 2), "unit": "tokens/s", "cores": _blas_threads(),
+            "kind": "oracle", "sample": f"numpy float64 oracle, KV group 0 of each of the {len(seqs)} sequences "
+                                        f"({cfg.G} query heads each), {t:.1f} s measured, scaled x{cfg.H_kv}"}
+
+
+def run_reference_ragged(args, rank, world):
+    """The oracle on the ragged batch: each step is KV group (step mod H_kv) of every sequence, x H_kv."""
+    if rank != 0:
+        return None
+    cfg = RAGGED[args.workload]
+    seqs = wl.make_ragged(cfg, args.seed)
+    from oracle import quoka_oracle as qo
+    times = []
+    for k in range(args.warmup + args.steps):
+        g = k % cfg.H_kv
+        t0 = time.perf_counter()
+        for x in seqs:
+            qo.chunk_attend(*_oracle_inputs(x, g, cfg.G), cfg.N_q, cfg.B, args.gqa)
+        if k >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_batch = statistics.mean(times) * cfg.H_kv
+    tokens = sum(x.Q.shape[1] for x in seqs)
+    value = round(tokens / per_batch, 2)
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(per_batch * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "nseq": len(seqs), "H_q": cfg.H_q, "H_kv": cfg.H_kv, "d": cfg.d,
+                   "C": cfg.C, "N_q": cfg.N_q, "B": cfg.B, "gqa_pool": args.gqa, "parallelism": "host cores"},
+        "impl": "reference",
+        "gpu_launches": 0,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+                         "sample": f"each step: one of {cfg.H_kv} KV groups of every sequence through the numpy "
+                                   f"float64 oracle, scaled x{cfg.H_kv} to the whole batch"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, rank, world):
+    if args.workload in RAGGED:
+        return run_reference_ragged(args, rank, world)
     if rank != 0:
         return None
     cfg = WORKLOADS[args.workload]
@@ -518,7 +755,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["quoka", "reference"], default="quoka")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa32k")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(RAGGED), default="gqa32k")
     ap.add_argument("--gqa", choices=["max", "mean"], default="max")
     ap.add_argument("--engine", choices=["auto", "simt", "tensor"], default="auto")
     ap.add_argument("--seed", type=int, default=0)
@@ -532,7 +769,8 @@ def main(argv=None):
         res = run_reference(args, rank, world)     # rank 0 alone; other ranks exit without work
     else:
         dist_init("nccl")
-        res = run_quoka(args, rank, world, local_rank)
+        run = run_quoka_ragged if args.workload in RAGGED else run_quoka
+        res = run(args, rank, world, local_rank)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if torch.distributed.is_available() and torch.distributed.is_initialized():

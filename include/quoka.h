@@ -29,7 +29,8 @@
  * index arrays are int32.
  *
  * Pointers: every tensor pointer is a DEVICE pointer (or managed memory)
- * owned by the caller and 16-byte aligned; the library never allocates,
+ * owned by the caller and 16-byte aligned (the lse and sel_out outputs of
+ * quoka_chunk_attend and its ragged form: 4-byte); the library never allocates,
  * frees or synchronises on these paths.  `stream` is a cudaStream_t (NULL is
  * the legacy default stream); every call only enqueues work on it and
  * returns.  Results are valid once the stream reaches that point.
@@ -189,6 +190,48 @@ int quoka_chunk_attend(const quoka_shape* shape, const void* Q, const void* K_hi
                        const void* K_chunk, const void* V_chunk, int N_q, int B,
                        const quoka_params* params, void* O, float* lse, int32_t* sel_out,
                        void* ws, size_t ws_bytes, void* stream);
+
+/* Shape of a ragged batch: nseq sequences, each with its own chunk length
+ * C_s and history length T_s, sharing the head layout and element type. */
+typedef struct {
+  int32_t nseq;            /* sequences, >= 1 */
+  int32_t H_q;             /* as quoka_shape */
+  int32_t H_kv;
+  int32_t d;
+  int32_t dtype;
+  int32_t reserved;        /* must be 0 */
+} quoka_varlen_shape;
+
+/* Workspace bytes for quoka_chunk_attend_varlen: the largest single-sequence
+ * requirement of the batch (the sequences run one after another on the
+ * stream and reuse it).  cu_T, cu_C as for quoka_chunk_attend_varlen. */
+int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
+                                int N_q, int B, const quoka_params* params, size_t* bytes);
+
+/* quoka_chunk_attend over a ragged batch in one call ([P1] "Chunked Prefill
+ * with QUOKA": every sequence's chunk is processed against its own cache; the
+ * sequences share nothing).  cu_T and cu_C are HOST int64 arrays of nseq + 1
+ * prefix sums (cu[0] = 0, non-decreasing): sequence s has
+ * T_s = cu_T[s+1] - cu_T[s] history keys and C_s = cu_C[s+1] - cu_C[s] chunk
+ * queries (C_s = 0: the sequence is skipped; each C_s <= 8192).
+ * Packed tensors, sequence-major: every sequence's block is laid out exactly
+ * as quoka_chunk_attend's tensors and the blocks are concatenated, so
+ * sequence s's
+ *   Q, O        start at element H_q  * d * cu_C[s]   ([H_q,  C_s, d])
+ *   K/V_chunk   start at element H_kv * d * cu_C[s]   ([H_kv, C_s, d])
+ *   K/V_hist    start at element H_kv * d * cu_T[s]   ([H_kv, T_s, d], heads T_s * d apart)
+ *   lse         starts at H_q * cu_C[s]               (fp32 [H_q, C_s]; may be NULL)
+ *   sel_out     starts at H_kv * cu_B[s], with cu_B the prefix sums of
+ *               B_s = min(B, T_s)                      (int32 [H_kv, B_s]; may be NULL;
+ *               a skipped sequence keeps its rows, left unwritten).
+ * lse and sel_out need only 4-byte alignment; the other tensors 16 bytes.
+ * N_q, B and params apply to every sequence.  Every sequence is checked before
+ * anything is enqueued; the sequences are then enqueued in order on `stream`,
+ * each through the same kernels as quoka_chunk_attend, reusing ws. */
+int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
+                              const void* Q, const void* K_hist, const void* V_hist, const void* K_chunk,
+                              const void* V_chunk, int N_q, int B, const quoka_params* params, void* O, float* lse,
+                              int32_t* sel_out, void* ws, size_t ws_bytes, void* stream);
 
 /* Dense chunked-prefill attention over every history key plus the causal
  * chunk ([P1] "Chunked prefill"): the reference QUOKA is measured against.

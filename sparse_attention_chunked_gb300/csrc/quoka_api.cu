@@ -4,6 +4,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "quoka.h"
 #include "common.cuh"
 #include "launch.h"
@@ -194,6 +197,84 @@ int run_attend(const quoka_shape* s, const void* Q, const void* Kh, const void* 
                                         p.scale, O, lse, st));
 }
 
+bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
+
+// Pointer checks shared by quoka_chunk_attend and each sequence of the ragged
+// entry point.  lse and sel_out are written one element at a time and need
+// only 4-byte alignment.
+int check_chunk_args(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
+                     const void* K_chunk, const void* V_chunk, int N_q, int B, const void* O, const float* lse,
+                     const int32_t* sel_out) {
+  if (N_q < 1 || B < 1 || Q == nullptr || K_chunk == nullptr || V_chunk == nullptr || O == nullptr)
+    return QUOKA_ERR_INVALID_ARG;
+  if (shape->T > 0 && (K_hist == nullptr || V_hist == nullptr)) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K_hist) || !aligned16(V_hist) || !aligned16(K_chunk) || !aligned16(V_chunk) ||
+      !aligned16(O) || !aligned4(lse) || !aligned4(sel_out))
+    return QUOKA_ERR_ALIGNMENT;
+  return QUOKA_OK;
+}
+
+// One chunk, arguments already checked: select queries, score the history,
+// keep the top-B keys, gather them and attend.  T = 0 or B >= T attends to the
+// whole history instead.
+int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist, const void* K_chunk,
+              const void* V_chunk, int N_q, int B, const Params& p, void* O, float* lse, int32_t* sel_out, void* ws,
+              const Layout& L, cudaStream_t st) {
+  const int T = shape->T;
+  if (T == 0 || B >= T) {   // every history key is kept: dense chunked-prefill attention
+    if (sel_out != nullptr && T > 0) QUOKA_CUDA(launch_topk(nullptr, shape->H_kv, T, T, sel_out, st));
+    return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), T, K_chunk, V_chunk, p, O, lse, ws, st);
+  }
+  const int n = n_sel_of(shape, N_q);
+  int32_t* q_idx = at<int32_t>(ws, L.q_idx);
+  float* scores = at<float>(ws, L.scores);
+  int32_t* sel = sel_out != nullptr ? sel_out : at<int32_t>(ws, L.sel);
+  QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
+  QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st));
+  QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st));
+  void* ksel = at<void>(ws, L.ksel);
+  void* vsel = at<void>(ws, L.vsel);
+  QUOKA_CUDA(launch_gather(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), sel, shape->H_kv, B,
+                           ksel, vsel, st));
+  return run_attend(shape, Q, ksel, vsel, (int64_t)B * shape->d, B, K_chunk, V_chunk, p, O, lse, ws, st);
+}
+
+// Ragged batch: the prefix sums must start at 0, never decrease, and give
+// every sequence C_s <= 8192 and T_s < 2^31.
+int check_varlen(const quoka_varlen_shape* v, const int64_t* cu_T, const int64_t* cu_C) {
+  if (v == nullptr || cu_T == nullptr || cu_C == nullptr) return QUOKA_ERR_INVALID_ARG;
+  if (v->nseq < 1 || v->reserved != 0 || cu_T[0] != 0 || cu_C[0] != 0) return QUOKA_ERR_INVALID_ARG;
+  for (int s = 0; s < v->nseq; ++s) {
+    const int64_t C = cu_C[s + 1] - cu_C[s], T = cu_T[s + 1] - cu_T[s];
+    if (C < 0 || T < 0) return QUOKA_ERR_INVALID_ARG;
+    if (C > 8192 || T > INT32_MAX) return QUOKA_ERR_UNSUPPORTED;
+  }
+  const quoka_shape first = {0, v->H_q, v->H_kv, 1, 0, v->d, v->dtype};
+  return check_shape(&first);   // the head layout, d and dtype
+}
+
+quoka_shape seq_shape(const quoka_varlen_shape* v, const int64_t* cu_T, const int64_t* cu_C, int s) {
+  quoka_shape sh;
+  sh.kv_head_stride = 0;
+  sh.H_q = v->H_q;
+  sh.H_kv = v->H_kv;
+  sh.C = (int32_t)(cu_C[s + 1] - cu_C[s]);
+  sh.T = (int32_t)(cu_T[s + 1] - cu_T[s]);
+  sh.d = v->d;
+  sh.dtype = v->dtype;
+  return sh;
+}
+
+struct SeqArgs {
+  quoka_shape shape;
+  const void *Q, *K_hist, *V_hist, *K_chunk, *V_chunk;
+  void* O;
+  float* lse;
+  int32_t* sel_out;
+  Params p;
+  Layout L;
+};
+
 }  // namespace
 
 namespace quoka {
@@ -325,32 +406,73 @@ int quoka_chunk_attend(const quoka_shape* shape, const void* Q, const void* K_hi
   QUOKA_TRY(check_shape(shape));
   Params p;
   QUOKA_TRY(read_params(params, shape, &p));
-  if (N_q < 1 || B < 1 || Q == nullptr || K_chunk == nullptr || V_chunk == nullptr || O == nullptr)
-    return QUOKA_ERR_INVALID_ARG;
-  if (shape->T > 0 && (K_hist == nullptr || V_hist == nullptr)) return QUOKA_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K_hist) || !aligned16(V_hist) || !aligned16(K_chunk) || !aligned16(V_chunk) ||
-      !aligned16(O) || !aligned16(lse) || !aligned16(sel_out))
-    return QUOKA_ERR_ALIGNMENT;
+  QUOKA_TRY(check_chunk_args(shape, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, O, lse, sel_out));
   const Layout L = make_layout(shape, N_q, B, p.gqa);
   QUOKA_TRY(check_ws(ws, ws_bytes, L.total));
-  cudaStream_t st = (cudaStream_t)stream;
-  const int T = shape->T;
-  if (T == 0 || B >= T) {   // every history key is kept: dense chunked-prefill attention
-    if (sel_out != nullptr && T > 0) QUOKA_CUDA(launch_topk(nullptr, shape->H_kv, T, T, sel_out, st));
-    return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), T, K_chunk, V_chunk, p, O, lse, ws, st);
+  return run_chunk(shape, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, p, O, lse, sel_out, ws, L,
+                   (cudaStream_t)stream);
+}
+
+int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
+                                int N_q, int B, const quoka_params* params, size_t* bytes) {
+  if (bytes == nullptr || N_q < 1 || B < 1) return QUOKA_ERR_INVALID_ARG;
+  QUOKA_TRY(check_varlen(shape, cu_T, cu_C));
+  size_t need = sizeof(WsHeader);
+  for (int s = 0; s < shape->nseq; ++s) {
+    const quoka_shape sh = seq_shape(shape, cu_T, cu_C, s);
+    if (sh.C == 0) continue;
+    Params p;
+    QUOKA_TRY(read_params(params, &sh, &p));
+    need = std::max(need, make_layout(&sh, N_q, B, p.gqa).total);
   }
-  const int n = n_sel_of(shape, N_q);
-  int32_t* q_idx = at<int32_t>(ws, L.q_idx);
-  float* scores = at<float>(ws, L.scores);
-  int32_t* sel = sel_out != nullptr ? sel_out : at<int32_t>(ws, L.sel);
-  QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
-  QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st));
-  QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st));
-  void* ksel = at<void>(ws, L.ksel);
-  void* vsel = at<void>(ws, L.vsel);
-  QUOKA_CUDA(launch_gather(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), sel, shape->H_kv, B,
-                           ksel, vsel, st));
-  return run_attend(shape, Q, ksel, vsel, (int64_t)B * shape->d, B, K_chunk, V_chunk, p, O, lse, ws, st);
+  *bytes = need;
+  return QUOKA_OK;
+}
+
+int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
+                              const void* Q, const void* K_hist, const void* V_hist, const void* K_chunk,
+                              const void* V_chunk, int N_q, int B, const quoka_params* params, void* O, float* lse,
+                              int32_t* sel_out, void* ws, size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_varlen(shape, cu_T, cu_C));
+  if (N_q < 1 || B < 1) return QUOKA_ERR_INVALID_ARG;
+  const int nseq = shape->nseq;
+  const size_t eb = elt_bytes(shape->dtype), d = shape->d;
+  // Every sequence is checked before the first one is enqueued.
+  std::vector<SeqArgs> seqs;
+  seqs.reserve(nseq);
+  int64_t cu_B = 0;
+  for (int s = 0; s < nseq; ++s) {
+    SeqArgs a;
+    a.shape = seq_shape(shape, cu_T, cu_C, s);
+    const int64_t c0 = cu_C[s], t0 = cu_T[s];
+    const int64_t B_s = std::min<int64_t>(B, a.shape.T);
+    auto off = [](const void* base, size_t elems, size_t bytes) -> const void* {
+      return base == nullptr ? nullptr : static_cast<const char*>(base) + elems * bytes;
+    };
+    a.Q = off(Q, (size_t)shape->H_q * d * c0, eb);
+    a.O = const_cast<void*>(off(O, (size_t)shape->H_q * d * c0, eb));
+    a.K_chunk = off(K_chunk, (size_t)shape->H_kv * d * c0, eb);
+    a.V_chunk = off(V_chunk, (size_t)shape->H_kv * d * c0, eb);
+    a.K_hist = a.shape.T > 0 ? off(K_hist, (size_t)shape->H_kv * d * t0, eb) : nullptr;
+    a.V_hist = a.shape.T > 0 ? off(V_hist, (size_t)shape->H_kv * d * t0, eb) : nullptr;
+    a.lse = lse == nullptr ? nullptr : lse + (size_t)shape->H_q * c0;
+    a.sel_out = sel_out == nullptr ? nullptr : sel_out + (size_t)shape->H_kv * cu_B;
+    cu_B += B_s;
+    if (a.shape.C == 0) continue;
+    Params p;
+    QUOKA_TRY(read_params(params, &a.shape, &p));
+    a.p = p;
+    QUOKA_TRY(check_chunk_args(&a.shape, a.Q, a.K_hist, a.V_hist, a.K_chunk, a.V_chunk, N_q, B, a.O, a.lse,
+                               a.sel_out));
+    a.L = make_layout(&a.shape, N_q, B, p.gqa);
+    QUOKA_TRY(check_ws(ws, ws_bytes, a.L.total));
+    seqs.push_back(a);
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  for (const SeqArgs& a : seqs)
+    QUOKA_TRY(run_chunk(&a.shape, a.Q, a.K_hist, a.V_hist, a.K_chunk, a.V_chunk, N_q, B, a.p, a.O, a.lse, a.sel_out,
+                        ws, a.L, st));
+  return QUOKA_OK;
 }
 
 int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const void* K_chunk, const void* V_chunk,

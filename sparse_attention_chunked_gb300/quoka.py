@@ -42,7 +42,13 @@ class Params(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class VarlenShape(ctypes.Structure):
+    _fields_ = [("nseq", ctypes.c_int32), ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _P = ctypes.c_void_p
+_I64P = ctypes.POINTER(ctypes.c_int64)
 _SIG = {
     "quoka_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "quoka_workspace_size": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.c_int, ctypes.c_int,
@@ -59,6 +65,12 @@ _SIG = {
                                            ctypes.POINTER(Params), _P, _P, _P, ctypes.c_size_t, _P]),
     "quoka_chunk_attend": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int,
                                           ctypes.POINTER(Params), _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "quoka_workspace_size_varlen": (ctypes.c_int, [ctypes.POINTER(VarlenShape), _I64P, _I64P, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.POINTER(Params),
+                                                   ctypes.POINTER(ctypes.c_size_t)]),
+    "quoka_chunk_attend_varlen": (ctypes.c_int, [ctypes.POINTER(VarlenShape), _I64P, _I64P, _P, _P, _P, _P, _P,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.POINTER(Params), _P, _P, _P, _P,
+                                                 ctypes.c_size_t, _P]),
     "quoka_dense_attend": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, ctypes.POINTER(Params), _P, _P,
                                           _P, ctypes.c_size_t, _P]),
     "quoka_append_kv": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
@@ -184,6 +196,32 @@ def quoka_chunk_attend(shape, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, param
     _check("quoka_chunk_attend", load().quoka_chunk_attend(
         ctypes.byref(shape), _ptr(Q), _ptr(K_hist), _ptr(V_hist), _ptr(K_chunk), _ptr(V_chunk), N_q, B,
         ctypes.byref(params), _ptr(O), _ptr(lse), _ptr(sel_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def _cu(offsets):
+    """Host int64 prefix-sum array for the ragged entry points."""
+    arr = (ctypes.c_int64 * len(offsets))(*[int(v) for v in offsets])
+    return arr
+
+
+def varlen_shape_of(nseq: int, H_q: int, H_kv: int, d: int, dtype) -> VarlenShape:
+    return VarlenShape(nseq, H_q, H_kv, d, DTYPE[dtype] if isinstance(dtype, torch.dtype) else dtype, 0)
+
+
+def quoka_workspace_size_varlen(vshape, cu_T, cu_C, N_q, B, params) -> int:
+    n = ctypes.c_size_t(0)
+    _check("quoka_workspace_size_varlen", load().quoka_workspace_size_varlen(
+        ctypes.byref(vshape), _cu(cu_T), _cu(cu_C), N_q, B, ctypes.byref(params), ctypes.byref(n)))
+    return n.value
+
+
+def quoka_chunk_attend_varlen(vshape, cu_T, cu_C, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, params, O, lse,
+                              sel_out, ws, stream=None):
+    """cu_T, cu_C: host sequences of nseq + 1 prefix sums; tensors packed sequence-major (see quoka.h)."""
+    _check("quoka_chunk_attend_varlen", load().quoka_chunk_attend_varlen(
+        ctypes.byref(vshape), _cu(cu_T), _cu(cu_C), _ptr(Q), _ptr(K_hist), _ptr(V_hist), _ptr(K_chunk),
+        _ptr(V_chunk), N_q, B, ctypes.byref(params), _ptr(O), _ptr(lse), _ptr(sel_out), _ptr(ws),
+        ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def quoka_dense_attend(shape, Q, K_hist, V_hist, K_chunk, V_chunk, params, O, lse, ws, stream=None):

@@ -101,6 +101,10 @@ class RaggedConfig:
     B: int
     dtype: str = "bf16"
 
+    @property
+    def G(self) -> int:
+        return self.H_q // self.H_kv
+
 
 RAGGED_8x_BF16 = RaggedConfig("ragged8_gqa64x8_d128_C1024_T4k-64k_bf16", 8, 64, 8, 128, 1024,
                               4096, 65536, 64, 2048)
@@ -272,3 +276,17 @@ def small_chunk(H_q=4, H_kv=2, d=64, C=64, T=300, N_q=8, B=40, dtype="fp32",
     """A small case for tests: returns (cfg, inputs)."""
     cfg = ChunkConfig(f"small_{H_q}x{H_kv}_d{d}_C{C}_T{T}_{dtype}", H_q, H_kv, d, C, T, N_q, B, dtype, recipe)
     return cfg, make_chunk(cfg, seed)
+
+
+def pack_varlen(seqs: list) -> dict:
+    """Concatenate per-sequence ChunkInputs sequence-major, the layout of the
+    ragged entry point: each sequence's tensors flattened in their own
+    [heads, length, d] order, one after another.  Returns the host prefix sums
+    cu_T, cu_C (lists of nseq + 1 ints) and the packed 1-D tensors."""
+    cu_T, cu_C = [0], [0]
+    for x in seqs:
+        cu_T.append(cu_T[-1] + x.K_hist.shape[1])
+        cu_C.append(cu_C[-1] + x.Q.shape[1])
+    cat = lambda name: torch.cat([getattr(x, name).reshape(-1) for x in seqs])
+    return dict(cu_T=cu_T, cu_C=cu_C, Q=cat("Q"), K_hist=cat("K_hist"), V_hist=cat("V_hist"),
+                K_chunk=cat("K_chunk"), V_chunk=cat("V_chunk"))

@@ -94,7 +94,7 @@ def test_chunk_attend_argument_errors(quoka):
     assert _chunk_call(q, s, B=0) == 1
     assert _chunk_call(q, s, Q=0) == 1                       # NULL query
     assert _chunk_call(q, s, Q=FAKE + 8) == 4                # misaligned query
-    assert _chunk_call(q, s, sel=FAKE + 4) == 4              # misaligned sel_out
+    assert _chunk_call(q, s, sel=FAKE + 2) == 4              # sel_out not 4-byte aligned (int32 elements)
     assert _chunk_call(q, s, ws=0) == 3                      # no workspace
     assert _chunk_call(q, s, ws=FAKE + 16) == 3              # workspace not 256-byte aligned
     need = q.workspace_size(s, 4, 16, q.params_of("max"))
@@ -124,3 +124,68 @@ def test_stage_argument_errors(quoka):
     # appending needs room for T + C rows per head
     assert lib.quoka_append_kv(ctypes.byref(s), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None) == 1
     assert lib.quoka_get_last_device_error(None, None) == 3
+
+
+# ---------------------------------------------------------------- ragged batch entry point
+
+def _vshape(q, **kw):
+    base = dict(nseq=3, H_q=8, H_kv=2, d=128, dtype=0, reserved=0)
+    base.update(kw)
+    return q.VarlenShape(**base)
+
+
+def _ws_varlen(q, vshape, cu_T, cu_C, N_q=16, B=64, gqa="max"):
+    n = ctypes.c_size_t(0)
+    rc = q.load().quoka_workspace_size_varlen(ctypes.byref(vshape), q._cu(cu_T), q._cu(cu_C), N_q, B,
+                                              ctypes.byref(q.params_of(gqa)), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_varlen_workspace_is_the_largest_sequence(quoka):
+    cu_T, cu_C = [0, 1000, 1000, 41000], [0, 128, 200, 201]
+    rc, n = _ws_varlen(quoka, _vshape(quoka), cu_T, cu_C)
+    assert rc == 0
+    per_seq = [quoka.workspace_size(_shape(quoka, C=c1 - c0, T=t1 - t0), 16, 64, quoka.params_of("max"))
+               for (c0, c1, t0, t1) in zip(cu_C, cu_C[1:], cu_T, cu_T[1:])]
+    assert n == max(per_seq)
+
+
+@pytest.mark.parametrize("cu_T,cu_C,kw,code", [
+    ([1, 10, 20, 30], [0, 1, 2, 3], {}, 1),          # prefix sums must start at 0
+    ([0, 10, 5, 30], [0, 1, 2, 3], {}, 1),           # decreasing history offsets
+    ([0, 10, 20, 30], [0, 2, 1, 3], {}, 1),          # decreasing chunk offsets
+    ([0, 10, 20, 30], [0, 1, 9002, 9003], {}, 2),    # a chunk longer than 8192
+    ([0, 10, 20, 30], [0, 1, 2, 3], dict(reserved=1), 1),
+    ([0, 10, 20, 30], [0, 1, 2, 3], dict(H_q=6, H_kv=4), 1),
+    ([0, 10, 20, 30], [0, 1, 2, 3], dict(d=96), 2),
+])
+def test_varlen_checks(quoka, cu_T, cu_C, kw, code):
+    rc, _ = _ws_varlen(quoka, _vshape(quoka, **kw), cu_T, cu_C)
+    assert rc == code, quoka.status_string(rc)
+
+
+def test_varlen_checks_every_sequence_before_enqueueing(quoka):
+    """Sequence 0 is valid and fits the workspace; sequence 1 needs more: nothing may be enqueued."""
+    q = quoka
+    vs = _vshape(q, nseq=2)
+    cu_T, cu_C = [0, 500, 100500], [0, 64, 128]
+    _, n0 = _ws_varlen(q, q.VarlenShape(1, 8, 2, 128, 0, 0), [0, 500], [0, 64])
+    rc = q.load().quoka_chunk_attend_varlen(
+        ctypes.byref(vs), q._cu(cu_T), q._cu(cu_C), *([ctypes.c_void_p(FAKE)] * 5), 16, 64,
+        ctypes.byref(q.params_of("max")), ctypes.c_void_p(FAKE), None, None, ctypes.c_void_p(FAKE), n0, None)
+    assert rc == 3, q.status_string(rc)
+
+
+def test_varlen_alignment_of_packed_offsets(quoka):
+    """lse of sequence 1 starts at H_q * C_0 floats: 4-byte alignment is all it needs."""
+    q = quoka
+    vs = _vshape(q, nseq=2)
+    cu_T, cu_C = [0, 500, 1000], [0, 3, 6]
+    rc = q.load().quoka_chunk_attend_varlen(
+        ctypes.byref(vs), q._cu(cu_T), q._cu(cu_C), *([ctypes.c_void_p(FAKE)] * 5), 16, 64,
+        ctypes.byref(q.params_of("max")), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 2), None, None, 0, None)
+    assert rc == 4, q.status_string(rc)   # lse not 4-byte aligned
+    rc = q.load().quoka_chunk_attend_varlen(
+        ctypes.byref(vs), q._cu(cu_T), q._cu(cu_C), *([ctypes.c_void_p(FAKE)] * 5), 16, 64,
+        ctypes.byref(q.params_of("max")), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4), None, None, 0, None)
+    assert rc == 3, q.status_string(rc)   # offsets fine; fails on the missing workspace
