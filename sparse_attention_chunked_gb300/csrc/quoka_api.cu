@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "quoka.h"
@@ -109,11 +110,14 @@ struct Layout {
   size_t q_idx, scores, sel, ksel, vsel, total;
 };
 
-Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa) {
+// Regions start at `start` (just past the header for a single call; a lane's
+// slice for the ragged entry point).  The header is always the workspace's
+// first 256 bytes, shared by every lane.
+Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa, size_t start = sizeof(WsHeader)) {
   Layout L;
   const size_t H_q = s->H_q, H_kv = s->H_kv, C = s->C, d = s->d, T = s->T;
   const size_t nblk = (C + 63) / 64;
-  size_t o = sizeof(WsHeader);
+  size_t o = start;
   L.qnorm = o;  o = align_up(o + H_q * C * 4);
   L.qpart = o;  o = align_up(o + H_q * nblk * d * 4);
   L.qcos = o;   o = align_up(o + H_q * C * 4);
@@ -273,7 +277,68 @@ struct SeqArgs {
   int32_t* sel_out;
   Params p;
   Layout L;
+  double work;
 };
+
+// Streams the ragged entry point runs sequences on: sequences of one batch
+// share nothing, so their launches may overlap on the GPU.
+constexpr int kMaxLanes = 4;
+
+int varlen_lanes(const quoka_varlen_shape* v, const int64_t* cu_C) {
+  int busy = 0;
+  for (int s = 0; s < v->nseq; ++s) busy += cu_C[s + 1] > cu_C[s];
+  return std::max(1, std::min(busy, kMaxLanes));
+}
+
+// Workspace of one lane: room for the largest sequence's regions.
+int varlen_lane_bytes(const quoka_varlen_shape* v, const int64_t* cu_T, const int64_t* cu_C, int N_q, int B,
+                      const quoka_params* params, size_t* out) {
+  size_t lane = 0;
+  for (int s = 0; s < v->nseq; ++s) {
+    const quoka_shape sh = seq_shape(v, cu_T, cu_C, s);
+    if (sh.C == 0) continue;
+    Params p;
+    QUOKA_TRY(read_params(params, &sh, &p));
+    lane = std::max(lane, make_layout(&sh, N_q, B, p.gqa).total - sizeof(WsHeader));
+  }
+  *out = align_up(lane);
+  return QUOKA_OK;
+}
+
+// Relative cost of a sequence, for balancing lanes: the history it scores and
+// the keys each query attends to.
+double seq_work(const quoka_shape& s, int B) {
+  const double Be = std::min(B, s.T);
+  return (double)s.H_kv * s.T * s.d * 2.0 / 8.0 + (double)s.H_q * s.C * (Be + 0.5 * s.C) * s.d * 4.0 / 1000.0;
+}
+
+struct LaneStreams {
+  std::mutex mu;
+  cudaStream_t stream[kMaxLanes - 1];
+  cudaEvent_t fork, join[kMaxLanes - 1];
+};
+
+// Per device, created on first use and kept for the life of the process.
+cudaError_t lane_streams(LaneStreams** out) {
+  static std::mutex mu;
+  static LaneStreams* per_dev[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> guard(mu);
+  if (per_dev[dev] == nullptr) {
+    LaneStreams* ls = new LaneStreams();
+    if ((e = cudaEventCreateWithFlags(&ls->fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    for (int l = 0; l < kMaxLanes - 1; ++l) {
+      if ((e = cudaStreamCreateWithFlags(&ls->stream[l], cudaStreamNonBlocking)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&ls->join[l], cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    per_dev[dev] = ls;
+  }
+  *out = per_dev[dev];
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -417,15 +482,9 @@ int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* 
                                 int N_q, int B, const quoka_params* params, size_t* bytes) {
   if (bytes == nullptr || N_q < 1 || B < 1) return QUOKA_ERR_INVALID_ARG;
   QUOKA_TRY(check_varlen(shape, cu_T, cu_C));
-  size_t need = sizeof(WsHeader);
-  for (int s = 0; s < shape->nseq; ++s) {
-    const quoka_shape sh = seq_shape(shape, cu_T, cu_C, s);
-    if (sh.C == 0) continue;
-    Params p;
-    QUOKA_TRY(read_params(params, &sh, &p));
-    need = std::max(need, make_layout(&sh, N_q, B, p.gqa).total);
-  }
-  *bytes = need;
+  size_t lane = 0;
+  QUOKA_TRY(varlen_lane_bytes(shape, cu_T, cu_C, N_q, B, params, &lane));
+  *bytes = sizeof(WsHeader) + (size_t)varlen_lanes(shape, cu_C) * lane;
   return QUOKA_OK;
 }
 
@@ -437,6 +496,9 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
   if (N_q < 1 || B < 1) return QUOKA_ERR_INVALID_ARG;
   const int nseq = shape->nseq;
   const size_t eb = elt_bytes(shape->dtype), d = shape->d;
+  size_t lane_bytes = 0;
+  QUOKA_TRY(varlen_lane_bytes(shape, cu_T, cu_C, N_q, B, params, &lane_bytes));
+  const int lanes = varlen_lanes(shape, cu_C);
   // Every sequence is checked before the first one is enqueued.
   std::vector<SeqArgs> seqs;
   seqs.reserve(nseq);
@@ -459,20 +521,60 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
     a.sel_out = sel_out == nullptr ? nullptr : sel_out + (size_t)shape->H_kv * cu_B;
     cu_B += B_s;
     if (a.shape.C == 0) continue;
-    Params p;
-    QUOKA_TRY(read_params(params, &a.shape, &p));
-    a.p = p;
+    QUOKA_TRY(read_params(params, &a.shape, &a.p));
     QUOKA_TRY(check_chunk_args(&a.shape, a.Q, a.K_hist, a.V_hist, a.K_chunk, a.V_chunk, N_q, B, a.O, a.lse,
                                a.sel_out));
-    a.L = make_layout(&a.shape, N_q, B, p.gqa);
-    QUOKA_TRY(check_ws(ws, ws_bytes, a.L.total));
+    a.work = seq_work(a.shape, B);
     seqs.push_back(a);
   }
+  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader) + (size_t)lanes * lane_bytes));
   cudaStream_t st = (cudaStream_t)stream;
-  for (const SeqArgs& a : seqs)
-    QUOKA_TRY(run_chunk(&a.shape, a.Q, a.K_hist, a.V_hist, a.K_chunk, a.V_chunk, N_q, B, a.p, a.O, a.lse, a.sel_out,
-                        ws, a.L, st));
-  return QUOKA_OK;
+  if (seqs.empty()) return QUOKA_OK;
+  // Longest first onto the least-loaded lane; each lane owns a workspace slice.
+  std::vector<int> order(seqs.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return seqs[a].work > seqs[b].work; });
+  std::vector<double> load(lanes, 0.0);
+  std::vector<std::vector<int>> plan(lanes);
+  for (int i : order) {
+    const int l = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+    load[l] += seqs[i].work;
+    plan[l].push_back(i);
+  }
+  for (int l = 0; l < lanes; ++l)
+    for (int i : plan[l])
+      seqs[i].L = make_layout(&seqs[i].shape, N_q, B, seqs[i].p.gqa, sizeof(WsHeader) + (size_t)l * lane_bytes);
+  if (lanes == 1) {
+    for (int i : plan[0])
+      QUOKA_TRY(run_chunk(&seqs[i].shape, seqs[i].Q, seqs[i].K_hist, seqs[i].V_hist, seqs[i].K_chunk,
+                          seqs[i].V_chunk, N_q, B, seqs[i].p, seqs[i].O, seqs[i].lse, seqs[i].sel_out, ws, seqs[i].L,
+                          st));
+    return QUOKA_OK;
+  }
+  // Fork: lane l > 0 runs on a library stream that first waits for everything
+  // enqueued on `stream` so far; lane 0 runs on `stream` itself.  Join: `stream`
+  // waits for every lane.  Stream capture follows the fork and the join.
+  LaneStreams* ls = nullptr;
+  QUOKA_CUDA(lane_streams(&ls));
+  std::lock_guard<std::mutex> guard(ls->mu);
+  QUOKA_CUDA(cudaEventRecord(ls->fork, st));
+  int rc = QUOKA_OK;
+  for (int l = 0; l < lanes && rc == QUOKA_OK; ++l) {
+    cudaStream_t lst = l == 0 ? st : ls->stream[l - 1];
+    if (l > 0 && (rc = cuda_status(cudaStreamWaitEvent(lst, ls->fork, 0))) != QUOKA_OK) break;
+    for (int i : plan[l]) {
+      rc = run_chunk(&seqs[i].shape, seqs[i].Q, seqs[i].K_hist, seqs[i].V_hist, seqs[i].K_chunk, seqs[i].V_chunk,
+                     N_q, B, seqs[i].p, seqs[i].O, seqs[i].lse, seqs[i].sel_out, ws, seqs[i].L, lst);
+      if (rc != QUOKA_OK) break;
+    }
+  }
+  // join every lane that was forked, even after an error, so that a capture stays well formed
+  for (int l = 1; l < lanes; ++l) {
+    const int j = cuda_status(cudaEventRecord(ls->join[l - 1], ls->stream[l - 1]));
+    const int w = j == QUOKA_OK ? cuda_status(cudaStreamWaitEvent(st, ls->join[l - 1], 0)) : j;
+    if (rc == QUOKA_OK) rc = w;
+  }
+  return rc;
 }
 
 int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const void* K_chunk, const void* V_chunk,

@@ -141,13 +141,16 @@ def _ws_varlen(q, vshape, cu_T, cu_C, N_q=16, B=64, gqa="max"):
     return rc, n.value
 
 
-def test_varlen_workspace_is_the_largest_sequence(quoka):
-    cu_T, cu_C = [0, 1000, 1000, 41000], [0, 128, 200, 201]
-    rc, n = _ws_varlen(quoka, _vshape(quoka), cu_T, cu_C)
-    assert rc == 0
-    per_seq = [quoka.workspace_size(_shape(quoka, C=c1 - c0, T=t1 - t0), 16, 64, quoka.params_of("max"))
-               for (c0, c1, t0, t1) in zip(cu_C, cu_C[1:], cu_T, cu_T[1:])]
-    assert n == max(per_seq)
+def test_varlen_workspace_is_one_slice_per_lane(quoka):
+    """Header + one slice per stream lane (up to 4, one per non-empty sequence), each for the largest sequence."""
+    for cu_T, cu_C, lanes in (([0, 1000, 1000, 41000], [0, 128, 200, 201], 3),
+                              ([0, 1000, 1000, 41000], [0, 128, 128, 201], 2),
+                              ([0, 5, 9, 13, 17, 21, 25], [0, 1, 2, 3, 4, 5, 6], 4)):
+        rc, n = _ws_varlen(quoka, _vshape(quoka, nseq=len(cu_T) - 1), cu_T, cu_C)
+        assert rc == 0
+        per_seq = [quoka.workspace_size(_shape(quoka, C=c1 - c0, T=t1 - t0), 16, 64, quoka.params_of("max"))
+                   for (c0, c1, t0, t1) in zip(cu_C, cu_C[1:], cu_T, cu_T[1:]) if c1 > c0]
+        assert n == 256 + lanes * (max(per_seq) - 256)
 
 
 @pytest.mark.parametrize("cu_T,cu_C,kw,code", [
@@ -165,14 +168,19 @@ def test_varlen_checks(quoka, cu_T, cu_C, kw, code):
 
 
 def test_varlen_checks_every_sequence_before_enqueueing(quoka):
-    """Sequence 0 is valid and fits the workspace; sequence 1 needs more: nothing may be enqueued."""
+    """Sequence 0 (no history) is valid; sequence 1 has history but K/V_hist are NULL: nothing may be enqueued."""
     q = quoka
     vs = _vshape(q, nseq=2)
-    cu_T, cu_C = [0, 500, 100500], [0, 64, 128]
-    _, n0 = _ws_varlen(q, q.VarlenShape(1, 8, 2, 128, 0, 0), [0, 500], [0, 64])
+    cu_T, cu_C = [0, 0, 500], [0, 64, 128]
+    P = ctypes.c_void_p
     rc = q.load().quoka_chunk_attend_varlen(
-        ctypes.byref(vs), q._cu(cu_T), q._cu(cu_C), *([ctypes.c_void_p(FAKE)] * 5), 16, 64,
-        ctypes.byref(q.params_of("max")), ctypes.c_void_p(FAKE), None, None, ctypes.c_void_p(FAKE), n0, None)
+        ctypes.byref(vs), q._cu(cu_T), q._cu(cu_C), P(FAKE), None, None, P(FAKE), P(FAKE), 16, 64,
+        ctypes.byref(q.params_of("max")), P(FAKE), None, None, P(FAKE), 1 << 30, None)
+    assert rc == 1, q.status_string(rc)
+    _, need = _ws_varlen(q, vs, cu_T, cu_C)
+    rc = q.load().quoka_chunk_attend_varlen(
+        ctypes.byref(vs), q._cu(cu_T), q._cu(cu_C), *([P(FAKE)] * 5), 16, 64,
+        ctypes.byref(q.params_of("max")), P(FAKE), None, None, P(FAKE), need - 1, None)
     assert rc == 3, q.status_string(rc)
 
 
