@@ -35,7 +35,11 @@ readings taken where they are silent or garbled:
   sorted ascending;
 * a norm below EPS is clamped to EPS (a zero vector scores 0);
 * only the history keys are scored and selected; the chunk's own keys are
-  always attended, causally.
+  always attended, causally;
+* the ablations the pages report (dot product instead of cosine, the mean
+  instead of the maximum over the selected queries) change the key score
+  only: query subselection stays on the cosine to the mean query, and with
+  per-head pooling the maximum over the group's heads stays.
 
 Parity pins for every function live in tests/test_oracle_pins.py.
 """
@@ -112,14 +116,29 @@ def normalize_rows(X: np.ndarray) -> np.ndarray:
     return X / np.maximum(np.sqrt((X * X).sum(axis=-1, keepdims=True)), EPS)
 
 
-def scoring_queries(Q: np.ndarray, q_idx: np.ndarray, H_kv: int, gqa: str) -> list:
+SCORE_FNS = ("cos", "dot")
+QUERY_AGGS = ("max", "mean")
+
+
+def _query_rows(X: np.ndarray, score_fn: str) -> np.ndarray:
+    """A query (or key) row as the score function sees it: unit length for
+    the cosine, as it is for the plain dot product (the ablation of
+    [P1 "Scoring via Cosine Similarity"])."""
+    if score_fn == "cos":
+        return normalize_rows(X)
+    if score_fn == "dot":
+        return X
+    raise ValueError(score_fn)
+
+
+def scoring_queries(Q: np.ndarray, q_idx: np.ndarray, H_kv: int, gqa: str, score_fn: str = "cos") -> list:
     """The rows each KV group scores its history with, one array [R, d] per group.
 
-    ``"max"``: the normalised selected query of every head of the group
-    (R = G * n).  ``"mean"``: pre-aggregation, the mean over the group's
-    heads of the normalised queries at each selected token (R = n); the mean
-    is not re-normalised, so its dot with a unit key is exactly the mean of
-    the per-head cosines.
+    ``"max"``: the selected query of every head of the group (R = G * n),
+    normalised for the cosine.  ``"mean"``: pre-aggregation, the mean over
+    the group's heads of the (normalised) queries at each selected token
+    (R = n); the mean is not re-normalised, so its dot with a unit key is
+    exactly the mean of the per-head cosines.
     """
     H_q = Q.shape[0]
     G = H_q // H_kv
@@ -127,9 +146,9 @@ def scoring_queries(Q: np.ndarray, q_idx: np.ndarray, H_kv: int, gqa: str) -> li
     for g in range(H_kv):
         heads = range(g * G, (g + 1) * G)
         if gqa == "max":
-            out.append(np.concatenate([normalize_rows(Q[h, q_idx[h]]) for h in heads], axis=0))
+            out.append(np.concatenate([_query_rows(Q[h, q_idx[h]], score_fn) for h in heads], axis=0))
         elif gqa == "mean":
-            out.append(sum(normalize_rows(Q[h, q_idx[g]]) for h in heads) / G)
+            out.append(sum(_query_rows(Q[h, q_idx[g]], score_fn) for h in heads) / G)
         else:
             raise ValueError(gqa)
     return out
@@ -140,19 +159,42 @@ def max_over_queries(S: np.ndarray) -> np.ndarray:
     return S.max(axis=0)
 
 
-def score_keys(Q: np.ndarray, K_hist: np.ndarray, q_idx: np.ndarray, gqa: str) -> np.ndarray:
-    """Aggregated cosine score of every history key of every KV group -> [H_kv, T].
+def mean_over_queries(S: np.ndarray) -> np.ndarray:
+    """The averaging alternative that [P2 "Why take the maximum"] sets against
+    the maximum (and [P1 "Aggregation Across Queries and KV Groups"] ablates):
+    one score per key, the mean over the rows of S [R, T]."""
+    return S.sum(axis=0) / S.shape[0]
 
-    score[g, t] = max over the group's scoring rows r of  r . k_t / |k_t|.
+
+def score_keys(Q: np.ndarray, K_hist: np.ndarray, q_idx: np.ndarray, gqa: str, score_fn: str = "cos",
+               query_agg: str = "max") -> np.ndarray:
+    """Aggregated score of every history key of every KV group -> [H_kv, T].
+
+    Per scoring row r and key t the score function gives r . k_t / |k_t|
+    (cosine: the rows are unit too) or r . k_t (dot).  The query axis, the
+    selected tokens, is aggregated by ``query_agg``; the GQA axis as the
+    pooling mode says: ``"mean"`` already pre-aggregated the heads into the
+    rows, ``"max"`` aggregates each head's tokens, then takes the maximum
+    over the group's heads.  With ``query_agg="max"`` the latter is the
+    maximum over every row of every head of the group.
     """
+    if query_agg not in QUERY_AGGS:
+        raise ValueError(query_agg)
+    agg = max_over_queries if query_agg == "max" else mean_over_queries
     H_kv, T = K_hist.shape[0], K_hist.shape[1]
-    rows = scoring_queries(Q, q_idx, H_kv, gqa)
+    rows = scoring_queries(Q, q_idx, H_kv, gqa, score_fn)
     out = np.zeros((H_kv, T))
     for g in range(H_kv):
         if T == 0:
             continue
-        S = rows[g] @ normalize_rows(K_hist[g]).T          # cosine of every row with every key
-        out[g] = max_over_queries(S)
+        S = rows[g] @ _query_rows(K_hist[g], score_fn).T     # score of every row with every key
+        if gqa == "max":
+            n = q_idx.shape[1]
+            G = rows[g].shape[0] // n
+            per_head = np.stack([agg(S[k * n:(k + 1) * n]) for k in range(G)])   # one row per head
+            out[g] = per_head.max(axis=0)
+        else:
+            out[g] = agg(S)
     return out
 
 
@@ -220,7 +262,7 @@ def attend(Q: np.ndarray, K_sel: np.ndarray, V_sel: np.ndarray, K_chunk: np.ndar
 # --------------------------------------------------------------------------
 
 def chunk_attend(Q, K_hist, V_hist, K_chunk, V_chunk, n_q: int, B: int, gqa: str,
-                 scale: float | None = None) -> dict:
+                 scale: float | None = None, score_fn: str = "cos", query_agg: str = "max") -> dict:
     """Select queries, score the history, keep the top-B keys, attend.
 
     With no history (T = 0) the chunk attends causally to itself only; with
@@ -232,7 +274,7 @@ def chunk_attend(Q, K_hist, V_hist, K_chunk, V_chunk, n_q: int, B: int, gqa: str
         sel = np.tile(np.arange(T, dtype=np.int64), (H_kv, 1))
     else:
         q_idx = select_queries(Q, n_q, H_kv, gqa)
-        scores = score_keys(Q, K_hist, q_idx, gqa)
+        scores = score_keys(Q, K_hist, q_idx, gqa, score_fn, query_agg)
         sel = select_keys(scores, B)
         out.update(q_idx=q_idx, scores=scores)
     O, lse = attend(Q, gather(K_hist, sel), gather(V_hist, sel), K_chunk, V_chunk, scale)

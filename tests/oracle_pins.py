@@ -324,4 +324,83 @@ def pin_needle_recovered(o):
         assert scores[g, t] > 0.99
 
 
+# ---------------------------------------------------------------- the ablation variants of the key score
+
+def pin_toy_mean_aggregation(o):
+    """Averaging the toy table's K1 column gives the .40 the page prints; a mean never exceeds the maximum."""
+    g = _golden("toy_max_aggregation.json")
+    S = np.array(g["scores"])
+    mean = o.mean_over_queries(S)
+    assert abs(mean[0] - g["mean_of_K1"]) < 1e-12, mean
+    assert np.all(mean <= o.max_over_queries(S) + 1e-15)
+    same = np.tile(S[:1], (5, 1))                 # identical rows: mean and maximum agree
+    assert np.allclose(o.mean_over_queries(same), o.max_over_queries(same), atol=1e-15)
+
+
+def _sim(a, b, score_fn):
+    return 1.0 - ssd.cosine(a, b) if score_fn == "cos" else float(np.dot(a, b))
+
+
+def _brute_scores_variant(Q, K, q_idx, gqa, G, score_fn, query_agg):
+    """Explicit loops: per (row, key) similarity, the query axis by max or mean, the GQA axis by the mode."""
+    H_kv, T = K.shape[0], K.shape[1]
+    agg = max if query_agg == "max" else (lambda v: math.fsum(v) / len(v))
+    out = np.zeros((H_kv, T))
+    for g in range(H_kv):
+        heads = range(g * G, (g + 1) * G)
+        for t in range(T):
+            if gqa == "max":
+                out[g, t] = max(agg([_sim(Q[h, i], K[g, t], score_fn) for i in q_idx[h]]) for h in heads)
+            else:
+                per_token = [math.fsum(_sim(Q[h, i], K[g, t], score_fn) for h in heads) / G for i in q_idx[g]]
+                out[g, t] = agg(per_token)
+    return out
+
+
+def pin_score_variants_brute(o):
+    """Cosine or dot, max or mean over the selected queries, both pooling modes, by explicit loops."""
+    r = _rng(11)
+    H_q, H_kv, C, T, d = 6, 2, 12, 15, 8
+    Q = r.standard_normal((H_q, C, d)) * r.uniform(0.2, 4.0, (H_q, C, 1))
+    K = r.standard_normal((H_kv, T, d)) * r.uniform(0.1, 5.0, (H_kv, T, 1))
+    for gqa in ("max", "mean"):
+        q_idx = o.select_queries(Q, 4, H_kv, gqa)
+        for score_fn in ("cos", "dot"):
+            for query_agg in ("max", "mean"):
+                got = o.score_keys(Q, K, q_idx, gqa, score_fn, query_agg)
+                ref = _brute_scores_variant(Q, K, q_idx, gqa, H_q // H_kv, score_fn, query_agg)
+                assert np.max(np.abs(got - ref)) < 1e-10 * max(1.0, np.abs(ref).max()), (gqa, score_fn, query_agg)
+
+
+def pin_dot_scales_cos_does_not(o):
+    """The dot score is positively homogeneous in the keys and queries; on unit vectors it is the cosine."""
+    r = _rng(12)
+    H_q, H_kv, C, T, d = 4, 2, 9, 20, 6
+    Q = r.standard_normal((H_q, C, d))
+    K = r.standard_normal((H_kv, T, d))
+    for gqa in ("max", "mean"):
+        q_idx = o.select_queries(Q, 3, H_kv, gqa)
+        for query_agg in ("max", "mean"):
+            s = o.score_keys(Q, K, q_idx, gqa, "dot", query_agg)
+            assert np.allclose(o.score_keys(Q, 3.0 * K, q_idx, gqa, "dot", query_agg), 3.0 * s, rtol=1e-12)
+            assert np.allclose(o.score_keys(2.0 * Q, K, q_idx, gqa, "dot", query_agg), 2.0 * s, rtol=1e-12)
+            Qu = Q / np.linalg.norm(Q, axis=-1, keepdims=True)
+            Ku = K / np.linalg.norm(K, axis=-1, keepdims=True)
+            assert np.allclose(o.score_keys(Qu, Ku, q_idx, gqa, "dot", query_agg),
+                               o.score_keys(Q, K, q_idx, gqa, "cos", query_agg), atol=1e-12)
+
+
+def pin_query_mean_with_one_query(o):
+    """With one selected query per set there is nothing to aggregate: mean and maximum agree."""
+    r = _rng(13)
+    H_q, H_kv, C, T, d = 4, 2, 7, 11, 5
+    Q = r.standard_normal((H_q, C, d))
+    K = r.standard_normal((H_kv, T, d))
+    for gqa in ("max", "mean"):
+        q_idx = o.select_queries(Q, 1, H_kv, gqa)
+        for score_fn in ("cos", "dot"):
+            assert np.allclose(o.score_keys(Q, K, q_idx, gqa, score_fn, "mean"),
+                               o.score_keys(Q, K, q_idx, gqa, score_fn, "max"), atol=1e-14)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -17,11 +17,18 @@ MUTANTS = [
     ("group_selection_uses_first_head", "u = cos.reshape(H_kv, G, -1).mean(axis=1)",
      "u = cos.reshape(H_kv, G, -1)[:, 0]"),
     ("mean_over_queries_instead_of_max", "return S.max(axis=0)", "return S.mean(axis=0)"),
-    ("keys_not_normalised", "S = rows[g] @ normalize_rows(K_hist[g]).T", "S = rows[g] @ K_hist[g].T"),
-    ("queries_not_normalised", "out.append(np.concatenate([normalize_rows(Q[h, q_idx[h]]) for h in heads], axis=0))",
+    ("keys_not_normalised", "S = rows[g] @ _query_rows(K_hist[g], score_fn).T", "S = rows[g] @ K_hist[g].T"),
+    ("queries_not_normalised",
+     "out.append(np.concatenate([_query_rows(Q[h, q_idx[h]], score_fn) for h in heads], axis=0))",
      "out.append(np.concatenate([Q[h, q_idx[h]] for h in heads], axis=0))"),
-    ("preaggregate_renormalised", "out.append(sum(normalize_rows(Q[h, q_idx[g]]) for h in heads) / G)",
-     "out.append(normalize_rows(sum(normalize_rows(Q[h, q_idx[g]]) for h in heads) / G))"),
+    ("preaggregate_renormalised", "out.append(sum(_query_rows(Q[h, q_idx[g]], score_fn) for h in heads) / G)",
+     "out.append(normalize_rows(sum(_query_rows(Q[h, q_idx[g]], score_fn) for h in heads) / G))"),
+    ("dot_still_normalises", 'if score_fn == "dot":\n        return X', 'if score_fn == "dot":\n        return normalize_rows(X)'),
+    ("query_mean_is_max", "return S.sum(axis=0) / S.shape[0]", "return S.max(axis=0)"),
+    ("query_mean_divides_by_keys", "return S.sum(axis=0) / S.shape[0]", "return S.sum(axis=0) / S.shape[1]"),
+    ("query_mean_over_all_heads_rows", "per_head = np.stack([agg(S[k * n:(k + 1) * n]) for k in range(G)])",
+     "per_head = agg(S)[None, :]"),
+    ("heads_averaged_in_max_mode", "out[g] = per_head.max(axis=0)", "out[g] = per_head.mean(axis=0)"),
     ("topb_keeps_smallest", 'order = np.argsort(-score_row, kind="stable")',
      'order = np.argsort(score_row, kind="stable")'),
     ("topb_ties_to_higher_index", 'order = np.argsort(-score_row, kind="stable")',
