@@ -98,12 +98,15 @@ def max_over_ranks(x: float, device="cpu") -> float:
 
 # ---------------------------------------------------------------- algorithmic work per stage
 
-def stage_work(cfg: wl.ChunkConfig, gqa: str) -> dict:
+def stage_work(cfg: wl.ChunkConfig, gqa: str, query_agg: str = "max") -> dict:
     """Bytes / flops each stage must move or compute (what the method needs, not what the kernels do)."""
     e = 2 if cfg.dtype == "bf16" else 4
     n = min(cfg.N_q, cfg.C)
     B_e = min(cfg.B, cfg.T)
-    R = cfg.G * n if gqa == "max" else n
+    if query_agg == "mean":       # the mean over tokens is one row per head (max) or per group (mean)
+        R = cfg.G if gqa == "max" else 1
+    else:
+        R = cfg.G * n if gqa == "max" else n
     return {
         "select": {"bytes": cfg.H_q * cfg.C * cfg.d * e},                               # read Q once
         "score": {"bytes": cfg.H_kv * cfg.T * cfg.d * e + cfg.H_kv * cfg.T * 4,         # read K, write scores
@@ -199,7 +202,7 @@ def run_quoka(args, rank, world, local_rank):
     Q, Kh, Vh = x.Q.to(dev), x.K_hist.to(dev), x.V_hist.to(dev)
     Kc, Vc = x.K_chunk.to(dev), x.V_chunk.to(dev)
     shape = q.shape_of(Q, Kh)
-    params = q.params_of(args.gqa, args.engine)
+    params = q.params_of(args.gqa, args.engine, score_fn=args.score_fn, query_agg=args.query_agg)
     ws = q.make_workspace(shape, cfg.N_q, cfg.B, params, device=dev)
     n = min(cfg.N_q, cfg.C)
     H_sel = cfg.H_q if args.gqa == "max" else cfg.H_kv
@@ -372,7 +375,7 @@ def run_quoka(args, rank, world, local_rank):
 
     if rank != 0:
         return None
-    work = stage_work(cfg, args.gqa)
+    work = stage_work(cfg, args.gqa, args.query_agg)
     peaks = load_peaks()
     att_ms = statistics.mean(stage_ms["attend"])
     tc_engine = q.uses_tensor_cores("attend", shape, params)
@@ -408,6 +411,7 @@ def run_quoka(args, rank, world, local_rank):
                 "5% outlier queries, planted needles)",
         "config": {"workload": cfg.name, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "d": cfg.d, "C": cfg.C, "T": cfg.T,
                    "N_q": cfg.N_q, "B": cfg.B, "gqa_pool": args.gqa, "engine": args.engine,
+                   **variant_keys(args),
                    "l2": f"inputs larger than L2: the timed steps rotate over {INPUT_SETS} copies of the inputs "
                          f"({INPUT_SETS * set_bytes / 2**20:.0f} MB), no flush; l2_write_flush: the same step after "
                          f"a {L2_FLUSH_BYTES >> 20} MB write",
@@ -434,7 +438,7 @@ def run_quoka(args, rank, world, local_rank):
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, x, args.gqa)
+        res["cpu_baseline"] = cpu_baseline(cfg, x, args.gqa, score_fn=args.score_fn, query_agg=args.query_agg)
     return res
 
 
@@ -456,7 +460,7 @@ def run_quoka_ragged(args, rank, world, local_rank):
     sets = [base] + [tuple(t.clone() for t in base) for _ in range(INPUT_SETS - 1)]
     set_bytes = sum(t.numel() * t.element_size() for t in base)
     vshape = q.varlen_shape_of(len(seqs), cfg.H_q, cfg.H_kv, cfg.d, base[0].dtype)
-    params = q.params_of(args.gqa, args.engine)
+    params = q.params_of(args.gqa, args.engine, score_fn=args.score_fn, query_agg=args.query_agg)
     T_max = max(b - a for a, b in zip(cu_T, cu_T[1:]))
     n_ws = max(q.quoka_workspace_size_varlen(vshape, cu_T, cu_C, cfg.N_q, cfg.B, params),
                q.quoka_workspace_size_varlen(vshape, cu_T, cu_C, cfg.N_q, T_max, params))
@@ -601,7 +605,7 @@ def run_quoka_ragged(args, rank, world, local_rank):
         "data": "synthetic (seeded massive-activation recipe per sequence, log-uniform history lengths)",
         "config": {"workload": cfg.name, "nseq": len(seqs), "H_q": cfg.H_q, "H_kv": cfg.H_kv, "d": cfg.d,
                    "C": cfg.C, "T_per_seq": [b - a for a, b in zip(cu_T, cu_T[1:])], "N_q": cfg.N_q, "B": cfg.B,
-                   "gqa_pool": args.gqa, "engine": args.engine,
+                   "gqa_pool": args.gqa, "engine": args.engine, **variant_keys(args),
                    "l2": f"inputs larger than L2: the timed steps rotate over {INPUT_SETS} copies of the packed "
                          f"inputs ({INPUT_SETS * set_bytes / 2**20:.0f} MB), no flush",
                    "timing": "step = one CUDA graph of one quoka_chunk_attend_varlen call, K steps back to back",
@@ -650,7 +654,17 @@ def _oracle_inputs(x, g, G):
             f(x.V_chunk[g:g + 1]))
 
 
-def cpu_baseline(cfg, x, gqa, groups=None):
+def variant_keys(args) -> dict:
+    """The key-score ablation in force, named in the config only when one is."""
+    out = {}
+    if args.score_fn != "cos":
+        out["score_fn"] = args.score_fn
+    if args.query_agg != "max":
+        out["query_agg"] = args.query_agg
+    return out
+
+
+def cpu_baseline(cfg, x, gqa, groups=None, score_fn="cos", query_agg="max"):
     """The oracle as it stands on this host's cores, on KV groups of the same chunk (each group is an
     independent 1/H_kv share of the chunk's work); reported as the equivalent chunk tokens/s."""
     from oracle import quoka_oracle as qo
@@ -659,7 +673,7 @@ def cpu_baseline(cfg, x, gqa, groups=None):
     for g in groups:
         args = _oracle_inputs(x, g, cfg.G)
         t0 = time.perf_counter()
-        qo.chunk_attend(*args, cfg.N_q, cfg.B, gqa)
+        qo.chunk_attend(*args, cfg.N_q, cfg.B, gqa, score_fn=score_fn, query_agg=query_agg)
         t += time.perf_counter() - t0
     per_chunk = t * cfg.H_kv / len(groups)
     return {"value": round(cfg.C / per_chunk, 2), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
@@ -728,7 +742,7 @@ def run_reference(args, rank, world):
         g = k % cfg.H_kv
         a = _oracle_inputs(x, g, cfg.G)
         t0 = time.perf_counter()
-        qo.chunk_attend(*a, cfg.N_q, cfg.B, args.gqa)
+        qo.chunk_attend(*a, cfg.N_q, cfg.B, args.gqa, score_fn=args.score_fn, query_agg=args.query_agg)
         dt = time.perf_counter() - t0
         if k >= args.warmup:
             times.append(dt)
@@ -739,7 +753,8 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(per_chunk * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "H_q": cfg.H_q, "H_kv": cfg.H_kv, "d": cfg.d, "C": cfg.C, "T": cfg.T,
-                   "N_q": cfg.N_q, "B": cfg.B, "gqa_pool": args.gqa, "parallelism": "host cores"},
+                   "N_q": cfg.N_q, "B": cfg.B, "gqa_pool": args.gqa, **variant_keys(args),
+                   "parallelism": "host cores"},
         "impl": "reference",
         "gpu_launches": 0,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
@@ -758,6 +773,10 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(RAGGED), default="gqa32k")
     ap.add_argument("--gqa", choices=["max", "mean"], default="max")
     ap.add_argument("--engine", choices=["auto", "simt", "tensor"], default="auto")
+    ap.add_argument("--score-fn", choices=["cos", "dot"], default="cos",
+                    help="key score: cosine (the method) or the dot-product ablation")
+    ap.add_argument("--query-agg", choices=["max", "mean"], default="max",
+                    help="aggregation over the selected queries: max (the method) or the mean ablation")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")

@@ -97,11 +97,26 @@ typedef struct {
   int32_t dtype;           /* quoka_dtype */
 } quoka_shape;
 
+/* Variants of the key score, OR-ed into quoka_params.flags.  The pages report
+ * both as ablations of the method ([P1] "Scoring via Cosine Similarity":
+ * cosine against the plain dot product; [P1] "Aggregation Across Queries and
+ * KV Groups", [P2] "Why take the maximum": the maximum against the mean over
+ * the selected queries).  0 is the method as published.  They change the key
+ * score only: query subselection is always on the cosine to the mean query,
+ * and attention is unchanged.
+ *  SCORE_DOT:  score rows and keys are not normalised: r . k_t.  With
+ *              MEAN_PREAGG the pre-aggregated row is the mean of the raw
+ *              query heads.
+ *  QUERY_MEAN: the selected tokens are aggregated by their mean instead of
+ *              the maximum.  With QUOKA_GQA_MAX each head's tokens are
+ *              averaged and the maximum over the group's heads is kept. */
+enum { QUOKA_FLAG_SCORE_DOT = 1, QUOKA_FLAG_QUERY_MEAN = 2 };
+
 typedef struct {
   int32_t gqa_pool;        /* quoka_gqa_pool */
   int32_t engine;          /* quoka_engine */
   float softmax_scale;     /* <= 0 means 1/sqrt(d) */
-  int32_t reserved;        /* must be 0 */
+  int32_t flags;           /* 0, or an OR of QUOKA_FLAG_*; other bits must be 0 */
 } quoka_params;
 
 /* Human-readable name of a status code (static storage). */
@@ -148,7 +163,8 @@ int quoka_select_queries_noalloc(const quoka_shape* shape, const void* Q, int N_
  *   scores[g, t] = max over the group's scoring rows r of  r . k_t / |k_t|
  * where the rows are the normalised selected queries of every head of g
  * (MAX) or their head average per selected token (MEAN_PREAGG).  Products
- * are accumulated in fp32.  q_idx as written by quoka_select_queries with the
+ * are accumulated in fp32.  params->flags selects the ablation variants
+ * (QUOKA_FLAG_*).  q_idx as written by quoka_select_queries with the
  * same N_q and pooling.  scores: fp32 [H_kv, T].  Uses ws. */
 int quoka_score_keys(const quoka_shape* shape, const void* Q, const int32_t* q_idx, int N_q,
                      const void* K_hist, const quoka_params* params, float* scores,

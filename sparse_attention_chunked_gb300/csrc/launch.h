@@ -42,20 +42,36 @@ cudaError_t launch_select_queries(int dtype, int d, const void* Q, int H_q, int 
                                   int32_t* q_idx, float* qnorm, float* qpart, float* qcos, WsHeader* hdr,
                                   cudaStream_t st);
 
-// Operand of the scoring stage.  op_f32 (CUDA-core scoring: unit or
-// pre-aggregated fp32 rows [H_kv][R][d]) and op_bf (tensor-core scoring) may
-// each be NULL.  op_bf rows, N_pad per pass (a multiple of 64, >= R):
+// Operand of the scoring stage: which rows score a KV group's keys.
+//   mode 1 (per-head max pooling): the selected (head, token) pairs of the
+//     group's heads; mode 0 (mean pooling): per selected token, the mean over
+//     the group's heads (pre-aggregation).
+//   unit: each query is normalised first (cosine score); else used as it is.
+//   qmean: the rows of a head (mode 1) or of the group (mode 0) are replaced
+//     by their mean (the mean over the selected tokens, folded into the
+//     operand since the score is linear in the row).
+struct OperandSpec {
+  int mode;
+  bool unit;
+  bool qmean;
+};
+
+// op_f32 (CUDA-core scoring: fp32 rows [H_kv][R][d]) and op_bf (tensor-core
+// scoring) may each be NULL.  op_bf rows, N_pad per pass (a multiple of 64,
+// >= R):
 //   op_scale == NULL: two passes, the fp32 row split into hi and lo bf16 rows,
 //                     [H_kv][2][N_pad][d];
-//   op_scale != NULL: max pooling with bf16 Q only, one pass holding the
+//   op_scale != NULL: mode 1 without qmean, bf16 Q only: one pass holding the
 //                     selected query rows as they are, [H_kv][N_pad][d], and
-//                     op_scale [H_kv][N_pad] = 1 / max(|q|, eps) (0 for padding).
+//                     op_scale [H_kv][N_pad] = 1 / max(|q|, eps) (1 when not
+//                     unit; 0 for padding).
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
-                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
-                                 cudaStream_t st);
+                                 int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
+                                 float* op_scale, cudaStream_t st);
 
+// score[g, t] = max_r (r . k_t) * (key_norm ? 1 / max(|k_t|, eps) : 1).
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
-                              const float* op_f32, int R, float* scores, cudaStream_t st);
+                              const float* op_f32, int R, bool key_norm, float* scores, cudaStream_t st);
 
 // Tensor-core scoring (bf16 keys).  op_bf / op_scale as written by
 // launch_build_operand with N_pad = score_tc_pad_rows(R); npass = 1 when
@@ -64,7 +80,7 @@ int score_tc_pad_rows(int R);
 size_t score_tc_smem(int d, int N_pad, int npass, int nst);
 struct WsHeader;
 cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
-                            const float* op_scale, int R, float* scores, WsHeader* hdr, int num_sms,
+                            const float* op_scale, int R, bool key_norm, float* scores, WsHeader* hdr, int num_sms,
                             cudaStream_t st);
 
 // Raises `func`'s dynamic shared-memory limit to `bytes` on the current device (cached).

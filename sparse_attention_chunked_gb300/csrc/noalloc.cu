@@ -63,7 +63,7 @@ extern "C" int quoka_select_queries_noalloc(const quoka_shape* s, const void* Q,
   int gqa = QUOKA_GQA_MEAN_PREAGG;
   if (params != nullptr) {
     if (params->gqa_pool != QUOKA_GQA_MEAN_PREAGG && params->gqa_pool != QUOKA_GQA_MAX) return QUOKA_ERR_INVALID_ARG;
-    if (params->reserved != 0) return QUOKA_ERR_INVALID_ARG;
+    if ((params->flags & ~(QUOKA_FLAG_SCORE_DOT | QUOKA_FLAG_QUERY_MEAN)) != 0) return QUOKA_ERR_INVALID_ARG;
     gqa = params->gqa_pool;
   }
   if (((uintptr_t)Q & 15u) != 0 || ((uintptr_t)q_idx & 15u) != 0) return QUOKA_ERR_ALIGNMENT;

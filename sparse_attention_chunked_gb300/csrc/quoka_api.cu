@@ -44,16 +44,21 @@ struct Params {
   int gqa;        // quoka_gqa_pool
   int engine;     // quoka_engine
   float scale;
+  bool dot;       // QUOKA_FLAG_SCORE_DOT
+  bool qmean;     // QUOKA_FLAG_QUERY_MEAN
 };
 
 int read_params(const quoka_params* p, const quoka_shape* s, Params* out) {
   out->gqa = QUOKA_GQA_MEAN_PREAGG;
   out->engine = QUOKA_ENGINE_AUTO;
   out->scale = 1.0f / sqrtf((float)s->d);
+  out->dot = out->qmean = false;
   if (p == nullptr) return QUOKA_OK;
   if (p->gqa_pool != QUOKA_GQA_MEAN_PREAGG && p->gqa_pool != QUOKA_GQA_MAX) return QUOKA_ERR_INVALID_ARG;
   if (p->engine < QUOKA_ENGINE_AUTO || p->engine > QUOKA_ENGINE_TENSOR) return QUOKA_ERR_INVALID_ARG;
-  if (p->reserved != 0) return QUOKA_ERR_INVALID_ARG;
+  if ((p->flags & ~(QUOKA_FLAG_SCORE_DOT | QUOKA_FLAG_QUERY_MEAN)) != 0) return QUOKA_ERR_INVALID_ARG;
+  out->dot = (p->flags & QUOKA_FLAG_SCORE_DOT) != 0;
+  out->qmean = (p->flags & QUOKA_FLAG_QUERY_MEAN) != 0;
   if (!(p->softmax_scale == p->softmax_scale)) return QUOKA_ERR_INVALID_ARG;   // NaN
   out->gqa = p->gqa_pool;
   out->engine = p->engine;
@@ -63,9 +68,14 @@ int read_params(const quoka_params* p, const quoka_shape* s, Params* out) {
 
 int n_sel_of(const quoka_shape* s, int N_q) { return N_q < s->C ? N_q : s->C; }
 
-int score_rows(const quoka_shape* s, int N_q, int gqa) {
+// Scoring rows per KV group: every selected (head, token) for per-head max
+// pooling, one pre-aggregated row per token for mean pooling; the mean over
+// the selected tokens is linear, so QUOKA_FLAG_QUERY_MEAN folds the tokens
+// into one row per head (max pooling) or per group (mean pooling).
+int score_rows(const quoka_shape* s, int N_q, const Params& p) {
   const int n = n_sel_of(s, N_q), G = s->H_q / s->H_kv;
-  return gqa == QUOKA_GQA_MAX ? G * n : n;
+  if (p.gqa == QUOKA_GQA_MAX) return p.qmean ? G : G * n;
+  return p.qmean ? 1 : n;
 }
 
 int num_sms() {
@@ -75,30 +85,31 @@ int num_sms() {
   return n;
 }
 
-// MMA passes of the tensor-core scoring operand.  Mean-pooled rows are fp32
-// and go in as hi + lo bf16 rows (two passes).  Max pooling can score with the
-// bf16 query rows themselves (one pass, a per-row scale in the epilogue), but
-// the scale loads slow the epilogue more than the second pass costs, so the
-// unit rows go in as hi + lo too whenever that operand fits shared memory
-// (up to 256 rows at d = 128); wider operands take the one-pass form.
-int score_npass(const quoka_shape* s, int N_pad, int gqa) {
-  if (gqa != QUOKA_GQA_MAX) return 2;
+// MMA passes of the tensor-core scoring operand.  Rows that are averages
+// (mean pooling, or the mean over tokens) are fp32 and go in as hi + lo bf16
+// rows (two passes).  Per-head max pooling can score with the bf16 query rows
+// themselves (one pass, a per-row scale in the epilogue), but the scale loads
+// slow the epilogue more than the second pass costs, so those rows go in as
+// hi + lo too whenever that operand fits shared memory (up to 256 rows at
+// d = 128); wider operands take the one-pass form.
+int score_npass(const quoka_shape* s, int N_pad, const Params& p) {
+  if (p.gqa != QUOKA_GQA_MAX || p.qmean) return 2;
   return score_tc_smem(s->d, N_pad, 2, 2) <= 227 * 1024 ? 2 : 1;
 }
 
 // Whether the scoring stage can run on the tensor cores: bf16 keys, at most
 // 512 scoring rows (the TMEM width) and an operand that fits shared memory
 // next to two key stages.
-bool score_tc_fits(const quoka_shape* s, int N_q, int gqa) {
+bool score_tc_fits(const quoka_shape* s, int N_q, const Params& p) {
   if (s->dtype != QUOKA_DTYPE_BF16) return false;
-  const int N_pad = score_tc_pad_rows(score_rows(s, N_q, gqa));
-  return N_pad <= 512 && score_tc_smem(s->d, N_pad, score_npass(s, N_pad, gqa), 2) <= 227 * 1024;
+  const int N_pad = score_tc_pad_rows(score_rows(s, N_q, p));
+  return N_pad <= 512 && score_tc_smem(s->d, N_pad, score_npass(s, N_pad, p), 2) <= 227 * 1024;
 }
 
 // Which kernels run (stage 0 = scoring, 1 = attention).  Tensor-core kernels are bf16 only.
 bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage, int N_q = 1) {
   if (p.engine == QUOKA_ENGINE_SIMT || s->dtype != QUOKA_DTYPE_BF16) return false;
-  if (stage == 0) return score_tc_fits(s, N_q, p.gqa);
+  if (stage == 0) return score_tc_fits(s, N_q, p);
   return attend_tc_smem(s->d) <= 227 * 1024;
 }
 
@@ -113,7 +124,7 @@ struct Layout {
 // Regions start at `start` (just past the header for a single call; a lane's
 // slice for the ragged entry point).  The header is always the workspace's
 // first 256 bytes, shared by every lane.
-Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa, size_t start = sizeof(WsHeader)) {
+Layout make_layout(const quoka_shape* s, int N_q, int B, const Params& p, size_t start = sizeof(WsHeader)) {
   Layout L;
   const size_t H_q = s->H_q, H_kv = s->H_kv, C = s->C, d = s->d, T = s->T;
   const size_t nblk = (C + 63) / 64;
@@ -122,10 +133,10 @@ Layout make_layout(const quoka_shape* s, int N_q, int B, int gqa, size_t start =
   L.qpart = o;  o = align_up(o + H_q * nblk * d * 4);
   L.qcos = o;   o = align_up(o + H_q * C * 4);
   L.select_end = o;
-  const size_t R = (size_t)score_rows(s, N_q > 0 ? N_q : 1, gqa);
+  const size_t R = (size_t)score_rows(s, N_q > 0 ? N_q : 1, p);
   const size_t N_pad = (size_t)score_tc_pad_rows((int)R);
   L.op_f32 = o;   o = align_up(o + H_kv * R * d * 4);
-  L.op_bf = o;    o = align_up(o + H_kv * (size_t)score_npass(s, (int)N_pad, gqa) * N_pad * d * 2);
+  L.op_bf = o;    o = align_up(o + H_kv * (size_t)score_npass(s, (int)N_pad, p) * N_pad * d * 2);
   L.op_scale = o; o = align_up(o + H_kv * N_pad * 4);
   L.score_end = o;
   const size_t n = (size_t)n_sel_of(s, N_q > 0 ? N_q : 1);
@@ -173,20 +184,24 @@ int run_select(const quoka_shape* s, const void* Q, int n, const Params& p, int3
 int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, const void* K_hist,
               const Params& p, float* scores, void* ws, const Layout& L, cudaStream_t st) {
   const int G = s->H_q / s->H_kv;
-  const int mode = p.gqa == QUOKA_GQA_MAX ? 1 : 0;
-  const int R = score_rows(s, n, p.gqa);
+  OperandSpec os;
+  os.mode = p.gqa == QUOKA_GQA_MAX ? 1 : 0;
+  os.unit = !p.dot;
+  os.qmean = p.qmean;
+  const int R = score_rows(s, n, p);
   const int N_pad = score_tc_pad_rows(R);
   const bool tc = use_tensor_cores(p, s, 0, n);
   if (p.engine == QUOKA_ENGINE_TENSOR && !tc) return QUOKA_ERR_UNSUPPORTED;
-  float* op_scale = tc && score_npass(s, N_pad, p.gqa) == 1 ? at<float>(ws, L.op_scale) : nullptr;
-  QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, mode, N_pad,
+  float* op_scale = tc && score_npass(s, N_pad, p) == 1 ? at<float>(ws, L.op_scale) : nullptr;
+  QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, os, N_pad,
                                   tc ? nullptr : at<float>(ws, L.op_f32), tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr,
                                   op_scale, st));
+  const bool key_norm = !p.dot;
   if (tc)
     return cuda_status(launch_score_tc(s->d, K_hist, head_stride(s), s->H_kv, s->T, at<__nv_bfloat16>(ws, L.op_bf),
-                                       op_scale, R, scores, at<WsHeader>(ws, 0), num_sms(), st));
+                                       op_scale, R, key_norm, scores, at<WsHeader>(ws, 0), num_sms(), st));
   return cuda_status(launch_score_simt(s->dtype, s->d, K_hist, head_stride(s), s->H_kv, s->T,
-                                       at<float>(ws, L.op_f32), R, scores, st));
+                                       at<float>(ws, L.op_f32), R, key_norm, scores, st));
 }
 
 int run_attend(const quoka_shape* s, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
@@ -299,7 +314,7 @@ int varlen_lane_bytes(const quoka_varlen_shape* v, const int64_t* cu_T, const in
     if (sh.C == 0) continue;
     Params p;
     QUOKA_TRY(read_params(params, &sh, &p));
-    lane = std::max(lane, make_layout(&sh, N_q, B, p.gqa).total - sizeof(WsHeader));
+    lane = std::max(lane, make_layout(&sh, N_q, B, p).total - sizeof(WsHeader));
   }
   *out = align_up(lane);
   return QUOKA_OK;
@@ -381,7 +396,7 @@ int quoka_workspace_size(const quoka_shape* shape, int N_q, int B, const quoka_p
   Params p;
   QUOKA_TRY(read_params(params, shape, &p));
   if (N_q < 1 || B < 1 || bytes == nullptr) return QUOKA_ERR_INVALID_ARG;
-  *bytes = make_layout(shape, N_q, B, p.gqa).total;
+  *bytes = make_layout(shape, N_q, B, p).total;
   return QUOKA_OK;
 }
 
@@ -392,7 +407,7 @@ int quoka_select_queries(const quoka_shape* shape, const void* Q, int N_q, const
   QUOKA_TRY(read_params(params, shape, &p));
   if (N_q < 1 || Q == nullptr || q_idx == nullptr) return QUOKA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(q_idx)) return QUOKA_ERR_ALIGNMENT;
-  const Layout L = make_layout(shape, N_q, 1, p.gqa);
+  const Layout L = make_layout(shape, N_q, 1, p);
   QUOKA_TRY(check_ws(ws, ws_bytes, L.select_end));
   return run_select(shape, Q, n_sel_of(shape, N_q), p, q_idx, ws, L, (cudaStream_t)stream);
 }
@@ -405,7 +420,7 @@ int quoka_score_keys(const quoka_shape* shape, const void* Q, const int32_t* q_i
   if (N_q < 1 || Q == nullptr || q_idx == nullptr || K_hist == nullptr || scores == nullptr)
     return QUOKA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(q_idx) || !aligned16(K_hist) || !aligned16(scores)) return QUOKA_ERR_ALIGNMENT;
-  const Layout L = make_layout(shape, N_q, 1, p.gqa);
+  const Layout L = make_layout(shape, N_q, 1, p);
   QUOKA_TRY(check_ws(ws, ws_bytes, L.score_end));
   if (shape->T == 0) return QUOKA_OK;
   return run_score(shape, Q, q_idx, n_sel_of(shape, N_q), K_hist, p, scores, ws, L, (cudaStream_t)stream);
@@ -472,7 +487,7 @@ int quoka_chunk_attend(const quoka_shape* shape, const void* Q, const void* K_hi
   Params p;
   QUOKA_TRY(read_params(params, shape, &p));
   QUOKA_TRY(check_chunk_args(shape, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, O, lse, sel_out));
-  const Layout L = make_layout(shape, N_q, B, p.gqa);
+  const Layout L = make_layout(shape, N_q, B, p);
   QUOKA_TRY(check_ws(ws, ws_bytes, L.total));
   return run_chunk(shape, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, p, O, lse, sel_out, ws, L,
                    (cudaStream_t)stream);
@@ -543,7 +558,7 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
   }
   for (int l = 0; l < lanes; ++l)
     for (int i : plan[l])
-      seqs[i].L = make_layout(&seqs[i].shape, N_q, B, seqs[i].p.gqa, sizeof(WsHeader) + (size_t)l * lane_bytes);
+      seqs[i].L = make_layout(&seqs[i].shape, N_q, B, seqs[i].p, sizeof(WsHeader) + (size_t)l * lane_bytes);
   if (lanes == 1) {
     for (int i : plan[0])
       QUOKA_TRY(run_chunk(&seqs[i].shape, seqs[i].Q, seqs[i].K_hist, seqs[i].V_hist, seqs[i].K_chunk,

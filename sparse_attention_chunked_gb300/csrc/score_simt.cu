@@ -19,10 +19,17 @@ namespace quoka {
 // Tensor-core copy of either: hi = bf16(row) in pass 0 and lo = bf16(row - hi)
 // in pass 1 (hi + lo carries the fp32 row to about 2^-16 relative).
 // Layouts: op_f32 [H_kv, R, D]; op_bf [H_kv, 2, N_pad, D].
+// One warp per scoring row.  Row r of group g is the weighted sum over its
+// (head, token) pairs of the (unit) query rows:
+//   mode 1:           pairs (head k, token i), r = k * n + i, weight 1;
+//   mode 1 + qmean:   r = k, pairs (head k, every selected token), weight 1/n;
+//   mode 0:           r = i, pairs (every head of g, token i), weight 1/G;
+//   mode 0 + qmean:   r = 0, every (head, token) of g, weight 1/(G n).
 template <typename T, int D>
 __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, const int32_t* __restrict__ q_idx,
-                                                      int C, int G, int n, int mode, int R, float* __restrict__ op_f32,
-                                                      __nv_bfloat16* __restrict__ op_bf, float* __restrict__ op_scale) {
+                                                      int C, int G, int n, OperandSpec spec, int R,
+                                                      float* __restrict__ op_f32, __nv_bfloat16* __restrict__ op_bf,
+                                                      float* __restrict__ op_scale) {
   pdl_launch_dependents();
   pdl_wait();
   constexpr int E = D / 32;
@@ -38,46 +45,48 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
     }
     return;
   }
+  // the (head, token) pairs of row r: heads [k0, k1) of the group, tokens [i0, i1) of the selection
+  int k0, k1, i0, i1;
+  if (spec.mode == 1) {
+    k0 = spec.qmean ? r : r / n;
+    i0 = spec.qmean ? 0 : r % n;
+    i1 = spec.qmean ? n : i0 + 1;
+  } else {
+    k0 = 0;
+    i0 = spec.qmean ? 0 : r;
+    i1 = spec.qmean ? n : r + 1;
+  }
+  k1 = spec.mode == 1 ? k0 + 1 : G;
   float acc[E];
-  if (mode == 1) {  // MAX
-    const int k = r / n, i = r % n, h = g * G + k;
-    const int c = q_idx[(size_t)h * n + i];
-    const T* q = Q + ((size_t)h * C + c) * D;
-    float x[E], ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < E; ++j) {
-      x[j] = to_f32(q[lane + 32 * j]);
-      ss = fmaf(x[j], x[j], ss);
-    }
-    ss = warp_sum(ss);
-    const float inv = 1.0f / fmaxf(sqrtf(ss), kNormEps);
-    if (op_scale != nullptr) {   // the query row itself (exact in bf16) and its scale
-#pragma unroll
-      for (int j = 0; j < E; ++j) op_bf[((size_t)g * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
-      if (lane == 0) op_scale[(size_t)g * N_pad + r] = inv;
-    }
-#pragma unroll
-    for (int j = 0; j < E; ++j) acc[j] = x[j] * inv;
-  } else {  // MEAN (pre-aggregation)
-    const int c = q_idx[(size_t)g * n + r];
-#pragma unroll
-    for (int j = 0; j < E; ++j) acc[j] = 0.f;
-    for (int k = 0; k < G; ++k) {
-      const T* q = Q + ((size_t)(g * G + k) * C + c) * D;
-      float x[E], ss = 0.f;
+  for (int j = 0; j < E; ++j) acc[j] = 0.f;
+  float x[E], inv = 1.f;
+  for (int k = k0; k < k1; ++k) {
+    const int h = g * G + k;
+    const int32_t* sel_row = q_idx + (size_t)(spec.mode == 1 ? h : g) * n;
+    for (int i = i0; i < i1; ++i) {
+      const T* q = Q + ((size_t)h * C + sel_row[i]) * D;
+      float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < E; ++j) {
         x[j] = to_f32(q[lane + 32 * j]);
         ss = fmaf(x[j], x[j], ss);
       }
-      ss = warp_sum(ss);
-      const float inv = 1.0f / fmaxf(sqrtf(ss), kNormEps);
+      inv = spec.unit ? 1.0f / fmaxf(sqrtf(warp_sum(ss)), kNormEps) : 1.f;
 #pragma unroll
       for (int j = 0; j < E; ++j) acc[j] = fmaf(x[j], inv, acc[j]);
     }
-    const float invG = 1.0f / (float)G;
+  }
+  const int pairs = (k1 - k0) * (i1 - i0);
+  if (pairs > 1) {
+    const float w = 1.0f / (float)pairs;
 #pragma unroll
-    for (int j = 0; j < E; ++j) acc[j] *= invG;
+    for (int j = 0; j < E; ++j) acc[j] *= w;
+  }
+  if (op_bf != nullptr && npass == 1) {   // one (head, token) pair: the query row itself and its scale
+#pragma unroll
+    for (int j = 0; j < E; ++j) op_bf[((size_t)g * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
+    if (lane == 0) op_scale[(size_t)g * N_pad + r] = inv;
   }
   if (op_bf != nullptr && npass == 2) {
 #pragma unroll
@@ -98,7 +107,7 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
 // stream through shared memory 32 at a time; score = max_r(r . k) / |k|.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int64_t head_stride, int T_len,
-                                                    const float* __restrict__ op_f32, int R,
+                                                    const float* __restrict__ op_f32, int R, bool key_norm,
                                                     float* __restrict__ scores) {
   pdl_launch_dependents();
   pdl_wait();
@@ -118,7 +127,7 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
 #pragma unroll
     for (int e = 0; e < D; ++e) k[e] = 0.f;
   }
-  const float rk = 1.0f / fmaxf(sqrtf(ss), kNormEps);
+  const float rk = key_norm ? 1.0f / fmaxf(sqrtf(ss), kNormEps) : 1.0f;
   float best = -INFINITY;
   const float* opg = op_f32 + (size_t)g * R * D;
   for (int r0 = 0; r0 < R; r0 += 32) {
@@ -137,25 +146,26 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
 }
 
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
-                                 int n, int mode, int N_pad, float* op_f32, __nv_bfloat16* op_bf, float* op_scale,
-                                 cudaStream_t st) {
-  const int R = mode == 1 ? G * n : n;
-  if (op_scale != nullptr && (mode != 1 || dtype != 0 || op_bf == nullptr)) return cudaErrorInvalidValue;
+                                 int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
+                                 float* op_scale, cudaStream_t st) {
+  const int R = spec.mode == 1 ? (spec.qmean ? G : G * n) : (spec.qmean ? 1 : n);
+  if (op_scale != nullptr && (spec.mode != 1 || spec.qmean || dtype != 0 || op_bf == nullptr))
+    return cudaErrorInvalidValue;
   dim3 grid(op_bf != nullptr ? N_pad : R, H_kv);
   cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
       e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n,
-                     mode, R, op_f32, op_bf, op_scale);
+                     spec, R, op_f32, op_bf, op_scale);
     else
       e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G,
-                     n, mode, R, op_f32, op_bf, op_scale);
+                     n, spec, R, op_f32, op_bf, op_scale);
   } else {
     if (d == 64)
-      e = launch_pdl(k_build_operand<float, 64>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R,
+      e = launch_pdl(k_build_operand<float, 64>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
                      op_f32, op_bf, op_scale);
     else
-      e = launch_pdl(k_build_operand<float, 128>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, mode, R,
+      e = launch_pdl(k_build_operand<float, 128>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
                      op_f32, op_bf, op_scale);
   }
   count_launches(1);
@@ -163,20 +173,20 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
 }
 
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
-                              const float* op_f32, int R, float* scores, cudaStream_t st) {
+                              const float* op_f32, int R, bool key_norm, float* scores, cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
   dim3 grid((T_len + 127) / 128, H_kv);
   cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, scores);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, key_norm, scores);
     else
-      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, scores);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, key_norm, scores);
   } else {
     if (d == 64)
-      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, scores);
+      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, key_norm, scores);
     else
-      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, scores);
+      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, key_norm, scores);
   }
   count_launches(1);
   return e;

@@ -39,7 +39,7 @@ class Shape(ctypes.Structure):
 
 class Params(ctypes.Structure):
     _fields_ = [("gqa_pool", ctypes.c_int32), ("engine", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
 
 
 class VarlenShape(ctypes.Structure):
@@ -138,8 +138,13 @@ def shape_of(Q: torch.Tensor, K_hist: torch.Tensor | None, H_kv: int | None = No
     return Shape(kv_head_stride, H_q, H_kv, C, T or 0, d, DTYPE[Q.dtype])
 
 
-def params_of(gqa: str = "mean", engine: str = "auto", softmax_scale: float = 0.0) -> Params:
-    return Params(GQA[gqa], ENGINE[engine], softmax_scale, 0)
+SCORE_FLAGS = {"cos": 0, "dot": 1}        # QUOKA_FLAG_SCORE_DOT
+QUERY_AGG_FLAGS = {"max": 0, "mean": 2}   # QUOKA_FLAG_QUERY_MEAN
+
+
+def params_of(gqa: str = "mean", engine: str = "auto", softmax_scale: float = 0.0, score_fn: str = "cos",
+              query_agg: str = "max") -> Params:
+    return Params(GQA[gqa], ENGINE[engine], softmax_scale, SCORE_FLAGS[score_fn] | QUERY_AGG_FLAGS[query_agg])
 
 
 def workspace_size(shape: Shape, N_q: int, B: int, params: Params) -> int:

@@ -101,7 +101,7 @@ def test_chunk_attend_argument_errors(quoka):
     assert _chunk_call(q, s, ws_bytes=need - 1) == 3         # workspace too small
     assert _chunk_call(q, s, params=q.Params(5, 0, 0.0, 0)) == 1     # unknown pooling
     assert _chunk_call(q, s, params=q.Params(0, 9, 0.0, 0)) == 1     # unknown engine
-    assert _chunk_call(q, s, params=q.Params(0, 0, 0.0, 1)) == 1     # reserved field set
+    assert _chunk_call(q, s, params=q.Params(0, 0, 0.0, 4)) == 1     # undefined flag bit
     assert _chunk_call(q, s, params=q.Params(0, 0, float("nan"), 0)) == 1
 
 

@@ -17,12 +17,12 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def run_stages(q, cfg, x, gqa, engine="auto"):
+def run_stages(q, cfg, x, gqa, engine="auto", score_fn="cos", query_agg="max"):
     """Every stage through its own entry point, then the fused call on the same inputs."""
     Q, Kh, Vh = x.Q.to(DEV), x.K_hist.to(DEV), x.V_hist.to(DEV)
     Kc, Vc = x.K_chunk.to(DEV), x.V_chunk.to(DEV)
     shape = q.shape_of(Q, Kh, H_kv=cfg.H_kv, T=cfg.T)
-    params = q.params_of(gqa, engine)
+    params = q.params_of(gqa, engine, score_fn=score_fn, query_agg=query_agg)
     ws = q.make_workspace(shape, cfg.N_q, cfg.B, params)
     n = min(cfg.N_q, cfg.C)
     H_sel = cfg.H_q if gqa == "max" else cfg.H_kv
@@ -50,15 +50,20 @@ def run_stages(q, cfg, x, gqa, engine="auto"):
     return out
 
 
-def check_stages(cfg, x, gqa, r):
+def check_stages(cfg, x, gqa, r, score_fn="cos", query_agg="max"):
     Q, Kh, Vh = f64(x.Q), f64(x.K_hist), f64(x.V_hist)
     Kc, Vc = f64(x.K_chunk), f64(x.V_chunk)
     # a1/a2: query subselection, modulo ties of the (group-averaged) cosine
     check_index_rows(r["q_idx"], oracle_query_values(Q, cfg.H_kv, gqa), cfg.N_q, largest=False, what="q_idx")
-    # a3: scores of the oracle on the GPU's selected queries
-    ref_scores = qo.score_keys(Q, Kh, r["q_idx"], gqa)
+    # a3: scores of the oracle on the GPU's selected queries; a dot-product score carries the
+    # norms, so its rounding scales with the largest |row| * |key|
+    ref_scores = qo.score_keys(Q, Kh, r["q_idx"], gqa, score_fn, query_agg)
+    mag = 1.0
+    if score_fn == "dot" and cfg.T > 0:
+        rows = qo.scoring_queries(Q, r["q_idx"], cfg.H_kv, gqa, "dot")
+        mag = max(1.0, max(np.linalg.norm(rw, axis=1).max() for rw in rows) * np.linalg.norm(Kh, axis=2).max())
     err = np.max(np.abs(f64(r["scores"]) - ref_scores))
-    assert err <= SCORE_ATOL, f"scores: max-abs error {err}"
+    assert err <= SCORE_ATOL * mag, f"scores: max-abs error {err} (scale {mag})"
     # a4: top-B on the oracle's scores, modulo ties
     check_index_rows(r["sel"], ref_scores, cfg.B, largest=True, what="sel")
     # a5: gather is a byte-exact copy
@@ -100,6 +105,32 @@ def test_small_cases(quoka, name, kw, gqa, engine):
     cfg, x = wl.small_chunk(**kw)
     r = run_stages(quoka, cfg, x, gqa, engine)
     check_stages(cfg, x, gqa, r)
+
+
+VARIANT_CASES = [
+    ("gqa4_bf16_d128", dict(H_q=8, H_kv=2, d=128, C=200, T=1000, N_q=12, B=300, dtype="bf16")),
+    ("gqa5_bf16_320_rows", dict(H_q=10, H_kv=2, d=128, C=256, T=2000, N_q=64, B=300, dtype="bf16")),
+    ("mha_fp32_ragged", dict(H_q=4, H_kv=4, d=64, C=77, T=333, N_q=9, B=50, dtype="fp32")),
+]
+
+
+@pytest.mark.parametrize("score_fn,query_agg", [("dot", "max"), ("cos", "mean"), ("dot", "mean")])
+@pytest.mark.parametrize("gqa", ["max", "mean"])
+@pytest.mark.parametrize("name,kw", VARIANT_CASES, ids=[c[0] for c in VARIANT_CASES])
+def test_score_variants(quoka, name, kw, gqa, score_fn, query_agg):
+    """The ablations of the key score (dot product, mean over the selected queries) against the oracle."""
+    cfg, x = wl.small_chunk(**kw)
+    r = run_stages(quoka, cfg, x, gqa, score_fn=score_fn, query_agg=query_agg)
+    check_stages(cfg, x, gqa, r, score_fn, query_agg)
+
+
+@pytest.mark.parametrize("score_fn,query_agg", [("dot", "max"), ("cos", "mean")])
+def test_score_variants_full_size(quoka, score_fn, query_agg):
+    """32K history, GQA 32/8, per-head max pooling: the variants on the tensor-core scorer at size."""
+    cfg = wl.GQA_32K_BF16
+    x = wl.make_chunk(cfg, 0)
+    r = run_stages(quoka, cfg, x, "max", score_fn=score_fn, query_agg=query_agg)
+    check_stages(cfg, x, "max", r, score_fn, query_agg)
 
 
 @pytest.mark.parametrize("gqa", ["max", "mean"])
