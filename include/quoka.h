@@ -192,7 +192,9 @@ int quoka_gather(const quoka_shape* shape, const void* K_hist, const void* V_his
  *   k = [K_sel[g, 0..B_e) ; K_chunk[g, 0..c]]   (causal within the chunk)
  * K_sel, V_sel [H_kv, B_e, d] contiguous (B_e may be 0).  lse, if not NULL,
  * receives fp32 [H_q, C] natural-log softmax denominators of the scaled
- * logits.  Uses ws (error word only). */
+ * logits.  Uses ws: the error word and, for chunks of at most 32 / G queries
+ * (decode), scratch for the split-key partial results (quoka_workspace_size
+ * covers it). */
 int quoka_sparse_attend(const quoka_shape* shape, const void* Q, const void* K_sel, const void* V_sel,
                         int B_e, const void* K_chunk, const void* V_chunk, const quoka_params* params,
                         void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
@@ -251,7 +253,8 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
 
 /* Dense chunked-prefill attention over every history key plus the causal
  * chunk ([P1] "Chunked prefill"): the reference QUOKA is measured against.
- * Arguments as quoka_chunk_attend without the selection. */
+ * Arguments as quoka_chunk_attend without the selection; ws as for
+ * quoka_sparse_attend. */
 int quoka_dense_attend(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
                        const void* K_chunk, const void* V_chunk, const quoka_params* params,
                        void* O, float* lse, void* ws, size_t ws_bytes, void* stream);

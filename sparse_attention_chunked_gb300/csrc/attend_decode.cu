@@ -1,0 +1,246 @@
+// Attention for chunks of a few queries (decode: C = 1), split over the keys.
+// Method: QUOKA paper summary, "Transformers and Attention" (softmax
+// attention with a causal mask), "Chunked prefill" (the chunk attends to the
+// earlier keys plus itself, causally), "QUOKA Method" (the reduced key set is
+// fed to attention); QUOKA Explained, "From scores to a smaller KV set" (a
+// kept key brings its value).
+//
+// With C small, a KV group has only G * C query rows, too few to fill a
+// tensor-core tile or the GPU, while the keys number B_e + C.  So the keys are
+// split into blocks of kDecKeys and every (block, KV group) is one CTA
+// (flash-decoding): the CTA scores its keys against the group's rows, takes
+// the block's softmax statistics (max m and sum l of exp2(s - m)) and the
+// unnormalised output sum p . V, and writes them to the workspace; a second
+// kernel merges the blocks of every row, rescaling each by exp2(m_b - M).
+// The kept history rows are read straight from the cache through `sel` (no
+// gathered copy), and every product and sum is an fp32 FMA on CUDA cores:
+// with so few rows the step is bound by reading the kept K and V rows.
+#include "common.cuh"
+#include "launch.h"
+
+namespace quoka {
+
+namespace {
+
+constexpr int kDecKeys = 64;       // keys per CTA
+constexpr int kDecThreads = 256;
+
+// 16 bytes of T (8 bf16 or 4 fp32) widened into fp32 shared memory.
+__device__ __forceinline__ void store16(float* dst, uint4 u, const float*) {
+  *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                                __uint_as_float(u.w));
+}
+__device__ __forceinline__ void store16(float* dst, uint4 u, const __nv_bfloat16*) {
+  *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                                __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+  *reinterpret_cast<float4*>(dst + 4) = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
+                                                    __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+}
+
+// Rows of a group handled by one CTA: G * C when that is at most 32.
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecThreads) k_attend_decode(
+    const T* __restrict__ Q, const T* __restrict__ Kh, const T* __restrict__ Vh, int64_t h_stride,
+    const int32_t* __restrict__ sel, int n_hist, const T* __restrict__ Kc, const T* __restrict__ Vc, int C, int G,
+    float scale_log2, float* __restrict__ part_ml, float* __restrict__ part_o) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int KP = D + 4;                       // padded key row (floats): conflict-free float4 reads
+  extern __shared__ __align__(16) float dsm[];
+  float* Qs = dsm;                                // [R][D]  scaled by scale * log2(e)
+  float* Ks = Qs + 32 * D;                        // [kDecKeys][KP]
+  float* Vs = Ks + kDecKeys * KP;                 // [kDecKeys][D]
+  float* Ps = Vs + kDecKeys * D;                  // [R][kDecKeys + 1]
+  const int blk = blockIdx.x, g = blockIdx.y, n_blk = gridDim.x;
+  const int R = G * C;
+  const int j0 = blk * kDecKeys;
+  const int n_keys = n_hist + C;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  for (int i = tid; i < R * D; i += kDecThreads) {
+    const int r = i / D, e = i % D;
+    const int h = g * G + r / C, c = r % C;
+    Qs[i] = to_f32(Q[((size_t)h * C + c) * D + e]) * scale_log2;
+  }
+  // the block's keys and values: kept history rows through sel, then the chunk's rows.
+  // Every 16-byte load of the block is issued before the first is used.
+  constexpr int VEC = 16 / (int)sizeof(T);                   // elements per load
+  constexpr int NV = D / VEC;                                // loads per row
+  constexpr int PER = kDecKeys * NV / kDecThreads;           // loads per thread, per tensor
+  static_assert(kDecKeys * NV % kDecThreads == 0, "whole loads per thread");
+  uint4 kr[PER], vr[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = tid + u * kDecThreads, jj = i / NV, e = (i % NV) * VEC;
+    const int j = j0 + jj;
+    kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (j < n_keys) {
+      const T *kp, *vp;
+      if (j < n_hist) {
+        const int64_t t = sel != nullptr ? sel[(size_t)g * n_hist + j] : j;
+        kp = Kh + (size_t)g * h_stride + (size_t)t * D + e;
+        vp = Vh + (size_t)g * h_stride + (size_t)t * D + e;
+      } else {
+        kp = Kc + ((size_t)g * C + (j - n_hist)) * D + e;
+        vp = Vc + ((size_t)g * C + (j - n_hist)) * D + e;
+      }
+      kr[u] = *reinterpret_cast<const uint4*>(kp);
+      vr[u] = *reinterpret_cast<const uint4*>(vp);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = tid + u * kDecThreads, jj = i / NV, e = (i % NV) * VEC;
+    store16(Ks + jj * KP + e, kr[u], Kh);
+    store16(Vs + jj * D + e, vr[u], Vh);
+  }
+  __syncthreads();
+  // scores: thread -> key jj = tid % 64 against rows r = tid / 64 + 4 i
+  {
+    const int jj = tid % kDecKeys, r0 = tid / kDecKeys;
+    const int j = j0 + jj;
+    for (int r = r0; r < R; r += kDecThreads / kDecKeys) {
+      float s0 = 0.f, s1 = 0.f;
+      const float* qr = Qs + r * D;
+      const float* kr = Ks + jj * KP;
+#pragma unroll 8
+      for (int e = 0; e < D; e += 8) {
+        const float4 a = *reinterpret_cast<const float4*>(kr + e);
+        const float4 b = *reinterpret_cast<const float4*>(kr + e + 4);
+        const float4 qa = *reinterpret_cast<const float4*>(qr + e);
+        const float4 qb = *reinterpret_cast<const float4*>(qr + e + 4);
+        s0 = fmaf(qa.x, a.x, s0); s1 = fmaf(qa.y, a.y, s1);
+        s0 = fmaf(qa.z, a.z, s0); s1 = fmaf(qa.w, a.w, s1);
+        s0 = fmaf(qb.x, b.x, s0); s1 = fmaf(qb.y, b.y, s1);
+        s0 = fmaf(qb.z, b.z, s0); s1 = fmaf(qb.w, b.w, s1);
+      }
+      // chunk key j - n_hist is visible to chunk row c iff it is not after it
+      const bool ok = j < n_keys && (j < n_hist || j - n_hist <= r % C);
+      Ps[r * (kDecKeys + 1) + jj] = ok ? s0 + s1 : -INFINITY;
+    }
+  }
+  __syncthreads();
+  // per row: block max and sum of exp2(s - m); p stored back in place
+  for (int r = warp; r < R; r += kDecThreads / 32) {
+    float* pr = Ps + r * (kDecKeys + 1);
+    const float a = pr[lane], b = pr[lane + 32];
+    float m = fmaxf(a, b);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float pa = m == -INFINITY ? 0.f : exp2f(a - m);
+    const float pb = m == -INFINITY ? 0.f : exp2f(b - m);
+    float l = pa + pb;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    pr[lane] = pa;
+    pr[lane + 32] = pb;
+    if (lane == 0) {
+      const size_t row = ((size_t)g * R + r) * n_blk + blk;
+      part_ml[2 * row] = m;
+      part_ml[2 * row + 1] = l;
+    }
+  }
+  __syncthreads();
+  // unnormalised output: thread -> column e = tid % D of rows r = tid / D + (256 / D) i
+  {
+    const int e = tid % D, rstep = kDecThreads / D;
+    for (int r = tid / D; r < R; r += rstep) {
+      const float* pr = Ps + r * (kDecKeys + 1);
+      float o0 = 0.f, o1 = 0.f;
+#pragma unroll 8
+      for (int jj = 0; jj < kDecKeys; jj += 2) {
+        o0 = fmaf(pr[jj], Vs[jj * D + e], o0);
+        o1 = fmaf(pr[jj + 1], Vs[(jj + 1) * D + e], o1);
+      }
+      part_o[(((size_t)g * R + r) * n_blk + blk) * D + e] = o0 + o1;
+    }
+  }
+}
+
+// One warp per (group row): M = max_b m_b, L = sum_b l_b 2^(m_b - M),
+// O = sum_b o_b 2^(m_b - M) / L, lse = (M + log2 L) ln 2 in the units of the
+// scaled logits.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) k_attend_decode_merge(const float* __restrict__ part_ml,
+                                                             const float* __restrict__ part_o, int n_rows, int n_blk,
+                                                             int C, int G, T* __restrict__ O,
+                                                             float* __restrict__ lse) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int E = D / 32;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  const float* ml = part_ml + (size_t)row * n_blk * 2;
+  float M = -INFINITY;
+  for (int b = lane; b < n_blk; b += 32) M = fmaxf(M, ml[2 * b]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = 0.f, acc[E];
+#pragma unroll
+  for (int k = 0; k < E; ++k) acc[k] = 0.f;
+  for (int b = 0; b < n_blk; ++b) {
+    const float mb = ml[2 * b];
+    if (mb == -INFINITY) continue;
+    const float w = exp2f(mb - M);
+    L = fmaf(ml[2 * b + 1], w, L);
+    const float* ob = part_o + ((size_t)row * n_blk + b) * D;
+#pragma unroll
+    for (int k = 0; k < E; ++k) acc[k] = fmaf(ob[lane + 32 * k], w, acc[k]);
+  }
+  // group row -> (head, chunk row)
+  const int g = row / (G * C), r = row % (G * C);
+  const int h = g * G + r / C, c = r % C;
+  const float inv = 1.0f / L;
+#pragma unroll
+  for (int k = 0; k < E; ++k) O[((size_t)h * C + c) * D + lane + 32 * k] = from_f32<T>(acc[k] * inv);
+  if (lse != nullptr && lane == 0) lse[(size_t)h * C + c] = (M + log2f(L)) * 0.69314718055994531f;
+}
+
+size_t decode_smem(int d, int R) {
+  return ((size_t)32 * d + (size_t)kDecKeys * (d + 4) + (size_t)kDecKeys * d + (size_t)R * (kDecKeys + 1)) * 4;
+}
+
+}  // namespace
+
+bool attend_decode_fits(int C, int G) { return C * G <= 32; }
+
+size_t attend_decode_ws_bytes(int d, int H_q, int C, int n_hist) {
+  const size_t n_blk = (size_t)(n_hist + C + kDecKeys - 1) / kDecKeys;
+  return (size_t)H_q * C * n_blk * (2 + (size_t)d) * 4;
+}
+
+cudaError_t launch_attend_decode(int dtype, int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,
+                                 const int32_t* sel, int n_hist, const void* Kc, const void* Vc, int H_q, int H_kv,
+                                 int C, float scale, void* O, float* lse, float* part, cudaStream_t st) {
+  const int G = H_q / H_kv, R = G * C;
+  if (!attend_decode_fits(C, G)) return cudaErrorInvalidValue;
+  const int n_blk = (n_hist + C + kDecKeys - 1) / kDecKeys;
+  float* part_ml = part;
+  float* part_o = part + (size_t)H_q * C * n_blk * 2;
+  const float scale_log2 = scale * 1.4426950408889634f;
+  const size_t smem = decode_smem(d, R);
+  const dim3 grid(n_blk, H_kv), mgrid((H_q * C + 3) / 4);
+  cudaError_t e;
+#define QUOKA_DEC(T, DD)                                                                                          \
+  do {                                                                                                            \
+    e = ensure_smem((const void*)k_attend_decode<T, DD>, smem);                                                   \
+    if (e == cudaSuccess)                                                                                         \
+      e = launch_pdl(k_attend_decode<T, DD>, grid, dim3(kDecThreads), smem, st, (const T*)Q, (const T*)Kh,        \
+                     (const T*)Vh, h_stride, sel, n_hist, (const T*)Kc, (const T*)Vc, C, G, scale_log2, part_ml,  \
+                     part_o);                                                                                     \
+    if (e == cudaSuccess)                                                                                         \
+      e = launch_pdl(k_attend_decode_merge<T, DD>, mgrid, dim3(128), 0, st, (const float*)part_ml,                \
+                     (const float*)part_o, H_q * C, n_blk, C, G, (T*)O, lse);                                     \
+  } while (0)
+  if (dtype == 0) {
+    if (d == 64) QUOKA_DEC(__nv_bfloat16, 64); else QUOKA_DEC(__nv_bfloat16, 128);
+  } else {
+    if (d == 64) QUOKA_DEC(float, 64); else QUOKA_DEC(float, 128);
+  }
+#undef QUOKA_DEC
+  if (e != cudaSuccess) return e;
+  count_launches(2);
+  return cudaGetLastError();
+}
+
+}  // namespace quoka

@@ -108,6 +108,16 @@ cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, in
 cudaError_t launch_append(int elt_bytes, int d, void* K, void* V, int64_t head_stride, int T_len, const void* Kc,
                           const void* Vc, int H_kv, int C, cudaStream_t st);
 
+// Attention for chunks of at most 32 / G queries (decode), split over the
+// keys: kept history rows read through sel ([H_kv][n_hist] positions; NULL =
+// the first n_hist rows) straight from the cache, then the causal chunk.
+// part: fp32 scratch of attend_decode_ws_bytes.
+bool attend_decode_fits(int C, int G);
+size_t attend_decode_ws_bytes(int d, int H_q, int C, int n_hist);
+cudaError_t launch_attend_decode(int dtype, int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,
+                                 const int32_t* sel, int n_hist, const void* Kc, const void* Vc, int H_q, int H_kv,
+                                 int C, float scale, void* O, float* lse, float* part, cudaStream_t st);
+
 cudaError_t launch_attend_simt(int dtype, int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,
                                int n_hist, const void* Kc, const void* Vc, int H_q, int C, int G, float scale,
                                void* O, float* lse, cudaStream_t st);

@@ -106,11 +106,17 @@ bool score_tc_fits(const quoka_shape* s, int N_q, const Params& p) {
   return N_pad <= 512 && score_tc_smem(s->d, N_pad, score_npass(s, N_pad, p), 2) <= 227 * 1024;
 }
 
+// Chunks of at most 32 / G queries (decode) attend through the split-key
+// CUDA-core kernel unless the tensor-core engine is forced.
+bool use_decode(const Params& p, const quoka_shape* s) {
+  return p.engine != QUOKA_ENGINE_TENSOR && attend_decode_fits(s->C, s->H_q / s->H_kv);
+}
+
 // Which kernels run (stage 0 = scoring, 1 = attention).  Tensor-core kernels are bf16 only.
 bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage, int N_q = 1) {
   if (p.engine == QUOKA_ENGINE_SIMT || s->dtype != QUOKA_DTYPE_BF16) return false;
   if (stage == 0) return score_tc_fits(s, N_q, p);
-  return attend_tc_smem(s->d) <= 227 * 1024;
+  return !use_decode(p, s) && attend_tc_smem(s->d) <= 227 * 1024;
 }
 
 // Workspace regions, in order; each stage only touches the prefix it needs:
@@ -118,7 +124,7 @@ bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage, int N_q 
 struct Layout {
   size_t qnorm, qpart, qcos, select_end;
   size_t op_f32, op_bf, op_scale, score_end;
-  size_t q_idx, scores, sel, ksel, vsel, total;
+  size_t q_idx, scores, sel, ksel, vsel, dec, total;
 };
 
 // Regions start at `start` (just past the header for a single call; a lane's
@@ -146,6 +152,7 @@ Layout make_layout(const quoka_shape* s, int N_q, int B, const Params& p, size_t
   L.sel = o;    o = align_up(o + H_kv * B_e * 4);
   L.ksel = o;   o = align_up(o + H_kv * B_e * d * elt_bytes(s->dtype));
   L.vsel = o;   o = align_up(o + H_kv * B_e * d * elt_bytes(s->dtype));
+  L.dec = o;    o = align_up(o + (use_decode(p, s) ? attend_decode_ws_bytes(s->d, s->H_q, s->C, s->T) : 0));
   L.total = o;
   return L;
 }
@@ -177,6 +184,9 @@ int run_select(const quoka_shape* s, const void* Q, int n, const Params& p, int3
                const Layout& L, cudaStream_t st) {
   const int G = s->H_q / s->H_kv;
   const int G_avg = p.gqa == QUOKA_GQA_MAX ? 1 : G;
+  // N_q >= C keeps every query (a decode step's one token, say): the ascending
+  // positions 0..C-1, with no cosines to compute
+  if (n >= s->C) return cuda_status(launch_topk(nullptr, s->H_q / G_avg, s->C, s->C, q_idx, st));
   return cuda_status(launch_select_queries(s->dtype, s->d, Q, s->H_q, G_avg, s->C, n, q_idx, at<float>(ws, L.qnorm),
                                            at<float>(ws, L.qpart), at<float>(ws, L.qcos), at<WsHeader>(ws, 0), st));
 }
@@ -204,9 +214,18 @@ int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, 
                                        at<float>(ws, L.op_f32), R, key_norm, scores, st));
 }
 
-int run_attend(const quoka_shape* s, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
-               const void* Kc, const void* Vc, const Params& p, void* O, float* lse, void* ws, cudaStream_t st) {
+// Attention over n_hist history rows (rows sel[g][0..n_hist) of Kh/Vh, or the
+// first n_hist when sel is NULL) plus the causal chunk.  The tensor-core and
+// prefill CUDA-core kernels take the rows contiguous (sel must be NULL); the
+// decode kernel reads them through sel and uses the scratch at ws + dec_off.
+int run_attend(const quoka_shape* s, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,
+               const int32_t* sel, int n_hist, const void* Kc, const void* Vc, const Params& p, void* O, float* lse,
+               void* ws, size_t dec_off, cudaStream_t st) {
   const int G = s->H_q / s->H_kv;
+  if (use_decode(p, s))
+    return cuda_status(launch_attend_decode(s->dtype, s->d, Q, Kh, Vh, h_stride, sel, n_hist, Kc, Vc, s->H_q,
+                                            s->H_kv, s->C, p.scale, O, lse, at<float>(ws, dec_off), st));
+  if (sel != nullptr) return QUOKA_ERR_DEVICE;   // not reached: only the decode kernel reads through sel
   const bool tc = use_tensor_cores(p, s, 1);
   if (p.engine == QUOKA_ENGINE_TENSOR && !tc) return QUOKA_ERR_UNSUPPORTED;
   if (tc)
@@ -242,7 +261,8 @@ int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const
   const int T = shape->T;
   if (T == 0 || B >= T) {   // every history key is kept: dense chunked-prefill attention
     if (sel_out != nullptr && T > 0) QUOKA_CUDA(launch_topk(nullptr, shape->H_kv, T, T, sel_out, st));
-    return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), T, K_chunk, V_chunk, p, O, lse, ws, st);
+    return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), nullptr, T, K_chunk, V_chunk, p, O, lse, ws,
+                      L.dec, st);
   }
   const int n = n_sel_of(shape, N_q);
   int32_t* q_idx = at<int32_t>(ws, L.q_idx);
@@ -251,11 +271,15 @@ int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const
   QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
   QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st));
   QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st));
+  if (use_decode(p, shape))   // the decode kernel reads the kept rows through sel: no gathered copy
+    return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), sel, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,
+                      st);
   void* ksel = at<void>(ws, L.ksel);
   void* vsel = at<void>(ws, L.vsel);
   QUOKA_CUDA(launch_gather(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), sel, shape->H_kv, B,
                            ksel, vsel, st));
-  return run_attend(shape, Q, ksel, vsel, (int64_t)B * shape->d, B, K_chunk, V_chunk, p, O, lse, ws, st);
+  return run_attend(shape, Q, ksel, vsel, (int64_t)B * shape->d, nullptr, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,
+                    st);
 }
 
 // Ragged batch: the prefix sums must start at 0, never decrease, and give
@@ -459,9 +483,11 @@ int quoka_sparse_attend(const quoka_shape* shape, const void* Q, const void* K_s
   if (!aligned16(Q) || !aligned16(K_sel) || !aligned16(V_sel) || !aligned16(K_chunk) || !aligned16(V_chunk) ||
       !aligned16(O) || !aligned16(lse))
     return QUOKA_ERR_ALIGNMENT;
-  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
-  return run_attend(shape, Q, K_sel, V_sel, (int64_t)B_e * shape->d, B_e, K_chunk, V_chunk, p, O, lse, ws,
-                    (cudaStream_t)stream);
+  // decode-size chunks need split scratch right after the header
+  const size_t dec = use_decode(p, shape) ? attend_decode_ws_bytes(shape->d, shape->H_q, shape->C, B_e) : 0;
+  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader) + dec));
+  return run_attend(shape, Q, K_sel, V_sel, (int64_t)B_e * shape->d, nullptr, B_e, K_chunk, V_chunk, p, O, lse, ws,
+                    sizeof(WsHeader), (cudaStream_t)stream);
 }
 
 int quoka_dense_attend(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
@@ -475,9 +501,10 @@ int quoka_dense_attend(const quoka_shape* shape, const void* Q, const void* K_hi
   if (!aligned16(Q) || !aligned16(K_hist) || !aligned16(V_hist) || !aligned16(K_chunk) || !aligned16(V_chunk) ||
       !aligned16(O) || !aligned16(lse))
     return QUOKA_ERR_ALIGNMENT;
-  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
-  return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), shape->T, K_chunk, V_chunk, p, O, lse, ws,
-                    (cudaStream_t)stream);
+  const size_t dec = use_decode(p, shape) ? attend_decode_ws_bytes(shape->d, shape->H_q, shape->C, shape->T) : 0;
+  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader) + dec));
+  return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), nullptr, shape->T, K_chunk, V_chunk, p, O, lse, ws,
+                    sizeof(WsHeader), (cudaStream_t)stream);
 }
 
 int quoka_chunk_attend(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,

@@ -19,24 +19,32 @@ namespace quoka {
 // Tensor-core copy of either: hi = bf16(row) in pass 0 and lo = bf16(row - hi)
 // in pass 1 (hi + lo carries the fp32 row to about 2^-16 relative).
 // Layouts: op_f32 [H_kv, R, D]; op_bf [H_kv, 2, N_pad, D].
-// One warp per scoring row.  Row r of group g is the weighted sum over its
+// One block per scoring row.  Row r of group g is the weighted sum over its
 // (head, token) pairs of the (unit) query rows:
 //   mode 1:           pairs (head k, token i), r = k * n + i, weight 1;
 //   mode 1 + qmean:   r = k, pairs (head k, every selected token), weight 1/n;
 //   mode 0:           r = i, pairs (every head of g, token i), weight 1/G;
 //   mode 0 + qmean:   r = 0, every (head, token) of g, weight 1/(G n).
+// A row of one pair is one warp's work; rows that average many pairs get a
+// block of kOpWarps warps, warp w taking pairs w, w + kOpWarps, ..., and the
+// warps' sums are added in shared memory.
+constexpr int kOpWarps = 8;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, const int32_t* __restrict__ q_idx,
-                                                      int C, int G, int n, OperandSpec spec, int R,
-                                                      float* __restrict__ op_f32, __nv_bfloat16* __restrict__ op_bf,
-                                                      float* __restrict__ op_scale) {
+__global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __restrict__ Q,
+                                                                 const int32_t* __restrict__ q_idx, int C, int G,
+                                                                 int n, OperandSpec spec, int R,
+                                                                 float* __restrict__ op_f32,
+                                                                 __nv_bfloat16* __restrict__ op_bf,
+                                                                 float* __restrict__ op_scale) {
   pdl_launch_dependents();
   pdl_wait();
   constexpr int E = D / 32;
-  const int g = blockIdx.y, r = blockIdx.x, N_pad = gridDim.x, lane = threadIdx.x;
+  const int g = blockIdx.y, r = blockIdx.x, N_pad = gridDim.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int npass = op_scale != nullptr ? 1 : 2;
   if (r >= R) {   // padding row of the tensor-core operand
-    if (op_bf != nullptr) {
+    if (op_bf != nullptr && warp == 0) {
       for (int p = 0; p < npass; ++p)
 #pragma unroll
         for (int j = 0; j < E; ++j)
@@ -57,27 +65,38 @@ __global__ void __launch_bounds__(32) k_build_operand(const T* __restrict__ Q, c
     i1 = spec.qmean ? n : r + 1;
   }
   k1 = spec.mode == 1 ? k0 + 1 : G;
+  const int ni = i1 - i0, pairs = (k1 - k0) * ni;
   float acc[E];
 #pragma unroll
   for (int j = 0; j < E; ++j) acc[j] = 0.f;
   float x[E], inv = 1.f;
-  for (int k = k0; k < k1; ++k) {
-    const int h = g * G + k;
-    const int32_t* sel_row = q_idx + (size_t)(spec.mode == 1 ? h : g) * n;
-    for (int i = i0; i < i1; ++i) {
-      const T* q = Q + ((size_t)h * C + sel_row[i]) * D;
-      float ss = 0.f;
+  for (int p = warp; p < pairs; p += nwarps) {
+    const int h = g * G + k0 + p / ni, i = i0 + p % ni;
+    const int c = q_idx[(size_t)(spec.mode == 1 ? h : g) * n + i];
+    const T* q = Q + ((size_t)h * C + c) * D;
+    float ss = 0.f;
 #pragma unroll
-      for (int j = 0; j < E; ++j) {
-        x[j] = to_f32(q[lane + 32 * j]);
-        ss = fmaf(x[j], x[j], ss);
-      }
-      inv = spec.unit ? 1.0f / fmaxf(sqrtf(warp_sum(ss)), kNormEps) : 1.f;
+    for (int j = 0; j < E; ++j) {
+      x[j] = to_f32(q[lane + 32 * j]);
+      ss = fmaf(x[j], x[j], ss);
+    }
+    inv = spec.unit ? 1.0f / fmaxf(sqrtf(warp_sum(ss)), kNormEps) : 1.f;
 #pragma unroll
-      for (int j = 0; j < E; ++j) acc[j] = fmaf(x[j], inv, acc[j]);
+    for (int j = 0; j < E; ++j) acc[j] = fmaf(x[j], inv, acc[j]);
+  }
+  if (nwarps > 1) {
+    __shared__ float part[kOpWarps][D];
+#pragma unroll
+    for (int j = 0; j < E; ++j) part[warp][lane + 32 * j] = acc[j];
+    __syncthreads();
+    if (warp != 0) return;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      float t = 0.f;
+      for (int w = 0; w < nwarps; ++w) t += part[w][lane + 32 * j];
+      acc[j] = t;
     }
   }
-  const int pairs = (k1 - k0) * (i1 - i0);
   if (pairs > 1) {
     const float w = 1.0f / (float)pairs;
 #pragma unroll
@@ -152,20 +171,23 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
   if (op_scale != nullptr && (spec.mode != 1 || spec.qmean || dtype != 0 || op_bf == nullptr))
     return cudaErrorInvalidValue;
   dim3 grid(op_bf != nullptr ? N_pad : R, H_kv);
+  // rows that average several (head, token) pairs get a block of warps, single-pair rows one warp
+  const int pairs = (spec.mode == 1 ? 1 : G) * (spec.qmean ? n : 1);
+  const dim3 block(pairs > 1 ? 32 * kOpWarps : 32);
   cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n,
+      e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, block, 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n,
                      spec, R, op_f32, op_bf, op_scale);
     else
-      e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, dim3(32), 0, st, (const __nv_bfloat16*)Q, q_idx, C, G,
+      e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, block, 0, st, (const __nv_bfloat16*)Q, q_idx, C, G,
                      n, spec, R, op_f32, op_bf, op_scale);
   } else {
     if (d == 64)
-      e = launch_pdl(k_build_operand<float, 64>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
+      e = launch_pdl(k_build_operand<float, 64>, grid, block, 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
                      op_f32, op_bf, op_scale);
     else
-      e = launch_pdl(k_build_operand<float, 128>, grid, dim3(32), 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
+      e = launch_pdl(k_build_operand<float, 128>, grid, block, 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
                      op_f32, op_bf, op_scale);
   }
   count_launches(1);

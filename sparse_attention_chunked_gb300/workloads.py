@@ -63,6 +63,9 @@ GQA_32K_BF16 = ChunkConfig("gqa32x8_d128_C2048_T32768_bf16", 32, 8, 128, 2048, 3
                            "bf16", "massive_act")
 GQA_128K_BF16 = ChunkConfig("gqa32x8_d128_C4096_T131072_bf16", 32, 8, 128, 4096, 131072, 128, 4096,
                             "bf16", "massive_act")
+# Decode: one new token per step (C = 1), so the one query is the selected set.
+DECODE_32K_BF16 = ChunkConfig("decode_gqa32x8_d128_C1_T32768_bf16", 32, 8, 128, 1, 32768, 1, 2048,
+                              "bf16", "massive_act")
 
 
 @dataclass(frozen=True)

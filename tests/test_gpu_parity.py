@@ -95,6 +95,10 @@ SMALL = [
     ("gqa5_bf16_320_rows", dict(H_q=10, H_kv=2, d=128, C=256, T=2000, N_q=64, B=300, dtype="bf16")),
     # max pooling with 576 scoring rows: wider than TMEM, the CUDA-core scorer takes it
     ("gqa8_bf16_576_rows", dict(H_q=16, H_kv=2, d=64, C=100, T=900, N_q=72, B=111, dtype="bf16")),
+    # decode-size chunks (G * C <= 32): the split-key attention, 64-key blocks with ragged tails
+    ("decode_c3_g8", dict(H_q=16, H_kv=2, d=128, C=3, T=700, N_q=2, B=100, dtype="bf16")),
+    ("decode_c8_g4_fp32_d64", dict(H_q=8, H_kv=2, d=64, C=8, T=500, N_q=4, B=64, dtype="fp32")),
+    ("decode_c1_g1", dict(H_q=3, H_kv=3, d=128, C=1, T=129, N_q=1, B=65, dtype="bf16")),
 ]
 
 
@@ -142,7 +146,7 @@ def test_tiny_mha_fp32_config(quoka, gqa):
 
 
 @pytest.mark.parametrize("gqa", ["max", "mean"])
-@pytest.mark.parametrize("cfg", [wl.GQA_32K_BF16, wl.GQA_128K_BF16], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [wl.GQA_32K_BF16, wl.GQA_128K_BF16, wl.DECODE_32K_BF16], ids=lambda c: c.name)
 def test_full_size_configs(quoka, cfg, gqa):
     x = wl.make_chunk(cfg, 0)
     r = run_stages(quoka, cfg, x, gqa)
@@ -153,6 +157,18 @@ def test_full_size_configs(quoka, cfg, gqa):
         for g, t, h, c in x.needles:
             if c in set(r["q_idx"][h].tolist()):
                 assert t in sel[g]
+
+
+@pytest.mark.parametrize("C", [1, 4])
+@pytest.mark.parametrize("T,B", [(0, 64), (300, 300), (1000, 5000)])
+def test_decode_budget_covers_history_is_dense(quoka, C, T, B):
+    """Decode-size chunks with no history or a budget covering it: dense attention, split over the keys."""
+    cfg, x = wl.small_chunk(H_q=8, H_kv=2, d=128, C=C, T=T, N_q=4, B=B, dtype="bf16")
+    Q, Kh, Vh, Kc, Vc = (t.to(DEV) for t in (x.Q, x.K_hist, x.V_hist, x.K_chunk, x.V_chunk))
+    O, lse, _ = quoka.chunk_attend(Q, Kh, Vh, Kc, Vc, cfg.N_q, B, gqa="max", with_lse=True)
+    O_ref, lse_ref = qo.dense_attend(f64(x.Q), f64(x.K_hist), f64(x.V_hist), f64(x.K_chunk), f64(x.V_chunk))
+    check_output(O, O_ref, "O")
+    assert np.max(np.abs(f64(lse) - lse_ref)) <= 1e-3
 
 
 @pytest.mark.parametrize("T,B", [(0, 64), (300, 300), (300, 5000)])

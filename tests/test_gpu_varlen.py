@@ -122,3 +122,17 @@ def test_varlen_ragged8_full_size(quoka, gqa):
         assert torch.equal(got[s]["sel"], ref["sel"]), f"sequence {s}"
         if s in (1, 6):
             check_against_oracle(quoka, x, cfg.H_q, cfg.H_kv, cfg.d, cfg.N_q, cfg.B, gqa, cfg.dtype, got[s])
+
+
+def test_varlen_decode_batch(quoka):
+    """Batched decode: twelve sequences of one new token each over histories of 1 to 3000 keys."""
+    H_q, H_kv, d, N_q, B = 8, 2, 128, 1, 64
+    Ts = [1, 63, 64, 65, 300, 1000, 3000, 7, 129, 2048, 511, 0]
+    seqs = [wl.small_chunk(H_q=H_q, H_kv=H_kv, d=d, C=1, T=T, N_q=N_q, B=B, dtype="bf16", seed=40 + i)[1]
+            for i, T in enumerate(Ts)]
+    for gqa in ("max", "mean"):
+        got = run_varlen(quoka, seqs, H_q, H_kv, d, N_q, B, gqa, "bf16")
+        for s, x in enumerate(seqs):
+            ref = single(quoka, x, N_q, B, gqa)
+            assert torch.equal(got[s]["O"], ref["O"]), f"sequence {s}"
+            check_against_oracle(quoka, x, H_q, H_kv, d, N_q, B, gqa, "bf16", got[s])
