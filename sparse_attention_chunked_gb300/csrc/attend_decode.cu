@@ -25,16 +25,41 @@ namespace {
 constexpr int kDecKeys = 64;       // keys per CTA
 constexpr int kDecThreads = 256;
 
-// 16 bytes of T (8 bf16 or 4 fp32) widened into fp32 shared memory.
-__device__ __forceinline__ void store16(float* dst, uint4 u, const float*) {
-  *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                                                __uint_as_float(u.w));
+// Eight consecutive elements of a 16-byte load as fp32 (bf16: one load;
+// fp32: the caller passes two).
+__device__ __forceinline__ void widen(uint4 u, float (&x)[8]) {
+  x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+  x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xFFFF0000u);
+  x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xFFFF0000u);
 }
-__device__ __forceinline__ void store16(float* dst, uint4 u, const __nv_bfloat16*) {
-  *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
-                                                __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-  *reinterpret_cast<float4*>(dst + 4) = make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
-                                                    __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u));
+
+// q . k over D elements: q fp32 in shared memory, k of type T in shared memory.
+template <int D>
+__device__ __forceinline__ float dot_row(const float* q, const __nv_bfloat16* k) {
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+  for (int e = 0; e < D; e += 8) {
+    float x[8];
+    widen(*reinterpret_cast<const uint4*>(k + e), x);
+    const float4 qa = *reinterpret_cast<const float4*>(q + e), qb = *reinterpret_cast<const float4*>(q + e + 4);
+    s0 = fmaf(qa.x, x[0], s0); s1 = fmaf(qa.y, x[1], s1);
+    s0 = fmaf(qa.z, x[2], s0); s1 = fmaf(qa.w, x[3], s1);
+    s0 = fmaf(qb.x, x[4], s0); s1 = fmaf(qb.y, x[5], s1);
+    s0 = fmaf(qb.z, x[6], s0); s1 = fmaf(qb.w, x[7], s1);
+  }
+  return s0 + s1;
+}
+template <int D>
+__device__ __forceinline__ float dot_row(const float* q, const float* k) {
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+  for (int e = 0; e < D; e += 4) {
+    const float4 a = *reinterpret_cast<const float4*>(k + e), qa = *reinterpret_cast<const float4*>(q + e);
+    s0 = fmaf(qa.x, a.x, s0); s1 = fmaf(qa.y, a.y, s1);
+    s0 = fmaf(qa.z, a.z, s0); s1 = fmaf(qa.w, a.w, s1);
+  }
+  return s0 + s1;
 }
 
 // Rows of a group handled by one CTA: G * C when that is at most 32.
@@ -45,12 +70,13 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
     float scale_log2, float* __restrict__ part_ml, float* __restrict__ part_o) {
   pdl_launch_dependents();
   pdl_wait();
-  constexpr int KP = D + 4;                       // padded key row (floats): conflict-free float4 reads
+  constexpr int VEC = 16 / (int)sizeof(T);        // elements per 16-byte load
+  constexpr int KP = D + VEC;                     // padded key row: conflict-free 16-byte reads across keys
   extern __shared__ __align__(16) float dsm[];
-  float* Qs = dsm;                                // [R][D]  scaled by scale * log2(e)
-  float* Ks = Qs + 32 * D;                        // [kDecKeys][KP]
-  float* Vs = Ks + kDecKeys * KP;                 // [kDecKeys][D]
-  float* Ps = Vs + kDecKeys * D;                  // [R][kDecKeys + 1]
+  float* Qs = dsm;                                // [32][D] fp32, scaled by scale * log2(e)
+  float* Ps = Qs + 32 * D;                        // [32][kDecKeys + 1]
+  T* Ks = reinterpret_cast<T*>(Ps + 32 * (kDecKeys + 1));   // [kDecKeys][KP], as stored in HBM
+  T* Vs = Ks + kDecKeys * KP;                     // [kDecKeys][D]
   const int blk = blockIdx.x, g = blockIdx.y, n_blk = gridDim.x;
   const int R = G * C;
   const int j0 = blk * kDecKeys;
@@ -64,7 +90,6 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
   }
   // the block's keys and values: kept history rows through sel, then the chunk's rows.
   // Every 16-byte load of the block is issued before the first is used.
-  constexpr int VEC = 16 / (int)sizeof(T);                   // elements per load
   constexpr int NV = D / VEC;                                // loads per row
   constexpr int PER = kDecKeys * NV / kDecThreads;           // loads per thread, per tensor
   static_assert(kDecKeys * NV % kDecThreads == 0, "whole loads per thread");
@@ -91,8 +116,8 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
     const int i = tid + u * kDecThreads, jj = i / NV, e = (i % NV) * VEC;
-    store16(Ks + jj * KP + e, kr[u], Kh);
-    store16(Vs + jj * D + e, vr[u], Vh);
+    *reinterpret_cast<uint4*>(Ks + jj * KP + e) = kr[u];
+    *reinterpret_cast<uint4*>(Vs + jj * D + e) = vr[u];
   }
   __syncthreads();
   // scores: thread -> key jj = tid % 64 against rows r = tid / 64 + 4 i
@@ -100,23 +125,10 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
     const int jj = tid % kDecKeys, r0 = tid / kDecKeys;
     const int j = j0 + jj;
     for (int r = r0; r < R; r += kDecThreads / kDecKeys) {
-      float s0 = 0.f, s1 = 0.f;
-      const float* qr = Qs + r * D;
-      const float* kr = Ks + jj * KP;
-#pragma unroll 8
-      for (int e = 0; e < D; e += 8) {
-        const float4 a = *reinterpret_cast<const float4*>(kr + e);
-        const float4 b = *reinterpret_cast<const float4*>(kr + e + 4);
-        const float4 qa = *reinterpret_cast<const float4*>(qr + e);
-        const float4 qb = *reinterpret_cast<const float4*>(qr + e + 4);
-        s0 = fmaf(qa.x, a.x, s0); s1 = fmaf(qa.y, a.y, s1);
-        s0 = fmaf(qa.z, a.z, s0); s1 = fmaf(qa.w, a.w, s1);
-        s0 = fmaf(qb.x, b.x, s0); s1 = fmaf(qb.y, b.y, s1);
-        s0 = fmaf(qb.z, b.z, s0); s1 = fmaf(qb.w, b.w, s1);
-      }
+      const float sc = dot_row<D>(Qs + r * D, Ks + jj * KP);
       // chunk key j - n_hist is visible to chunk row c iff it is not after it
       const bool ok = j < n_keys && (j < n_hist || j - n_hist <= r % C);
-      Ps[r * (kDecKeys + 1) + jj] = ok ? s0 + s1 : -INFINITY;
+      Ps[r * (kDecKeys + 1) + jj] = ok ? sc : -INFINITY;
     }
   }
   __syncthreads();
@@ -149,8 +161,8 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
       float o0 = 0.f, o1 = 0.f;
 #pragma unroll 8
       for (int jj = 0; jj < kDecKeys; jj += 2) {
-        o0 = fmaf(pr[jj], Vs[jj * D + e], o0);
-        o1 = fmaf(pr[jj + 1], Vs[(jj + 1) * D + e], o1);
+        o0 = fmaf(pr[jj], to_f32(Vs[jj * D + e]), o0);
+        o1 = fmaf(pr[jj + 1], to_f32(Vs[(jj + 1) * D + e]), o1);
       }
       part_o[(((size_t)g * R + r) * n_blk + blk) * D + e] = o0 + o1;
     }
@@ -159,7 +171,9 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
 
 // One warp per (group row): M = max_b m_b, L = sum_b l_b 2^(m_b - M),
 // O = sum_b o_b 2^(m_b - M) / L, lse = (M + log2 L) ln 2 in the units of the
-// scaled logits.
+// scaled logits.  Lane b % 32 holds block b's weight; the output sums then
+// take the weights by shuffle, with the block loads unrolled so that several
+// are in flight at once.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) k_attend_decode_merge(const float* __restrict__ part_ml,
                                                              const float* __restrict__ part_o, int n_rows, int n_blk,
@@ -173,20 +187,29 @@ __global__ void __launch_bounds__(128) k_attend_decode_merge(const float* __rest
   const float* ml = part_ml + (size_t)row * n_blk * 2;
   float M = -INFINITY;
   for (int b = lane; b < n_blk; b += 32) M = fmaxf(M, ml[2 * b]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  M = warp_max(M);
   float L = 0.f, acc[E];
 #pragma unroll
   for (int k = 0; k < E; ++k) acc[k] = 0.f;
-  for (int b = 0; b < n_blk; ++b) {
-    const float mb = ml[2 * b];
-    if (mb == -INFINITY) continue;
-    const float w = exp2f(mb - M);
-    L = fmaf(ml[2 * b + 1], w, L);
-    const float* ob = part_o + ((size_t)row * n_blk + b) * D;
+  const float* ob = part_o + (size_t)row * n_blk * D + lane;
+  for (int b0 = 0; b0 < n_blk; b0 += 32) {
+    const int b = b0 + lane;
+    float w = 0.f;
+    if (b < n_blk) {
+      const float mb = ml[2 * b];
+      w = mb == -INFINITY ? 0.f : exp2f(mb - M);
+      L = fmaf(ml[2 * b + 1], w, L);
+    }
+    const int nb = min(32, n_blk - b0);
+#pragma unroll 4
+    for (int k = 0; k < nb; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      const float* o = ob + (size_t)(b0 + k) * D;
 #pragma unroll
-    for (int k = 0; k < E; ++k) acc[k] = fmaf(ob[lane + 32 * k], w, acc[k]);
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(o[32 * e], wk, acc[e]);
+    }
   }
+  L = warp_sum(L);
   // group row -> (head, chunk row)
   const int g = row / (G * C), r = row % (G * C);
   const int h = g * G + r / C, c = r % C;
@@ -196,8 +219,9 @@ __global__ void __launch_bounds__(128) k_attend_decode_merge(const float* __rest
   if (lse != nullptr && lane == 0) lse[(size_t)h * C + c] = (M + log2f(L)) * 0.69314718055994531f;
 }
 
-size_t decode_smem(int d, int R) {
-  return ((size_t)32 * d + (size_t)kDecKeys * (d + 4) + (size_t)kDecKeys * d + (size_t)R * (kDecKeys + 1)) * 4;
+size_t decode_smem(int d, int elt) {
+  const int vec = 16 / elt;
+  return ((size_t)32 * d + (size_t)32 * (kDecKeys + 1)) * 4 + ((size_t)kDecKeys * (d + vec) + (size_t)kDecKeys * d) * elt;
 }
 
 }  // namespace
@@ -212,13 +236,13 @@ size_t attend_decode_ws_bytes(int d, int H_q, int C, int n_hist) {
 cudaError_t launch_attend_decode(int dtype, int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,
                                  const int32_t* sel, int n_hist, const void* Kc, const void* Vc, int H_q, int H_kv,
                                  int C, float scale, void* O, float* lse, float* part, cudaStream_t st) {
-  const int G = H_q / H_kv, R = G * C;
+  const int G = H_q / H_kv;
   if (!attend_decode_fits(C, G)) return cudaErrorInvalidValue;
   const int n_blk = (n_hist + C + kDecKeys - 1) / kDecKeys;
   float* part_ml = part;
   float* part_o = part + (size_t)H_q * C * n_blk * 2;
   const float scale_log2 = scale * 1.4426950408889634f;
-  const size_t smem = decode_smem(d, R);
+  const size_t smem = decode_smem(d, dtype == 0 ? 2 : 4);
   const dim3 grid(n_blk, H_kv), mgrid((H_q * C + 3) / 4);
   cudaError_t e;
 #define QUOKA_DEC(T, DD)                                                                                          \
