@@ -233,9 +233,23 @@ def run_quoka(args, rank, world, local_rank):
     sets = [(Q, Kh, Vh, Kc, Vc)] + [tuple(t.clone() for t in (Q, Kh, Vh, Kc, Vc)) for _ in range(INPUT_SETS - 1)]
     set_bytes = sum(t.numel() * t.element_size() for t in sets[0])
 
+    # the key-norm cache of every input set, as quoka_append_kv_norms would have left it when the
+    # history was appended (built once, outside the timed region)
+    inv_sets = {}
+    if args.key_norm_cache:
+        for xs in sets:
+            inv = torch.empty((cfg.H_kv, cfg.T), dtype=torch.float32, device=dev)
+            q.quoka_key_inv_norms(shape, xs[1], 0, cfg.T, inv, stream)
+            inv_sets[id(xs[1])] = inv
+        torch.cuda.synchronize(dev)
+
     def step_fns(Qx, Khx, Vhx, Kcx, Vcx):
         # the step: one quoka_chunk_attend (every stage of the path; top-B and the
         # gather share one launch there)
+        if args.key_norm_cache:
+            inv = inv_sets[id(Khx)]
+            return [lambda: q.quoka_chunk_attend_cached(shape, Qx, Khx, Vhx, Kcx, Vcx, inv, cfg.N_q, cfg.B, params, O,
+                                                        None, None, ws, stream)]
         return [lambda: q.quoka_chunk_attend(shape, Qx, Khx, Vhx, Kcx, Vcx, cfg.N_q, cfg.B, params, O, None, None, ws,
                                              stream)]
 
@@ -353,7 +367,11 @@ def run_quoka(args, rank, world, local_rank):
         Qd.copy_(Qh, non_blocking=True)
         Kcd.copy_(Kch, non_blocking=True)
         Vcd.copy_(Vch, non_blocking=True)
-        q.quoka_chunk_attend(shape, Qd, Kh, Vh, Kcd, Vcd, cfg.N_q, cfg.B, params, Od2, None, None, ws, stream)
+        if args.key_norm_cache:
+            q.quoka_chunk_attend_cached(shape, Qd, Kh, Vh, Kcd, Vcd, inv_sets[id(Kh)], cfg.N_q, cfg.B, params, Od2,
+                                        None, None, ws, stream)
+        else:
+            q.quoka_chunk_attend(shape, Qd, Kh, Vh, Kcd, Vcd, cfg.N_q, cfg.B, params, Od2, None, None, ws, stream)
         Oh.copy_(Od2, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -669,8 +687,10 @@ def _oracle_inputs(x, g, G):
 
 
 def variant_keys(args) -> dict:
-    """The key-score ablation in force, named in the config only when one is."""
+    """The key-score ablation and the key-norm cache, named in the config only when in force."""
     out = {}
+    if getattr(args, "key_norm_cache", False):
+        out["key_norm_cache"] = True
     if args.score_fn != "cos":
         out["score_fn"] = args.score_fn
     if args.query_agg != "max":
@@ -791,6 +811,8 @@ def main(argv=None):
                     help="key score: cosine (the method) or the dot-product ablation")
     ap.add_argument("--query-agg", choices=["max", "mean"], default="max",
                     help="aggregation over the selected queries: max (the method) or the mean ablation")
+    ap.add_argument("--key-norm-cache", action="store_true",
+                    help="score with the history's key norms from the cache written at append time")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")

@@ -170,6 +170,22 @@ int quoka_score_keys(const quoka_shape* shape, const void* Q, const int32_t* q_i
                      const void* K_hist, const quoka_params* params, float* scores,
                      void* ws, size_t ws_bytes, void* stream);
 
+/* Key-norm cache ([P1] "Chunked Prefill with QUOKA": the keys enter the cache
+ * once and are scored by every later chunk, so their norms can be stored when
+ * they are written).  k_inv_norm[g * norm_head_stride + t] =
+ * 1 / max(|K_hist[g, t]|, 1e-12) in fp32 for t in [t0, t1), t1 <= T.
+ * k_inv_norm: device fp32, 4-byte aligned, norm_head_stride >= t1. */
+int quoka_key_inv_norms(const quoka_shape* shape, const void* K_hist, int t0, int t1, float* k_inv_norm,
+                        int64_t norm_head_stride, void* stream);
+
+/* quoka_score_keys with the key norms taken from the cache (norm_head_stride
+ * >= T) instead of recomputed from the keys; the cache must hold the norms of
+ * exactly these keys (quoka_key_inv_norms / quoka_append_kv_norms).  Scores
+ * agree with quoka_score_keys to fp32 rounding of the norms. */
+int quoka_score_keys_cached(const quoka_shape* shape, const void* Q, const int32_t* q_idx, int N_q,
+                            const void* K_hist, const float* k_inv_norm, int64_t norm_head_stride,
+                            const quoka_params* params, float* scores, void* ws, size_t ws_bytes, void* stream);
+
 /* Top-B history keys per KV head ([P2] "From scores to a smaller KV set").
  * Reads scores fp32 [H_kv, T] (shape->H_kv, shape->T); writes sel int32
  * [H_kv, B_e], B_e = min(B, T), the positions of the B_e largest scores in
@@ -251,6 +267,13 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
                               const void* V_chunk, int N_q, int B, const quoka_params* params, void* O, float* lse,
                               int32_t* sel_out, void* ws, size_t ws_bytes, void* stream);
 
+/* quoka_chunk_attend with the history's key norms from the cache (as
+ * quoka_score_keys_cached). */
+int quoka_chunk_attend_cached(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
+                              const void* K_chunk, const void* V_chunk, const float* k_inv_norm,
+                              int64_t norm_head_stride, int N_q, int B, const quoka_params* params, void* O,
+                              float* lse, int32_t* sel_out, void* ws, size_t ws_bytes, void* stream);
+
 /* Dense chunked-prefill attention over every history key plus the causal
  * chunk ([P1] "Chunked prefill"): the reference QUOKA is measured against.
  * Arguments as quoka_chunk_attend without the selection; ws as for
@@ -264,6 +287,12 @@ int quoka_dense_attend(const quoka_shape* shape, const void* Q, const void* K_hi
  * likewise V, for c < C.  Requires kv_head_stride >= (T + C) * d. */
 int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const void* K_chunk,
                     const void* V_chunk, void* stream);
+
+/* quoka_append_kv, and the appended keys' entries of the key-norm cache:
+ * k_inv_norm[g * norm_head_stride + T + c] = 1 / max(|K_chunk[g, c]|, 1e-12)
+ * for c < C (norm_head_stride >= T + C). */
+int quoka_append_kv_norms(const quoka_shape* shape, void* K_hist, void* V_hist, const void* K_chunk,
+                          const void* V_chunk, float* k_inv_norm, int64_t norm_head_stride, void* stream);
 
 /* Which kernel family a stage runs for this shape and params:
  * QUOKA_ENGINE_TENSOR (tcgen05 tensor cores) or QUOKA_ENGINE_SIMT (CUDA

@@ -47,6 +47,33 @@ __global__ void k_append_rows(uint4* __restrict__ K, uint4* __restrict__ V, int6
   }
 }
 
+// Key-norm cache: inv[g * inv_stride + t] = 1 / max(|K[g, t]|, eps) for
+// t in [t0, t1).  One warp per key row; the squared norm is summed in fp32
+// over the row's bf16 or fp32 elements.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) k_key_inv_norms(const T* __restrict__ K, int64_t head_stride, int t0, int t1,
+                                                       int H_kv, float* __restrict__ inv, int64_t inv_stride) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int E = D / 32;
+  const int n = t1 - t0;
+  const size_t rows = (size_t)H_kv * n;
+  const int lane = threadIdx.x & 31;
+  for (size_t w = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; w < rows;
+       w += ((size_t)gridDim.x * blockDim.x) >> 5) {
+    const int g = (int)(w / n), t = t0 + (int)(w % n);
+    const T* k = K + (size_t)g * head_stride + (size_t)t * D;
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const float x = to_f32(k[lane + 32 * j]);
+      ss = fmaf(x, x, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) inv[(size_t)g * inv_stride + t] = 1.0f / fmaxf(sqrtf(ss), kNormEps);
+  }
+}
+
 static int grid_for(size_t work) {
   size_t b = (work + 255) / 256;
   return (int)(b < 152 * 16 ? (b == 0 ? 1 : b) : 152 * 16);
@@ -69,6 +96,30 @@ cudaError_t launch_append(int elt_bytes, int d, void* K, void* V, int64_t head_s
   const int64_t hsv = head_stride * elt_bytes / 16;
   cudaError_t e = launch_pdl(k_append_rows, dim3(grid_for((size_t)2 * H_kv * C * vpr)), dim3(256), 0, st, (uint4*)K,
                              (uint4*)V, hsv, T_len, (const uint4*)Kc, (const uint4*)Vc, H_kv, C, vpr);
+  count_launches(1);
+  return e;
+}
+
+cudaError_t launch_key_inv_norms(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int t0, int t1,
+                                 float* inv, int64_t inv_stride, cudaStream_t st) {
+  if (t1 <= t0) return cudaSuccess;
+  const dim3 grid(grid_for((size_t)H_kv * (t1 - t0) * 32));
+  cudaError_t e;
+  if (dtype == 0) {
+    if (d == 64)
+      e = launch_pdl(k_key_inv_norms<__nv_bfloat16, 64>, grid, dim3(256), 0, st, (const __nv_bfloat16*)K, head_stride,
+                     t0, t1, H_kv, inv, inv_stride);
+    else
+      e = launch_pdl(k_key_inv_norms<__nv_bfloat16, 128>, grid, dim3(256), 0, st, (const __nv_bfloat16*)K,
+                     head_stride, t0, t1, H_kv, inv, inv_stride);
+  } else {
+    if (d == 64)
+      e = launch_pdl(k_key_inv_norms<float, 64>, grid, dim3(256), 0, st, (const float*)K, head_stride, t0, t1, H_kv,
+                     inv, inv_stride);
+    else
+      e = launch_pdl(k_key_inv_norms<float, 128>, grid, dim3(256), 0, st, (const float*)K, head_stride, t0, t1, H_kv,
+                     inv, inv_stride);
+  }
   count_launches(1);
   return e;
 }

@@ -69,9 +69,18 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
                                  int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
                                  float* op_scale, cudaStream_t st);
 
-// score[g, t] = max_r (r . k_t) * (key_norm ? 1 / max(|k_t|, eps) : 1).
+// How a key's score is scaled: key_norm false: 1 (dot product); else
+// 1 / max(|k_t|, eps), read from k_inv[g * k_inv_stride + t] when k_inv is
+// given (the key-norm cache), else computed from the key.
+struct KeyScale {
+  bool key_norm;
+  const float* k_inv;
+  int64_t k_inv_stride;
+};
+
+// score[g, t] = max_r (r . k_t) * scale(t).
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
-                              const float* op_f32, int R, bool key_norm, float* scores, cudaStream_t st);
+                              const float* op_f32, int R, KeyScale ks, float* scores, cudaStream_t st);
 
 // Tensor-core scoring (bf16 keys).  op_bf / op_scale as written by
 // launch_build_operand with N_pad = score_tc_pad_rows(R); npass = 1 when
@@ -80,7 +89,7 @@ int score_tc_pad_rows(int R);
 size_t score_tc_smem(int d, int N_pad, int npass, int nst);
 struct WsHeader;
 cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
-                            const float* op_scale, int R, bool key_norm, float* scores, WsHeader* hdr, int num_sms,
+                            const float* op_scale, int R, KeyScale ks, float* scores, WsHeader* hdr, int num_sms,
                             cudaStream_t st);
 
 // Raises `func`'s dynamic shared-memory limit to `bytes` on the current device (cached).
@@ -104,6 +113,10 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
 
 cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, int64_t head_stride, const int32_t* sel,
                           int H_kv, int B_e, void* Ks, void* Vs, cudaStream_t st);
+
+// inv[g * inv_stride + t] = 1 / max(|K[g, t]|, eps), t in [t0, t1).
+cudaError_t launch_key_inv_norms(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int t0, int t1,
+                                 float* inv, int64_t inv_stride, cudaStream_t st);
 
 cudaError_t launch_append(int elt_bytes, int d, void* K, void* V, int64_t head_stride, int T_len, const void* Kc,
                           const void* Vc, int H_kv, int C, cudaStream_t st);

@@ -191,8 +191,15 @@ int run_select(const quoka_shape* s, const void* Q, int n, const Params& p, int3
                                            at<float>(ws, L.qpart), at<float>(ws, L.qcos), at<WsHeader>(ws, 0), st));
 }
 
+// An optional cache of 1 / max(|k_t|, eps) for the history keys ([H_kv] rows
+// `stride` apart), written when the keys were appended.
+struct KeyCache {
+  const float* inv = nullptr;
+  int64_t stride = 0;
+};
+
 int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, const void* K_hist,
-              const Params& p, float* scores, void* ws, const Layout& L, cudaStream_t st) {
+              const Params& p, float* scores, void* ws, const Layout& L, cudaStream_t st, KeyCache kc = KeyCache()) {
   const int G = s->H_q / s->H_kv;
   OperandSpec os;
   os.mode = p.gqa == QUOKA_GQA_MAX ? 1 : 0;
@@ -206,12 +213,12 @@ int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, 
   QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, os, N_pad,
                                   tc ? nullptr : at<float>(ws, L.op_f32), tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr,
                                   op_scale, st));
-  const bool key_norm = !p.dot;
+  const KeyScale ks{!p.dot, kc.inv, kc.stride};
   if (tc)
     return cuda_status(launch_score_tc(s->d, K_hist, head_stride(s), s->H_kv, s->T, at<__nv_bfloat16>(ws, L.op_bf),
-                                       op_scale, R, key_norm, scores, at<WsHeader>(ws, 0), num_sms(), st));
+                                       op_scale, R, ks, scores, at<WsHeader>(ws, 0), num_sms(), st));
   return cuda_status(launch_score_simt(s->dtype, s->d, K_hist, head_stride(s), s->H_kv, s->T,
-                                       at<float>(ws, L.op_f32), R, key_norm, scores, st));
+                                       at<float>(ws, L.op_f32), R, ks, scores, st));
 }
 
 // Attention over n_hist history rows (rows sel[g][0..n_hist) of Kh/Vh, or the
@@ -237,6 +244,15 @@ int run_attend(const quoka_shape* s, const void* Q, const void* Kh, const void* 
 
 bool aligned4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
 
+// The key-norm cache: a 4-byte aligned fp32 array with rows of at least
+// `len` entries, one row per KV head.
+int check_norm_cache(const quoka_shape* s, const float* inv, int64_t stride, int64_t len) {
+  if (inv == nullptr || stride < len || stride < 1) return QUOKA_ERR_INVALID_ARG;
+  if (((uintptr_t)inv & 3u) != 0) return QUOKA_ERR_ALIGNMENT;
+  (void)s;
+  return QUOKA_OK;
+}
+
 // Pointer checks shared by quoka_chunk_attend and each sequence of the ragged
 // entry point.  lse and sel_out are written one element at a time and need
 // only 4-byte alignment.
@@ -257,7 +273,7 @@ int check_chunk_args(const quoka_shape* shape, const void* Q, const void* K_hist
 // whole history instead.
 int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist, const void* K_chunk,
               const void* V_chunk, int N_q, int B, const Params& p, void* O, float* lse, int32_t* sel_out, void* ws,
-              const Layout& L, cudaStream_t st) {
+              const Layout& L, cudaStream_t st, KeyCache kc = KeyCache()) {
   const int T = shape->T;
   if (T == 0 || B >= T) {   // every history key is kept: dense chunked-prefill attention
     if (sel_out != nullptr && T > 0) QUOKA_CUDA(launch_topk(nullptr, shape->H_kv, T, T, sel_out, st));
@@ -269,7 +285,7 @@ int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const
   float* scores = at<float>(ws, L.scores);
   int32_t* sel = sel_out != nullptr ? sel_out : at<int32_t>(ws, L.sel);
   QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
-  QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st));
+  QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st, kc));
   QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st));
   if (use_decode(p, shape))   // the decode kernel reads the kept rows through sel: no gathered copy
     return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), sel, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,
@@ -450,6 +466,35 @@ int quoka_score_keys(const quoka_shape* shape, const void* Q, const int32_t* q_i
   return run_score(shape, Q, q_idx, n_sel_of(shape, N_q), K_hist, p, scores, ws, L, (cudaStream_t)stream);
 }
 
+int quoka_score_keys_cached(const quoka_shape* shape, const void* Q, const int32_t* q_idx, int N_q,
+                            const void* K_hist, const float* k_inv_norm, int64_t norm_head_stride,
+                            const quoka_params* params, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  QUOKA_TRY(check_norm_cache(shape, k_inv_norm, norm_head_stride, shape->T));
+  if (N_q < 1 || Q == nullptr || q_idx == nullptr || K_hist == nullptr || scores == nullptr)
+    return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(q_idx) || !aligned16(K_hist) || !aligned16(scores)) return QUOKA_ERR_ALIGNMENT;
+  const Layout L = make_layout(shape, N_q, 1, p);
+  QUOKA_TRY(check_ws(ws, ws_bytes, L.score_end));
+  if (shape->T == 0) return QUOKA_OK;
+  KeyCache kc;
+  kc.inv = k_inv_norm;
+  kc.stride = norm_head_stride;
+  return run_score(shape, Q, q_idx, n_sel_of(shape, N_q), K_hist, p, scores, ws, L, (cudaStream_t)stream, kc);
+}
+
+int quoka_key_inv_norms(const quoka_shape* shape, const void* K_hist, int t0, int t1, float* k_inv_norm,
+                        int64_t norm_head_stride, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  if (K_hist == nullptr || t0 < 0 || t1 < t0 || t1 > shape->T) return QUOKA_ERR_INVALID_ARG;
+  QUOKA_TRY(check_norm_cache(shape, k_inv_norm, norm_head_stride, t1));
+  if (!aligned16(K_hist)) return QUOKA_ERR_ALIGNMENT;
+  return cuda_status(launch_key_inv_norms(shape->dtype, shape->d, K_hist, head_stride(shape), shape->H_kv, t0, t1,
+                                          k_inv_norm, norm_head_stride, (cudaStream_t)stream));
+}
+
 int quoka_topk(const quoka_shape* shape, const float* scores, int B, int32_t* sel, void* ws, size_t ws_bytes,
                void* stream) {
   QUOKA_TRY(check_shape(shape));
@@ -518,6 +563,24 @@ int quoka_chunk_attend(const quoka_shape* shape, const void* Q, const void* K_hi
   QUOKA_TRY(check_ws(ws, ws_bytes, L.total));
   return run_chunk(shape, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, p, O, lse, sel_out, ws, L,
                    (cudaStream_t)stream);
+}
+
+int quoka_chunk_attend_cached(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist,
+                              const void* K_chunk, const void* V_chunk, const float* k_inv_norm,
+                              int64_t norm_head_stride, int N_q, int B, const quoka_params* params, void* O,
+                              float* lse, int32_t* sel_out, void* ws, size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  QUOKA_TRY(check_chunk_args(shape, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, O, lse, sel_out));
+  QUOKA_TRY(check_norm_cache(shape, k_inv_norm, norm_head_stride, shape->T));
+  const Layout L = make_layout(shape, N_q, B, p);
+  QUOKA_TRY(check_ws(ws, ws_bytes, L.total));
+  KeyCache kc;
+  kc.inv = k_inv_norm;
+  kc.stride = norm_head_stride;
+  return run_chunk(shape, Q, K_hist, V_hist, K_chunk, V_chunk, N_q, B, p, O, lse, sel_out, ws, L,
+                   (cudaStream_t)stream, kc);
 }
 
 int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
@@ -628,6 +691,16 @@ int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const 
     return QUOKA_ERR_ALIGNMENT;
   return cuda_status(launch_append(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), shape->T,
                                    K_chunk, V_chunk, shape->H_kv, shape->C, (cudaStream_t)stream));
+}
+
+int quoka_append_kv_norms(const quoka_shape* shape, void* K_hist, void* V_hist, const void* K_chunk,
+                          const void* V_chunk, float* k_inv_norm, int64_t norm_head_stride, void* stream) {
+  QUOKA_TRY(check_norm_cache(shape, k_inv_norm, norm_head_stride, shape->T + shape->C));
+  QUOKA_TRY(quoka_append_kv(shape, K_hist, V_hist, K_chunk, V_chunk, stream));
+  // the appended keys' norms, from the chunk's own rows (the same values)
+  return cuda_status(launch_key_inv_norms(shape->dtype, shape->d, K_chunk, (int64_t)shape->C * shape->d,
+                                          shape->H_kv, 0, shape->C, k_inv_norm + shape->T, norm_head_stride,
+                                          (cudaStream_t)stream));
 }
 
 int quoka_selftest_expire_wait(void* ws, size_t ws_bytes, long long cycles, void* stream) {

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
 // stream through shared memory 32 at a time; score = max_r(r . k) / |k|.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int64_t head_stride, int T_len,
-                                                    const float* __restrict__ op_f32, int R, bool key_norm,
+                                                    const float* __restrict__ op_f32, int R, KeyScale ks,
                                                     float* __restrict__ scores) {
   pdl_launch_dependents();
   pdl_wait();
@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
 #pragma unroll
     for (int e = 0; e < D; ++e) k[e] = 0.f;
   }
-  const float rk = key_norm ? 1.0f / fmaxf(sqrtf(ss), kNormEps) : 1.0f;
+  const float rk = !ks.key_norm ? 1.0f
+                  : ks.k_inv != nullptr ? (t < T_len ? ks.k_inv[(size_t)g * ks.k_inv_stride + t] : 0.f)
+                                        : 1.0f / fmaxf(sqrtf(ss), kNormEps);
   float best = -INFINITY;
   const float* opg = op_f32 + (size_t)g * R * D;
   for (int r0 = 0; r0 < R; r0 += 32) {
@@ -195,20 +197,20 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
 }
 
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
-                              const float* op_f32, int R, bool key_norm, float* scores, cudaStream_t st) {
+                              const float* op_f32, int R, KeyScale ks, float* scores, cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
   dim3 grid((T_len + 127) / 128, H_kv);
   cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, key_norm, scores);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores);
     else
-      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, key_norm, scores);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores);
   } else {
     if (d == 64)
-      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, key_norm, scores);
+      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores);
     else
-      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, key_norm, scores);
+      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores);
   }
   count_launches(1);
   return e;

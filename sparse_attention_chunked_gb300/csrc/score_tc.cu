@@ -128,7 +128,7 @@ template <int D, bool SCALED>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     k_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
                const float* __restrict__ op_scale, int T_len, int R, int N_pad, int nst, int cw,
-               uint32_t tmem_cols, bool key_norm, float* __restrict__ scores, WsHeader* hdr) {
+               uint32_t tmem_cols, KeyScale ks, float* __restrict__ scores, WsHeader* hdr) {
   constexpr int HALVES = D / 64;
   constexpr int NPASS = SCALED ? 1 : 2;
   constexpr uint32_t kHalfBytes = kTileKeys * 128;            // one 64-column half of a key tile
@@ -256,8 +256,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     for (int it = 0; it < ntiles; ++it) {
       const int s = it % nst;
       if (alive) alive = warp_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105);
-      float ss = 0.f;
-      if (alive && key_norm) {
+      float ss = 0.f, rk = 1.f;
+      const int t = (tile0 + it) * kTileKeys + row;
+      if (ks.key_norm && ks.k_inv != nullptr && half == 0)   // the key-norm cache: one load, issued early
+        rk = t < T_len ? ks.k_inv[(size_t)g * ks.k_inv_stride + t] : 0.f;
+      if (alive && ks.key_norm && ks.k_inv == nullptr) {
         // this half's share of |k|^2 (16-byte chunks; chunk c of row r sits at c ^ (r & 7))
         const uint8_t* rp = ktiles + (size_t)s * kStageBytes + (row >> 3) * 1024 + (row & 7) * 128;
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
@@ -311,8 +314,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (half == 0) {
         m = fmaxf(m, sm->part_max[buf][quad][lane]);
         ss += sm->part_ss[buf][quad][lane];
-        const int t = (tile0 + it) * kTileKeys + row;
-        const float rk = key_norm ? 1.0f / fmaxf(sqrtf(ss), kNormEps) : 1.0f;
+        if (ks.key_norm && ks.k_inv == nullptr) rk = 1.0f / fmaxf(sqrtf(ss), kNormEps);
         if (alive && t < T_len) scores[(size_t)g * T_len + t] = m * rk;
       }
     }
@@ -328,11 +330,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 template <int D, bool SCALED>
 cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t st, const CUtensorMap& kmap, const CUtensorMap& omap,
                        const float* op_scale, int T_len, int R, int N_pad, int nst, int cw, uint32_t cols,
-                       bool key_norm, float* scores, WsHeader* hdr) {
+                       KeyScale ks, float* scores, WsHeader* hdr) {
   cudaError_t e = ensure_smem((const void*)k_score_tc<D, SCALED>, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_score_tc<D, SCALED>, grid, dim3(kScoreThreads), smem, st, kmap, omap, op_scale, T_len, R, N_pad,
-                    nst, cw, cols, key_norm, scores, hdr);
+                    nst, cw, cols, ks, scores, hdr);
 }
 
 }  // namespace
@@ -347,7 +349,7 @@ size_t score_tc_smem(int d, int N_pad, int npass, int nst) {
 }
 
 cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
-                            const float* op_scale, int R, bool key_norm, float* scores, WsHeader* hdr,
+                            const float* op_scale, int R, KeyScale ks, float* scores, WsHeader* hdr,
                             int num_sms, cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
   const int N_pad = score_tc_pad_rows(R);
@@ -373,11 +375,11 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
   if (per_head > tiles_head) per_head = tiles_head;
   dim3 grid(per_head, H_kv);
   if (d == 64)
-    e = npass == 1 ? launch_one<64, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, key_norm, scores, hdr)
-                   : launch_one<64, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, key_norm, scores, hdr);
+    e = npass == 1 ? launch_one<64, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hdr)
+                   : launch_one<64, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hdr);
   else
-    e = npass == 1 ? launch_one<128, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, key_norm, scores, hdr)
-                   : launch_one<128, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, key_norm, scores, hdr);
+    e = npass == 1 ? launch_one<128, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hdr)
+                   : launch_one<128, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hdr);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();

@@ -71,6 +71,14 @@ _SIG = {
     "quoka_chunk_attend_varlen": (ctypes.c_int, [ctypes.POINTER(VarlenShape), _I64P, _I64P, _P, _P, _P, _P, _P,
                                                  ctypes.c_int, ctypes.c_int, ctypes.POINTER(Params), _P, _P, _P, _P,
                                                  ctypes.c_size_t, _P]),
+    "quoka_key_inv_norms": (ctypes.c_int, [ctypes.POINTER(Shape), _P, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int64,
+                                           _P]),
+    "quoka_score_keys_cached": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, ctypes.c_int, _P, _P, ctypes.c_int64,
+                                               ctypes.POINTER(Params), _P, _P, ctypes.c_size_t, _P]),
+    "quoka_chunk_attend_cached": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, ctypes.c_int64,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.POINTER(Params), _P, _P, _P, _P,
+                                                 ctypes.c_size_t, _P]),
+    "quoka_append_kv_norms": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, ctypes.c_int64, _P]),
     "quoka_dense_attend": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, ctypes.POINTER(Params), _P, _P,
                                           _P, ctypes.c_size_t, _P]),
     "quoka_append_kv": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
@@ -233,6 +241,32 @@ def quoka_dense_attend(shape, Q, K_hist, V_hist, K_chunk, V_chunk, params, O, ls
     _check("quoka_dense_attend", load().quoka_dense_attend(
         ctypes.byref(shape), _ptr(Q), _ptr(K_hist), _ptr(V_hist), _ptr(K_chunk), _ptr(V_chunk), ctypes.byref(params),
         _ptr(O), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def quoka_key_inv_norms(shape, K_hist, t0, t1, k_inv_norm, stream=None):
+    """k_inv_norm: fp32 [H_kv, >= t1] (its row stride is the cache's head stride)."""
+    _check("quoka_key_inv_norms", load().quoka_key_inv_norms(
+        ctypes.byref(shape), _ptr(K_hist), t0, t1, _ptr(k_inv_norm), k_inv_norm.stride(0), _stream(stream)))
+
+
+def quoka_score_keys_cached(shape, Q, q_idx, N_q, K_hist, k_inv_norm, params, scores, ws, stream=None):
+    _check("quoka_score_keys_cached", load().quoka_score_keys_cached(
+        ctypes.byref(shape), _ptr(Q), _ptr(q_idx), N_q, _ptr(K_hist), _ptr(k_inv_norm), k_inv_norm.stride(0),
+        ctypes.byref(params), _ptr(scores), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def quoka_chunk_attend_cached(shape, Q, K_hist, V_hist, K_chunk, V_chunk, k_inv_norm, N_q, B, params, O, lse,
+                              sel_out, ws, stream=None):
+    _check("quoka_chunk_attend_cached", load().quoka_chunk_attend_cached(
+        ctypes.byref(shape), _ptr(Q), _ptr(K_hist), _ptr(V_hist), _ptr(K_chunk), _ptr(V_chunk), _ptr(k_inv_norm),
+        k_inv_norm.stride(0), N_q, B, ctypes.byref(params), _ptr(O), _ptr(lse), _ptr(sel_out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def quoka_append_kv_norms(shape, K_hist, V_hist, K_chunk, V_chunk, k_inv_norm, stream=None):
+    _check("quoka_append_kv_norms", load().quoka_append_kv_norms(
+        ctypes.byref(shape), _ptr(K_hist), _ptr(V_hist), _ptr(K_chunk), _ptr(V_chunk), _ptr(k_inv_norm),
+        k_inv_norm.stride(0), _stream(stream)))
 
 
 def quoka_append_kv(shape, K_hist, V_hist, K_chunk, V_chunk, stream=None):

@@ -197,3 +197,23 @@ def test_varlen_alignment_of_packed_offsets(quoka):
         ctypes.byref(vs), q._cu(cu_T), q._cu(cu_C), *([ctypes.c_void_p(FAKE)] * 5), 16, 64,
         ctypes.byref(q.params_of("max")), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4), None, None, 0, None)
     assert rc == 3, q.status_string(rc)   # offsets fine; fails on the missing workspace
+
+
+def test_key_norm_cache_argument_errors(quoka):
+    q = quoka
+    lib = q.load()
+    s = _shape(q)                       # T = 1000
+    P = ctypes.c_void_p
+    assert lib.quoka_key_inv_norms(ctypes.byref(s), P(FAKE), 0, 1001, P(FAKE), 2000, None) == 1    # t1 > T
+    assert lib.quoka_key_inv_norms(ctypes.byref(s), P(FAKE), 5, 4, P(FAKE), 2000, None) == 1       # t1 < t0
+    assert lib.quoka_key_inv_norms(ctypes.byref(s), P(FAKE), 0, 1000, P(FAKE), 999, None) == 1     # row too short
+    assert lib.quoka_key_inv_norms(ctypes.byref(s), P(FAKE), 0, 1000, None, 2000, None) == 1        # no cache
+    assert lib.quoka_key_inv_norms(ctypes.byref(s), P(FAKE), 0, 1000, P(FAKE + 2), 2000, None) == 4 # misaligned
+    p = q.params_of("max")
+    assert lib.quoka_chunk_attend_cached(ctypes.byref(s), *([P(FAKE)] * 5), P(FAKE), 999, 4, 16, ctypes.byref(p),
+                                         P(FAKE), None, None, P(FAKE), 1 << 30, None) == 1         # stride < T
+    assert lib.quoka_score_keys_cached(ctypes.byref(s), P(FAKE), P(FAKE), 4, P(FAKE), None, 1000, ctypes.byref(p),
+                                       P(FAKE), P(FAKE), 1 << 30, None) == 1
+    # appending C = 128 keys needs room for T + C norms per row
+    assert lib.quoka_append_kv_norms(ctypes.byref(_shape(q, kv_head_stride=2000 * 128)), *([P(FAKE)] * 4), P(FAKE),
+                                     1100, None) == 1
