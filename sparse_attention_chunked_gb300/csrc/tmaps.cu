@@ -40,7 +40,9 @@ cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, u
 // Raises a kernel's dynamic shared-memory limit on the current device, once
 // per (kernel, device) unless a larger size is asked for later.
 cudaError_t ensure_smem(const void* func, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
+  // The 48 KB default covers static plus dynamic shared memory, so a kernel
+  // with static shared memory needs the opt-in below 48 KB of dynamic too.
+  if (bytes == 0) return cudaSuccess;
   struct Entry {
     const void* func;
     int dev;

@@ -329,7 +329,7 @@ def test_ragged_batch(quoka, gqa):
             check_stages(sub, x, gqa, r)
 
 
-@pytest.mark.parametrize("T,B", [(400_000, 5000), (70_000, 4096), (9, 8)])
+@pytest.mark.parametrize("T,B", [(400_000, 5000), (90_000, 3000), (70_000, 4096), (12_288, 2048), (9, 8)])
 def test_topk_sizes_and_slices(quoka, T, B):
     """Slices that do and do not fit in shared memory, and tiny rows, with frequent exact ties."""
     H_kv = 2
