@@ -83,16 +83,26 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
   const int n_keys = n_hist + C;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  for (int i = tid; i < R * D; i += kDecThreads) {
-    const int r = i / D, e = i % D;
-    const int h = g * G + r / C, c = r % C;
-    Qs[i] = to_f32(Q[((size_t)h * C + c) * D + e]) * scale_log2;
-  }
-  // the block's keys and values: kept history rows through sel, then the chunk's rows.
-  // Every 16-byte load of the block is issued before the first is used.
+  // The block's keys and values: kept history rows through sel, then the
+  // chunk's rows.  The kept positions are fetched first, the query rows while
+  // they are in flight, then every 16-byte K/V load of the block is issued
+  // before the first is used: two dependent memory latencies in all.
   constexpr int NV = D / VEC;                                // loads per row
   constexpr int PER = kDecKeys * NV / kDecThreads;           // loads per thread, per tensor
   static_assert(kDecKeys * NV % kDecThreads == 0, "whole loads per thread");
+  int64_t pos[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int j = j0 + (tid + u * kDecThreads) / NV;
+    pos[u] = j < n_hist ? (sel != nullptr ? (int64_t)sel[(size_t)g * n_hist + j] : (int64_t)j) : -1;
+  }
+  constexpr int QPER = 32 * D / kDecThreads;                 // query elements per thread (rows < R used)
+  float qv[QPER];
+#pragma unroll
+  for (int u = 0; u < QPER; ++u) {
+    const int i = tid + u * kDecThreads, r = i / D, e = i % D;
+    qv[u] = r < R ? to_f32(Q[((size_t)(g * G + r / C) * C + r % C) * D + e]) : 0.f;
+  }
   uint4 kr[PER], vr[PER];
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
@@ -102,9 +112,8 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
     if (j < n_keys) {
       const T *kp, *vp;
       if (j < n_hist) {
-        const int64_t t = sel != nullptr ? sel[(size_t)g * n_hist + j] : j;
-        kp = Kh + (size_t)g * h_stride + (size_t)t * D + e;
-        vp = Vh + (size_t)g * h_stride + (size_t)t * D + e;
+        kp = Kh + (size_t)g * h_stride + (size_t)pos[u] * D + e;
+        vp = Vh + (size_t)g * h_stride + (size_t)pos[u] * D + e;
       } else {
         kp = Kc + ((size_t)g * C + (j - n_hist)) * D + e;
         vp = Vc + ((size_t)g * C + (j - n_hist)) * D + e;
@@ -113,6 +122,8 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
       vr[u] = *reinterpret_cast<const uint4*>(vp);
     }
   }
+#pragma unroll
+  for (int u = 0; u < QPER; ++u) Qs[tid + u * kDecThreads] = qv[u] * scale_log2;
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
     const int i = tid + u * kDecThreads, jj = i / NV, e = (i % NV) * VEC;
@@ -169,54 +180,70 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
   }
 }
 
-// One warp per (group row): M = max_b m_b, L = sum_b l_b 2^(m_b - M),
-// O = sum_b o_b 2^(m_b - M) / L, lse = (M + log2 L) ln 2 in the units of the
-// scaled logits.  Lane b % 32 holds block b's weight; the output sums then
-// take the weights by shuffle, with the block loads unrolled so that several
-// are in flight at once.
+// One CTA per (group row): M = max_b m_b, w_b = 2^(m_b - M), L = sum_b l_b w_b,
+// O = sum_b o_b w_b / L, lse = (M + log2 L) ln 2 in the units of the scaled
+// logits.  The weights go to shared memory; then thread (e, s) sums column e
+// over blocks s, s + S, ... (S = 256 / D), its loads independent of one
+// another, and the S partial sums are added in shared memory.
+constexpr int kMergeThreads = 256;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(128) k_attend_decode_merge(const float* __restrict__ part_ml,
-                                                             const float* __restrict__ part_o, int n_rows, int n_blk,
-                                                             int C, int G, T* __restrict__ O,
-                                                             float* __restrict__ lse) {
+__global__ void __launch_bounds__(kMergeThreads) k_attend_decode_merge(const float* __restrict__ part_ml,
+                                                                       const float* __restrict__ part_o, int n_blk,
+                                                                       int C, int G, T* __restrict__ O,
+                                                                       float* __restrict__ lse) {
   pdl_launch_dependents();
   pdl_wait();
-  constexpr int E = D / 32;
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (row >= n_rows) return;
+  extern __shared__ float w_s[];                 // [n_blk]
+  __shared__ float red[kMergeThreads / 32];
+  __shared__ float part[kMergeThreads];
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* ml = part_ml + (size_t)row * n_blk * 2;
   float M = -INFINITY;
-  for (int b = lane; b < n_blk; b += 32) M = fmaxf(M, ml[2 * b]);
+  for (int b = tid; b < n_blk; b += kMergeThreads) M = fmaxf(M, ml[2 * b]);
   M = warp_max(M);
-  float L = 0.f, acc[E];
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
 #pragma unroll
-  for (int k = 0; k < E; ++k) acc[k] = 0.f;
-  const float* ob = part_o + (size_t)row * n_blk * D + lane;
-  for (int b0 = 0; b0 < n_blk; b0 += 32) {
-    const int b = b0 + lane;
-    float w = 0.f;
-    if (b < n_blk) {
-      const float mb = ml[2 * b];
-      w = mb == -INFINITY ? 0.f : exp2f(mb - M);
-      L = fmaf(ml[2 * b + 1], w, L);
-    }
-    const int nb = min(32, n_blk - b0);
-#pragma unroll 4
-    for (int k = 0; k < nb; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      const float* o = ob + (size_t)(b0 + k) * D;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(o[32 * e], wk, acc[e]);
-    }
+  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  float L = 0.f;
+  for (int b = tid; b < n_blk; b += kMergeThreads) {
+    const float mb = ml[2 * b];
+    const float w = mb == -INFINITY ? 0.f : exp2f(mb - M);
+    w_s[b] = w;
+    L = fmaf(ml[2 * b + 1], w, L);
   }
   L = warp_sum(L);
-  // group row -> (head, chunk row)
-  const int g = row / (G * C), r = row % (G * C);
-  const int h = g * G + r / C, c = r % C;
-  const float inv = 1.0f / L;
+  if (lane == 0) red[warp] = L;
+  __syncthreads();
+  L = 0.f;
 #pragma unroll
-  for (int k = 0; k < E; ++k) O[((size_t)h * C + c) * D + lane + 32 * k] = from_f32<T>(acc[k] * inv);
-  if (lse != nullptr && lane == 0) lse[(size_t)h * C + c] = (M + log2f(L)) * 0.69314718055994531f;
+  for (int w = 0; w < kMergeThreads / 32; ++w) L += red[w];
+  constexpr int S = kMergeThreads / D;
+  const int e = tid % D, sub = tid / D;
+  const float* ob = part_o + (size_t)row * n_blk * D + e;
+  float a0 = 0.f, a1 = 0.f;
+  int b = sub;
+#pragma unroll 4
+  for (; b + S < n_blk; b += 2 * S) {
+    a0 = fmaf(ob[(size_t)b * D], w_s[b], a0);
+    a1 = fmaf(ob[(size_t)(b + S) * D], w_s[b + S], a1);
+  }
+  if (b < n_blk) a0 = fmaf(ob[(size_t)b * D], w_s[b], a0);
+  part[tid] = a0 + a1;
+  __syncthreads();
+  if (tid < D) {
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < S; ++k) acc += part[tid + k * D];
+    // group row -> (head, chunk row)
+    const int g = row / (G * C), r = row % (G * C);
+    const int h = g * G + r / C, c = r % C;
+    O[((size_t)h * C + c) * D + tid] = from_f32<T>(acc / L);
+    if (lse != nullptr && tid == 0) lse[(size_t)h * C + c] = (M + log2f(L)) * 0.69314718055994531f;
+  }
 }
 
 size_t decode_smem(int d, int elt) {
@@ -243,7 +270,8 @@ cudaError_t launch_attend_decode(int dtype, int d, const void* Q, const void* Kh
   float* part_o = part + (size_t)H_q * C * n_blk * 2;
   const float scale_log2 = scale * 1.4426950408889634f;
   const size_t smem = decode_smem(d, dtype == 0 ? 2 : 4);
-  const dim3 grid(n_blk, H_kv), mgrid((H_q * C + 3) / 4);
+  const dim3 grid(n_blk, H_kv), mgrid(H_q * C);
+  const size_t msmem = (size_t)n_blk * 4;
   cudaError_t e;
 #define QUOKA_DEC(T, DD)                                                                                          \
   do {                                                                                                            \
@@ -252,9 +280,10 @@ cudaError_t launch_attend_decode(int dtype, int d, const void* Q, const void* Kh
       e = launch_pdl(k_attend_decode<T, DD>, grid, dim3(kDecThreads), smem, st, (const T*)Q, (const T*)Kh,        \
                      (const T*)Vh, h_stride, sel, n_hist, (const T*)Kc, (const T*)Vc, C, G, scale_log2, part_ml,  \
                      part_o);                                                                                     \
+    if (e == cudaSuccess) e = ensure_smem((const void*)k_attend_decode_merge<T, DD>, msmem);                     \
     if (e == cudaSuccess)                                                                                         \
-      e = launch_pdl(k_attend_decode_merge<T, DD>, mgrid, dim3(128), 0, st, (const float*)part_ml,                \
-                     (const float*)part_o, H_q * C, n_blk, C, G, (T*)O, lse);                                     \
+      e = launch_pdl(k_attend_decode_merge<T, DD>, mgrid, dim3(kMergeThreads), msmem, st, (const float*)part_ml,  \
+                     (const float*)part_o, n_blk, C, G, (T*)O, lse);                                              \
   } while (0)
   if (dtype == 0) {
     if (d == 64) QUOKA_DEC(__nv_bfloat16, 64); else QUOKA_DEC(__nv_bfloat16, 128);
