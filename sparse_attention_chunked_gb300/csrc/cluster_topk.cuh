@@ -30,29 +30,37 @@ struct ClusterTopkShared {
 // aligned) when `cache`, else key_at(i) yields key t0 + i.  Every thread of
 // every CTA of the cluster calls it; it ends with a cluster barrier, so the
 // CTA's shared memory outlives every remote read of it.
+// hist0: NULL, or the whole row's histogram of the first digit (bits 31..24)
+// already counted where the keys were produced; it then replaces the first
+// pass's histogram and cluster merge.
 template <int NC, typename KeyAt>
 __device__ void cluster_radix_topk(cooperative_groups::cluster_group& cluster, bool cache, const uint4* keys4,
                                    const KeyAt& key_at, int n, int t0, int k, int32_t* __restrict__ out,
-                                   ClusterTopkShared& sm) {
+                                   ClusterTopkShared& sm, const unsigned* __restrict__ hist0 = nullptr) {
   const int rank = (int)cluster.block_rank();
   uint32_t prefix = 0, mask = 0;
   int need = k;
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass, buf = pass & 1;
-    radix_zero(&sm.sub[0][0], kRadixSubHists * 256);
-    __syncthreads();
-    if (cache) radix_hist4(keys4, n, prefix, mask, shift, sm.sub);
-    else radix_hist(key_at, n, prefix, mask, shift, sm.sub);
-    __syncthreads();
-    radix_reduce(sm.sub, sm.hist[buf]);
-    cluster.sync();                       // every CTA's histogram of this pass is ready
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) {   // merge bin b across the cluster
-      unsigned t = 0;
+    if (pass == 0 && hist0 != nullptr) {
+      for (int b = threadIdx.x; b < 256; b += blockDim.x) sm.merged[b] = hist0[b];
+      __syncthreads();
+    } else {
+      radix_zero(&sm.sub[0][0], kRadixSubHists * 256);
+      __syncthreads();
+      if (cache) radix_hist4(keys4, n, prefix, mask, shift, sm.sub);
+      else radix_hist(key_at, n, prefix, mask, shift, sm.sub);
+      __syncthreads();
+      radix_reduce(sm.sub, sm.hist[buf]);
+      cluster.sync();                       // every CTA's histogram of this pass is ready
+      for (int b = threadIdx.x; b < 256; b += blockDim.x) {   // merge bin b across the cluster
+        unsigned t = 0;
 #pragma unroll
-      for (int q = 0; q < NC; ++q) t += cluster.map_shared_rank(&sm.hist[buf][0], q)[b];
-      sm.merged[b] = t;
+        for (int q = 0; q < NC; ++q) t += cluster.map_shared_rank(&sm.hist[buf][0], q)[b];
+        sm.merged[b] = t;
+      }
+      __syncthreads();
     }
-    __syncthreads();
     if (threadIdx.x < 32) {
       unsigned c[8];
 #pragma unroll

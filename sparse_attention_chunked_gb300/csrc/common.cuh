@@ -59,6 +59,15 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Histogram of the top 8 bits of order keys (the first digit of the top-B
+// radix select), counted where the scores are produced: lanes of a warp with
+// the same digit add once.  All 32 lanes call it; `valid` false skips a lane.
+__device__ __forceinline__ void digit0_add(unsigned int* hist, uint32_t key, bool valid) {
+  const uint32_t bin = valid ? key >> 24 : 0xFFFFFFFFu;
+  const unsigned peers = __match_any_sync(0xffffffffu, bin);
+  if (valid && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
+}
+
 // Exclusive prefix sum over a block of exactly blockDim.x threads (a multiple
 // of 32, at most 1024).  `scratch` holds 32 ints.  Returns the exclusive
 // prefix of `v`; *total receives the block sum.  Contains __syncthreads().

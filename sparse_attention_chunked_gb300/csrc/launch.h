@@ -67,7 +67,7 @@ struct OperandSpec {
 //                     unit; 0 for padding).
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
                                  int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
-                                 float* op_scale, cudaStream_t st);
+                                 float* op_scale, unsigned* hist0, cudaStream_t st);
 
 // How a key's score is scaled: key_norm false: 1 (dot product); else
 // 1 / max(|k_t|, eps), read from k_inv[g * k_inv_stride + t] when k_inv is
@@ -78,9 +78,12 @@ struct KeyScale {
   int64_t k_inv_stride;
 };
 
-// score[g, t] = max_r (r . k_t) * scale(t).
+// score[g, t] = max_r (r . k_t) * scale(t).  hist0, if not NULL, receives
+// (adds) the histogram of the top 8 bits of order_key(score) per head,
+// [H_kv][256]; launch_build_operand with the same hist0 zeroes it first.
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
-                              const float* op_f32, int R, KeyScale ks, float* scores, cudaStream_t st);
+                              const float* op_f32, int R, KeyScale ks, float* scores, unsigned* hist0,
+                              cudaStream_t st);
 
 // Tensor-core scoring (bf16 keys).  op_bf / op_scale as written by
 // launch_build_operand with N_pad = score_tc_pad_rows(R); npass = 1 when
@@ -89,8 +92,8 @@ int score_tc_pad_rows(int R);
 size_t score_tc_smem(int d, int N_pad, int npass, int nst);
 struct WsHeader;
 cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
-                            const float* op_scale, int R, KeyScale ks, float* scores, WsHeader* hdr, int num_sms,
-                            cudaStream_t st);
+                            const float* op_scale, int R, KeyScale ks, float* scores, unsigned* hist0,
+                            WsHeader* hdr, int num_sms, cudaStream_t st);
 
 // Raises `func`'s dynamic shared-memory limit to `bytes` on the current device (cached).
 cudaError_t ensure_smem(const void* func, size_t bytes);
@@ -109,7 +112,10 @@ cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* V
 // Bounded-wait self-test (see selftest.cu).
 cudaError_t launch_expire_wait(WsHeader* hdr, long long limit, cudaStream_t st);
 
-cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st);
+// hist0: NULL, or the first-digit histogram the scorer built for these
+// scores ([H_kv][256]), which replaces the select's first histogram pass.
+cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st,
+                        const unsigned* hist0 = nullptr);
 
 cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, int64_t head_stride, const int32_t* sel,
                           int H_kv, int B_e, void* Ks, void* Vs, cudaStream_t st);

@@ -36,9 +36,12 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
                                                                  int n, OperandSpec spec, int R,
                                                                  float* __restrict__ op_f32,
                                                                  __nv_bfloat16* __restrict__ op_bf,
-                                                                 float* __restrict__ op_scale) {
+                                                                 float* __restrict__ op_scale,
+                                                                 unsigned* __restrict__ hist0) {
   pdl_launch_dependents();
   pdl_wait();
+  if (hist0 != nullptr && blockIdx.x == 0)   // the scorer that follows accumulates into it
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist0[(size_t)blockIdx.y * 256 + b] = 0;
   constexpr int E = D / 32;
   const int g = blockIdx.y, r = blockIdx.x, N_pad = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
 template <typename T, int D>
 __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int64_t head_stride, int T_len,
                                                     const float* __restrict__ op_f32, int R, KeyScale ks,
-                                                    float* __restrict__ scores) {
+                                                    float* __restrict__ scores, unsigned* __restrict__ hist0) {
   pdl_launch_dependents();
   pdl_wait();
   const int g = blockIdx.y;
@@ -164,11 +167,20 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
     }
   }
   if (t < T_len) scores[(size_t)g * T_len + t] = best * rk;
+  if (hist0 != nullptr) {   // this block's share of the head's first-digit histogram
+    __shared__ unsigned int digit0[256];
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) digit0[b] = 0;
+    __syncthreads();
+    digit0_add(digit0, order_key(best * rk), t < T_len);
+    __syncthreads();
+    for (int b = threadIdx.x; b < 256; b += blockDim.x)
+      if (digit0[b] != 0) atomicAdd(&hist0[(size_t)g * 256 + b], digit0[b]);
+  }
 }
 
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
                                  int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
-                                 float* op_scale, cudaStream_t st) {
+                                 float* op_scale, unsigned* hist0, cudaStream_t st) {
   const int R = spec.mode == 1 ? (spec.qmean ? G : G * n) : (spec.qmean ? 1 : n);
   if (op_scale != nullptr && (spec.mode != 1 || spec.qmean || dtype != 0 || op_bf == nullptr))
     return cudaErrorInvalidValue;
@@ -180,37 +192,38 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
   if (dtype == 0) {
     if (d == 64)
       e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, block, 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n,
-                     spec, R, op_f32, op_bf, op_scale);
+                     spec, R, op_f32, op_bf, op_scale, hist0);
     else
       e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, block, 0, st, (const __nv_bfloat16*)Q, q_idx, C, G,
-                     n, spec, R, op_f32, op_bf, op_scale);
+                     n, spec, R, op_f32, op_bf, op_scale, hist0);
   } else {
     if (d == 64)
       e = launch_pdl(k_build_operand<float, 64>, grid, block, 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
-                     op_f32, op_bf, op_scale);
+                     op_f32, op_bf, op_scale, hist0);
     else
       e = launch_pdl(k_build_operand<float, 128>, grid, block, 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
-                     op_f32, op_bf, op_scale);
+                     op_f32, op_bf, op_scale, hist0);
   }
   count_launches(1);
   return e;
 }
 
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
-                              const float* op_f32, int R, KeyScale ks, float* scores, cudaStream_t st) {
+                              const float* op_f32, int R, KeyScale ks, float* scores, unsigned* hist0,
+                              cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
   dim3 grid((T_len + 127) / 128, H_kv);
   cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
     else
-      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
   } else {
     if (d == 64)
-      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores);
+      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
     else
-      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores);
+      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
   }
   count_launches(1);
   return e;

@@ -63,6 +63,7 @@ struct ScoreSmem {
   uint64_t acc_empty[2];
   uint64_t op_full;
   uint64_t drain;
+  unsigned int digit0[256];     // first radix digit of this CTA's scores (when asked for)
   float part_max[2][4][32];     // upper warp of a quadrant -> lower warp, by tile parity
   float part_ss[2][4][32];
   uint32_t tmem_base;
@@ -128,7 +129,8 @@ template <int D, bool SCALED>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     k_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
                const float* __restrict__ op_scale, int T_len, int R, int N_pad, int nst, int cw,
-               uint32_t tmem_cols, KeyScale ks, float* __restrict__ scores, WsHeader* hdr) {
+               uint32_t tmem_cols, KeyScale ks, float* __restrict__ scores, unsigned* __restrict__ hist0,
+               WsHeader* hdr) {
   constexpr int HALVES = D / 64;
   constexpr int NPASS = SCALED ? 1 : 2;
   constexpr uint32_t kHalfBytes = kTileKeys * 128;            // one 64-column half of a key tile
@@ -164,6 +166,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     sm->abort = 0;
     tc::fence_mbar_init();
   }
+  for (int b = threadIdx.x; b < 256; b += blockDim.x) sm->digit0[b] = 0;
   if (warp == 1) {
     tc::tmem_alloc(&sm->tmem_base, tmem_cols);
     tc::tmem_relinquish();
@@ -316,6 +319,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         ss += sm->part_ss[buf][quad][lane];
         if (ks.key_norm && ks.k_inv == nullptr) rk = 1.0f / fmaxf(sqrtf(ss), kNormEps);
         if (alive && t < T_len) scores[(size_t)g * T_len + t] = m * rk;
+        if (hist0 != nullptr) digit0_add(sm->digit0, order_key(m * rk), alive && t < T_len);
       }
     }
   }
@@ -325,16 +329,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, tmem_cols);
   }
+  if (hist0 != nullptr)   // this CTA's share of the head's first-digit histogram
+    for (int b = threadIdx.x; b < 256; b += blockDim.x)
+      if (sm->digit0[b] != 0) atomicAdd(&hist0[(size_t)g * 256 + b], sm->digit0[b]);
 }
 
 template <int D, bool SCALED>
 cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t st, const CUtensorMap& kmap, const CUtensorMap& omap,
                        const float* op_scale, int T_len, int R, int N_pad, int nst, int cw, uint32_t cols,
-                       KeyScale ks, float* scores, WsHeader* hdr) {
+                       KeyScale ks, float* scores, unsigned* hist0, WsHeader* hdr) {
   cudaError_t e = ensure_smem((const void*)k_score_tc<D, SCALED>, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_score_tc<D, SCALED>, grid, dim3(kScoreThreads), smem, st, kmap, omap, op_scale, T_len, R, N_pad,
-                    nst, cw, cols, ks, scores, hdr);
+                    nst, cw, cols, ks, scores, hist0, hdr);
 }
 
 }  // namespace
@@ -349,8 +356,8 @@ size_t score_tc_smem(int d, int N_pad, int npass, int nst) {
 }
 
 cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
-                            const float* op_scale, int R, KeyScale ks, float* scores, WsHeader* hdr,
-                            int num_sms, cudaStream_t st) {
+                            const float* op_scale, int R, KeyScale ks, float* scores, unsigned* hist0,
+                            WsHeader* hdr, int num_sms, cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
   const int N_pad = score_tc_pad_rows(R);
   const int npass = op_scale != nullptr ? 1 : 2;
@@ -375,11 +382,11 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
   if (per_head > tiles_head) per_head = tiles_head;
   dim3 grid(per_head, H_kv);
   if (d == 64)
-    e = npass == 1 ? launch_one<64, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hdr)
-                   : launch_one<64, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hdr);
+    e = npass == 1 ? launch_one<64, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr)
+                   : launch_one<64, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr);
   else
-    e = npass == 1 ? launch_one<128, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hdr)
-                   : launch_one<128, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hdr);
+    e = npass == 1 ? launch_one<128, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr)
+                   : launch_one<128, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();

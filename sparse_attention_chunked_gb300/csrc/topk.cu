@@ -23,7 +23,7 @@ constexpr int kTopkSliceCap = 40 * 1024;   // keys per CTA cached in shared memo
 
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
     k_topk_cluster(const float* __restrict__ scores, int T_len, int B_e, int32_t* __restrict__ sel, int per,
-                   int cache) {
+                   int cache, const unsigned* __restrict__ hist0) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ __align__(16) uint32_t keys_s[];
@@ -54,7 +54,8 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   auto key_at = [&](int i) -> uint32_t { return cache ? keys_s[i] : order_key(s[i]); };
   const uint4* keys4 = reinterpret_cast<const uint4*>(keys_s);
 
-  cluster_radix_topk<kTopkCluster>(cluster, cache != 0, keys4, key_at, n, t0, B_e, sel + (size_t)g * B_e, sm);
+  cluster_radix_topk<kTopkCluster>(cluster, cache != 0, keys4, key_at, n, t0, B_e, sel + (size_t)g * B_e, sm,
+                                   hist0 != nullptr ? hist0 + (size_t)g * 256 : nullptr);
 }
 
 __global__ void k_iota_rows(int32_t* __restrict__ sel, int rows, int n) {
@@ -65,7 +66,8 @@ __global__ void k_iota_rows(int32_t* __restrict__ sel, int rows, int n) {
     sel[i] = (int32_t)(i % n);
 }
 
-cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st) {
+cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st,
+                        const unsigned* hist0) {
   if (B_e == 0) return cudaSuccess;
   if (B_e >= T_len) {
     const size_t total = (size_t)H_kv * T_len;
@@ -81,7 +83,7 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
   cudaError_t e = ensure_smem((const void*)k_topk_cluster, smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(k_topk_cluster, dim3(kTopkCluster, H_kv), dim3(kTopkThreads), smem, st, scores, T_len, B_e, sel, per,
-                 cache);
+                 cache, hist0);
   count_launches(1);
   return e;
 }
