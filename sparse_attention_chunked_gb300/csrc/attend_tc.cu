@@ -290,6 +290,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     tc::tmem_relinquish();
   }
   pdl_launch_dependents();
+  if (threadIdx.x == 0 && cta < n_items) {
+    // The first item's query tiles do not come from the previous kernel (the
+    // kept K/V rows do): start them towards L2 while that kernel finishes.
+    const AttItem it0 = att_item(att_item_index(cta, 0, P), n_qt, H_kv_pairs, pairs, G, nh);
+    tc::tma_prefetch_desc(&qmap);
+    for (int s = 0; s < it0.n_slots; ++s)
+      for (int hf = 0; hf < HALVES; ++hf) tc::tma_prefetch_l2_3d(&qmap, hf * 64, it0.qt * 128, it0.h0 + s);
+  }
   pdl_wait();                                   // inputs may come from the previous kernel
   tc::tc_fence_before();
   __syncthreads();
