@@ -9,22 +9,22 @@
 namespace quoka {
 
 // K_sel[g, j] = K_hist[g, sel[g, j]] and likewise V; row = vec_per_row uint4.
+// A thread copies the same 16 bytes of the key row and of the value row, so
+// the index is read once for both and the two loads are in flight together.
 __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restrict__ V, int64_t head_stride_vec,
                               const int32_t* __restrict__ sel, int H_kv, int B_e, int vec_per_row,
                               uint4* __restrict__ Ks, uint4* __restrict__ Vs) {
   pdl_launch_dependents();
   pdl_wait();
   const size_t per_mat = (size_t)H_kv * B_e * vec_per_row;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * per_mat;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const bool is_v = i >= per_mat;
-    const size_t w = is_v ? i - per_mat : i;
+  for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < per_mat; w += (size_t)gridDim.x * blockDim.x) {
     const int v = (int)(w % vec_per_row);
     const size_t row = w / vec_per_row;              // g * B_e + j
     const int g = (int)(row / B_e);
-    const int t = sel[row];
-    const uint4* src = (is_v ? V : K) + (size_t)g * head_stride_vec + (size_t)t * vec_per_row + v;
-    (is_v ? Vs : Ks)[w] = *src;
+    const size_t off = (size_t)g * head_stride_vec + (size_t)sel[row] * vec_per_row + v;
+    const uint4 k = K[off], x = V[off];
+    Ks[w] = k;
+    Vs[w] = x;
   }
 }
 
@@ -84,7 +84,7 @@ cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, in
   if (B_e == 0) return cudaSuccess;
   const int vpr = d * elt_bytes / 16;
   const int64_t hsv = head_stride * elt_bytes / 16;
-  cudaError_t e = launch_pdl(k_gather_rows, dim3(grid_for((size_t)2 * H_kv * B_e * vpr)), dim3(256), 0, st,
+  cudaError_t e = launch_pdl(k_gather_rows, dim3(grid_for((size_t)H_kv * B_e * vpr)), dim3(256), 0, st,
                              (const uint4*)K, (const uint4*)V, hsv, sel, H_kv, B_e, vpr, (uint4*)Ks, (uint4*)Vs);
   count_launches(1);
   return e;
