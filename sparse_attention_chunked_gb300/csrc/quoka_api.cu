@@ -341,7 +341,7 @@ struct SeqArgs {
 
 // Streams the ragged entry point runs sequences on: sequences of one batch
 // share nothing, so their launches may overlap on the GPU.
-constexpr int kMaxLanes = 4;
+constexpr int kMaxLanes = 8;
 
 int varlen_lanes(const quoka_varlen_shape* v, const int64_t* cu_C) {
   int busy = 0;

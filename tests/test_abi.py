@@ -142,10 +142,11 @@ def _ws_varlen(q, vshape, cu_T, cu_C, N_q=16, B=64, gqa="max"):
 
 
 def test_varlen_workspace_is_one_slice_per_lane(quoka):
-    """Header + one slice per stream lane (up to 4, one per non-empty sequence), each for the largest sequence."""
+    """Header + one slice per stream lane (up to 8, one per non-empty sequence), each for the largest sequence."""
     for cu_T, cu_C, lanes in (([0, 1000, 1000, 41000], [0, 128, 200, 201], 3),
                               ([0, 1000, 1000, 41000], [0, 128, 128, 201], 2),
-                              ([0, 5, 9, 13, 17, 21, 25], [0, 1, 2, 3, 4, 5, 6], 4)):
+                              ([0, 5, 9, 13, 17, 21, 25], [0, 1, 2, 3, 4, 5, 6], 6),
+                              (list(range(0, 55, 5)), list(range(0, 11)), 8)):
         rc, n = _ws_varlen(quoka, _vshape(quoka, nseq=len(cu_T) - 1), cu_T, cu_C)
         assert rc == 0
         per_seq = [quoka.workspace_size(_shape(quoka, C=c1 - c0, T=t1 - t0), 16, 64, quoka.params_of("max"))
