@@ -236,9 +236,10 @@ typedef struct {
   int32_t reserved;        /* must be 0 */
 } quoka_varlen_shape;
 
-/* Workspace bytes for quoka_chunk_attend_varlen: the largest single-sequence
- * requirement of the batch (the sequences run one after another on the
- * stream and reuse it).  cu_T, cu_C as for quoka_chunk_attend_varlen. */
+/* Workspace bytes for quoka_chunk_attend_varlen: the 256-byte error header
+ * plus one slice per stream lane (one lane per sequence with C_s > 0, at most
+ * 8), each slice the largest single-sequence requirement of the batch.
+ * cu_T, cu_C as for quoka_chunk_attend_varlen. */
 int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
                                 int N_q, int B, const quoka_params* params, size_t* bytes);
 
@@ -260,8 +261,14 @@ int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* 
  *               a skipped sequence keeps its rows, left unwritten).
  * lse and sel_out need only 4-byte alignment; the other tensors 16 bytes.
  * N_q, B and params apply to every sequence.  Every sequence is checked before
- * anything is enqueued; the sequences are then enqueued in order on `stream`,
- * each through the same kernels as quoka_chunk_attend, reusing ws. */
+ * anything is enqueued.  The sequences then go through the same kernels as
+ * quoka_chunk_attend on up to 8 stream lanes: `stream` itself and
+ * library-owned streams (created once per device) that first wait for
+ * everything enqueued on `stream` so far; `stream` then waits for every lane,
+ * so the call behaves as one unit of work on `stream` (and stream capture
+ * records the fork and the join).  Each lane uses its own slice of ws; the
+ * error header is shared.  Concurrent calls from several host threads are
+ * serialised on the lane streams. */
 int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
                               const void* Q, const void* K_hist, const void* V_hist, const void* K_chunk,
                               const void* V_chunk, int N_q, int B, const quoka_params* params, void* O, float* lse,
