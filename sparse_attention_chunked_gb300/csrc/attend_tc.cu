@@ -174,25 +174,26 @@ __device__ __noinline__ bool softmax_item(AttSmem* sm, uint8_t* p_row, int s, in
       m_used = m_new;
     }
     const float neg_m = -m_used * scale_log2;
-    // PV_s of the previous block must be done before P_s is overwritten and before O is rescaled
-    // (for an item's first block the previous item's epilogue already waited for it)
-    if (jb > 0 && !(ok = warp_wait(&sm->o_done[s], (nb + jb - 1) & 1, abort, hdr, 0x209))) break;
+    // The probabilities are computed into registers (packed bf16, in place of the logits)
+    // while PV_s of the previous block may still be reading P_s; they are stored once it is
+    // done, which is also when O may be rescaled (for an item's first block the previous
+    // item's epilogue already waited for it).
     float sa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {             // 8 keys = one 16-byte chunk of P at a time
-      uint32_t w[4];
+    for (int i2 = 0; i2 < 128; i2 += 2) {
+      float x0 = __uint_as_float(sv[i2]), x1 = __uint_as_float(sv[i2 + 1]);
+      fma2(x0, x1, scale_log2, neg_m);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      if ((i2 >> 1) & 1) add2(sa[2], sa[3], p0, p1);
+      else add2(sa[0], sa[1], p0, p1);
+      sv[i2 >> 1] = pack_bf16x2(p0, p1);       // packed pair j lands in sv[j], below every unread logit
+    }
+    if (jb > 0 && !(ok = warp_wait(&sm->o_done[s], (nb + jb - 1) & 1, abort, hdr, 0x209))) break;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i2 = 8 * q + 2 * j;
-        float x0 = __uint_as_float(sv[i2]), x1 = __uint_as_float(sv[i2 + 1]);
-        fma2(x0, x1, scale_log2, neg_m);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        if (j & 1) add2(sa[2], sa[3], p0, p1);
-        else add2(sa[0], sa[1], p0, p1);
-        w[j] = pack_bf16x2(p0, p1);
-      }
+    for (int q = 0; q < 16; ++q) {             // 8 keys = one 16-byte chunk of P at a time
       const int hf = q >> 3, ch = q & 7;
-      *reinterpret_cast<uint4*>(p_row + hf * kHalfBytes + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(p_row + hf * kHalfBytes + ((ch ^ (r & 7)) << 4)) =
+          make_uint4(sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]);
     }
     l = l * alpha + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
     if (jb > 0 && __any_sync(0xffffffffu, rescale)) {   // O *= alpha in TMEM (rows without a rescale: alpha = 1)
