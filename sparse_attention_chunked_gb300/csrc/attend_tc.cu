@@ -330,6 +330,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             tc::tma_load_3d(q_s + s * kTileBytes + hf * kHalfBytes, &qmap, &sm->q_full, hf * 64, it.qt * 128,
                             it.h0 + s);
         ++n_done;
+        // the next item's query tiles towards L2, so that its Q load after this item is a short one
+        const int i_next = att_item_index(cta, round + 1, P);
+        if (i_next < n_items) {
+          const AttItem nx = att_item(i_next, n_qt, H_kv_pairs, pairs, G, nh);
+          for (int s = 0; s < nx.n_slots; ++s)
+            for (int hf = 0; hf < HALVES; ++hf) tc::tma_prefetch_l2_3d(&qmap, hf * 64, nx.qt * 128, nx.h0 + s);
+        }
         // Ring items in the order the MMA warps consume them: K_0, then for every
         // block j: K_{j+1} (used early, by S of the next block) and V_j (used late).
         auto load = [&](int jb, int which) {    // which: 0 = K, 1 = V
