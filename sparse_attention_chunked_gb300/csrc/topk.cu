@@ -6,7 +6,9 @@
 // r of the cluster owns the r-th contiguous eighth of the head's keys and
 // caches them in shared memory (up to 40K keys per CTA; larger slices are
 // re-read from global memory, where they are L2-resident right after the
-// scoring kernel).
+// scoring kernel).  In the fused chunk path the scoring kernel has already
+// counted the first radix digit of every score (hist0), so the select starts
+// at the second digit.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
