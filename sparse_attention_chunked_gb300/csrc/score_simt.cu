@@ -139,12 +139,28 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
   float k[D];
   float ss = 0.f;
   if (t < T_len) {
-    const T* kp = K + (size_t)g * head_stride + (size_t)t * D;
+    // the key row with 16-byte loads, all issued before the first is used
+    const uint4* kp = reinterpret_cast<const uint4*>(K + (size_t)g * head_stride + (size_t)t * D);
+    constexpr int NV = D * (int)sizeof(T) / 16;
+    uint4 raw[NV];
 #pragma unroll
-    for (int e = 0; e < D; ++e) {
-      k[e] = to_f32(kp[e]);
-      ss = fmaf(k[e], k[e], ss);
+    for (int v = 0; v < NV; ++v) raw[v] = kp[v];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const uint32_t w[4] = {raw[v].x, raw[v].y, raw[v].z, raw[v].w};
+      if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          k[8 * v + 2 * j] = __uint_as_float(w[j] << 16);
+          k[8 * v + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) k[4 * v + j] = __uint_as_float(w[j]);
+      }
     }
+#pragma unroll
+    for (int e = 0; e < D; ++e) ss = fmaf(k[e], k[e], ss);
   } else {
 #pragma unroll
     for (int e = 0; e < D; ++e) k[e] = 0.f;
