@@ -85,13 +85,14 @@ int num_sms() {
   return n;
 }
 
-// MMA passes of the tensor-core scoring operand.  Rows that are averages
-// (mean pooling, or the mean over tokens) are fp32 and go in as hi + lo bf16
-// rows (two passes).  Per-head max pooling can score with the bf16 query rows
-// themselves (one pass, a per-row scale in the epilogue), but the scale loads
-// slow the epilogue more than the second pass costs, so those rows go in as
-// hi + lo too whenever that operand fits shared memory (up to 256 rows at
-// d = 128); wider operands take the one-pass form.
+// Operand rows per scoring row of the tensor-core scorer: 2 = hi + lo bf16
+// rows, 1 = the raw bf16 query rows with an fp32 scale per row applied in the
+// epilogue.  Rows that are averages (mean pooling, or the mean over tokens)
+// have no exact bf16 form and always go in as hi + lo.  Per-head max pooling
+// takes hi + lo too wherever that operand fits shared memory next to two key
+// stages (up to 256 rows at d = 128): the epilogue's per-column scale loads
+// cost more than the second MMA pass (up to 128 rows the two halves even
+// share one MMA).  Wider operands take the one-pass form.
 int score_npass(const quoka_shape* s, int N_pad, const Params& p) {
   if (p.gqa != QUOKA_GQA_MAX || p.qmean) return 2;
   return score_tc_smem(s->d, N_pad, 2, 2) <= 227 * 1024 ? 2 : 1;

@@ -5,28 +5,36 @@
 //
 // One pass over the history keys, each read from HBM once.  A CTA owns a
 // contiguous range of 128-key tiles of one KV head.  Per tile:
-//   D[128 keys x N_pad rows] = K_tile[128 x d] . OP[N_pad x d]^T
+//   D[128 keys x N rows] = K_tile[128 x d] . OP[N x d]^T
 // (tcgen05, fp32 in TMEM), the keys on the TMEM lanes, so the threads of a key
 // reduce the maximum over the scoring rows from their own lane:
 //   score[t] = max_r (D[t, r] * s_r) / |k_t|.
-// Two operand forms, both exact to fp32 rounding:
-//  * scaled (max pooling): OP holds the selected query rows as they are
-//    (bf16, exact) and s_r = 1 / |q_r| is applied per column in the epilogue;
-//    one MMA pass.
-//  * hi/lo (mean pooling): the pre-aggregated row is an fp32 vector with no
-//    exact bf16 form, so k_build_operand splits it into hi + lo bf16 rows and
-//    both passes accumulate into the same TMEM columns; s_r = 1.
-// |k_t| comes from the key tile in shared memory, in fp32.
+// Operand forms, all exact to fp32 rounding:
+//  * scaled (max pooling with more than 256 rows, where a hi/lo operand does
+//    not fit shared memory): OP holds the selected query rows as they are
+//    (bf16, exact) and s_r = 1 / |q_r| is applied per column in the
+//    epilogue; one MMA pass.
+//  * hi/lo: a row with no exact bf16 form (a unit query, a pre-aggregated
+//    mean) is split by k_build_operand into hi + lo bf16 rows.  Up to 128
+//    rows, one MMA of N = 2 N_pad covers [hi rows ; lo rows] and the
+//    epilogue adds the two columns of a row; wider operands take two passes
+//    into the same TMEM columns.  s_r = 1.
+// The MMA reads its operands from shared memory at a fixed cost per
+// instruction below N = 128, and shared-memory loads of the epilogue compete
+// with those reads, which is why the forms above avoid a second pass and
+// per-tile scale loads where they can.  |k_t| comes from the key tile in
+// shared memory, in fp32 (or from the key-norm cache).
 //
 // Warp roles (320 threads): warp 0 issues TMA loads (operand once, then a ring
 // of key tiles), warp 1 owns TMEM and issues the MMAs, warps 2-9 are the
 // epilogue: the two warps of a TMEM lane quadrant share its 32 keys, each
 // taking half of the columns (and half of |k|^2), and combine through shared
 // memory.  The accumulator is a ring of two TMEM units of up to 256 columns;
-// a tile with more than 256 scoring rows fills both in turn, so the epilogue
-// drains one unit while the tensor core fills the other.  Every wait is
-// bounded; on a timeout the CTA records QUOKA_ERR_TIMEOUT, lets in-flight
-// copies and MMAs land, frees TMEM and exits.
+// a tile with more than 256 scoring rows fills both in turn.  The epilogue
+// copies a unit to registers and hands it back before its arithmetic, so the
+// tensor core refills it meanwhile.  Every wait is bounded; on a timeout the
+// CTA records QUOKA_ERR_TIMEOUT, lets in-flight copies and MMAs land, frees
+// TMEM and exits.
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -39,6 +47,13 @@ constexpr int kEpiWarps = 8;
 constexpr int kScoreThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 8;
 constexpr int kUnitCols = 256;     // widest accumulator unit (one MMA's N)
+
+// Operand forms (see the top of the file).
+enum ScoreMode : int {
+  kScaled = 0,      // raw rows, one pass, scales read from shared memory
+  kHiLo = 1,        // hi/lo rows, two passes into the same columns
+  kHiLoWide = 2,    // hi/lo rows, one MMA over 2 N_pad rows (N_pad <= 128)
+};
 
 // Rows of one operand TMA box: at most 256 and a divisor of NT (a multiple of 64).
 __host__ __device__ inline int op_box_rows(int NT) { return NT % 256 == 0 ? 256 : NT % 128 == 0 ? 128 : 64; }
@@ -76,6 +91,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// (a0, a1) += (b0, b1) elementwise, one packed fp32 add.
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  uint64_t x, y, z;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(z));
+}
+
 // (a0, a1) * (b0, b1) elementwise, one packed fp32 multiply.
 __device__ __forceinline__ void fmul2(float& a0, float& a1, float b0, float b1) {
   uint64_t x, y, z;
@@ -85,60 +109,121 @@ __device__ __forceinline__ void fmul2(float& a0, float& a1, float b0, float b1) 
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(z));
 }
 
-// Maximum over N (32 or 64) TMEM columns of this thread's lane starting at
-// taddr, each multiplied by its row scale sc[j] when SCALED; columns at index
-// >= lim (the operand's padding rows) are skipped.
-template <int N, bool SCALED>
-__device__ __forceinline__ float tmem_max(uint32_t taddr, const float* sc, int lim, float m) {
-  uint32_t v[N];
-  float4 s4[SCALED ? N / 4 : 1];
-  if constexpr (SCALED) {
-#pragma unroll
-    for (int j = 0; j < N / 4; ++j) s4[j] = reinterpret_cast<const float4*>(sc)[j];   // same address in every lane
-  }
-  if constexpr (N == 64) tc::tmem_ld64(taddr, v); else tc::tmem_ld32(taddr, v);
-  float x[N];
-#pragma unroll
-  for (int j = 0; j < N; ++j) x[j] = __uint_as_float(v[j]);
-  if constexpr (SCALED) {
-#pragma unroll
-    for (int j = 0; j < N / 4; ++j) {
-      fmul2(x[4 * j], x[4 * j + 1], s4[j].x, s4[j].y);
-      fmul2(x[4 * j + 2], x[4 * j + 3], s4[j].z, s4[j].w);
-    }
-  }
-  if (lim < N) {
-#pragma unroll
-    for (int j = 0; j < N; ++j)
-      if (j >= lim) x[j] = -INFINITY;
-  }
+// Maximum over HW (32, 64, 96 or 128) TMEM columns of this thread's lane
+// starting at taddr, each multiplied by its row scale sc[j] when SCALED;
+// columns at index >= lim (the operand's padding rows) are skipped.  The
+// columns are copied to registers and the accumulator unit is handed back
+// (arrive on `empty`) before any arithmetic, so the scale loads from shared
+// memory and the maximum run while the tensor core refills the unit.
+template <int HW, bool SCALED, bool MASK>
+__device__ __forceinline__ float max_cols(const uint32_t (&v)[HW], const float* sc, int lim, float m) {
   float m0 = m, m1 = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < N / 4; ++j) {
-    m0 = fmax3(m0, x[4 * j], x[4 * j + 1]);
-    m1 = fmax3(m1, x[4 * j + 2], x[4 * j + 3]);
+  for (int j4 = 0; j4 < HW / 4; ++j4) {
+    float x0 = __uint_as_float(v[4 * j4]), x1 = __uint_as_float(v[4 * j4 + 1]);
+    float x2 = __uint_as_float(v[4 * j4 + 2]), x3 = __uint_as_float(v[4 * j4 + 3]);
+    if constexpr (SCALED) {
+      const float4 s4 = reinterpret_cast<const float4*>(sc)[j4];   // same address in every lane
+      fmul2(x0, x1, s4.x, s4.y);
+      fmul2(x2, x3, s4.z, s4.w);
+    }
+    if constexpr (MASK) {
+      if (4 * j4 >= lim) x0 = -INFINITY;
+      if (4 * j4 + 1 >= lim) x1 = -INFINITY;
+      if (4 * j4 + 2 >= lim) x2 = -INFINITY;
+      if (4 * j4 + 3 >= lim) x3 = -INFINITY;
+    }
+    m0 = fmax3(m0, x0, x1);
+    m1 = fmax3(m1, x2, x3);
   }
   return fmaxf(m0, m1);
 }
 
-// Operand rows in shared memory: [HALVES][NT = NPASS * N_pad][128 B]; row
-// p * N_pad + r is pass p of scoring row r.  Column chunk c of a tile covers
-// scoring rows [c * cw, c * cw + width) and goes to accumulator unit q & 1,
-// q counting (tile, chunk) pairs.
-template <int D, bool SCALED>
+template <int HW, bool SCALED>
+__device__ __forceinline__ float drain_max(uint32_t taddr, const float* sc, int lim, float m, uint64_t* empty,
+                                           int lane) {
+  uint32_t v[HW];
+  if constexpr (HW == 128) {
+    tc::tmem_ld128(taddr, v);
+  } else if constexpr (HW == 96) {
+    tc::tmem_ld64(taddr, v);
+    tc::tmem_ld32(taddr + 64, v + 64);
+  } else if constexpr (HW == 64) {
+    tc::tmem_ld64(taddr, v);
+  } else {
+    tc::tmem_ld32(taddr, v);
+  }
+  tc::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive(empty);
+  return lim < HW ? max_cols<HW, SCALED, true>(v, sc, lim, m) : max_cols<HW, SCALED, false>(v, sc, lim, m);
+}
+
+// Copies HW consecutive TMEM columns of this thread's lane to registers.
+template <int HW>
+__device__ __forceinline__ void tmem_cols(uint32_t taddr, uint32_t (&v)[HW]) {
+  static_assert(HW == 32 || HW == 64, "32 or 64 columns");
+  if constexpr (HW == 64) tc::tmem_ld64(taddr, v);
+  else tc::tmem_ld32(taddr, v);
+}
+
+// hi/lo in one MMA: this thread's HW rows have their hi dot products at
+// hi_addr and their lo dot products at lo_addr; score row j = hi_j + lo_j.
+template <int HW, bool MASK>
+__device__ __forceinline__ float max_hilo(const uint32_t (&a)[HW], const uint32_t (&b)[HW], int lim, float m) {
+  float m0 = m, m1 = -INFINITY;
+#pragma unroll
+  for (int j4 = 0; j4 < HW / 4; ++j4) {
+    float x0 = __uint_as_float(a[4 * j4]), x1 = __uint_as_float(a[4 * j4 + 1]);
+    float x2 = __uint_as_float(a[4 * j4 + 2]), x3 = __uint_as_float(a[4 * j4 + 3]);
+    add2(x0, x1, __uint_as_float(b[4 * j4]), __uint_as_float(b[4 * j4 + 1]));
+    add2(x2, x3, __uint_as_float(b[4 * j4 + 2]), __uint_as_float(b[4 * j4 + 3]));
+    if constexpr (MASK) {
+      if (4 * j4 >= lim) x0 = -INFINITY;
+      if (4 * j4 + 1 >= lim) x1 = -INFINITY;
+      if (4 * j4 + 2 >= lim) x2 = -INFINITY;
+      if (4 * j4 + 3 >= lim) x3 = -INFINITY;
+    }
+    m0 = fmax3(m0, x0, x1);
+    m1 = fmax3(m1, x2, x3);
+  }
+  return fmaxf(m0, m1);
+}
+
+template <int HW>
+__device__ __forceinline__ float drain_hilo(uint32_t hi_addr, uint32_t lo_addr, int lim, float m, uint64_t* empty,
+                                            int lane) {
+  uint32_t a[HW], b[HW];
+  tmem_cols<HW>(hi_addr, a);
+  tmem_cols<HW>(lo_addr, b);
+  tc::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive(empty);
+  return lim < HW ? max_hilo<HW, true>(a, b, lim, m) : max_hilo<HW, false>(a, b, lim, m);
+}
+
+
+// Operand rows in shared memory: [HALVES][NT][128 B] with NT = N_pad (scaled)
+// or 2 N_pad (hi/lo: row p * N_pad + r is part p of scoring row r).  Column
+// chunk c of a tile covers scoring rows [c * cw, c * cw + width) and goes to
+// accumulator unit q & 1, q counting (tile, chunk) pairs; in the kHiLoWide
+// form the single chunk is [hi columns ; lo columns], cw = 2 N_pad.
+template <int D, int MODE>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     k_score_tc(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap omap,
                const float* __restrict__ op_scale, int T_len, int R, int N_pad, int nst, int cw,
                uint32_t tmem_cols, KeyScale ks, float* __restrict__ scores, unsigned* __restrict__ hist0,
                WsHeader* hdr) {
   constexpr int HALVES = D / 64;
-  constexpr int NPASS = SCALED ? 1 : 2;
+  constexpr bool SCALED = MODE == kScaled;
+  constexpr int NPASS = SCALED ? 1 : 2;          // operand rows per scoring row
+  constexpr int NMMA = MODE == kHiLo ? 2 : 1;     // MMA passes into the same columns
   constexpr uint32_t kHalfBytes = kTileKeys * 128;            // one 64-column half of a key tile
   constexpr uint32_t kStageBytes = HALVES * kHalfBytes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NT = NPASS * N_pad;
-  const int nch = (N_pad + cw - 1) / cw;
+  const int nch = MODE == kHiLoWide ? 1 : (N_pad + cw - 1) / cw;
   const uint32_t op_bytes = (uint32_t)HALVES * NT * 128;
   uint8_t* op_s = smem;                                         // [HALVES][NT][128 B]
   uint8_t* ktiles = smem + op_bytes;                            // [nst][HALVES][128][128 B]
@@ -226,10 +311,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           const int u = q & 1;
           if (q >= 2 && !(ok = tc::mbar_wait(&sm->acc_empty[u], ((q >> 1) - 1) & 1, abort, hdr, 0x104))) break;
           tc::tc_fence_after();
-          const int c0 = c * cw, width = min(cw, N_pad - c0);
+          const int c0 = c * cw, width = MODE == kHiLoWide ? NT : min(cw, N_pad - c0);
           const uint32_t idesc = tc::idesc_bf16_f32(128, width, false);
 #pragma unroll
-          for (int p = 0; p < NPASS; ++p)
+          for (int p = 0; p < NMMA; ++p)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const int hf = kk >> 2, kin = kk & 3;
@@ -296,16 +381,28 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         if (alive) alive = warp_wait(&sm->acc_full[u], (q >> 1) & 1, abort, hdr, 0x106);
         if (alive) {
           tc::tc_fence_after();
-          const int c0 = c * cw, hw = min(cw, N_pad - c0) >> 1;   // this warp's columns: a multiple of 32
-          const int col = c0 + half * hw;
-          const uint32_t base = tmem + lane_addr + (uint32_t)(u * cw + half * hw);
-          int j = 0;
-          for (; j + 64 <= hw; j += 64) m = tmem_max<64, SCALED>(base + j, sc_s + col + j, R - (col + j), m);
-          if (j < hw) m = tmem_max<32, SCALED>(base + j, sc_s + col + j, R - (col + j), m);
-          tc::tc_fence_before();
+          uint64_t* empty = &sm->acc_empty[u];
+          const uint32_t unit = tmem + lane_addr + (uint32_t)(u * cw);
+          if constexpr (MODE == kHiLoWide) {
+            // scoring rows [half * hw, half * hw + hw): hi at those columns, lo N_pad further
+            const int hw = N_pad >> 1, col = half * hw;
+            const uint32_t hi = unit + (uint32_t)col, lo = hi + (uint32_t)N_pad;
+            if (hw == 64) m = drain_hilo<64>(hi, lo, R - col, m, empty, lane);
+            else m = drain_hilo<32>(hi, lo, R - col, m, empty, lane);
+          } else {
+            const int c0 = c * cw, hw = min(cw, N_pad - c0) >> 1;   // this warp's columns: 32, 64, 96 or 128
+            const int col = c0 + half * hw;
+            const uint32_t base = unit + (uint32_t)(half * hw);
+            const float* sc = sc_s + col;
+            if (hw == 128) m = drain_max<128, SCALED>(base, sc, R - col, m, empty, lane);
+            else if (hw == 96) m = drain_max<96, SCALED>(base, sc, R - col, m, empty, lane);
+            else if (hw == 64) m = drain_max<64, SCALED>(base, sc, R - col, m, empty, lane);
+            else m = drain_max<32, SCALED>(base, sc, R - col, m, empty, lane);
+          }
+        } else {
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sm->acc_empty[u]);
         }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sm->acc_empty[u]);
       }
       // the quadrant's upper warp hands its half to the lower warp, which writes the score
       const int buf = it & 1;
@@ -334,13 +431,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       if (sm->digit0[b] != 0) atomicAdd(&hist0[(size_t)g * 256 + b], sm->digit0[b]);
 }
 
-template <int D, bool SCALED>
+template <int D, int MODE>
 cudaError_t launch_one(dim3 grid, size_t smem, cudaStream_t st, const CUtensorMap& kmap, const CUtensorMap& omap,
                        const float* op_scale, int T_len, int R, int N_pad, int nst, int cw, uint32_t cols,
                        KeyScale ks, float* scores, unsigned* hist0, WsHeader* hdr) {
-  cudaError_t e = ensure_smem((const void*)k_score_tc<D, SCALED>, smem);
+  cudaError_t e = ensure_smem((const void*)k_score_tc<D, MODE>, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_score_tc<D, SCALED>, grid, dim3(kScoreThreads), smem, st, kmap, omap, op_scale, T_len, R, N_pad,
+  return launch_pdl(k_score_tc<D, MODE>, grid, dim3(kScoreThreads), smem, st, kmap, omap, op_scale, T_len, R, N_pad,
                     nst, cw, cols, ks, scores, hist0, hdr);
 }
 
@@ -368,7 +465,9 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
   const size_t smem = score_tc_smem(d, N_pad, npass, nst);
   if (smem > budget) return cudaErrorInvalidValue;
   const int NT = npass * N_pad;
-  const int cw = N_pad < kUnitCols ? N_pad : kUnitCols;   // accumulator unit width
+  // operand form: see ScoreMode
+  const int mode = npass == 1 ? kScaled : (N_pad <= 128 ? kHiLoWide : kHiLo);
+  const int cw = mode == kHiLoWide ? 2 * N_pad : (N_pad < kUnitCols ? N_pad : kUnitCols);   // accumulator unit width
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * cw)) cols <<= 1;
   CUtensorMap kmap, omap;
@@ -381,12 +480,17 @@ cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv,
   int per_head = (num_sms + H_kv - 1) / H_kv;
   if (per_head > tiles_head) per_head = tiles_head;
   dim3 grid(per_head, H_kv);
+#define QUOKA_SCORE_LAUNCH(DD, MM)                                                                             \
+  launch_one<DD, MM>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr)
   if (d == 64)
-    e = npass == 1 ? launch_one<64, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr)
-                   : launch_one<64, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr);
+    e = mode == kScaled ? QUOKA_SCORE_LAUNCH(64, kScaled)
+        : mode == kHiLo ? QUOKA_SCORE_LAUNCH(64, kHiLo)
+                        : QUOKA_SCORE_LAUNCH(64, kHiLoWide);
   else
-    e = npass == 1 ? launch_one<128, true>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr)
-                   : launch_one<128, false>(grid, smem, st, kmap, omap, op_scale, T_len, R, N_pad, nst, cw, cols, ks, scores, hist0, hdr);
+    e = mode == kScaled ? QUOKA_SCORE_LAUNCH(128, kScaled)
+        : mode == kHiLo ? QUOKA_SCORE_LAUNCH(128, kHiLo)
+                        : QUOKA_SCORE_LAUNCH(128, kHiLoWide);
+#undef QUOKA_SCORE_LAUNCH
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
