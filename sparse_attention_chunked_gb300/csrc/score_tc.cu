@@ -301,14 +301,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (lane == 0 && ntiles > 0) {
       bool ok = tc::mbar_wait(&sm->op_full, 0, abort, hdr, 0x102);
       tc::tc_fence_after();
-      const uint32_t b_base = tc::smem_u32(op_s);
-      int q = 0;
+      // descriptors: a base descriptor plus (byte offset >> 4) in its address field
+      // (shared addresses are below 256 KB, so the 14-bit field never carries)
+      const uint64_t b_desc = tc::sw128_desc(tc::smem_u32(op_s), 16, 1024);
       for (int it = 0; ok && it < ntiles; ++it) {
         const int s = it % nst;
         if (!(ok = tc::mbar_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x103))) break;
-        const uint32_t a_base = tc::smem_u32(ktiles + (size_t)s * kStageBytes);
-        for (int c = 0; c < nch; ++c, ++q) {
-          const int u = q & 1;
+        const uint64_t a_desc = tc::sw128_desc(tc::smem_u32(ktiles + (size_t)s * kStageBytes), 16, 1024);
+        for (int c = 0; c < nch; ++c) {
+          const int q = it * nch + c, u = q & 1;
           if (q >= 2 && !(ok = tc::mbar_wait(&sm->acc_empty[u], ((q >> 1) - 1) & 1, abort, hdr, 0x104))) break;
           tc::tc_fence_after();
           const int c0 = c * cw, width = MODE == kHiLoWide ? NT : min(cw, N_pad - c0);
@@ -318,9 +319,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const int hf = kk >> 2, kin = kk & 3;
-              const uint64_t adesc = tc::sw128_desc(a_base + hf * kHalfBytes + kin * 32, 16, 1024);
-              const uint64_t bdesc =
-                  tc::sw128_desc(b_base + ((uint32_t)hf * NT + p * N_pad + c0) * 128 + kin * 32, 16, 1024);
+              const uint64_t adesc = a_desc + (uint64_t)((hf * kHalfBytes + kin * 32) >> 4);
+              const uint64_t bdesc = b_desc + (uint64_t)((((uint32_t)hf * NT + p * N_pad + c0) * 128 + kin * 32) >> 4);
               tc::mma_ss(tmem + (uint32_t)(u * cw), adesc, bdesc, idesc, (p | kk) > 0 ? 1u : 0u);
             }
           if (c == nch - 1) tc::mma_commit(&sm->kv_empty[s]);
