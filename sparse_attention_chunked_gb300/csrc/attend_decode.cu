@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
     const int32_t* __restrict__ sel, int n_hist, const T* __restrict__ Kc, const T* __restrict__ Vc, int C, int G,
     float scale_log2, float* __restrict__ part_ml, float* __restrict__ part_o) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(Q, Kh, Vh, sel, Kc, Vc);
   constexpr int VEC = 16 / (int)sizeof(T);        // elements per 16-byte load
   constexpr int KP = D + VEC;                     // padded key row: conflict-free 16-byte reads across keys
   extern __shared__ __align__(16) float dsm[];
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_attend_decode_merge(const flo
                                                                        int C, int G, T* __restrict__ O,
                                                                        float* __restrict__ lse) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(part_ml, part_o);
   extern __shared__ float w_s[];                 // [n_blk]
   __shared__ float red[kMergeThreads / 32];
   __shared__ float part[kMergeThreads];

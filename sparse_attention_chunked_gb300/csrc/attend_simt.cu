@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(128) k_attend_simt(const T* __restrict__ Q, co
                                                      int G, float scale_log2, T* __restrict__ O,
                                                      float* __restrict__ lse) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(Q, Kh, Vh, Kc, Vc);
   constexpr int E = D / 32;
   constexpr int RPW = kAttRows / 4;   // rows per warp
   extern __shared__ float smem[];

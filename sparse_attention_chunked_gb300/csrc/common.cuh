@@ -30,6 +30,23 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// pdl_wait(), then every pointer passed is laundered through an empty asm:
+// loads from a `const __restrict__` pointer may be treated as invariant and
+// scheduled above griddepcontrol.wait, where they would read what was there
+// before the previous kernel wrote it; a load through the laundered value
+// depends on the asm, which stays after the wait.
+template <typename... P>
+__device__ __forceinline__ void pdl_wait_for(P&... ptrs) {
+  pdl_wait();
+  (
+      [&] {
+        uintptr_t v = (uintptr_t)ptrs;
+        asm volatile("" : "+l"(v)::"memory");
+        ptrs = (P)v;
+      }(),
+      ...);
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 

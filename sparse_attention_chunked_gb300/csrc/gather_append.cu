@@ -15,7 +15,7 @@ __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restri
                               const int32_t* __restrict__ sel, int H_kv, int B_e, int vec_per_row,
                               uint4* __restrict__ Ks, uint4* __restrict__ Vs) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(K, V, sel);
   const size_t per_mat = (size_t)H_kv * B_e * vec_per_row;
   for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < per_mat; w += (size_t)gridDim.x * blockDim.x) {
     const int v = (int)(w % vec_per_row);
@@ -33,7 +33,7 @@ __global__ void k_append_rows(uint4* __restrict__ K, uint4* __restrict__ V, int6
                               const uint4* __restrict__ Kc, const uint4* __restrict__ Vc, int H_kv, int C,
                               int vec_per_row) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(Kc, Vc);
   const size_t per_mat = (size_t)H_kv * C * vec_per_row;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * per_mat;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -54,7 +54,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) k_key_inv_norms(const T* __restrict__ K, int64_t head_stride, int t0, int t1,
                                                        int H_kv, float* __restrict__ inv, int64_t inv_stride) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(K);
   constexpr int E = D / 32;
   const int n = t1 - t0;
   const size_t rows = (size_t)H_kv * n;

@@ -78,6 +78,10 @@ struct KeyScale {
   int64_t k_inv_stride;
 };
 
+// Scoring rows up to which the CUDA-core scorer takes k_score_rows (a few
+// rows, each key shared by a group of lanes) instead of one key per thread.
+constexpr int kScoreRowsMax = 8;
+
 // score[g, t] = max_r (r . k_t) * scale(t).  hist0, if not NULL, receives
 // (adds) the histogram of the top 8 bits of order_key(score) per head,
 // [H_kv][256]; launch_build_operand with the same hist0 zeroes it first.

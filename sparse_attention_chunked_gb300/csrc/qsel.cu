@@ -227,7 +227,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   for (int i = threadIdx.x; i < per; i += blockDim.x) u_s[i] = 0.f;
   __syncthreads();
   volatile int* abort = &abort_flag;
-  pdl_wait();                                     // Q may come from the previous kernel
+  pdl_wait_for(Q);   // Q may come from the previous kernel
 
   // Stage rows [p0, p0 + pn) of head k's slice; every thread calls it (it syncs), thread 0 issues.
   int round = 0;                                  // staging rounds so far: chunk barriers' phase
@@ -384,7 +384,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) k_qstats(const T* __restrict__ Q, int C, float* __restrict__ qnorm,
                                                 float* __restrict__ qpart) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(Q);
   constexpr int E = D / 32;
   const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -429,7 +429,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, const float* __restrict__ qpart,
                                               const float* __restrict__ qnorm, float* __restrict__ qcos) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(Q, qpart, qnorm);
   constexpr int E = D / 32;
   const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, co
 __global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos, int C, int G_avg, int n_sel,
                                                   int32_t* __restrict__ q_idx) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(qcos);
   extern __shared__ __align__(16) uint32_t keys_s[];
   __shared__ RadixSelectShared rs;
   const int row = blockIdx.x;

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
                                                                  float* __restrict__ op_scale,
                                                                  unsigned* __restrict__ hist0) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(Q, q_idx);
   if (hist0 != nullptr && blockIdx.x == 0)   // the scorer that follows accumulates into it
     for (int b = threadIdx.x; b < 256; b += blockDim.x) hist0[(size_t)blockIdx.y * 256 + b] = 0;
   constexpr int E = D / 32;
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
                                                     const float* __restrict__ op_f32, int R, KeyScale ks,
                                                     float* __restrict__ scores, unsigned* __restrict__ hist0) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(K, op_f32);
   const int g = blockIdx.y;
   const int t = blockIdx.x * 128 + threadIdx.x;
   __shared__ float rows[32][D];
@@ -194,6 +194,106 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
   }
 }
 
+// Few scoring rows (R <= 8, e.g. a decode step's G unit queries): LPK lanes
+// share one key row, each holding D / LPK of its elements, so a warp load
+// reads LPK * 16 contiguous bytes of each of 32 / LPK rows; the scoring rows'
+// matching elements stay in the lane's registers for the whole block.  Per
+// key a lane does (R + 1) * D / LPK FMAs (R dot products and |k|^2), then
+// log2(LPK) xor-shuffle steps per value give every lane of the group the
+// totals; the group's first lane writes the score.  U key slots per warp are
+// loaded before any is used.
+template <typename T, int D, int LPK, int RMAX>
+__global__ void __launch_bounds__(256) k_score_rows(const T* __restrict__ K, int64_t head_stride, int T_len,
+                                                    const float* __restrict__ op_f32, int R, KeyScale ks,
+                                                    float* __restrict__ scores, unsigned* __restrict__ hist0) {
+  constexpr int EPC = 16 / (int)sizeof(T);            // elements per 16-byte chunk
+  constexpr int NCH = D / EPC;                        // chunks per key row
+  constexpr int VPL = NCH / LPK;                      // chunks per lane per key
+  constexpr int KPW = 32 / LPK;                       // keys per warp per slot
+  constexpr int U = 4;                                // slots per warp
+  constexpr int KPB = 8 * KPW * U;                    // keys per block
+  static_assert(NCH % LPK == 0, "LPK must divide the chunks of a row");
+  __shared__ unsigned int digit0[256];
+  pdl_launch_dependents();
+  if (hist0 != nullptr) {   // (uniform) the bins are zero before any thread adds to them
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) digit0[b] = 0;
+    __syncthreads();
+  }
+  pdl_wait_for(K, op_f32);   // the scoring rows come from the previous kernel
+  const int g = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane % LPK, kw = lane / LPK;
+  // this lane's elements of every scoring row: chunk sub + LPK * v
+  float q[RMAX][VPL][EPC];
+  const float* opg = op_f32 + (size_t)g * R * D;
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+#pragma unroll
+      for (int j = 0; j < EPC; ++j) q[r][v][j] = r < R ? opg[(size_t)r * D + (sub + LPK * v) * EPC + j] : 0.f;
+  // the key rows of the warp's U slots, every load issued before any is used
+  const int t0 = blockIdx.x * KPB + warp * KPW * U;
+  uint4 raw[U][VPL];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int t = t0 + u * KPW + kw;
+    const uint4* kp = reinterpret_cast<const uint4*>(K + (size_t)g * head_stride + (size_t)t * D);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) raw[u][v] = t < T_len ? kp[sub + LPK * v] : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int t = t0 + u * KPW + kw;
+    float dot[RMAX], ss = 0.f;
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) dot[r] = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const uint32_t w[4] = {raw[u][v].x, raw[u][v].y, raw[u][v].z, raw[u][v].w};
+      float x[EPC];
+      if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // bf16 pair -> two fp32 (exact: shift into the high half)
+          x[2 * j] = __uint_as_float(w[j] << 16);
+          x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = __uint_as_float(w[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < EPC; ++j) {
+        ss = fmaf(x[j], x[j], ss);
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) dot[r] = fmaf(x[j], q[r][v][j], dot[r]);
+      }
+    }
+#pragma unroll
+    for (int o = LPK / 2; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xffffffffu, ss, o);
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
+    }
+    float best = dot[0];
+#pragma unroll
+    for (int r = 1; r < RMAX; ++r)
+      if (r < R) best = fmaxf(best, dot[r]);
+    const bool valid = t < T_len;
+    const float rk = !ks.key_norm ? 1.0f
+                    : ks.k_inv != nullptr ? (valid ? ks.k_inv[(size_t)g * ks.k_inv_stride + t] : 0.f)
+                                          : 1.0f / fmaxf(sqrtf(ss), kNormEps);
+    const float sc = best * rk;
+    if (sub == 0 && valid) scores[(size_t)g * T_len + t] = sc;
+    if (hist0 != nullptr) digit0_add(digit0, order_key(sc), sub == 0 && valid);
+  }
+  if (hist0 != nullptr) {   // this block's share of the head's first-digit histogram
+    __syncthreads();
+    for (int b = threadIdx.x; b < 256; b += blockDim.x)
+      if (digit0[b] != 0) atomicAdd(&hist0[(size_t)g * 256 + b], digit0[b]);
+  }
+}
+
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
                                  int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
                                  float* op_scale, unsigned* hist0, cudaStream_t st) {
@@ -224,10 +324,39 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
   return e;
 }
 
+template <typename T, int D, int LPK, int RMAX>
+static cudaError_t launch_rows(const void* K, int64_t head_stride, int H_kv, int T_len, const float* op_f32, int R,
+                               KeyScale ks, float* scores, unsigned* hist0, cudaStream_t st) {
+  constexpr int KPB = 8 * (32 / LPK) * 4;
+  return launch_pdl(k_score_rows<T, D, LPK, RMAX>, dim3((T_len + KPB - 1) / KPB, H_kv), dim3(256), 0, st,
+                    (const T*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
+}
+
+// Lanes per key row of k_score_rows: 8 up to 4 rows; 16 up to 8 rows where a
+// row has 16 or more 16-byte chunks (the lane then keeps 64 operand values).
+template <typename T, int D>
+static cudaError_t launch_rows_r(const void* K, int64_t head_stride, int H_kv, int T_len, const float* op_f32, int R,
+                                 KeyScale ks, float* scores, unsigned* hist0, cudaStream_t st) {
+  constexpr int NCH = D * (int)sizeof(T) / 16;
+  if (R <= 4) return launch_rows<T, D, 8, 4>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st);
+  return launch_rows<T, D, (NCH >= 16 ? 16 : 8), 8>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st);
+}
+
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
                               const float* op_f32, int R, KeyScale ks, float* scores, unsigned* hist0,
                               cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
+  if (R <= kScoreRowsMax) {
+    cudaError_t e;
+    if (dtype == 0)
+      e = d == 64 ? launch_rows_r<__nv_bfloat16, 64>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st)
+                  : launch_rows_r<__nv_bfloat16, 128>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st);
+    else
+      e = d == 64 ? launch_rows_r<float, 64>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st)
+                  : launch_rows_r<float, 128>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st);
+    count_launches(1);
+    return e;
+  }
   dim3 grid((T_len + 127) / 128, H_kv);
   cudaError_t e;
   if (dtype == 0) {

@@ -27,7 +27,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     k_topk_cluster(const float* __restrict__ scores, int T_len, int B_e, int32_t* __restrict__ sel, int per,
                    int cache, const unsigned* __restrict__ hist0) {
   pdl_launch_dependents();
-  pdl_wait();
+  pdl_wait_for(scores, hist0);
   extern __shared__ __align__(16) uint32_t keys_s[];
   __shared__ ClusterTopkShared sm;
   cg::cluster_group cluster = cg::this_cluster();
