@@ -3,8 +3,8 @@
 // order).  Used for the top-B history keys (topk.cu) and for query
 // subselection (qsel.cu).
 //
-// CTA `rank` of the cluster owns keys [t0, t0 + n) of the row.  Each of the 4
-// digit passes (radix_select.cuh) builds this CTA's histogram; after a cluster
+// CTA `rank` of the cluster owns keys [t0, t0 + n) of the row.  Each digit
+// pass (radix_select.cuh) builds this CTA's histogram; after a cluster
 // barrier every CTA sums the NC histograms through distributed shared memory
 // and finds the digit.  At the end each CTA counts its keys above / equal to
 // the threshold, reads the counts of the lower-ranked CTAs, and writes its
@@ -30,37 +30,66 @@ struct ClusterTopkShared {
 // aligned) when `cache`, else key_at(i) yields key t0 + i.  Every thread of
 // every CTA of the cluster calls it; it ends with a cluster barrier, so the
 // CTA's shared memory outlives every remote read of it.
-// hist0: NULL, or the whole row's histogram of the first digit (bits 31..24)
-// already counted where the keys were produced; it then replaces the first
-// pass's histogram and cluster merge.
+// hist12: NULL, or the whole row's histogram of the top 12 bits of the keys,
+// counted where the keys were produced; the select then starts from that
+// digit and needs three passes (8, 8 and 4 bits) instead of four of 8 bits.
 template <int NC, typename KeyAt>
 __device__ void cluster_radix_topk(cooperative_groups::cluster_group& cluster, bool cache, const uint4* keys4,
                                    const KeyAt& key_at, int n, int t0, int k, int32_t* __restrict__ out,
-                                   ClusterTopkShared& sm, const unsigned* __restrict__ hist0 = nullptr) {
+                                   ClusterTopkShared& sm, const unsigned* __restrict__ hist12 = nullptr) {
   const int rank = (int)cluster.block_rank();
   uint32_t prefix = 0, mask = 0;
   int need = k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass, buf = pass & 1;
-    if (pass == 0 && hist0 != nullptr) {
-      for (int b = threadIdx.x; b < 256; b += blockDim.x) sm.merged[b] = hist0[b];
-      __syncthreads();
-    } else {
-      radix_zero(&sm.sub[0][0], kRadixSubHists * 256);
-      __syncthreads();
-      if (cache) radix_hist4(keys4, n, prefix, mask, shift, sm.sub);
-      else radix_hist(key_at, n, prefix, mask, shift, sm.sub);
-      __syncthreads();
-      radix_reduce(sm.sub, sm.hist[buf]);
-      cluster.sync();                       // every CTA's histogram of this pass is ready
-      for (int b = threadIdx.x; b < 256; b += blockDim.x) {   // merge bin b across the cluster
-        unsigned t = 0;
+  if (hist12 != nullptr) {
+    // the 12-bit digit holding the k-th largest key: bins in descending order, 8 per thread
+    constexpr int kPer = 4096 / 512;
+    static_assert(kPer * 512 == 4096, "512 threads take 8 bins each");
+    unsigned c[kPer], tot = 0;
+    const int hi = 4095 - kPer * (int)threadIdx.x;   // this thread's highest bin
 #pragma unroll
-        for (int q = 0; q < NC; ++q) t += cluster.map_shared_rank(&sm.hist[buf][0], q)[b];
-        sm.merged[b] = t;
-      }
-      __syncthreads();
+    for (int j = 0; j < kPer; ++j) {
+      c[j] = threadIdx.x < 512 ? hist12[hi - j] : 0u;
+      tot += c[j];
     }
+    int total;
+    const int excl = block_exclusive_scan((int)tot, sm.scan, &total);   // keys in higher bins
+    if (threadIdx.x < 512 && excl < need && need <= excl + (int)tot) {
+      unsigned cum = (unsigned)excl;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        if (cum + c[j] >= (unsigned)need) {
+          sm.bin = hi - j;
+          sm.need = need - (int)cum;
+          break;
+        }
+        cum += c[j];
+      }
+    }
+    __syncthreads();
+    prefix = (uint32_t)sm.bin << 20;
+    mask = 0xFFF00000u;
+    need = sm.need;
+  }
+  const int npass = hist12 != nullptr ? 3 : 4;
+  for (int pass = 0; pass < npass; ++pass) {
+    // digits: 8 bits at 24, 16, 8, 0; after the 12-bit start 8 bits at 12 and 4, then 4 bits at 0
+    const int shift = hist12 != nullptr ? (pass == 0 ? 12 : pass == 1 ? 4 : 0) : 24 - 8 * pass;
+    const uint32_t dmask = (hist12 != nullptr && pass == 2) ? 15u : 255u;
+    const int buf = pass & 1;
+    radix_zero(&sm.sub[0][0], kRadixSubHists * 256);
+    __syncthreads();
+    if (cache) radix_hist4(keys4, n, prefix, mask, shift, sm.sub, dmask);
+    else radix_hist(key_at, n, prefix, mask, shift, sm.sub, dmask);
+    __syncthreads();
+    radix_reduce(sm.sub, sm.hist[buf]);
+    cluster.sync();                       // every CTA's histogram of this pass is ready
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) {   // merge bin b across the cluster
+      unsigned t = 0;
+#pragma unroll
+      for (int q = 0; q < NC; ++q) t += cluster.map_shared_rank(&sm.hist[buf][0], q)[b];
+      sm.merged[b] = t;
+    }
+    __syncthreads();
     if (threadIdx.x < 32) {
       unsigned c[8];
 #pragma unroll
@@ -69,7 +98,7 @@ __device__ void cluster_radix_topk(cooperative_groups::cluster_group& cluster, b
     }
     __syncthreads();
     prefix |= (uint32_t)sm.bin << shift;
-    mask |= 255u << shift;
+    mask |= dmask << shift;
     need = sm.need;
     // hist[buf] is next written two passes later, after a cluster barrier every CTA
     // reaches only once it has finished reading this pass's histograms.

@@ -76,11 +76,12 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Histogram of the top 8 bits of order keys (the first digit of the top-B
-// radix select), counted where the scores are produced: lanes of a warp with
-// the same digit add once.  All 32 lanes call it; `valid` false skips a lane.
-__device__ __forceinline__ void digit0_add(unsigned int* hist, uint32_t key, bool valid) {
-  const uint32_t bin = valid ? key >> 24 : 0xFFFFFFFFu;
+// Histogram of the top 12 bits of order keys (the first digit of the top-B
+// select), counted where the scores are produced: lanes of a warp with the
+// same bin add once.  `hist` may be shared or global memory.  All 32 lanes
+// call it; `valid` false skips a lane.
+__device__ __forceinline__ void hist12_add(unsigned int* hist, uint32_t key, bool valid) {
+  const uint32_t bin = valid ? key >> 20 : 0xFFFFFFFFu;
   const unsigned peers = __match_any_sync(0xffffffffu, bin);
   if (valid && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
 }

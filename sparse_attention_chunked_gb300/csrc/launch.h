@@ -64,10 +64,13 @@ struct OperandSpec {
 //   op_scale != NULL: mode 1 without qmean, bf16 Q only: one pass holding the
 //                     selected query rows as they are, [H_kv][N_pad][d], and
 //                     op_scale [H_kv][N_pad] = 1 / max(|q|, eps) (1 when not
-//                     unit; 0 for padding).
+//                     unit).
+// Padding rows R..N_pad-1 of op_bf (and their scales) repeat row 0, so they
+// never change a maximum.  hist (NULL or [H_kv][kScoreHistBins]) is zeroed
+// for the scorer that follows.
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
                                  int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
-                                 float* op_scale, unsigned* hist0, cudaStream_t st);
+                                 float* op_scale, unsigned* hist, cudaStream_t st);
 
 // How a key's score is scaled: key_norm false: 1 (dot product); else
 // 1 / max(|k_t|, eps), read from k_inv[g * k_inv_stride + t] when k_inv is
@@ -78,25 +81,31 @@ struct KeyScale {
   int64_t k_inv_stride;
 };
 
+// The scorers can count the first digit of the top-B select: the top
+// kScoreHistBits bits of order_key(score), per KV head.
+constexpr int kScoreHistBits = 12;
+constexpr int kScoreHistBins = 1 << kScoreHistBits;
+
 // Scoring rows up to which the CUDA-core scorer takes k_score_rows (a few
 // rows, each key shared by a group of lanes) instead of one key per thread.
 constexpr int kScoreRowsMax = 8;
 
-// score[g, t] = max_r (r . k_t) * scale(t).  hist0, if not NULL, receives
-// (adds) the histogram of the top 8 bits of order_key(score) per head,
-// [H_kv][256]; launch_build_operand with the same hist0 zeroes it first.
+// score[g, t] = max_r (r . k_t) * scale(t).  hist, if not NULL, receives
+// (adds) the histogram of the top kScoreHistBits bits of order_key(score) per
+// head, [H_kv][kScoreHistBins]; launch_build_operand with the same hist zeroes
+// it first.
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
-                              const float* op_f32, int R, KeyScale ks, float* scores, unsigned* hist0,
+                              const float* op_f32, int R, KeyScale ks, float* scores, unsigned* hist,
                               cudaStream_t st);
 
 // Tensor-core scoring (bf16 keys).  op_bf / op_scale as written by
 // launch_build_operand with N_pad = score_tc_pad_rows(R); npass = 1 when
 // op_scale is given, else 2.
 int score_tc_pad_rows(int R);
-size_t score_tc_smem(int d, int N_pad, int npass, int nst);
+size_t score_tc_smem(int d, int N_pad, int npass, int nst, bool hist);
 struct WsHeader;
 cudaError_t launch_score_tc(int d, const void* K, int64_t head_stride, int H_kv, int T_len, const __nv_bfloat16* op_bf,
-                            const float* op_scale, int R, KeyScale ks, float* scores, unsigned* hist0,
+                            const float* op_scale, int R, KeyScale ks, float* scores, unsigned* hist,
                             WsHeader* hdr, int num_sms, cudaStream_t st);
 
 // Raises `func`'s dynamic shared-memory limit to `bytes` on the current device (cached).
@@ -116,10 +125,10 @@ cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* V
 // Bounded-wait self-test (see selftest.cu).
 cudaError_t launch_expire_wait(WsHeader* hdr, long long limit, cudaStream_t st);
 
-// hist0: NULL, or the first-digit histogram the scorer built for these
-// scores ([H_kv][256]), which replaces the select's first histogram pass.
+// hist: NULL, or the first-digit histogram the scorer built for these scores
+// ([H_kv][kScoreHistBins]), which replaces the select's first histogram pass.
 cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st,
-                        const unsigned* hist0 = nullptr);
+                        const unsigned* hist = nullptr);
 
 cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, int64_t head_stride, const int32_t* sel,
                           int H_kv, int B_e, void* Ks, void* Vs, cudaStream_t st);

@@ -88,23 +88,22 @@ int num_sms() {
 // Operand rows per scoring row of the tensor-core scorer: 2 = hi + lo bf16
 // rows, 1 = the raw bf16 query rows with an fp32 scale per row applied in the
 // epilogue.  Rows that are averages (mean pooling, or the mean over tokens)
-// have no exact bf16 form and always go in as hi + lo.  Per-head max pooling
-// takes hi + lo too wherever that operand fits shared memory next to two key
-// stages (up to 256 rows at d = 128): the epilogue's per-column scale loads
-// cost more than the second MMA pass (up to 128 rows the two halves even
-// share one MMA).  Wider operands take the one-pass form.
+// have no exact bf16 form and go in as hi + lo; per-head max pooling scores
+// with the query rows themselves (one MMA pass, half the tensor work).
 int score_npass(const quoka_shape* s, int N_pad, const Params& p) {
-  if (p.gqa != QUOKA_GQA_MAX || p.qmean) return 2;
-  return score_tc_smem(s->d, N_pad, 2, 2) <= 227 * 1024 ? 2 : 1;
+  (void)s;
+  (void)N_pad;
+  return (p.gqa == QUOKA_GQA_MAX && !p.qmean) ? 1 : 2;
 }
 
 // Whether the scoring stage can run on the tensor cores: bf16 keys, at most
-// 512 scoring rows (the TMEM width) and an operand that fits shared memory
-// next to two key stages.
+// 512 scaled rows or 256 hi/lo rows, and an operand that fits shared memory
+// next to two key stages and the first-digit histogram.
 bool score_tc_fits(const quoka_shape* s, int N_q, const Params& p) {
   if (s->dtype != QUOKA_DTYPE_BF16) return false;
   const int N_pad = score_tc_pad_rows(score_rows(s, N_q, p));
-  return N_pad <= 512 && score_tc_smem(s->d, N_pad, score_npass(s, N_pad, p), 2) <= 227 * 1024;
+  const int npass = score_npass(s, N_pad, p);
+  return N_pad <= (npass == 1 ? 512 : 256) && score_tc_smem(s->d, N_pad, npass, 2, true) <= 227 * 1024;
 }
 
 // Chunks of at most 32 / G queries (decode) attend through the split-key
@@ -125,7 +124,7 @@ bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage, int N_q 
 struct Layout {
   size_t qnorm, qpart, qcos, select_end;
   size_t op_f32, op_bf, op_scale, score_end;
-  size_t q_idx, scores, hist0, sel, ksel, vsel, dec, total;
+  size_t q_idx, scores, hist, sel, ksel, vsel, dec, total;
 };
 
 // Regions start at `start` (just past the header for a single call; a lane's
@@ -150,7 +149,7 @@ Layout make_layout(const quoka_shape* s, int N_q, int B, const Params& p, size_t
   const size_t B_e = (size_t)(B < s->T ? B : s->T);
   L.q_idx = o;  o = align_up(o + H_q * n * 4);
   L.scores = o; o = align_up(o + H_kv * T * 4);
-  L.hist0 = o;  o = align_up(o + H_kv * 256 * 4);
+  L.hist = o;   o = align_up(o + H_kv * kScoreHistBins * 4);
   L.sel = o;    o = align_up(o + H_kv * B_e * 4);
   L.ksel = o;   o = align_up(o + H_kv * B_e * d * elt_bytes(s->dtype));
   L.vsel = o;   o = align_up(o + H_kv * B_e * d * elt_bytes(s->dtype));
@@ -202,7 +201,7 @@ struct KeyCache {
 
 int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, const void* K_hist,
               const Params& p, float* scores, void* ws, const Layout& L, cudaStream_t st, KeyCache kc = KeyCache(),
-              unsigned* hist0 = nullptr) {
+              unsigned* hist = nullptr) {
   const int G = s->H_q / s->H_kv;
   OperandSpec os;
   os.mode = p.gqa == QUOKA_GQA_MAX ? 1 : 0;
@@ -215,13 +214,13 @@ int run_score(const quoka_shape* s, const void* Q, const int32_t* q_idx, int n, 
   float* op_scale = tc && score_npass(s, N_pad, p) == 1 ? at<float>(ws, L.op_scale) : nullptr;
   QUOKA_CUDA(launch_build_operand(s->dtype, s->d, Q, q_idx, s->H_kv, s->C, G, n, os, N_pad,
                                   tc ? nullptr : at<float>(ws, L.op_f32), tc ? at<__nv_bfloat16>(ws, L.op_bf) : nullptr,
-                                  op_scale, hist0, st));
+                                  op_scale, hist, st));
   const KeyScale ks{!p.dot, kc.inv, kc.stride};
   if (tc)
     return cuda_status(launch_score_tc(s->d, K_hist, head_stride(s), s->H_kv, s->T, at<__nv_bfloat16>(ws, L.op_bf),
-                                       op_scale, R, ks, scores, hist0, at<WsHeader>(ws, 0), num_sms(), st));
+                                       op_scale, R, ks, scores, hist, at<WsHeader>(ws, 0), num_sms(), st));
   return cuda_status(launch_score_simt(s->dtype, s->d, K_hist, head_stride(s), s->H_kv, s->T,
-                                       at<float>(ws, L.op_f32), R, ks, scores, hist0, st));
+                                       at<float>(ws, L.op_f32), R, ks, scores, hist, st));
 }
 
 // Attention over n_hist history rows (rows sel[g][0..n_hist) of Kh/Vh, or the
@@ -288,10 +287,10 @@ int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const
   float* scores = at<float>(ws, L.scores);
   int32_t* sel = sel_out != nullptr ? sel_out : at<int32_t>(ws, L.sel);
   QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
-  // the scorer also counts the first radix digit of its scores, which the top-B select then skips
-  unsigned* hist0 = at<unsigned>(ws, L.hist0);
-  QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st, kc, hist0));
-  QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st, hist0));
+  // the scorer also counts the top 12 bits of its scores, where the top-B select then starts
+  unsigned* hist = at<unsigned>(ws, L.hist);
+  QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st, kc, hist));
+  QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st, hist));
   if (use_decode(p, shape))   // the decode kernel reads the kept rows through sel: no gathered copy
     return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), sel, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,
                       st);

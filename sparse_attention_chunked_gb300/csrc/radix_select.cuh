@@ -30,14 +30,14 @@ __device__ __forceinline__ void radix_zero(unsigned int* h, int count) {
   for (int i = threadIdx.x; i < count; i += blockDim.x) h[i] = 0;
 }
 
-// Histogram of digit (key >> shift) & 255 over keys i < n with (key & mask) == prefix.
+// Histogram of digit (key >> shift) & dmask over keys i < n with (key & mask) == prefix.
 // Keys of neighbouring positions usually share the digit (in the first pass
 // nearly all keys do) or do not match the prefix at all, so each warp adds
 // the lanes that share the first matching lane's digit with one atomic (a
 // ballot) and only the remaining lanes add one by one.
 template <typename KeyAt>
 __device__ __forceinline__ void radix_hist(const KeyAt& key_at, int n, uint32_t prefix, uint32_t mask, int shift,
-                                           unsigned int (*sub)[256]) {
+                                           unsigned int (*sub)[256], uint32_t dmask = 255u) {
   const int lane = threadIdx.x & 31;
   unsigned int* my_hist = sub[(threadIdx.x >> 5) & (kRadixSubHists - 1)];
   for (int base = 0; base < n; base += blockDim.x) {
@@ -45,7 +45,7 @@ __device__ __forceinline__ void radix_hist(const KeyAt& key_at, int n, uint32_t 
     uint32_t bin = 0xFFFFFFFFu;
     if (i < n) {
       const uint32_t u = key_at(i);
-      if ((u & mask) == prefix) bin = (u >> shift) & 255u;
+      if ((u & mask) == prefix) bin = (u >> shift) & dmask;
     }
     const unsigned valid = __ballot_sync(0xffffffffu, bin != 0xFFFFFFFFu);
     if (valid != 0u) {
@@ -147,7 +147,7 @@ __device__ __forceinline__ void radix_hist_one(uint32_t bin, int lane, unsigned 
 }
 
 __device__ __forceinline__ void radix_hist4(const uint4* __restrict__ keys4, int n, uint32_t prefix, uint32_t mask,
-                                            int shift, unsigned int (*sub)[256]) {
+                                            int shift, unsigned int (*sub)[256], uint32_t dmask = 255u) {
   const int lane = threadIdx.x & 31;
   unsigned int* my_hist = sub[(threadIdx.x >> 5) & (kRadixSubHists - 1)];
   const int nv = (n + 3) >> 2;
@@ -159,7 +159,7 @@ __device__ __forceinline__ void radix_hist4(const uint4* __restrict__ keys4, int
       const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (4 * v + j < n && (u[j] & mask) == prefix) b[j] = (u[j] >> shift) & 255u;
+        if (4 * v + j < n && (u[j] & mask) == prefix) b[j] = (u[j] >> shift) & dmask;
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) radix_hist_one(b[j], lane, my_hist);

@@ -8,8 +8,8 @@
 
 namespace quoka {
 
-// One warp per scoring row; grid.x covers N_pad >= R rows (padding rows are
-// zero in the tensor-core copy and never read by the epilogue).  Row r of
+// One warp per scoring row; grid.x covers N_pad >= R rows (padding rows of
+// the tensor-core copy repeat row 0, so they never change a maximum).  Row r of
 // KV group g:
 //   MAX : r = k * n + i  -> query head h = g*G + k, position q_idx[h, i];
 //         fp32 row q / |q|.
@@ -37,25 +37,17 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
                                                                  float* __restrict__ op_f32,
                                                                  __nv_bfloat16* __restrict__ op_bf,
                                                                  float* __restrict__ op_scale,
-                                                                 unsigned* __restrict__ hist0) {
+                                                                 unsigned* __restrict__ hist) {
   pdl_launch_dependents();
   pdl_wait_for(Q, q_idx);
-  if (hist0 != nullptr && blockIdx.x == 0)   // the scorer that follows accumulates into it
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist0[(size_t)blockIdx.y * 256 + b] = 0;
+  if (hist != nullptr && blockIdx.x == 0)   // the scorer that follows accumulates into it
+    for (int b = threadIdx.x; b < kScoreHistBins; b += blockDim.x) hist[(size_t)blockIdx.y * kScoreHistBins + b] = 0;
   constexpr int E = D / 32;
-  const int g = blockIdx.y, r = blockIdx.x, N_pad = gridDim.x;
+  const int g = blockIdx.y, r_out = blockIdx.x, N_pad = gridDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int npass = op_scale != nullptr ? 1 : 2;
-  if (r >= R) {   // padding row of the tensor-core operand
-    if (op_bf != nullptr && warp == 0) {
-      for (int p = 0; p < npass; ++p)
-#pragma unroll
-        for (int j = 0; j < E; ++j)
-          op_bf[(((size_t)g * npass + p) * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(0.f);
-      if (op_scale != nullptr && lane == 0) op_scale[(size_t)g * N_pad + r] = 0.f;
-    }
-    return;
-  }
+  if (r_out >= R && op_bf == nullptr) return;   // padding rows exist in the tensor-core copy only
+  const int r = r_out < R ? r_out : 0;          // a padding row repeats row 0
   // the (head, token) pairs of row r: heads [k0, k1) of the group, tokens [i0, i1) of the selection
   int k0, k1, i0, i1;
   if (spec.mode == 1) {
@@ -107,19 +99,19 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
   }
   if (op_bf != nullptr && npass == 1) {   // one (head, token) pair: the query row itself and its scale
 #pragma unroll
-    for (int j = 0; j < E; ++j) op_bf[((size_t)g * N_pad + r) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
-    if (lane == 0) op_scale[(size_t)g * N_pad + r] = inv;
+    for (int j = 0; j < E; ++j) op_bf[((size_t)g * N_pad + r_out) * D + lane + 32 * j] = __float2bfloat16_rn(x[j]);
+    if (lane == 0) op_scale[(size_t)g * N_pad + r_out] = inv;
   }
   if (op_bf != nullptr && npass == 2) {
 #pragma unroll
     for (int j = 0; j < E; ++j) {
       const __nv_bfloat16 hi = __float2bfloat16_rn(acc[j]);
       const __nv_bfloat16 lo = __float2bfloat16_rn(acc[j] - __bfloat162float(hi));
-      op_bf[(((size_t)g * 2 + 0) * N_pad + r) * D + lane + 32 * j] = hi;
-      op_bf[(((size_t)g * 2 + 1) * N_pad + r) * D + lane + 32 * j] = lo;
+      op_bf[(((size_t)g * 2 + 0) * N_pad + r_out) * D + lane + 32 * j] = hi;
+      op_bf[(((size_t)g * 2 + 1) * N_pad + r_out) * D + lane + 32 * j] = lo;
     }
   }
-  if (op_f32 != nullptr) {
+  if (op_f32 != nullptr && r_out < R) {
 #pragma unroll
     for (int j = 0; j < E; ++j) op_f32[((size_t)g * R + r) * D + lane + 32 * j] = acc[j];
   }
@@ -130,7 +122,7 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
 template <typename T, int D>
 __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int64_t head_stride, int T_len,
                                                     const float* __restrict__ op_f32, int R, KeyScale ks,
-                                                    float* __restrict__ scores, unsigned* __restrict__ hist0) {
+                                                    float* __restrict__ scores, unsigned* __restrict__ hist) {
   pdl_launch_dependents();
   pdl_wait_for(K, op_f32);
   const int g = blockIdx.y;
@@ -183,15 +175,8 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
     }
   }
   if (t < T_len) scores[(size_t)g * T_len + t] = best * rk;
-  if (hist0 != nullptr) {   // this block's share of the head's first-digit histogram
-    __shared__ unsigned int digit0[256];
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) digit0[b] = 0;
-    __syncthreads();
-    digit0_add(digit0, order_key(best * rk), t < T_len);
-    __syncthreads();
-    for (int b = threadIdx.x; b < 256; b += blockDim.x)
-      if (digit0[b] != 0) atomicAdd(&hist0[(size_t)g * 256 + b], digit0[b]);
-  }
+  if (hist != nullptr)   // the first digit of the top-B select, straight into the head's histogram
+    hist12_add(hist + (size_t)g * kScoreHistBins, order_key(best * rk), t < T_len);
 }
 
 // Few scoring rows (R <= 8, e.g. a decode step's G unit queries): LPK lanes
@@ -205,7 +190,7 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
 template <typename T, int D, int LPK, int RMAX>
 __global__ void __launch_bounds__(256) k_score_rows(const T* __restrict__ K, int64_t head_stride, int T_len,
                                                     const float* __restrict__ op_f32, int R, KeyScale ks,
-                                                    float* __restrict__ scores, unsigned* __restrict__ hist0) {
+                                                    float* __restrict__ scores, unsigned* __restrict__ hist) {
   constexpr int EPC = 16 / (int)sizeof(T);            // elements per 16-byte chunk
   constexpr int NCH = D / EPC;                        // chunks per key row
   constexpr int VPL = NCH / LPK;                      // chunks per lane per key
@@ -213,12 +198,7 @@ __global__ void __launch_bounds__(256) k_score_rows(const T* __restrict__ K, int
   constexpr int U = 4;                                // slots per warp
   constexpr int KPB = 8 * KPW * U;                    // keys per block
   static_assert(NCH % LPK == 0, "LPK must divide the chunks of a row");
-  __shared__ unsigned int digit0[256];
   pdl_launch_dependents();
-  if (hist0 != nullptr) {   // (uniform) the bins are zero before any thread adds to them
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) digit0[b] = 0;
-    __syncthreads();
-  }
   pdl_wait_for(K, op_f32);   // the scoring rows come from the previous kernel
   const int g = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -285,18 +265,13 @@ __global__ void __launch_bounds__(256) k_score_rows(const T* __restrict__ K, int
                                           : 1.0f / fmaxf(sqrtf(ss), kNormEps);
     const float sc = best * rk;
     if (sub == 0 && valid) scores[(size_t)g * T_len + t] = sc;
-    if (hist0 != nullptr) digit0_add(digit0, order_key(sc), sub == 0 && valid);
-  }
-  if (hist0 != nullptr) {   // this block's share of the head's first-digit histogram
-    __syncthreads();
-    for (int b = threadIdx.x; b < 256; b += blockDim.x)
-      if (digit0[b] != 0) atomicAdd(&hist0[(size_t)g * 256 + b], digit0[b]);
+    if (hist != nullptr) hist12_add(hist + (size_t)g * kScoreHistBins, order_key(sc), sub == 0 && valid);
   }
 }
 
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
                                  int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
-                                 float* op_scale, unsigned* hist0, cudaStream_t st) {
+                                 float* op_scale, unsigned* hist, cudaStream_t st) {
   const int R = spec.mode == 1 ? (spec.qmean ? G : G * n) : (spec.qmean ? 1 : n);
   if (op_scale != nullptr && (spec.mode != 1 || spec.qmean || dtype != 0 || op_bf == nullptr))
     return cudaErrorInvalidValue;
@@ -308,17 +283,17 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
   if (dtype == 0) {
     if (d == 64)
       e = launch_pdl(k_build_operand<__nv_bfloat16, 64>, grid, block, 0, st, (const __nv_bfloat16*)Q, q_idx, C, G, n,
-                     spec, R, op_f32, op_bf, op_scale, hist0);
+                     spec, R, op_f32, op_bf, op_scale, hist);
     else
       e = launch_pdl(k_build_operand<__nv_bfloat16, 128>, grid, block, 0, st, (const __nv_bfloat16*)Q, q_idx, C, G,
-                     n, spec, R, op_f32, op_bf, op_scale, hist0);
+                     n, spec, R, op_f32, op_bf, op_scale, hist);
   } else {
     if (d == 64)
       e = launch_pdl(k_build_operand<float, 64>, grid, block, 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
-                     op_f32, op_bf, op_scale, hist0);
+                     op_f32, op_bf, op_scale, hist);
     else
       e = launch_pdl(k_build_operand<float, 128>, grid, block, 0, st, (const float*)Q, q_idx, C, G, n, spec, R,
-                     op_f32, op_bf, op_scale, hist0);
+                     op_f32, op_bf, op_scale, hist);
   }
   count_launches(1);
   return e;
@@ -326,34 +301,34 @@ cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t*
 
 template <typename T, int D, int LPK, int RMAX>
 static cudaError_t launch_rows(const void* K, int64_t head_stride, int H_kv, int T_len, const float* op_f32, int R,
-                               KeyScale ks, float* scores, unsigned* hist0, cudaStream_t st) {
+                               KeyScale ks, float* scores, unsigned* hist, cudaStream_t st) {
   constexpr int KPB = 8 * (32 / LPK) * 4;
   return launch_pdl(k_score_rows<T, D, LPK, RMAX>, dim3((T_len + KPB - 1) / KPB, H_kv), dim3(256), 0, st,
-                    (const T*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
+                    (const T*)K, head_stride, T_len, op_f32, R, ks, scores, hist);
 }
 
 // Lanes per key row of k_score_rows: 8 up to 4 rows; 16 up to 8 rows where a
 // row has 16 or more 16-byte chunks (the lane then keeps 64 operand values).
 template <typename T, int D>
 static cudaError_t launch_rows_r(const void* K, int64_t head_stride, int H_kv, int T_len, const float* op_f32, int R,
-                                 KeyScale ks, float* scores, unsigned* hist0, cudaStream_t st) {
+                                 KeyScale ks, float* scores, unsigned* hist, cudaStream_t st) {
   constexpr int NCH = D * (int)sizeof(T) / 16;
-  if (R <= 4) return launch_rows<T, D, 8, 4>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st);
-  return launch_rows<T, D, (NCH >= 16 ? 16 : 8), 8>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st);
+  if (R <= 4) return launch_rows<T, D, 8, 4>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist, st);
+  return launch_rows<T, D, (NCH >= 16 ? 16 : 8), 8>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist, st);
 }
 
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
-                              const float* op_f32, int R, KeyScale ks, float* scores, unsigned* hist0,
+                              const float* op_f32, int R, KeyScale ks, float* scores, unsigned* hist,
                               cudaStream_t st) {
   if (T_len == 0) return cudaSuccess;
   if (R <= kScoreRowsMax) {
     cudaError_t e;
     if (dtype == 0)
-      e = d == 64 ? launch_rows_r<__nv_bfloat16, 64>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st)
-                  : launch_rows_r<__nv_bfloat16, 128>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st);
+      e = d == 64 ? launch_rows_r<__nv_bfloat16, 64>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist, st)
+                  : launch_rows_r<__nv_bfloat16, 128>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist, st);
     else
-      e = d == 64 ? launch_rows_r<float, 64>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st)
-                  : launch_rows_r<float, 128>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist0, st);
+      e = d == 64 ? launch_rows_r<float, 64>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist, st)
+                  : launch_rows_r<float, 128>(K, head_stride, H_kv, T_len, op_f32, R, ks, scores, hist, st);
     count_launches(1);
     return e;
   }
@@ -361,14 +336,14 @@ cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stri
   cudaError_t e;
   if (dtype == 0) {
     if (d == 64)
-      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 64>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores, hist);
     else
-      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
+      e = launch_pdl(k_score_simt<__nv_bfloat16, 128>, grid, dim3(128), 0, st, (const __nv_bfloat16*)K, head_stride, T_len, op_f32, R, ks, scores, hist);
   } else {
     if (d == 64)
-      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
+      e = launch_pdl(k_score_simt<float, 64>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores, hist);
     else
-      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores, hist0);
+      e = launch_pdl(k_score_simt<float, 128>, grid, dim3(128), 0, st, (const float*)K, head_stride, T_len, op_f32, R, ks, scores, hist);
   }
   count_launches(1);
   return e;

@@ -7,8 +7,8 @@
 // caches them in shared memory (up to 40K keys per CTA; larger slices are
 // re-read from global memory, where they are L2-resident right after the
 // scoring kernel).  In the fused chunk path the scoring kernel has already
-// counted the first radix digit of every score (hist0), so the select starts
-// at the second digit.
+// counted the top 12 bits of every score (hist), so the select starts from
+// that digit.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -25,9 +25,9 @@ constexpr int kTopkSliceCap = 40 * 1024;   // keys per CTA cached in shared memo
 
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
     k_topk_cluster(const float* __restrict__ scores, int T_len, int B_e, int32_t* __restrict__ sel, int per,
-                   int cache, const unsigned* __restrict__ hist0) {
+                   int cache, const unsigned* __restrict__ hist) {
   pdl_launch_dependents();
-  pdl_wait_for(scores, hist0);
+  pdl_wait_for(scores, hist);
   extern __shared__ __align__(16) uint32_t keys_s[];
   __shared__ ClusterTopkShared sm;
   cg::cluster_group cluster = cg::this_cluster();
@@ -57,7 +57,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   const uint4* keys4 = reinterpret_cast<const uint4*>(keys_s);
 
   cluster_radix_topk<kTopkCluster>(cluster, cache != 0, keys4, key_at, n, t0, B_e, sel + (size_t)g * B_e, sm,
-                                   hist0 != nullptr ? hist0 + (size_t)g * 256 : nullptr);
+                                   hist != nullptr ? hist + (size_t)g * kScoreHistBins : nullptr);
 }
 
 __global__ void k_iota_rows(int32_t* __restrict__ sel, int rows, int n) {
@@ -69,7 +69,7 @@ __global__ void k_iota_rows(int32_t* __restrict__ sel, int rows, int n) {
 }
 
 cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st,
-                        const unsigned* hist0) {
+                        const unsigned* hist) {
   if (B_e == 0) return cudaSuccess;
   if (B_e >= T_len) {
     const size_t total = (size_t)H_kv * T_len;
@@ -85,7 +85,7 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
   cudaError_t e = ensure_smem((const void*)k_topk_cluster, smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(k_topk_cluster, dim3(kTopkCluster, H_kv), dim3(kTopkThreads), smem, st, scores, T_len, B_e, sel, per,
-                 cache, hist0);
+                 cache, hist);
   count_launches(1);
   return e;
 }
