@@ -64,7 +64,7 @@ typedef enum {
   QUOKA_ERR_ALIGNMENT = 4,     /* a tensor pointer is not 16-byte aligned */
   QUOKA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
   QUOKA_ERR_TIMEOUT = 6,       /* device side: a bounded wait expired (kernel exited early) */
-  QUOKA_ERR_DEVICE = 7         /* device side: an internal consistency check failed */
+  QUOKA_ERR_DEVICE = 7         /* device side: a kept position outside [0, T) was skipped */
 } quoka_status;
 
 typedef enum { QUOKA_DTYPE_BF16 = 0, QUOKA_DTYPE_FP32 = 1 } quoka_dtype;
@@ -143,16 +143,22 @@ int quoka_select_queries(const quoka_shape* shape, const void* Q, int N_q, const
  * is a calling convention, not a step of the method).  For callers that
  * cannot provide device scratch memory at all -- inference-engine plugins
  * whose enqueue path may not allocate, and runtimes that plan every byte of
- * device memory ahead of time -- the scratch of the query-selection kernels
- * lives in a 4 MiB device array owned by the library, which every GPU that
- * loads libquoka.so holds until the process exits.  Same arguments, layout and
- * results as quoka_select_queries, minus (ws, ws_bytes).
- * Limit: 8*H_q*C + 4*H_q*ceil(C/64)*d bytes (each region rounded up to 256)
- * must fit in 4 MiB, e.g. 64 heads x 4096 queries at d = 128; larger problems
- * return QUOKA_ERR_UNSUPPORTED.  The first call on a device looks up the
- * array's device address (make that first call before any stream capture).
- * Every call shares the one array: calls that overlap on the GPU (different
- * streams or host threads) race and must be serialised by the caller. */
+ * device memory ahead of time -- the scratch lives in a 4 MiB device array
+ * owned by the library, which every GPU that loads libquoka.so holds until
+ * the process exits.  Same arguments, checks, layout and results as
+ * quoka_select_queries, minus (ws, ws_bytes); nothing is allocated.
+ * Limit: only very large groups (the clustered one-launch kernel's shared
+ * memory above 160 KB, e.g. mean pooling over 64 query heads of one KV head
+ * at C = 1024) use the array beyond its 256-byte error header; for them
+ * 256 + 8*H_q*C + 4*H_q*ceil(C/64)*d bytes (each region rounded up to 256)
+ * must fit in 4 MiB, else QUOKA_ERR_UNSUPPORTED.  The first call on a device
+ * looks up the array's device address (make that first call before any
+ * stream capture).  Every call shares the one array, which keeps the last
+ * call's contents: calls that overlap on the GPU (different streams or host
+ * threads) race and must be serialised by the caller.  A device-side failure
+ * (an expired bounded wait) is recorded in the array's header, which the C
+ * ABI does not expose: callers that need device errors reported use
+ * quoka_select_queries with a workspace and quoka_get_last_device_error. */
 int quoka_select_queries_noalloc(const quoka_shape* shape, const void* Q, int N_q, const quoka_params* params,
                                  int32_t* q_idx, void* stream);
 
@@ -197,7 +203,10 @@ int quoka_topk(const quoka_shape* shape, const float* scores, int B, int32_t* se
 /* Gather the selected rows: K_sel[g, j] = K_hist[g, sel[g, j]], same for V
  * ([P2] "From scores to a smaller KV set": the value comes with its key).
  * sel int32 [H_kv, B_e], every entry in [0, T); K_sel, V_sel [H_kv, B_e, d]
- * contiguous, dtype of the shape. */
+ * contiguous, dtype of the shape.  An entry outside [0, T) is checked on the
+ * device and never dereferenced: its rows are written as zeros.  (This call
+ * has no workspace, so it cannot record the error; inside quoka_chunk_attend
+ * the same check records QUOKA_ERR_DEVICE in the workspace header.) */
 int quoka_gather(const quoka_shape* shape, const void* K_hist, const void* V_hist, const int32_t* sel,
                  int B_e, void* K_sel, void* V_sel, void* stream);
 

@@ -37,6 +37,11 @@ extern std::atomic<unsigned long long> g_launch_count;
 inline void count_launches(unsigned n) { g_launch_count.fetch_add(n, std::memory_order_relaxed); }
 
 struct WsHeader;
+// Whether launch_select_queries runs the one-launch clustered kernel for this
+// problem (which keeps its intermediates in shared memory and never touches
+// qnorm / qpart / qcos) rather than the three-launch fallback.
+bool select_queries_one_launch(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel);
+
 // hdr: where device-side errors (an expired wait) are recorded; may be NULL.
 cudaError_t launch_select_queries(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel,
                                   int32_t* q_idx, float* qnorm, float* qpart, float* qcos, WsHeader* hdr,
@@ -122,6 +127,11 @@ cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* V
                              const void* Kc, const void* Vc, int H_q, int H_kv, int C, float scale, void* O,
                              float* lse, WsHeader* hdr, cudaStream_t st);
 
+// The library-owned scratch of quoka_select_queries_noalloc: its device
+// address on the current device (looked up on the first call per device).
+constexpr size_t kNoAllocScratchBytes = 4u << 20;
+cudaError_t noalloc_scratch(void** base);
+
 // Bounded-wait self-test (see selftest.cu).
 cudaError_t launch_expire_wait(WsHeader* hdr, long long limit, cudaStream_t st);
 
@@ -130,8 +140,11 @@ cudaError_t launch_expire_wait(WsHeader* hdr, long long limit, cudaStream_t st);
 cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st,
                         const unsigned* hist = nullptr);
 
+// Rows sel[g, j] of K and V (T_len rows per head).  An index outside
+// [0, T_len) is not read: the row is written as zeros and QUOKA_ERR_DEVICE is
+// recorded in hdr (when given).
 cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, int64_t head_stride, const int32_t* sel,
-                          int H_kv, int B_e, void* Ks, void* Vs, cudaStream_t st);
+                          int H_kv, int B_e, int T_len, void* Ks, void* Vs, WsHeader* hdr, cudaStream_t st);
 
 // inv[g * inv_stride + t] = 1 / max(|K[g, t]|, eps), t in [t0, t1).
 cudaError_t launch_key_inv_norms(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int t0, int t1,
@@ -142,13 +155,16 @@ cudaError_t launch_append(int elt_bytes, int d, void* K, void* V, int64_t head_s
 
 // Attention for chunks of at most 32 / G queries (decode), split over the
 // keys: kept history rows read through sel ([H_kv][n_hist] positions; NULL =
-// the first n_hist rows) straight from the cache, then the causal chunk.
+// the first n_hist rows) straight from the cache of T_cache rows per head,
+// then the causal chunk.  A position outside [0, T_cache) is not read (its
+// key and value count as zero rows) and QUOKA_ERR_DEVICE is recorded in hdr.
 // part: fp32 scratch of attend_decode_ws_bytes.
 bool attend_decode_fits(int C, int G);
 size_t attend_decode_ws_bytes(int d, int H_q, int C, int n_hist);
 cudaError_t launch_attend_decode(int dtype, int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,
-                                 const int32_t* sel, int n_hist, const void* Kc, const void* Vc, int H_q, int H_kv,
-                                 int C, float scale, void* O, float* lse, float* part, cudaStream_t st);
+                                 const int32_t* sel, int n_hist, int T_cache, const void* Kc, const void* Vc, int H_q,
+                                 int H_kv, int C, float scale, void* O, float* lse, float* part, WsHeader* hdr,
+                                 cudaStream_t st);
 
 cudaError_t launch_attend_simt(int dtype, int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,
                                int n_hist, const void* Kc, const void* Vc, int H_q, int C, int G, float scale,

@@ -497,15 +497,33 @@ __global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos,
   block_radix_topk4(reinterpret_cast<const uint4*>(keys_s), C, n_sel, q_idx + (size_t)row * n_sel, rs);
 }
 
+// The one-launch kernel's parameters: slice length per CTA, list length
+// 32 * sel_p >= n_sel (0: radix select), dynamic shared memory.
+static void qselect_fused_plan(int d, int G_avg, int C, int n_sel, int* per, int* sel_p, size_t* smem) {
+  *per = ((C + kSelCluster - 1) / kSelCluster + 3) & ~3;
+  *sel_p = n_sel <= 32 ? 1 : n_sel <= 64 ? 2 : n_sel <= 128 ? 4 : n_sel <= 256 ? 8 : 0;
+  *smem = qselect_fused_smem(*per, G_avg, d, *sel_p);
+}
+
+// The clustered kernel runs when its shared memory stays within 160 KB and Q
+// is 16-byte aligned (bulk copies want 16-byte aligned rows).
+bool select_queries_one_launch(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel) {
+  (void)dtype;
+  (void)H_q;
+  int per, sel_p;
+  size_t fsmem;
+  qselect_fused_plan(d, G_avg, C, n_sel, &per, &sel_p, &fsmem);
+  return fsmem <= 160 * 1024 && ((uintptr_t)Q & 15u) == 0;
+}
+
 template <typename T, int D>
 static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel, int32_t* q_idx,
                              float* qnorm, float* qpart, float* qcos, WsHeader* hdr, cudaStream_t st) {
   const int rows = H_q / G_avg;
-  const int per = ((C + kSelCluster - 1) / kSelCluster + 3) & ~3;
-  // the network's list length L = 32 * sel_p >= n_sel (0: radix select)
-  const int sel_p = n_sel <= 32 ? 1 : n_sel <= 64 ? 2 : n_sel <= 128 ? 4 : n_sel <= 256 ? 8 : 0;
-  const size_t fsmem = qselect_fused_smem(per, G_avg, D, sel_p);
-  if (fsmem <= 160 * 1024 && ((uintptr_t)Q & 15u) == 0) {   // bulk copies want 16-byte aligned rows
+  int per, sel_p;
+  size_t fsmem;
+  qselect_fused_plan(D, G_avg, C, n_sel, &per, &sel_p, &fsmem);
+  if (select_queries_one_launch(0, D, Q, H_q, G_avg, C, n_sel)) {
     cudaError_t e = ensure_smem((const void*)k_qselect_fused<T, D>, fsmem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(k_qselect_fused<T, D>, dim3(kSelCluster, rows), dim3(kSelThreads), fsmem, st, (const T*)Q, C, G_avg,

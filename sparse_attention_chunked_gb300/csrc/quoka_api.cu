@@ -231,9 +231,10 @@ int run_attend(const quoka_shape* s, const void* Q, const void* Kh, const void* 
                const int32_t* sel, int n_hist, const void* Kc, const void* Vc, const Params& p, void* O, float* lse,
                void* ws, size_t dec_off, cudaStream_t st) {
   const int G = s->H_q / s->H_kv;
-  if (use_decode(p, s))
-    return cuda_status(launch_attend_decode(s->dtype, s->d, Q, Kh, Vh, h_stride, sel, n_hist, Kc, Vc, s->H_q,
-                                            s->H_kv, s->C, p.scale, O, lse, at<float>(ws, dec_off), st));
+  if (use_decode(p, s))   // rows read through sel come from a cache of T rows, else Kh holds n_hist rows
+    return cuda_status(launch_attend_decode(s->dtype, s->d, Q, Kh, Vh, h_stride, sel, n_hist,
+                                            sel != nullptr ? s->T : n_hist, Kc, Vc, s->H_q, s->H_kv, s->C, p.scale, O,
+                                            lse, at<float>(ws, dec_off), at<WsHeader>(ws, 0), st));
   if (sel != nullptr) return QUOKA_ERR_DEVICE;   // not reached: only the decode kernel reads through sel
   const bool tc = use_tensor_cores(p, s, 1);
   if (p.engine == QUOKA_ENGINE_TENSOR && !tc) return QUOKA_ERR_UNSUPPORTED;
@@ -297,7 +298,7 @@ int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const
   void* ksel = at<void>(ws, L.ksel);
   void* vsel = at<void>(ws, L.vsel);
   QUOKA_CUDA(launch_gather(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), sel, shape->H_kv, B,
-                           ksel, vsel, st));
+                           T, ksel, vsel, at<WsHeader>(ws, 0), st));
   return run_attend(shape, Q, ksel, vsel, (int64_t)B * shape->d, nullptr, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,
                     st);
 }
@@ -456,6 +457,28 @@ int quoka_select_queries(const quoka_shape* shape, const void* Q, int N_q, const
   return run_select(shape, Q, n_sel_of(shape, N_q), p, q_idx, ws, L, (cudaStream_t)stream);
 }
 
+int quoka_select_queries_noalloc(const quoka_shape* shape, const void* Q, int N_q, const quoka_params* params,
+                                 int32_t* q_idx, void* stream) {
+  QUOKA_TRY(check_shape(shape));
+  Params p;
+  QUOKA_TRY(read_params(params, shape, &p));
+  if (N_q < 1 || Q == nullptr || q_idx == nullptr) return QUOKA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(q_idx)) return QUOKA_ERR_ALIGNMENT;
+  // The library's scratch array stands in for the workspace, laid out the same
+  // way (error header first).  Only the three-launch fallback of very large
+  // groups reads and writes the regions after the header, so the size limit
+  // applies to that path alone.
+  const Layout L = make_layout(shape, N_q, 1, p);
+  const int n = n_sel_of(shape, N_q);
+  const int G_avg = p.gqa == QUOKA_GQA_MAX ? 1 : shape->H_q / shape->H_kv;
+  const bool fallback =
+      n < shape->C && !select_queries_one_launch(shape->dtype, shape->d, Q, shape->H_q, G_avg, shape->C, n);
+  if (fallback && L.select_end > kNoAllocScratchBytes) return QUOKA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  QUOKA_CUDA(noalloc_scratch(&scratch));
+  return run_select(shape, Q, n, p, q_idx, scratch, L, (cudaStream_t)stream);
+}
+
 int quoka_score_keys(const quoka_shape* shape, const void* Q, const int32_t* q_idx, int N_q, const void* K_hist,
                      const quoka_params* params, float* scores, void* ws, size_t ws_bytes, void* stream) {
   QUOKA_TRY(check_shape(shape));
@@ -518,7 +541,7 @@ int quoka_gather(const quoka_shape* shape, const void* K_hist, const void* V_his
   if (!aligned16(K_hist) || !aligned16(V_hist) || !aligned16(sel) || !aligned16(K_sel) || !aligned16(V_sel))
     return QUOKA_ERR_ALIGNMENT;
   return cuda_status(launch_gather(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), sel,
-                                   shape->H_kv, B_e, K_sel, V_sel, (cudaStream_t)stream));
+                                   shape->H_kv, B_e, shape->T, K_sel, V_sel, nullptr, (cudaStream_t)stream));
 }
 
 int quoka_sparse_attend(const quoka_shape* shape, const void* Q, const void* K_sel, const void* V_sel, int B_e,

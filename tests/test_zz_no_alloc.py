@@ -1,6 +1,13 @@
-"""The workspace-free query selection (quoka_select_queries_noalloc), for callers
-that cannot give the library any device scratch memory, against the workspace
-entry point on the same inputs, over two calls in a row.
+"""The workspace-free query selection (quoka_select_queries_noalloc), against
+the workspace entry point on the same inputs, over two calls in a row.
+
+Some callers cannot give the library any device scratch memory (engine
+plugins whose enqueue path may not allocate, runtimes that plan all device
+memory up front); this entry point keeps the selection kernels' scratch in a
+library-owned device array.  The cases cover both launch paths: the
+one-launch clustered kernel (which needs no scratch beyond the error header)
+and the three-launch fallback of very large groups, which reads and writes
+the array, so a wrong array address or layout offset fails here.
 
 Collected last on purpose (file name), so that a run stopping at the first
 failure has already run every other test."""
@@ -17,35 +24,68 @@ pytestmark = pytest.mark.gpu
 
 
 def _select(quoka, x, cfg, gqa, noalloc):
+    """q_idx from one entry point, and how many kernels the call launched."""
     Q = x.Q.cuda()
     shape = quoka.shape_of(Q, x.K_hist.cuda())
     params = quoka.params_of(gqa)
     H_sel = cfg.H_q if gqa == "max" else cfg.H_kv
     q_idx = torch.full((H_sel, min(cfg.N_q, cfg.C)), -1, dtype=torch.int32, device="cuda")
+    before = quoka.quoka_launch_count()
     if noalloc:
         quoka.quoka_select_queries_noalloc(shape, Q, cfg.N_q, params, q_idx)
     else:
         ws = quoka.make_workspace(shape, cfg.N_q, cfg.B, params)
         quoka.quoka_select_queries(shape, Q, cfg.N_q, params, q_idx, ws)
+    launches = quoka.quoka_launch_count() - before
     torch.cuda.synchronize()
-    return q_idx.cpu().numpy()
+    return q_idx.cpu().numpy(), launches
+
+
+def _check_two_calls(quoka, cases, gqa, launches_expected):
+    for cfg, x in cases:            # two calls in a row: the shared scratch keeps the first call's contents
+        for _ in range(2):
+            got, n_launch = _select(quoka, x, cfg, gqa, noalloc=True)
+            ref, _ = _select(quoka, x, cfg, gqa, noalloc=False)
+            assert n_launch == launches_expected, (cfg.name, n_launch)
+            assert np.array_equal(got, ref), cfg.name
+            check_index_rows(got, oracle_query_values(f64(x.Q), cfg.H_kv, gqa), cfg.N_q, largest=False,
+                             what="noalloc q_idx")
 
 
 @pytest.mark.parametrize("gqa", ["max", "mean"])
-def test_noalloc_matches_workspace_entry_on_two_calls(quoka, gqa):
+def test_noalloc_matches_workspace_entry_one_launch(quoka, gqa):
+    """Groups small enough for the clustered kernel: one launch, no scratch regions used."""
     cases = [wl.small_chunk(H_q=8, H_kv=2, d=128, C=300, T=64, N_q=20, B=8, dtype="bf16", seed=1),
              wl.small_chunk(H_q=4, H_kv=4, d=64, C=97, T=64, N_q=9, B=8, dtype="fp32", seed=2)]
-    for cfg, x in cases:            # two calls in a row: the shared scratch keeps the first call's contents
-        got = _select(quoka, x, cfg, gqa, noalloc=True)
-        ref = _select(quoka, x, cfg, gqa, noalloc=False)
-        assert np.array_equal(got, ref)
-        check_index_rows(got, oracle_query_values(f64(x.Q), cfg.H_kv, gqa), cfg.N_q, largest=False,
-                         what="noalloc q_idx")
+    _check_two_calls(quoka, cases, gqa, launches_expected=1)
+
+
+def test_noalloc_matches_workspace_entry_three_launch_fallback(quoka):
+    """Mean pooling over 64 or 32 query heads of one KV head: the clustered kernel's shared memory is
+    above its 160 KB limit, so the statistics / cosine / select launches run on the library's array
+    (about 1 and 2 MiB of it)."""
+    cases = [wl.small_chunk(H_q=64, H_kv=1, d=128, C=1024, T=64, N_q=64, B=8, dtype="bf16", seed=3),
+             wl.small_chunk(H_q=32, H_kv=1, d=128, C=4096, T=64, N_q=64, B=8, dtype="bf16", seed=4)]
+    _check_two_calls(quoka, cases, "mean", launches_expected=3)
+
+
+def test_noalloc_keeps_every_query_when_n_q_reaches_c(quoka):
+    """N_q >= C keeps the positions 0..C-1 without any cosine (the workspace entry point's branch)."""
+    cfg, x = wl.small_chunk(H_q=8, H_kv=2, d=128, C=40, T=64, N_q=64, B=8, dtype="bf16", seed=5)
+    for gqa in ("max", "mean"):
+        for _ in range(2):
+            got, _ = _select(quoka, x, cfg, gqa, noalloc=True)
+            ref, _ = _select(quoka, x, cfg, gqa, noalloc=False)
+            assert np.array_equal(got, ref)
+            assert np.array_equal(got, np.tile(np.arange(cfg.C, dtype=np.int32), (got.shape[0], 1)))
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(quoka):
-    shape = quoka.Shape(0, 128, 8, 8192, 0, 128, 0)       # 128 heads x 8192 queries: more than 4 MiB of scratch
+    """A fallback-sized problem whose scratch exceeds the 4 MiB array is refused before anything is
+    enqueued (the pointers are never dereferenced): mean pooling over 128 query heads of one KV head
+    at C = 8192 needs about 16 MiB."""
+    shape = quoka.Shape(0, 128, 1, 8192, 0, 128, 0)
     rc = quoka.load().quoka_select_queries_noalloc(ctypes.byref(shape), ctypes.c_void_p(1 << 20), 8,
-                                                   ctypes.byref(quoka.params_of("max")), ctypes.c_void_p(1 << 20),
+                                                   ctypes.byref(quoka.params_of("mean")), ctypes.c_void_p(1 << 20),
                                                    None)
     assert rc == 2   # QUOKA_ERR_UNSUPPORTED
