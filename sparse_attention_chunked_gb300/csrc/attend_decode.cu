@@ -66,8 +66,8 @@ __device__ __forceinline__ float dot_row(const float* q, const float* k) {
 template <typename T, int D>
 __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
     const T* __restrict__ Q, const T* __restrict__ Kh, const T* __restrict__ Vh, int64_t h_stride,
-    const int32_t* __restrict__ sel, int n_hist, const T* __restrict__ Kc, const T* __restrict__ Vc, int C, int G,
-    float scale_log2, float* __restrict__ part_ml, float* __restrict__ part_o) {
+    const int32_t* __restrict__ sel, int n_hist, int T_cache, const T* __restrict__ Kc, const T* __restrict__ Vc,
+    int C, int G, float scale_log2, float* __restrict__ part_ml, float* __restrict__ part_o, WsHeader* hdr) {
   pdl_launch_dependents();
   pdl_wait_for(Q, Kh, Vh, sel, Kc, Vc);
   constexpr int VEC = 16 / (int)sizeof(T);        // elements per 16-byte load
@@ -96,6 +96,17 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
     const int j = j0 + (tid + u * kDecThreads) / NV;
     pos[u] = j < n_hist ? (sel != nullptr ? (int64_t)sel[(size_t)g * n_hist + j] : (int64_t)j) : -1;
   }
+  // a kept position outside the cache is never read (its key and value stay zero rows)
+  bool bad = false;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int j = j0 + (tid + u * kDecThreads) / NV;
+    if (j < n_hist && (pos[u] < 0 || pos[u] >= T_cache)) {
+      bad = true;
+      pos[u] = -2;
+    }
+  }
+  if (bad) record_error(hdr, 7u /* QUOKA_ERR_DEVICE */, (unsigned)(g * n_hist + j0));
   constexpr int QPER = 32 * D / kDecThreads;                 // query elements per thread (rows < R used)
   float qv[QPER];
 #pragma unroll
@@ -109,7 +120,7 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
     const int i = tid + u * kDecThreads, jj = i / NV, e = (i % NV) * VEC;
     const int j = j0 + jj;
     kr[u] = vr[u] = make_uint4(0u, 0u, 0u, 0u);
-    if (j < n_keys) {
+    if (j < n_keys && pos[u] != -2) {
       const T *kp, *vp;
       if (j < n_hist) {
         kp = Kh + (size_t)g * h_stride + (size_t)pos[u] * D + e;
@@ -261,8 +272,9 @@ size_t attend_decode_ws_bytes(int d, int H_q, int C, int n_hist) {
 }
 
 cudaError_t launch_attend_decode(int dtype, int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride,
-                                 const int32_t* sel, int n_hist, const void* Kc, const void* Vc, int H_q, int H_kv,
-                                 int C, float scale, void* O, float* lse, float* part, cudaStream_t st) {
+                                 const int32_t* sel, int n_hist, int T_cache, const void* Kc, const void* Vc, int H_q,
+                                 int H_kv, int C, float scale, void* O, float* lse, float* part, WsHeader* hdr,
+                                 cudaStream_t st) {
   const int G = H_q / H_kv;
   if (!attend_decode_fits(C, G)) return cudaErrorInvalidValue;
   const int n_blk = (n_hist + C + kDecKeys - 1) / kDecKeys;
@@ -278,8 +290,8 @@ cudaError_t launch_attend_decode(int dtype, int d, const void* Q, const void* Kh
     e = ensure_smem((const void*)k_attend_decode<T, DD>, smem);                                                   \
     if (e == cudaSuccess)                                                                                         \
       e = launch_pdl(k_attend_decode<T, DD>, grid, dim3(kDecThreads), smem, st, (const T*)Q, (const T*)Kh,        \
-                     (const T*)Vh, h_stride, sel, n_hist, (const T*)Kc, (const T*)Vc, C, G, scale_log2, part_ml,  \
-                     part_o);                                                                                     \
+                     (const T*)Vh, h_stride, sel, n_hist, T_cache, (const T*)Kc, (const T*)Vc, C, G, scale_log2,   \
+                     part_ml, part_o, hdr);                                                                       \
     if (e == cudaSuccess) e = ensure_smem((const void*)k_attend_decode_merge<T, DD>, msmem);                     \
     if (e == cudaSuccess)                                                                                         \
       e = launch_pdl(k_attend_decode_merge<T, DD>, mgrid, dim3(kMergeThreads), msmem, st, (const float*)part_ml,  \

@@ -11,9 +11,11 @@ namespace quoka {
 // K_sel[g, j] = K_hist[g, sel[g, j]] and likewise V; row = vec_per_row uint4.
 // A thread copies the same 16 bytes of the key row and of the value row, so
 // the index is read once for both and the two loads are in flight together.
+// An index outside [0, T_len) is never dereferenced: its row is written as
+// zeros and QUOKA_ERR_DEVICE is recorded in hdr (when given) with the row.
 __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restrict__ V, int64_t head_stride_vec,
-                              const int32_t* __restrict__ sel, int H_kv, int B_e, int vec_per_row,
-                              uint4* __restrict__ Ks, uint4* __restrict__ Vs) {
+                              const int32_t* __restrict__ sel, int H_kv, int B_e, int vec_per_row, int T_len,
+                              uint4* __restrict__ Ks, uint4* __restrict__ Vs, WsHeader* hdr) {
   pdl_launch_dependents();
   pdl_wait_for(K, V, sel);
   const size_t per_mat = (size_t)H_kv * B_e * vec_per_row;
@@ -21,7 +23,13 @@ __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restri
     const int v = (int)(w % vec_per_row);
     const size_t row = w / vec_per_row;              // g * B_e + j
     const int g = (int)(row / B_e);
-    const size_t off = (size_t)g * head_stride_vec + (size_t)sel[row] * vec_per_row + v;
+    const int t = sel[row];
+    if ((unsigned)t >= (unsigned)T_len) {
+      if (v == 0) record_error(hdr, 7u /* QUOKA_ERR_DEVICE */, (unsigned)row);
+      Ks[w] = Vs[w] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    const size_t off = (size_t)g * head_stride_vec + (size_t)t * vec_per_row + v;
     const uint4 k = K[off], x = V[off];
     Ks[w] = k;
     Vs[w] = x;
@@ -80,12 +88,13 @@ static int grid_for(size_t work) {
 }
 
 cudaError_t launch_gather(int elt_bytes, int d, const void* K, const void* V, int64_t head_stride, const int32_t* sel,
-                          int H_kv, int B_e, void* Ks, void* Vs, cudaStream_t st) {
+                          int H_kv, int B_e, int T_len, void* Ks, void* Vs, WsHeader* hdr, cudaStream_t st) {
   if (B_e == 0) return cudaSuccess;
   const int vpr = d * elt_bytes / 16;
   const int64_t hsv = head_stride * elt_bytes / 16;
   cudaError_t e = launch_pdl(k_gather_rows, dim3(grid_for((size_t)H_kv * B_e * vpr)), dim3(256), 0, st,
-                             (const uint4*)K, (const uint4*)V, hsv, sel, H_kv, B_e, vpr, (uint4*)Ks, (uint4*)Vs);
+                             (const uint4*)K, (const uint4*)V, hsv, sel, H_kv, B_e, vpr, T_len, (uint4*)Ks, (uint4*)Vs,
+                             hdr);
   count_launches(1);
   return e;
 }
