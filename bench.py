@@ -189,7 +189,9 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- the GPU arm
 
-def run_quoka(args, rank, world, local_rank):
+def run_quoka(args, rank, world, local_rank, light=False):
+    """One chunk of a WORKLOADS entry.  light: a sub-record of the suite (no end-to-end legs, the CPU
+    baseline on one KV group)."""
     from sparse_attention_chunked_gb300 import build as qbuild
     from sparse_attention_chunked_gb300 import quoka as q
 
@@ -355,86 +357,93 @@ def run_quoka(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         dense_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ts), dev)
 
-    # end to end through quoka_chunk_attend: every step's Q, K, V come from pinned host memory and
-    # its O goes back to it inside the timed region; the history is a device-resident cache (rotated
-    # over the input sets, so it is read from HBM).  Measured two ways: one step at a time on one
-    # stream, and as a serving loop where step k's compute overlaps step k+1's upload and step k-1's
-    # download (two device buffers, three streams).
-    Qh, Kch, Vch = x.Q.pin_memory(), x.K_chunk.pin_memory(), x.V_chunk.pin_memory()
-    Ohs = [torch.empty(O.shape, dtype=O.dtype).pin_memory() for _ in range(2)]
-    bufs = [(torch.empty_like(Q), torch.empty_like(Kc), torch.empty_like(Vc), torch.empty_like(O)) for _ in range(2)]
-    h2d = Qh.numel() * Qh.element_size() + 2 * Kch.numel() * Kch.element_size()
-    d2h = Ohs[0].numel() * Ohs[0].element_size()
+    def measure_e2e():
+        # end to end through quoka_chunk_attend: every step's Q, K, V come from pinned host memory and
+        # its O goes back to it inside the timed region; the history is a device-resident cache (rotated
+        # over the input sets, so it is read from HBM).  Measured two ways: one step at a time on one
+        # stream, and as a serving loop where step k's compute overlaps step k+1's upload and step k-1's
+        # download (two device buffers, three streams).
+        Qh, Kch, Vch = x.Q.pin_memory(), x.K_chunk.pin_memory(), x.V_chunk.pin_memory()
+        Ohs = [torch.empty(O.shape, dtype=O.dtype).pin_memory() for _ in range(2)]
+        bufs = [(torch.empty_like(Q), torch.empty_like(Kc), torch.empty_like(Vc), torch.empty_like(O)) for _ in range(2)]
+        h2d = Qh.numel() * Qh.element_size() + 2 * Kch.numel() * Kch.element_size()
+        d2h = Ohs[0].numel() * Ohs[0].element_size()
 
-    def attend_call(xs, Qd, Kcd, Vcd, Od, st):
-        if args.key_norm_cache:
-            q.quoka_chunk_attend_cached(shape, Qd, xs[1], xs[2], Kcd, Vcd, inv_sets[id(xs[1])], cfg.N_q, cfg.B, params,
-                                        Od, None, None, ws, st)
-        else:
-            q.quoka_chunk_attend(shape, Qd, xs[1], xs[2], Kcd, Vcd, cfg.N_q, cfg.B, params, Od, None, None, ws, st)
+        def attend_call(xs, Qd, Kcd, Vcd, Od, st):
+            if args.key_norm_cache:
+                q.quoka_chunk_attend_cached(shape, Qd, xs[1], xs[2], Kcd, Vcd, inv_sets[id(xs[1])], cfg.N_q, cfg.B, params,
+                                            Od, None, None, ws, st)
+            else:
+                q.quoka_chunk_attend(shape, Qd, xs[1], xs[2], Kcd, Vcd, cfg.N_q, cfg.B, params, Od, None, None, ws, st)
 
-    def e2e_serial_step(k):
-        Qd, Kcd, Vcd, Od = bufs[0]
-        Qd.copy_(Qh, non_blocking=True)
-        Kcd.copy_(Kch, non_blocking=True)
-        Vcd.copy_(Vch, non_blocking=True)
-        attend_call(sets[k % INPUT_SETS], Qd, Kcd, Vcd, Od, stream)
-        Ohs[0].copy_(Od, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for k in range(args.warmup):
-            e2e_serial_step(k)
-        torch.cuda.synchronize(dev)
-        e = new_events(2)
-        e[0].record(stream)
-        for k in range(args.steps):
-            e2e_serial_step(k)
-        e[1].record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_serial_ms = max_over_ranks(e[0].elapsed_time(e[1]) / args.steps, dev)
-
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    def e2e_pipelined(n):
-        ev_in = [torch.cuda.Event() for _ in range(n)]
-        ev_done = [torch.cuda.Event() for _ in range(n)]
-        ev_out = [torch.cuda.Event() for _ in range(n)]
-        for k in range(n):
-            b = k % 2
-            Qd, Kcd, Vcd, Od = bufs[b]
-            with torch.cuda.stream(up):
-                if k >= 2:
-                    up.wait_event(ev_done[k - 2])     # buffer b's inputs were consumed by step k-2
-                Qd.copy_(Qh, non_blocking=True)
-                Kcd.copy_(Kch, non_blocking=True)
-                Vcd.copy_(Vch, non_blocking=True)
-                ev_in[k].record(up)
-            stream.wait_event(ev_in[k])
-            if k >= 2:
-                stream.wait_event(ev_out[k - 2])      # buffer b's output was read back
+        def e2e_serial_step(k):
+            Qd, Kcd, Vcd, Od = bufs[0]
+            Qd.copy_(Qh, non_blocking=True)
+            Kcd.copy_(Kch, non_blocking=True)
+            Vcd.copy_(Vch, non_blocking=True)
             attend_call(sets[k % INPUT_SETS], Qd, Kcd, Vcd, Od, stream)
-            ev_done[k].record(stream)
-            with torch.cuda.stream(down):
-                down.wait_event(ev_done[k])
-                Ohs[b].copy_(Od, non_blocking=True)
-                ev_out[k].record(down)
-        return ev_out[n - 1]
+            Ohs[0].copy_(Od, non_blocking=True)
 
-    e2e_pipelined(args.warmup)
-    torch.cuda.synchronize(dev)
-    barrier()
-    torch.cuda.synchronize(dev)
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e_start.record(up)
-    stream.wait_event(e_start)
-    last = e2e_pipelined(args.steps)
-    down.wait_event(last)
-    e_end.record(down)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, dev)
-    Od2 = bufs[(args.steps - 1) % 2][3]
+        with torch.cuda.stream(stream):
+            for k in range(args.warmup):
+                e2e_serial_step(k)
+            torch.cuda.synchronize(dev)
+            e = new_events(2)
+            e[0].record(stream)
+            for k in range(args.steps):
+                e2e_serial_step(k)
+            e[1].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_serial_ms = max_over_ranks(e[0].elapsed_time(e[1]) / args.steps, dev)
+
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        def e2e_pipelined(n):
+            ev_in = [torch.cuda.Event() for _ in range(n)]
+            ev_done = [torch.cuda.Event() for _ in range(n)]
+            ev_out = [torch.cuda.Event() for _ in range(n)]
+            for k in range(n):
+                b = k % 2
+                Qd, Kcd, Vcd, Od = bufs[b]
+                with torch.cuda.stream(up):
+                    if k >= 2:
+                        up.wait_event(ev_done[k - 2])     # buffer b's inputs were consumed by step k-2
+                    Qd.copy_(Qh, non_blocking=True)
+                    Kcd.copy_(Kch, non_blocking=True)
+                    Vcd.copy_(Vch, non_blocking=True)
+                    ev_in[k].record(up)
+                stream.wait_event(ev_in[k])
+                if k >= 2:
+                    stream.wait_event(ev_out[k - 2])      # buffer b's output was read back
+                attend_call(sets[k % INPUT_SETS], Qd, Kcd, Vcd, Od, stream)
+                ev_done[k].record(stream)
+                with torch.cuda.stream(down):
+                    down.wait_event(ev_done[k])
+                    Ohs[b].copy_(Od, non_blocking=True)
+                    ev_out[k].record(down)
+            return ev_out[n - 1]
+
+        e2e_pipelined(args.warmup)
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+        e_start.record(up)
+        stream.wait_event(e_start)
+        last = e2e_pipelined(args.steps)
+        down.wait_event(last)
+        e_end.record(down)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, dev)
+        Od2 = bufs[(args.steps - 1) % 2][3]
+        assert torch.equal(Od2, O), "chunk_attend and the stage calls disagree"
+        return e2e_ms, e2e_serial_ms, h2d, d2h
+
+    e2e_ms = e2e_serial_ms = None
+    h2d = d2h = 0
+    if not light:
+        e2e_ms, e2e_serial_ms, h2d, d2h = measure_e2e()
     clocks = sampler.stop()
-    assert torch.equal(Od2, O), "chunk_attend and the stage calls disagree"
 
     if rank != 0:
         return None
@@ -510,20 +519,24 @@ def run_quoka(args, rank, world, local_rank):
         "dense": None if dense_ms is None else {
             "ms_per_step": round(dense_ms, 4), "speedup": round(dense_ms / step_ms, 2),
             "TFLOPs": round(dense_flops(cfg) / (dense_ms * 1e-3) / 1e12, 2)},
-        "e2e": {"value": round(cfg.C * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "mode": "serving loop: step k's compute overlaps step k+1's upload and step k-1's download "
-                        "(two device buffers, three streams); history cache rotated over the input sets",
-                "serial_ms_per_step": round(e2e_serial_ms, 4),
-                "serial_value": round(cfg.C * world / (e2e_serial_ms * 1e-3), 1)},
+        "e2e": None if e2e_ms is None else {
+            "value": round(cfg.C * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "mode": "serving loop: step k's compute overlaps step k+1's upload and step k-1's download "
+                    "(two device buffers, three streams); history cache rotated over the input sets",
+            "serial_ms_per_step": round(e2e_serial_ms, 4),
+            "serial_value": round(cfg.C * world / (e2e_serial_ms * 1e-3), 1)},
         "clocks": clocks,
     }
+    if light:
+        del res["e2e"]
     if not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, x, args.gqa, score_fn=args.score_fn, query_agg=args.query_agg)
+        res["cpu_baseline"] = cpu_baseline(cfg, x, args.gqa, groups=[0] if light else None, score_fn=args.score_fn,
+                                           query_agg=args.query_agg)
     return res
 
 
-def run_quoka_ragged(args, rank, world, local_rank):
+def run_quoka_ragged(args, rank, world, local_rank, light=False):
     """The ragged batch: one quoka_chunk_attend_varlen call per step over every sequence's chunk."""
     from sparse_attention_chunked_gb300 import build as qbuild
     from sparse_attention_chunked_gb300 import quoka as q
@@ -642,56 +655,60 @@ def run_quoka_ragged(args, rank, world, local_rank):
     att_ms = statistics.mean(a.elapsed_time(b) for a, b in att)
     dense_ms = statistics.mean(a.elapsed_time(b) for a, b in dense) if dense else None
 
-    # end to end: the packed chunk tensors come from pinned host memory, O goes back; a serving loop
-    # (step k's compute overlaps step k+1's upload and step k-1's download), as for one chunk
-    host = [pk[k].pin_memory() for k in ("Q", "K_chunk", "V_chunk")]
-    bufs = [[torch.empty_like(base[i]) for i in (0, 3, 4)] + [torch.empty_like(O)] for _ in range(2)]
-    Ohs = [torch.empty(O.shape, dtype=O.dtype).pin_memory() for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host)
-    d2h = Ohs[0].numel() * Ohs[0].element_size()
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    def measure_e2e():
+        # end to end: the packed chunk tensors come from pinned host memory, O goes back; a serving loop
+        # (step k's compute overlaps step k+1's upload and step k-1's download), as for one chunk
+        host = [pk[k].pin_memory() for k in ("Q", "K_chunk", "V_chunk")]
+        bufs = [[torch.empty_like(base[i]) for i in (0, 3, 4)] + [torch.empty_like(O)] for _ in range(2)]
+        Ohs = [torch.empty(O.shape, dtype=O.dtype).pin_memory() for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in host)
+        d2h = Ohs[0].numel() * Ohs[0].element_size()
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_pipelined(n):
-        ev_in = [torch.cuda.Event() for _ in range(n)]
-        ev_done = [torch.cuda.Event() for _ in range(n)]
-        ev_out = [torch.cuda.Event() for _ in range(n)]
-        for k in range(n):
-            b = k % 2
-            Qd, Kcd, Vcd, Od = bufs[b]
-            with torch.cuda.stream(up):
+        def e2e_pipelined(n):
+            ev_in = [torch.cuda.Event() for _ in range(n)]
+            ev_done = [torch.cuda.Event() for _ in range(n)]
+            ev_out = [torch.cuda.Event() for _ in range(n)]
+            for k in range(n):
+                b = k % 2
+                Qd, Kcd, Vcd, Od = bufs[b]
+                with torch.cuda.stream(up):
+                    if k >= 2:
+                        up.wait_event(ev_done[k - 2])
+                    for hd, dv in zip(host, (Qd, Kcd, Vcd)):
+                        dv.copy_(hd, non_blocking=True)
+                    ev_in[k].record(up)
+                stream.wait_event(ev_in[k])
                 if k >= 2:
-                    up.wait_event(ev_done[k - 2])
-                for hd, dv in zip(host, (Qd, Kcd, Vcd)):
-                    dv.copy_(hd, non_blocking=True)
-                ev_in[k].record(up)
-            stream.wait_event(ev_in[k])
-            if k >= 2:
-                stream.wait_event(ev_out[k - 2])
-            xs = sets[k % INPUT_SETS]
-            call((Qd, xs[1], xs[2], Kcd, Vcd), cfg.B, Od)
-            ev_done[k].record(stream)
-            with torch.cuda.stream(down):
-                down.wait_event(ev_done[k])
-                Ohs[b].copy_(Od, non_blocking=True)
-                ev_out[k].record(down)
-        return ev_out[n - 1]
+                    stream.wait_event(ev_out[k - 2])
+                xs = sets[k % INPUT_SETS]
+                call((Qd, xs[1], xs[2], Kcd, Vcd), cfg.B, Od)
+                ev_done[k].record(stream)
+                with torch.cuda.stream(down):
+                    down.wait_event(ev_done[k])
+                    Ohs[b].copy_(Od, non_blocking=True)
+                    ev_out[k].record(down)
+            return ev_out[n - 1]
 
-    e2e_pipelined(args.warmup)
-    torch.cuda.synchronize(dev)
-    barrier()
-    torch.cuda.synchronize(dev)
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e_start.record(up)
-    stream.wait_event(e_start)
-    last = e2e_pipelined(args.steps)
-    down.wait_event(last)
-    e_end.record(down)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, dev)
-    O2 = bufs[(args.steps - 1) % 2][3]
+        e2e_pipelined(args.warmup)
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+        e_start.record(up)
+        stream.wait_event(e_start)
+        last = e2e_pipelined(args.steps)
+        down.wait_event(last)
+        e_end.record(down)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, dev)
+        O2 = bufs[(args.steps - 1) % 2][3]
+        assert torch.equal(O2, O), "the end-to-end call and the timed steps disagree"
+        return e2e_ms, h2d, d2h
+
+    e2e_ms, h2d, d2h = (None, 0, 0) if light else measure_e2e()
     clocks = sampler.stop()
-    assert torch.equal(O2, O), "the end-to-end call and the timed steps disagree"
     if rank != 0:
         return None
     peaks = load_peaks()
@@ -726,14 +743,118 @@ def run_quoka_ragged(args, rank, world, local_rank):
         "attend_ms_per_batch": round(att_ms, 5),
         "dense": None if dense_ms is None else {"ms_per_step": round(dense_ms, 4),
                                                 "speedup": round(dense_ms / step_ms, 2)},
-        "e2e": {"value": round(tokens * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "mode": "serving loop: step k's compute overlaps step k+1's upload and step k-1's download "
-                        "(two device buffers, three streams); histories rotated over the input sets"},
+        "e2e": None if e2e_ms is None else {
+            "value": round(tokens * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "mode": "serving loop: step k's compute overlaps step k+1's upload and step k-1's download "
+                    "(two device buffers, three streams); histories rotated over the input sets"},
         "clocks": clocks,
     }
+    if light:
+        del res["e2e"]
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_ragged(cfg, seqs, args.gqa)
+    return res
+
+
+def run_sweep(args, rank, world, local_rank):
+    """The chunked-prefill sweep: one prompt of 65536 tokens in 32 chunks of 2048, each chunk scored,
+    selected and attended against the cache of every earlier chunk, then appended to it (with its key
+    norms, which the next chunks' scoring reads).  A step is the whole prompt; per-chunk times are
+    reported too.  The cache is preallocated for the whole prompt and filled in place."""
+    from sparse_attention_chunked_gb300 import build as qbuild
+    from sparse_attention_chunked_gb300 import quoka as q
+
+    qbuild.build()
+    q.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = wl.SWEEP_64K_BF16
+    sw = wl.make_sweep(cfg, args.seed)
+    K_all, V_all = sw.K_all.to(dev), sw.V_all.to(dev)
+    Kcache, Vcache = torch.zeros_like(K_all), torch.zeros_like(V_all)
+    inv = torch.zeros((cfg.H_kv, cfg.total), dtype=torch.float32, device=dev)   # key-norm cache
+    Qs = [t.to(dev) for t in sw.Q]
+    Kcs = [K_all[:, i * cfg.C:(i + 1) * cfg.C].contiguous() for i in range(cfg.n_chunks)]
+    Vcs = [V_all[:, i * cfg.C:(i + 1) * cfg.C].contiguous() for i in range(cfg.n_chunks)]
+    params = q.params_of(args.gqa, args.engine)
+    ws = q.make_workspace(q.shape_of(Qs[0], Kcache, T=cfg.total - cfg.C), cfg.N_q, cfg.total, params, device=dev)
+    O = torch.empty_like(Qs[0])
+    stream = torch.cuda.Stream(dev)
+
+    def chunk_fn(i, B):
+        shape = q.shape_of(Qs[i], Kcache, T=i * cfg.C)
+        q.quoka_chunk_attend_cached(shape, Qs[i], Kcache, Vcache, Kcs[i], Vcs[i], inv, cfg.N_q, B, params, O, None,
+                                    None, ws, stream)
+        q.quoka_append_kv_norms(shape, Kcache, Vcache, Kcs[i], Vcs[i], inv, stream)
+
+    def graphs_for(B):
+        gs, launches = [], 0
+        with torch.cuda.stream(stream):
+            for i in range(cfg.n_chunks):
+                chunk_fn(i, B)
+        torch.cuda.synchronize(dev)
+        for i in range(cfg.n_chunks):
+            g = torch.cuda.CUDAGraph()
+            before = q.quoka_launch_count()
+            with torch.cuda.graph(g, stream=stream):
+                chunk_fn(i, B)
+            launches += q.quoka_launch_count() - before
+            gs.append(g)
+        return gs, launches
+
+    def time_sweep(gs, reps):
+        per = [[] for _ in gs]
+        tot = []
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(gs) + 1)]
+                evs[0].record(stream)
+                for i, g in enumerate(gs):
+                    g.replay()
+                    evs[i + 1].record(stream)
+                torch.cuda.synchronize(dev)
+                for i in range(len(gs)):
+                    per[i].append(evs[i].elapsed_time(evs[i + 1]))
+                tot.append(evs[0].elapsed_time(evs[-1]))
+        return [statistics.mean(p) for p in per], statistics.mean(tot)
+
+    gs, launches = graphs_for(cfg.B)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        t_w = time.perf_counter()
+        while time.perf_counter() - t_w < 0.3:
+            for g in gs:
+                g.replay()
+        torch.cuda.synchronize(dev)
+    barrier()
+    reps = max(3, args.steps // 4)
+    per_ms, total_ms = time_sweep(gs, reps)
+    total_ms = max_over_ranks(total_ms, dev)
+    clocks = sampler.stop()
+    assert torch.equal(Kcache, K_all) and torch.equal(Vcache, V_all), "the sweep did not rebuild the cache"
+    assert q.quoka_get_last_device_error(ws, stream) == 0
+    dense_total = None
+    if not args.no_dense:   # a budget covering every history: dense chunked prefill of the same prompt
+        dgs, _ = graphs_for(cfg.total)
+        _, dense_total = time_sweep(dgs, max(2, reps // 2))
+    if rank != 0:
+        return None
+    res = {"workload": cfg.name, "gqa_pool": args.gqa, "n_chunks": cfg.n_chunks, "C": cfg.C, "N_q": cfg.N_q,
+           "B": cfg.B, "total_tokens": cfg.total,
+           "value": round(cfg.total * world / (total_ms * 1e-3), 1), "unit": "tokens/s",
+           "ms_total": round(total_ms, 4),
+           "ms_per_chunk": [round(x, 4) for x in per_ms],
+           "timing": f"each chunk (quoka_chunk_attend_cached + quoka_append_kv_norms) one CUDA graph; the 32 "
+                     f"graphs replayed in order, events between them, mean of {reps} sweeps; the cache grows to "
+                     f"{2 * K_all.numel() * 2 >> 20} MB, so later chunks read their history from HBM",
+           "gpu_launches_per_sweep": int(launches),
+           "dense": None if dense_total is None else {"ms_total": round(dense_total, 4),
+                                                      "speedup": round(dense_total / total_ms, 2)},
+           "clocks": clocks}
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_sweep(cfg, sw, args.gqa)
     return res
 
 
@@ -807,6 +928,26 @@ def cpu_baseline_ragged(cfg, seqs, gqa):
                                         f"({cfg.G} query heads each), {t:.1f} s measured, scaled x{cfg.H_kv}"}
 
 
+def cpu_baseline_sweep(cfg, sw, gqa, sample=(4, 12, 20, 28)):
+    """The oracle on KV group 0 of a few chunks of the sweep, spread over the prompt; the mean chunk
+    time, scaled by the chunk count and H_kv, stands for the whole sweep."""
+    from oracle import quoka_oracle as qo
+    G = cfg.H_q // cfg.H_kv
+    f = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    t = 0.0
+    for i in sample:
+        T = i * cfg.C
+        args = (f(sw.Q[i][:G]), f(sw.K_all[:1, :T]), f(sw.V_all[:1, :T]), f(sw.K_all[:1, T:T + cfg.C]),
+                f(sw.V_all[:1, T:T + cfg.C]))
+        t0 = time.perf_counter()
+        qo.chunk_attend(*args, cfg.N_q, cfg.B, gqa)
+        t += time.perf_counter() - t0
+    per_sweep = t / len(sample) * cfg.n_chunks * cfg.H_kv
+    return {"value": round(cfg.total / per_sweep, 2), "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"numpy float64 oracle, KV group 0 of chunks {list(sample)} ({G} query heads each), "
+                      f"{t:.1f} s measured, mean chunk x {cfg.n_chunks} chunks x {cfg.H_kv} groups"}
+
+
 def run_reference_ragged(args, rank, world):
     """The oracle on the ragged batch: each step is KV group (step mod H_kv) of every sequence, x H_kv."""
     if rank != 0:
@@ -848,16 +989,16 @@ def run_reference(args, rank, world):
     cfg = WORKLOADS[args.workload]
     x = wl.make_chunk(cfg, args.seed)
     from oracle import quoka_oracle as qo
+    inputs = [_oracle_inputs(x, g, cfg.G) for g in range(cfg.H_kv)]
     times = []
-    for k in range(args.warmup + args.steps):
-        g = k % cfg.H_kv
-        a = _oracle_inputs(x, g, cfg.G)
+    for k in range(args.warmup + args.steps):   # a step: the whole chunk, every KV group
         t0 = time.perf_counter()
-        qo.chunk_attend(*a, cfg.N_q, cfg.B, args.gqa, score_fn=args.score_fn, query_agg=args.query_agg)
+        for a in inputs:
+            qo.chunk_attend(*a, cfg.N_q, cfg.B, args.gqa, score_fn=args.score_fn, query_agg=args.query_agg)
         dt = time.perf_counter() - t0
         if k >= args.warmup:
             times.append(dt)
-    per_chunk = statistics.mean(times) * cfg.H_kv
+    per_chunk = statistics.mean(times)
     value = round(cfg.C / per_chunk, 2)
     return {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -869,10 +1010,36 @@ def run_reference(args, rank, world):
         "impl": "reference",
         "gpu_launches": 0,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
-                         "sample": f"each step: one of {cfg.H_kv} KV groups of the chunk through the numpy "
-                                   f"float64 oracle, scaled x{cfg.H_kv} to a whole chunk"},
+                         "sample": f"each step: the whole chunk (all {cfg.H_kv} KV groups) through the numpy "
+                                   f"float64 oracle on this host's cores (BLAS threads: {_blas_threads()})"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+# The other configurations, measured after the headline in the same run (each a sub-record of the
+# headline JSON line with its own step time, stages, roofline, dense reference and CPU sample).
+SUITE = (("gqa32k", "mean"), ("gqa128k", "max"), ("gqa128k", "mean"), ("sweep64k", "max"), ("ragged8", "max"))
+
+
+def run_suite(args, rank, world, local_rank):
+    import copy
+    out = {}
+    for workload, gqa in SUITE:
+        sub = copy.copy(args)
+        sub.workload, sub.gqa = workload, gqa
+        sub.steps = max(10, args.steps // 2)
+        if workload == "sweep64k":
+            r = run_sweep(sub, rank, world, local_rank)
+        elif workload in RAGGED:
+            r = run_quoka_ragged(sub, rank, world, local_rank, light=True)
+        else:
+            r = run_quoka(sub, rank, world, local_rank, light=True)
+        torch.cuda.empty_cache()
+        if r is not None:
+            for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data", "impl"):
+                r.pop(k, None)
+            out[f"{workload}_{gqa}"] = r
+    return out
 
 
 def main(argv=None):
@@ -881,7 +1048,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["quoka", "reference"], default="quoka")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(RAGGED), default="gqa32k")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(RAGGED) + ["sweep64k"], default="gqa32k")
     ap.add_argument("--gqa", choices=["max", "mean"], default="max")
     ap.add_argument("--engine", choices=["auto", "simt", "tensor"], default="auto")
     ap.add_argument("--score-fn", choices=["cos", "dot"], default="cos",
@@ -893,6 +1060,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-suite", action="store_true",
+                    help="only the headline line: skip the sub-records of the other configurations")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -901,8 +1070,15 @@ def main(argv=None):
         res = run_reference(args, rank, world)     # rank 0 alone; other ranks exit without work
     else:
         dist_init("nccl")
-        run = run_quoka_ragged if args.workload in RAGGED else run_quoka
-        res = run(args, rank, world, local_rank)
+        if args.workload == "sweep64k":
+            res = run_sweep(args, rank, world, local_rank)
+        else:
+            run = run_quoka_ragged if args.workload in RAGGED else run_quoka
+            res = run(args, rank, world, local_rank)
+            if not args.no_suite and args.workload == "gqa32k" and args.gqa == "max" and not variant_keys(args):
+                suite = run_suite(args, rank, world, local_rank)
+                if res is not None:
+                    res["suite"] = suite
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if torch.distributed.is_available() and torch.distributed.is_initialized():
