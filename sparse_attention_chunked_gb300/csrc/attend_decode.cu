@@ -68,7 +68,6 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
     const T* __restrict__ Q, const T* __restrict__ Kh, const T* __restrict__ Vh, int64_t h_stride,
     const int32_t* __restrict__ sel, int n_hist, int T_cache, const T* __restrict__ Kc, const T* __restrict__ Vc,
     int C, int G, float scale_log2, float* __restrict__ part_ml, float* __restrict__ part_o, WsHeader* hdr) {
-  pdl_launch_dependents();
   pdl_wait_for(Q, Kh, Vh, sel, Kc, Vc);
   constexpr int VEC = 16 / (int)sizeof(T);        // elements per 16-byte load
   constexpr int KP = D + VEC;                     // padded key row: conflict-free 16-byte reads across keys
@@ -189,6 +188,7 @@ __global__ void __launch_bounds__(kDecThreads) k_attend_decode(
       part_o[(((size_t)g * R + r) * n_blk + blk) * D + e] = o0 + o1;
     }
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 // One CTA per (group row): M = max_b m_b, w_b = 2^(m_b - M), L = sum_b l_b w_b,
@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(kMergeThreads) k_attend_decode_merge(const flo
                                                                        const float* __restrict__ part_o, int n_blk,
                                                                        int C, int G, T* __restrict__ O,
                                                                        float* __restrict__ lse) {
-  pdl_launch_dependents();
   pdl_wait_for(part_ml, part_o);
   extern __shared__ float w_s[];                 // [n_blk]
   __shared__ float red[kMergeThreads / 32];
@@ -255,6 +254,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_attend_decode_merge(const flo
     O[((size_t)h * C + c) * D + tid] = from_f32<T>(acc / L);
     if (lse != nullptr && tid == 0) lse[(size_t)h * C + c] = (M + log2f(L)) * 0.69314718055994531f;
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 size_t decode_smem(int d, int elt) {

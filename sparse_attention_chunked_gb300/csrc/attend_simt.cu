@@ -23,7 +23,6 @@ __global__ void __launch_bounds__(128) k_attend_simt(const T* __restrict__ Q, co
                                                      const T* __restrict__ Kc, const T* __restrict__ Vc, int C,
                                                      int G, float scale_log2, T* __restrict__ O,
                                                      float* __restrict__ lse) {
-  pdl_launch_dependents();
   pdl_wait_for(Q, Kh, Vh, Kc, Vc);
   constexpr int E = D / 32;
   constexpr int RPW = kAttRows / 4;   // rows per warp
@@ -104,6 +103,7 @@ __global__ void __launch_bounds__(128) k_attend_simt(const T* __restrict__ Q, co
     for (int e = 0; e < E; ++e) O[((size_t)h * C + c) * D + lane + 32 * e] = from_f32<T>(acc[i][e] * inv);
     if (lse != nullptr && lane == 0) lse[(size_t)h * C + c] = m[i] * 0.69314718055994531f + logf(l[i]);
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 template <typename T, int D>

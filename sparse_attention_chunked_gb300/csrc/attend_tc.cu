@@ -290,7 +290,6 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     tc::tmem_alloc(&sm->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
-  pdl_launch_dependents();
   if (threadIdx.x == 0 && cta < n_items) {
     // The first item's query tiles do not come from the previous kernel (the
     // kept K/V rows do): start them towards L2 while that kernel finishes.
@@ -475,6 +474,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 }  // namespace

@@ -22,9 +22,12 @@ __device__ __forceinline__ void record_error(WsHeader* hdr, unsigned int code, u
 }
 
 // Programmatic dependent launch.  Every kernel of the library is launched with
-// programmatic stream serialisation: it lets the next kernel in the stream
-// start launching right away and, before touching global memory, waits until
-// the kernels before it have completed (a no-op without the launch attribute).
+// programmatic stream serialisation and, before touching global memory, waits
+// until the kernels before it have completed (a no-op without the launch
+// attribute).  Each kernel releases its dependents only when a CTA has done
+// its work (the last statement of every kernel): released at the start, the
+// next kernels' CTAs sat resident and waiting on the SMs while this kernel
+// ran, and the whole step was 8% slower.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

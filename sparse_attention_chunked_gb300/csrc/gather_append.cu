@@ -16,7 +16,6 @@ namespace quoka {
 __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restrict__ V, int64_t head_stride_vec,
                               const int32_t* __restrict__ sel, int H_kv, int B_e, int vec_per_row, int T_len,
                               uint4* __restrict__ Ks, uint4* __restrict__ Vs, WsHeader* hdr) {
-  pdl_launch_dependents();
   pdl_wait_for(K, V, sel);
   const size_t per_mat = (size_t)H_kv * B_e * vec_per_row;
   for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < per_mat; w += (size_t)gridDim.x * blockDim.x) {
@@ -34,13 +33,13 @@ __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restri
     Ks[w] = k;
     Vs[w] = x;
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 // K_hist[g, T + c] = K_chunk[g, c] and likewise V.
 __global__ void k_append_rows(uint4* __restrict__ K, uint4* __restrict__ V, int64_t head_stride_vec, int T_len,
                               const uint4* __restrict__ Kc, const uint4* __restrict__ Vc, int H_kv, int C,
                               int vec_per_row) {
-  pdl_launch_dependents();
   pdl_wait_for(Kc, Vc);
   const size_t per_mat = (size_t)H_kv * C * vec_per_row;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < 2 * per_mat;
@@ -53,6 +52,7 @@ __global__ void k_append_rows(uint4* __restrict__ K, uint4* __restrict__ V, int6
     uint4* dst = (is_v ? V : K) + (size_t)g * head_stride_vec + (size_t)(T_len + c) * vec_per_row + v;
     *dst = (is_v ? Vc : Kc)[w];
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 // Key-norm cache: inv[g * inv_stride + t] = 1 / max(|K[g, t]|, eps) for
@@ -61,7 +61,6 @@ __global__ void k_append_rows(uint4* __restrict__ K, uint4* __restrict__ V, int6
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_key_inv_norms(const T* __restrict__ K, int64_t head_stride, int t0, int t1,
                                                        int H_kv, float* __restrict__ inv, int64_t inv_stride) {
-  pdl_launch_dependents();
   pdl_wait_for(K);
   constexpr int E = D / 32;
   const int n = t1 - t0;
@@ -80,6 +79,7 @@ __global__ void __launch_bounds__(256) k_key_inv_norms(const T* __restrict__ K, 
     ss = warp_sum(ss);
     if (lane == 0) inv[(size_t)g * inv_stride + t] = 1.0f / fmaxf(sqrtf(ss), kNormEps);
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 static int grid_for(size_t work) {

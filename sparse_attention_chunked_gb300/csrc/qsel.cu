@@ -196,7 +196,6 @@ template <typename T, int D>
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
     k_qselect_fused(const T* __restrict__ Q, int C, int G_avg, int n_sel, int per, int sel_p,
                     int32_t* __restrict__ q_idx, WsHeader* hdr) {
-  pdl_launch_dependents();
   constexpr int E = D / 32;
   extern __shared__ __align__(1024) uint8_t dsm_raw[];
   T* rows_s = reinterpret_cast<T*>(dsm_raw);                                 // staged rows of a piece
@@ -378,12 +377,12 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
                                       tk);
     }
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_qstats(const T* __restrict__ Q, int C, float* __restrict__ qnorm,
                                                 float* __restrict__ qpart) {
-  pdl_launch_dependents();
   pdl_wait_for(Q);
   constexpr int E = D / 32;
   const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
@@ -423,12 +422,12 @@ __global__ void __launch_bounds__(256) k_qstats(const T* __restrict__ Q, int C, 
     for (int w = 0; w < 8; ++w) s += sp[w][threadIdx.x];
     qpart[((size_t)h * nblk + blk) * D + threadIdx.x] = s;
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, const float* __restrict__ qpart,
                                               const float* __restrict__ qnorm, float* __restrict__ qcos) {
-  pdl_launch_dependents();
   pdl_wait_for(Q, qpart, qnorm);
   constexpr int E = D / 32;
   const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
@@ -473,11 +472,11 @@ __global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, co
     const int c = c0 + lane;
     qcos[(size_t)h * C + c] = v / (fmaxf(qnorm[(size_t)h * C + c], kNormEps) * mnorm);
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 __global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos, int C, int G_avg, int n_sel,
                                                   int32_t* __restrict__ q_idx) {
-  pdl_launch_dependents();
   pdl_wait_for(qcos);
   extern __shared__ __align__(16) uint32_t keys_s[];
   __shared__ RadixSelectShared rs;
@@ -495,6 +494,7 @@ __global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos,
   }
   __syncthreads();
   block_radix_topk4(reinterpret_cast<const uint4*>(keys_s), C, n_sel, q_idx + (size_t)row * n_sel, rs);
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 // The one-launch kernel's parameters: slice length per CTA, list length

@@ -38,7 +38,6 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
                                                                  __nv_bfloat16* __restrict__ op_bf,
                                                                  float* __restrict__ op_scale,
                                                                  unsigned* __restrict__ hist) {
-  pdl_launch_dependents();
   pdl_wait_for(Q, q_idx);
   if (hist != nullptr && blockIdx.x == 0)   // the scorer that follows accumulates into it
     for (int b = threadIdx.x; b < kScoreHistBins; b += blockDim.x) hist[(size_t)blockIdx.y * kScoreHistBins + b] = 0;
@@ -115,6 +114,7 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
 #pragma unroll
     for (int j = 0; j < E; ++j) op_f32[((size_t)g * R + r) * D + lane + 32 * j] = acc[j];
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 // One thread per history key: its row is held in registers, the scoring rows
@@ -123,7 +123,6 @@ template <typename T, int D>
 __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int64_t head_stride, int T_len,
                                                     const float* __restrict__ op_f32, int R, KeyScale ks,
                                                     float* __restrict__ scores, unsigned* __restrict__ hist) {
-  pdl_launch_dependents();
   pdl_wait_for(K, op_f32);
   const int g = blockIdx.y;
   const int t = blockIdx.x * 128 + threadIdx.x;
@@ -177,6 +176,7 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
   if (t < T_len) scores[(size_t)g * T_len + t] = best * rk;
   if (hist != nullptr)   // the first digit of the top-B select, straight into the head's histogram
     hist12_add(hist + (size_t)g * kScoreHistBins, order_key(best * rk), t < T_len);
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 // Few scoring rows (R <= 8, e.g. a decode step's G unit queries): LPK lanes
@@ -198,7 +198,6 @@ __global__ void __launch_bounds__(256) k_score_rows(const T* __restrict__ K, int
   constexpr int U = 4;                                // slots per warp
   constexpr int KPB = 8 * KPW * U;                    // keys per block
   static_assert(NCH % LPK == 0, "LPK must divide the chunks of a row");
-  pdl_launch_dependents();
   pdl_wait_for(K, op_f32);   // the scoring rows come from the previous kernel
   const int g = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -267,6 +266,7 @@ __global__ void __launch_bounds__(256) k_score_rows(const T* __restrict__ K, int
     if (sub == 0 && valid) scores[(size_t)g * T_len + t] = sc;
     if (hist != nullptr) hist12_add(hist + (size_t)g * kScoreHistBins, order_key(sc), sub == 0 && valid);
   }
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,

@@ -214,7 +214,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     tc::tmem_alloc(&sm->tmem_base, tmem_cols);
     tc::tmem_relinquish();
   }
-  pdl_launch_dependents();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -428,6 +427,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (hist != nullptr)   // this CTA's share of the head's histogram
     for (int b = threadIdx.x; b < kScoreHistBins; b += blockDim.x)
       if (hist_s[b] != 0) atomicAdd(&hist[(size_t)g * kScoreHistBins + b], hist_s[b]);
+  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 template <int D, int MODE>
