@@ -197,7 +197,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
       tc::mbar_init(&sm->kv_full[s], 1);
-      tc::mbar_init(&sm->kv_empty[s], 1 + (nch == 1 ? 4 : 8));   // the MMAs + the warps reading |k|^2
+      // the MMAs, plus the epilogue warps when they read |k|^2 from the stage
+      tc::mbar_init(&sm->kv_empty[s], 1 + (ks.key_norm && ks.k_inv == nullptr ? (nch == 1 ? 4 : 8) : 0));
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&sm->acc_full[a], 1);
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       float rk = 1.f;
       if (ks.key_norm && ks.k_inv != nullptr)      // the key-norm cache: one load, issued early
         rk = t < T_len ? ks.k_inv[(size_t)g * ks.k_inv_stride + t] : 0.f;
-      if (alive) alive = warp_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105);
+      if (alive && norm_from_keys) alive = warp_wait(&sm->kv_full[s], (it / nst) & 1, abort, hdr, 0x105);
       float ss[4] = {0.f, 0.f, 0.f, 0.f};
       if (alive && norm_from_keys) {
         const uint8_t* stage = ktiles + (size_t)s * kStageBytes;
@@ -348,8 +349,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
           ss[i] = s0 + s1;
         }
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm->kv_empty[s]);
+      if (norm_from_keys) {   // done with the key stage
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm->kv_empty[s]);
+      }
       const int q = it * nch + chunk;
       float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (alive) alive = warp_wait(&sm->acc_full[grp], (q >> 1) & 1, abort, hdr, 0x106);
