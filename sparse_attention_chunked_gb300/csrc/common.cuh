@@ -24,10 +24,11 @@ __device__ __forceinline__ void record_error(WsHeader* hdr, unsigned int code, u
 // Programmatic dependent launch.  Every kernel of the library is launched with
 // programmatic stream serialisation and, before touching global memory, waits
 // until the kernels before it have completed (a no-op without the launch
-// attribute).  Each kernel releases its dependents only when a CTA has done
-// its work (the last statement of every kernel): released at the start, the
-// next kernels' CTAs sat resident and waiting on the SMs while this kernel
-// ran, and the whole step was 8% slower.
+// attribute).  A kernel releases its dependents either at its start (short or
+// SM-filling kernels, so that the next kernel's launch and prologue overlap
+// it) or as its last statement; never two in a row at the start, which would
+// launch a whole chain of kernels whose CTAs then sit waiting on the SMs
+// (released at the start everywhere, the step was 8% slower).
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -16,6 +16,7 @@ namespace quoka {
 __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restrict__ V, int64_t head_stride_vec,
                               const int32_t* __restrict__ sel, int H_kv, int B_e, int vec_per_row, int T_len,
                               uint4* __restrict__ Ks, uint4* __restrict__ Vs, WsHeader* hdr) {
+  pdl_launch_dependents();   // early: the attention's prologue overlaps this copy
   pdl_wait_for(K, V, sel);
   const size_t per_mat = (size_t)H_kv * B_e * vec_per_row;
   for (size_t w = blockIdx.x * (size_t)blockDim.x + threadIdx.x; w < per_mat; w += (size_t)gridDim.x * blockDim.x) {
@@ -33,7 +34,6 @@ __global__ void k_gather_rows(const uint4* __restrict__ K, const uint4* __restri
     Ks[w] = k;
     Vs[w] = x;
   }
-  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 // K_hist[g, T + c] = K_chunk[g, c] and likewise V.

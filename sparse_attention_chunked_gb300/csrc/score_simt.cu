@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
                                                                  __nv_bfloat16* __restrict__ op_bf,
                                                                  float* __restrict__ op_scale,
                                                                  unsigned* __restrict__ hist) {
+  pdl_launch_dependents();   // early: the scorer's prologue overlaps this short kernel
   pdl_wait_for(Q, q_idx);
   if (hist != nullptr && blockIdx.x == 0)   // the scorer that follows accumulates into it
     for (int b = threadIdx.x; b < kScoreHistBins; b += blockDim.x) hist[(size_t)blockIdx.y * kScoreHistBins + b] = 0;
@@ -114,7 +115,6 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
 #pragma unroll
     for (int j = 0; j < E; ++j) op_f32[((size_t)g * R + r) * D + lane + 32 * j] = acc[j];
   }
-  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 // One thread per history key: its row is held in registers, the scoring rows

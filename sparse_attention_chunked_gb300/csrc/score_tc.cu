@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                const float* __restrict__ op_scale, int T_len, int N_pad, int nst, int nch, int cw,
                uint32_t tmem_cols, KeyScale ks, float* __restrict__ scores, unsigned* __restrict__ hist,
                WsHeader* hdr) {
+  pdl_launch_dependents();   // early: the top-B CTAs take SMs as this kernel's CTAs finish
   constexpr int HALVES = D / 64;
   constexpr bool SCALED = MODE == kScaled;
   constexpr int NPASS = SCALED ? 1 : 2;          // operand rows per scoring row
@@ -430,7 +431,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   if (hist != nullptr)   // this CTA's share of the head's histogram
     for (int b = threadIdx.x; b < kScoreHistBins; b += blockDim.x)
       if (hist_s[b] != 0) atomicAdd(&hist[(size_t)g * kScoreHistBins + b], hist_s[b]);
-  pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
 template <int D, int MODE>

@@ -23,6 +23,8 @@
 // from global memory, where they are L2-resident after the scoring kernel).
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "cluster_topk.cuh"
@@ -313,7 +315,10 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
     return e;
   }
   const int per = ((T_len + kTopkCluster - 1) / kTopkCluster + 3) & ~3;
-  const size_t fused_smem = (size_t)per * 4 + (size_t)kScoreHistBins * 4 + (size_t)kCandCap * 8;
+  // at least 120 KB: one CTA per SM (two sharing an SM, as they do when they take SMs while the
+  // scorer's CTAs finish, were 40% slower)
+  const size_t fused_smem = std::max<size_t>((size_t)per * 4 + (size_t)kScoreHistBins * 4 + (size_t)kCandCap * 8,
+                                             120 * 1024);
   cudaError_t e;
   if (hist != nullptr && fused_smem <= 200 * 1024) {
     if ((e = ensure_smem((const void*)k_topk_fused, fused_smem)) != cudaSuccess) return e;
