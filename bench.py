@@ -209,22 +209,10 @@ def run_quoka(args, rank, world, local_rank, light=False):
     n = min(cfg.N_q, cfg.C)
     H_sel = cfg.H_q if args.gqa == "max" else cfg.H_kv
     B_e = min(cfg.B, cfg.T)
-    q_idx = torch.empty((H_sel, n), dtype=torch.int32, device=dev)
-    scores = torch.empty((cfg.H_kv, cfg.T), dtype=torch.float32, device=dev)
-    sel = torch.empty((cfg.H_kv, B_e), dtype=torch.int32, device=dev)
-    Ks = torch.empty((cfg.H_kv, B_e, cfg.d), dtype=Q.dtype, device=dev)
-    Vs = torch.empty_like(Ks)
     O = torch.empty_like(Q)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
     names = ["select", "score", "topk", "gather", "attend"]
-    stage_fns = [
-        lambda: q.quoka_select_queries(shape, Q, cfg.N_q, params, q_idx, ws, stream),
-        lambda: q.quoka_score_keys(shape, Q, q_idx, cfg.N_q, Kh, params, scores, ws, stream),
-        lambda: q.quoka_topk(shape, scores, cfg.B, sel, ws, stream),
-        lambda: q.quoka_gather(shape, Kh, Vh, sel, B_e, Ks, Vs, stream),
-        lambda: q.quoka_sparse_attend(shape, Q, Ks, Vs, B_e, Kc, Vc, params, O, None, ws, stream),
-    ]
 
     def new_events(k):
         return [torch.cuda.Event(enable_timing=True) for _ in range(k)]
@@ -234,6 +222,26 @@ def run_quoka(args, rank, world, local_rank, light=False):
     # hundred MB of traffic) earlier, i.e. from HBM, without a flush kernel.
     sets = [(Q, Kh, Vh, Kc, Vc)] + [tuple(t.clone() for t in (Q, Kh, Vh, Kc, Vc)) for _ in range(INPUT_SETS - 1)]
     set_bytes = sum(t.numel() * t.element_size() for t in sets[0])
+    # each input set's own stage intermediates, for the stage-by-stage breakdown
+    inter = [{"q_idx": torch.empty((H_sel, n), dtype=torch.int32, device=dev),
+              "scores": torch.empty((cfg.H_kv, cfg.T), dtype=torch.float32, device=dev),
+              "sel": torch.empty((cfg.H_kv, B_e), dtype=torch.int32, device=dev),
+              "Ks": torch.empty((cfg.H_kv, B_e, cfg.d), dtype=Q.dtype, device=dev),
+              "Vs": torch.empty((cfg.H_kv, B_e, cfg.d), dtype=Q.dtype, device=dev)} for _ in sets]
+
+    def stage_call(i, si):
+        Qx, Khx, Vhx, Kcx, Vcx = sets[si]
+        t = inter[si]
+        if i == 0:
+            q.quoka_select_queries(shape, Qx, cfg.N_q, params, t["q_idx"], ws, stream)
+        elif i == 1:
+            q.quoka_score_keys(shape, Qx, t["q_idx"], cfg.N_q, Khx, params, t["scores"], ws, stream)
+        elif i == 2:
+            q.quoka_topk(shape, t["scores"], cfg.B, t["sel"], ws, stream)
+        elif i == 3:
+            q.quoka_gather(shape, Khx, Vhx, t["sel"], B_e, t["Ks"], t["Vs"], stream)
+        else:
+            q.quoka_sparse_attend(shape, Qx, t["Ks"], t["Vs"], B_e, Kcx, Vcx, params, O, None, ws, stream)
 
     # the key-norm cache of every input set, as quoka_append_kv_norms would have left it when the
     # history was appended (built once, outside the timed region)
@@ -245,65 +253,52 @@ def run_quoka(args, rank, world, local_rank, light=False):
             inv_sets[id(xs[1])] = inv
         torch.cuda.synchronize(dev)
 
-    def step_fns(Qx, Khx, Vhx, Kcx, Vcx):
-        # the step: one quoka_chunk_attend (every stage of the path; top-B and the
-        # gather share one launch there)
+    def step_call(si):
+        # the step: one quoka_chunk_attend (every stage of the path)
+        Qx, Khx, Vhx, Kcx, Vcx = sets[si]
         if args.key_norm_cache:
-            inv = inv_sets[id(Khx)]
-            return [lambda: q.quoka_chunk_attend_cached(shape, Qx, Khx, Vhx, Kcx, Vcx, inv, cfg.N_q, cfg.B, params, O,
-                                                        None, None, ws, stream)]
-        return [lambda: q.quoka_chunk_attend(shape, Qx, Khx, Vhx, Kcx, Vcx, cfg.N_q, cfg.B, params, O, None, None, ws,
-                                             stream)]
+            q.quoka_chunk_attend_cached(shape, Qx, Khx, Vhx, Kcx, Vcx, inv_sets[id(Khx)], cfg.N_q, cfg.B, params, O,
+                                        None, None, ws, stream)
+        else:
+            q.quoka_chunk_attend(shape, Qx, Khx, Vhx, Kcx, Vcx, cfg.N_q, cfg.B, params, O, None, None, ws, stream)
 
-    # Each stage is captured once into its own CUDA graph (the library only
-    # enqueues kernels, so a captured call replays the identical launches); a
-    # step replays the five graphs back to back with events between them.
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            for fn in stage_fns:
-                fn()
+    def capture(calls):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls:
+                c()
+        return g
+
+    with torch.cuda.stream(stream):   # every call once per set (fills the intermediates, sets up the kernels)
+        for si in range(INPUT_SETS):
+            for i in range(len(names)):
+                stage_call(i, si)
+            step_call(si)
     torch.cuda.synchronize(dev)
-    graphs = []
-    for fn in stage_fns:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            fn()
-        graphs.append(g)
-    # the whole step as one graph per input set: consecutive kernels overlap launch
-    # and prologue (programmatic dependent launch); these are the timed steps
-    step_graphs = []
-    for si, xs in enumerate(sets):
-        g = torch.cuda.CUDAGraph()
-        launches_before = q.quoka_launch_count()
-        with torch.cuda.graph(g, stream=stream):
-            for fn in step_fns(*xs):
-                fn()
-        if si == 0:
-            launches_per_step = q.quoka_launch_count() - launches_before
-        step_graphs.append(g)
-    step_graph = step_graphs[0]
-
-    def staged(evs):
-        evs[0].record(stream)
-        for i, g in enumerate(graphs):
-            g.replay()
-            evs[i + 1].record(stream)
+    # The timed steps: K consecutive steps, rotating over the input sets, captured as ONE graph (the
+    # library only enqueues kernels, so a captured call replays the identical launches; consecutive
+    # kernels overlap launch and prologue through programmatic dependent launch).  Warm-up: W steps.
+    before = q.quoka_launch_count()
+    step_graph_k = capture([(lambda si=k % INPUT_SETS: step_call(si)) for k in range(args.steps)])
+    launches_per_step = (q.quoka_launch_count() - before) // args.steps
+    warm_graph = capture([(lambda si=k % INPUT_SETS: step_call(si)) for k in range(args.warmup)])
+    one_step = capture([lambda: step_call(0)])
+    # Stage breakdown: each stage call R times back to back on the rotating input sets, one graph each.
+    R = max(args.steps, 2 * INPUT_SETS)
+    stage_graphs = [capture([(lambda i=i, si=k % INPUT_SETS: stage_call(i, si)) for k in range(R)])
+                    for i in range(len(names))]
 
     sampler = ClockSampler(local_rank)
     sampler.start()
     with torch.cuda.stream(stream):
         t_w = time.perf_counter()
         done = 0
-        while done < args.warmup or time.perf_counter() - t_w < 0.5:   # also gives the clock sampler a lead-in
-            for g in step_graphs:
+        while done < 1 or time.perf_counter() - t_w < 0.5:   # W warm-up steps; also the clock sampler's lead-in
+            warm_graph.replay()
+            for g in stage_graphs:
                 g.replay()
-            flush.zero_()
-            step_graph.replay()
-            flush.zero_()
-            staged(new_events(6))
             done += 1
-            if done % 50 == 0:
-                torch.cuda.synchronize(dev)
+        warm_graph.replay()
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
@@ -311,32 +306,34 @@ def run_quoka(args, rank, world, local_rank, light=False):
         e_rot = new_events(2)               # the headline: K steps back to back, rotating input sets
         torch.cuda.nvtx.range_push("timed_steps")   # lets a profiler select exactly these launches
         e_rot[0].record(stream)
-        for k in range(args.steps):
-            step_graphs[k % INPUT_SETS].replay()
+        step_graph_k.replay()
         e_rot[1].record(stream)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(dev)
         barrier()
         wall = time.perf_counter() - wall0
-        step_evs, all_evs = [], []
-        for _ in range(args.steps):
+        stage_ms = {}
+        for i, nm in enumerate(names):
+            e = new_events(2)
+            e[0].record(stream)
+            stage_graphs[i].replay()
+            e[1].record(stream)
+            torch.cuda.synchronize(dev)
+            stage_ms[nm] = [e[0].elapsed_time(e[1]) / R]
+        step_evs = []
+        for _ in range(max(3, args.steps // 4)):
             flush.zero_()                   # L2 written over before this replay (outside the events)
             e = new_events(2)
             e[0].record(stream)
-            step_graph.replay()
+            one_step.replay()
             e[1].record(stream)
             step_evs.append(e)
-            flush.zero_()
-            evs = new_events(6)             # the same step stage by stage, for the per-stage breakdown
-            staged(evs)
-            all_evs.append(evs)
         torch.cuda.synchronize(dev)
     launches = launches_per_step * args.steps
     assert q.quoka_get_last_device_error(ws, stream) == 0
-    stage_ms = {nm: [e[i].elapsed_time(e[i + 1]) for e in all_evs] for i, nm in enumerate(names)}
     step_ms = max_over_ranks(e_rot[0].elapsed_time(e_rot[1]) / args.steps, dev)
     flush_step_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in step_evs), dev)
-    staged_ms = statistics.mean(e[0].elapsed_time(e[5]) for e in all_evs)
+    staged_ms = sum(v[0] for v in stage_ms.values())
 
     # dense full-history attention on the same chunk: the speedup reference
     dense_ms = None
@@ -501,8 +498,11 @@ def run_quoka(args, rank, world, local_rank, light=False):
                    "l2": f"inputs larger than L2: the timed steps rotate over {INPUT_SETS} copies of the inputs "
                          f"({INPUT_SETS * set_bytes / 2**20:.0f} MB), no flush; l2_write_flush: the same step after "
                          f"a {L2_FLUSH_BYTES >> 20} MB write",
-                   "timing": "step = one CUDA graph of one quoka_chunk_attend call, K steps timed back to back; "
-                             "the five stage calls replayed one graph each (after a flush) for the breakdown",
+                   "timing": "K consecutive quoka_chunk_attend calls (rotating input sets) captured as one CUDA graph, "
+                             "timed with events around its replay; stages: each stage's C-ABI call "
+                             f"{max(args.steps, 2 * INPUT_SETS)} times back to back on the rotating sets (the "
+                             "separate quoka_topk call does not start from the scorer's histogram as the fused "
+                             "step's select does)",
                    "parallelism": f"replicas x{world}"},
         "impl": "quoka",
         "gpu_launches": int(launches),
@@ -573,15 +573,17 @@ def run_quoka_ragged(args, rank, world, local_rank, light=False):
         call(base, cfg.B, O, sel)       # also leaves every sequence's kept set in sel
         call(base, cfg.B, O)
     torch.cuda.synchronize(dev)
-    step_graphs = []
-    for si, xs in enumerate(sets):
+    # K consecutive batches (rotating input sets) as one graph, and W for the warm-up
+    def k_graph(k_steps):
         g = torch.cuda.CUDAGraph()
-        before = q.quoka_launch_count()
         with torch.cuda.graph(g, stream=stream):
-            call(xs, cfg.B, O)
-        if si == 0:
-            launches_per_step = q.quoka_launch_count() - before
-        step_graphs.append(g)
+            for k in range(k_steps):
+                call(sets[k % INPUT_SETS], cfg.B, O)
+        return g
+    before = q.quoka_launch_count()
+    step_graph_k = k_graph(args.steps)
+    launches_per_step = (q.quoka_launch_count() - before) // args.steps
+    warm_graph = k_graph(args.warmup)
     # the attention stage alone over the batch (kept rows gathered once up front), for the roofline
     att_fns, att_flops, off = [], 0, 0
     for s, x in enumerate(seqs):
@@ -613,31 +615,30 @@ def run_quoka_ragged(args, rank, world, local_rank, light=False):
     with torch.cuda.stream(stream):
         t_w = time.perf_counter()
         done = 0
-        while done < args.warmup or time.perf_counter() - t_w < 0.5:
-            for g in step_graphs:
-                g.replay()
+        while done < 1 or time.perf_counter() - t_w < 0.5:
+            warm_graph.replay()
             att_graph.replay()
             done += 1
+        warm_graph.replay()
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
         e_rot = new_events(2)
         torch.cuda.nvtx.range_push("timed_steps")
         e_rot[0].record(stream)
-        for k in range(args.steps):
-            step_graphs[k % INPUT_SETS].replay()
+        step_graph_k.replay()
         e_rot[1].record(stream)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(dev)
         barrier()
-        att = []
-        for _ in range(max(3, args.steps // 2)):
-            flush.zero_()
-            e = new_events(2)
-            e[0].record(stream)
+        att = []                        # the attention stage: back-to-back replays
+        n_att = max(3, args.steps // 2)
+        e = new_events(2)
+        e[0].record(stream)
+        for _ in range(n_att):
             att_graph.replay()
-            e[1].record(stream)
-            att.append(e)
+        e[1].record(stream)
+        att.append(e)
         dense = []
         Od = torch.empty_like(O)
         if not args.no_dense:
@@ -652,7 +653,7 @@ def run_quoka_ragged(args, rank, world, local_rank, light=False):
         torch.cuda.synchronize(dev)
     assert q.quoka_get_last_device_error(ws, stream) == 0
     step_ms = max_over_ranks(e_rot[0].elapsed_time(e_rot[1]) / args.steps, dev)
-    att_ms = statistics.mean(a.elapsed_time(b) for a, b in att)
+    att_ms = statistics.mean(a.elapsed_time(b) for a, b in att) / n_att
     dense_ms = statistics.mean(a.elapsed_time(b) for a, b in dense) if dense else None
 
     def measure_e2e():
@@ -732,7 +733,8 @@ def run_quoka_ragged(args, rank, world, local_rank, light=False):
                    "gqa_pool": args.gqa, "engine": args.engine, **variant_keys(args),
                    "l2": f"inputs larger than L2: the timed steps rotate over {INPUT_SETS} copies of the packed "
                          f"inputs ({INPUT_SETS * set_bytes / 2**20:.0f} MB), no flush",
-                   "timing": "step = one CUDA graph of one quoka_chunk_attend_varlen call, K steps back to back",
+                   "timing": "K consecutive quoka_chunk_attend_varlen calls (rotating input sets) captured as one "
+                             "CUDA graph, timed with events around its replay",
                    "parallelism": f"replicas x{world}"},
         "impl": "quoka",
         "gpu_launches": int(launches_per_step * args.steps),
@@ -820,6 +822,10 @@ def run_sweep(args, rank, world, local_rank):
         return [statistics.mean(p) for p in per], statistics.mean(tot)
 
     gs, launches = graphs_for(cfg.B)
+    whole = torch.cuda.CUDAGraph()        # the whole prompt as one graph: the total time
+    with torch.cuda.graph(whole, stream=stream):
+        for i in range(cfg.n_chunks):
+            chunk_fn(i, cfg.B)
     sampler = ClockSampler(local_rank)
     sampler.start()
     with torch.cuda.stream(stream):
@@ -830,8 +836,15 @@ def run_sweep(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     barrier()
     reps = max(3, args.steps // 4)
-    per_ms, total_ms = time_sweep(gs, reps)
-    total_ms = max_over_ranks(total_ms, dev)
+    per_ms, _ = time_sweep(gs, reps)
+    with torch.cuda.stream(stream):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        for _ in range(reps):
+            whole.replay()
+        e[1].record(stream)
+        torch.cuda.synchronize(dev)
+    total_ms = max_over_ranks(e[0].elapsed_time(e[1]) / reps, dev)
     clocks = sampler.stop()
     assert torch.equal(Kcache, K_all) and torch.equal(Vcache, V_all), "the sweep did not rebuild the cache"
     assert q.quoka_get_last_device_error(ws, stream) == 0
@@ -846,9 +859,10 @@ def run_sweep(args, rank, world, local_rank):
            "value": round(cfg.total * world / (total_ms * 1e-3), 1), "unit": "tokens/s",
            "ms_total": round(total_ms, 4),
            "ms_per_chunk": [round(x, 4) for x in per_ms],
-           "timing": f"each chunk (quoka_chunk_attend_cached + quoka_append_kv_norms) one CUDA graph; the 32 "
-                     f"graphs replayed in order, events between them, mean of {reps} sweeps; the cache grows to "
-                     f"{2 * K_all.numel() * 2 >> 20} MB, so later chunks read their history from HBM",
+           "timing": f"total: the 32 chunks (quoka_chunk_attend_cached + quoka_append_kv_norms each) as one CUDA "
+                     f"graph, mean of {reps} replays; per chunk: one graph per chunk, replayed in order with events "
+                     f"between them; the cache grows to {2 * K_all.numel() * 2 >> 20} MB, so later chunks read "
+                     f"their history from HBM",
            "gpu_launches_per_sweep": int(launches),
            "dense": None if dense_total is None else {"ms_total": round(dense_total, 4),
                                                       "speedup": round(dense_total / total_ms, 2)},
