@@ -3,24 +3,16 @@
 //
 // A thread-block cluster of 8 CTAs per KV head selects on the
 // order-preserving 32-bit keys of the scores; CTA r of the cluster owns the
-// r-th contiguous eighth of the head's keys and caches them in shared memory.
+// r-th contiguous eighth of the head's keys.
 //
 // In the fused chunk path the scoring kernel has already counted the top 12
-// bits of every key (hist), and k_topk_fused needs two cluster barriers:
-// every CTA finds the 12-bit bin b* that holds the B-th largest key, keeps the
-// keys above it and lists its keys inside it (the candidates); CTA 0 gathers
-// the candidates of the whole cluster over distributed shared memory, finds
-// the exact threshold among them in two 10-bit radix passes, and pushes to
-// every CTA its output offset and its share of the keys equal to the
-// threshold (ties go to the lower position, and the CTAs own increasing
-// positions); each CTA then writes its kept positions in ascending order.
-// When the bin holds more candidates than CTA 0 can hold (many equal
-// scores), every CTA runs the general select below instead.
-//
-// k_topk_cluster is the general select (cluster_topk.cuh): four 8-bit radix
-// passes, or three after the 12-bit histogram, each with a cluster barrier
-// (slices up to 40K keys per CTA in shared memory; larger slices are re-read
-// from global memory, where they are L2-resident after the scoring kernel).
+// bits of every key, and k_topk_fused needs one cluster barrier (described at
+// the kernel).  k_topk_cluster is the general select (cluster_topk.cuh): four
+// 8-bit radix passes, or three after the 12-bit histogram, each with a
+// cluster barrier (slices up to 40K keys per CTA in shared memory; larger
+// slices are re-read from global memory, where they are L2-resident after the
+// scoring kernel).  Ties go to the lower position, and the output is
+// ascending.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -74,224 +66,278 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
-constexpr int kCandCap = 8192;   // candidates CTA 0 resolves in shared memory
+constexpr int kCandCap = 12288;   // candidates, copied into every CTA of the cluster (96 KB)
+constexpr int kStageCap = 4096;   // one CTA's own candidates, staged before the copy (32 KB)
 
 struct FusedTopkShared {
-  ClusterTopkShared general;     // the general select, when the bin is too full
-  unsigned hist10[1024];         // CTA 0: 10-bit digit histogram of the candidates
-  int gt[kTopkCluster], eq[kTopkCluster], def[kTopkCluster];   // CTA 0: per CTA of the cluster
+  ClusterTopkShared general;     // the general select, when the list would overflow
+  alignas(16) unsigned hist10[2][1024];   // 10-bit digit histograms of the candidates (bits 19-10,
+                                          // 9-0), read as uint4
+  int def_of[kTopkCluster];      // pushed by CTA q: its keys above the bin b*
+  int cand_of[kTopkCluster];     // pushed by CTA q: its keys inside b*
+  int red[kTopkThreads / 32][3];
   int scan[32];
   uint32_t bstar;                // the 12-bit bin of the B-th largest key
   int need;                      // keys to take from that bin
-  int n_bin;                     // keys of the head in that bin
-  int n_cand;                    // CTA 0: candidates pushed so far (by every CTA)
-  int cand_base;                 // this CTA's first slot in CTA 0's candidate list
-  int bin, bin_need;             // CTA 0: digit found by a pass
-  uint32_t theta;                // pushed by CTA 0: the B-th largest key
-  int quota, offset;             // pushed by CTA 0: this CTA's keys equal to theta to take, output offset
+  int n_cand;                    // CTA 0: candidate slots handed out
+  int cand_base;                 // this CTA's first candidate slot
+  int bin, bin_need;             // digit found by a pass
 };
+
+static_assert(offsetof(FusedTopkShared, hist10) % 16 == 0, "16-byte loads of the digit histograms");
 
 // Split cluster barrier: arrive (release) now, wait (acquire) later.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-// Shared-memory histogram add where the lanes of a warp with the same bin add once.
-__device__ __forceinline__ void hist_add_warp(unsigned* hist, uint32_t bin, bool valid) {
-  const uint32_t b = valid ? bin : 0xFFFFFFFFu;
-  const unsigned peers = __match_any_sync(0xffffffffu, b);
-  if (valid && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
-}
-
-// Block-wide: the bin of a 1024-bin histogram (descending order) holding the
-// need-th largest key, and the rank of that key inside the bin.
-__device__ __forceinline__ void find_desc_1024(const unsigned* h, int need, FusedTopkShared& sm) {
-  const int i = threadIdx.x;                       // bins 1023 - 2i and 1022 - 2i
-  const unsigned c0 = i < 512 ? h[1023 - 2 * i] : 0u, c1 = i < 512 ? h[1022 - 2 * i] : 0u;
-  int total;
-  const int excl = block_exclusive_scan((int)(c0 + c1), sm.scan, &total);
-  if (i < 512 && excl < need && need <= excl + (int)(c0 + c1)) {
-    if (need <= excl + (int)c0) {
-      sm.bin = 1023 - 2 * i;
-      sm.bin_need = need - excl;
-    } else {
-      sm.bin = 1022 - 2 * i;
-      sm.bin_need = need - excl - (int)c0;
+// One warp: the bin of a 1024-bin histogram (descending order) holding the
+// need-th largest key, and the rank of that key inside the bin.  Lane l sums
+// bins 1023 - 32 l down to 992 - 32 l; a warp scan finds the lane whose range
+// holds the key, and that lane walks its 32 bins.
+__device__ __forceinline__ void warp_find_desc_1024(const unsigned* h, int need, FusedTopkShared& sm) {
+  const int lane = threadIdx.x & 31;
+  const uint4* h4 = reinterpret_cast<const uint4*>(h + 992 - 32 * lane);
+  unsigned c[32];
+  int tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 v = h4[i];
+    c[4 * i] = v.x;
+    c[4 * i + 1] = v.y;
+    c[4 * i + 2] = v.z;
+    c[4 * i + 3] = v.w;
+  }
+#pragma unroll
+  for (int e = 0; e < 32; ++e) tot += (int)c[e];
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (incl - tot < need && need <= incl) {
+    int cum = incl - tot;
+#pragma unroll
+    for (int e = 31; e >= 0; --e) {
+      if (cum < need && need <= cum + (int)c[e]) {
+        sm.bin = 992 - 32 * lane + e;
+        sm.bin_need = need - cum;
+      }
+      cum += (int)c[e];
     }
   }
-  __syncthreads();
 }
 
+// The fused select (the scorer has counted the top 12 bits of every key).
+// CTA r of the cluster owns positions [r per, (r + 1) per) of the head and
+// thread t of it the KPT consecutive positions from KPT t, held in registers.
+// Every CTA finds the bin b* of the B-th largest key from the histogram,
+// counts its keys above b* and lists its keys inside b* (the candidates, with
+// their positions) in shared memory; it takes a range of slots from an atomic
+// counter in CTA 0 and copies its list, with coalesced stores, to those slots
+// of the candidate list of EVERY CTA of the cluster.  After the one cluster
+// barrier each CTA holds the whole candidate list and every CTA's counts, and
+// finds on its own the exact threshold key theta (two 10-bit radix passes
+// over the candidates), the number r of keys equal to theta to keep (lowest
+// positions first), and its output offset: the kept keys of the lower ranks.
+// It then writes its kept positions in ascending order.  No shared memory is
+// touched remotely after the barrier.  A list that would overflow (many equal
+// scores) sends every CTA to the general select.
+template <int KPT>
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
     k_topk_fused(const float* __restrict__ scores, int T_len, int B_e, int32_t* __restrict__ sel, int per,
-                 const unsigned* __restrict__ hist) {
-  extern __shared__ __align__(16) uint32_t keys_s[];          // [per] this CTA's keys
-  unsigned* h_s = keys_s + per;                                 // [4096] the head's 12-bit histogram
-  uint2* gath = reinterpret_cast<uint2*>(h_s + kScoreHistBins); // [kCandCap] (key, position), CTA 0
+                 const unsigned* __restrict__ hist, int vec) {
+  extern __shared__ __align__(16) uint2 cand[];   // [kCandCap] (key, position), then [kStageCap] staged
+  uint2* stage = cand + kCandCap;
   __shared__ FusedTopkShared sm;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y;
   const int t0 = min(T_len, rank * per);
   const int n = min(T_len, t0 + per) - t0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int32_t* out = sel + (size_t)g * B_e;
-  if (rank == 0 && threadIdx.x == 0) sm.n_cand = 0;
-  cluster_arrive();            // CTA 0's counter is set before any CTA adds to it (waited for below)
+  sm.hist10[0][tid] = sm.hist10[0][tid + kTopkThreads] = 0u;
+  sm.hist10[1][tid] = sm.hist10[1][tid + kTopkThreads] = 0u;
+  if (tid == 0) {
+    sm.n_cand = 0;
+    sm.bstar = 0xFFFu;   // kept only if the histogram does not sum to T (cannot happen)
+    sm.need = B_e;
+  }
+  cluster_arrive();      // CTA 0's counter is set before any CTA adds to it (waited for below)
   pdl_wait_for(scores, hist);
   const unsigned* h = hist + (size_t)g * kScoreHistBins;
   const float* s = scores + (size_t)g * T_len + t0;
-  // the head's histogram and this CTA's keys into shared memory, all loads in flight together
+
+  // this thread's keys: positions i0 .. i0 + KPT - 1 of the slice (nv of them valid)
+  const int i0 = KPT * tid;
+  const int nv = max(0, min(KPT, n - i0));
+  uint32_t k[KPT];
+  if (vec) {   // T a multiple of 4 and 16-byte aligned rows: a float4 is wholly valid or wholly past n
+#pragma unroll
+    for (int q = 0; q < KPT / 4; ++q) {
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (4 * q < nv) f = *reinterpret_cast<const float4*>(s + i0 + 4 * q);
+      k[4 * q] = order_key(f.x);
+      k[4 * q + 1] = order_key(f.y);
+      k[4 * q + 2] = order_key(f.z);
+      k[4 * q + 3] = order_key(f.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) k[j] = j < nv ? order_key(s[i0 + j]) : 0u;
+  }
+  // the 12-bit bin holding the B-th largest key: 8 bins per thread, descending
   {
-    const uint4* h4 = reinterpret_cast<const uint4*>(h);
-    uint4 hv[kScoreHistBins / 4 / kTopkThreads];
+    const uint4 a = reinterpret_cast<const uint4*>(h)[1023 - 2 * tid];   // bins 4095 - 8t - 3 .. 4095 - 8t
+    const uint4 b = reinterpret_cast<const uint4*>(h)[1022 - 2 * tid];   // bins 4095 - 8t - 7 .. 4095 - 8t - 4
+    const int c[8] = {(int)a.w, (int)a.z, (int)a.y, (int)a.x, (int)b.w, (int)b.z, (int)b.y, (int)b.x};
+    int tot = 0;
 #pragma unroll
-    for (int j = 0; j < kScoreHistBins / 4 / kTopkThreads; ++j) hv[j] = h4[threadIdx.x + j * kTopkThreads];
-    for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
-      float f[4];
+    for (int j = 0; j < 8; ++j) tot += c[j];
+    int total;
+    const int above = block_exclusive_scan(tot, sm.scan, &total);
+    if (above < B_e && B_e <= above + tot) {
+      int cum = above;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = i0 + j * blockDim.x;
-        f[j] = i < n ? s[i] : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = i0 + j * blockDim.x;
-        if (i < n) keys_s[i] = order_key(f[j]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kScoreHistBins / 4 / kTopkThreads; ++j)
-      reinterpret_cast<uint4*>(h_s)[threadIdx.x + j * kTopkThreads] = hv[j];
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // the 12-bit bin holding the B_e-th largest key: lane l sums bins
-    // [4096 - 128 (l + 1), 4096 - 128 l); a scan over the lanes (highest bins
-    // first) finds the lane whose range crosses B_e, then the warp scans that
-    // range 4 bins per lane
-    unsigned tot = 0;
-#pragma unroll 8
-    for (int j = 0; j < 128; ++j) tot += h_s[kScoreHistBins - 128 * (lane + 1) + ((j + 4 * lane) & 127)];
-    unsigned incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, incl - tot < (unsigned)B_e && (unsigned)B_e <= incl);
-    const int L = __ffs(hit) - 1;                   // hit != 0: the bins sum to T >= B_e
-    const unsigned above = __shfl_sync(0xffffffffu, incl - tot, L);
-    const int hi = kScoreHistBins - 1 - 128 * L - 4 * lane;    // this lane's 4 bins: hi, hi - 1, hi - 2, hi - 3
-    unsigned c[4], t4 = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      c[e] = h_s[hi - e];
-      t4 += c[e];
-    }
-    unsigned in4 = t4;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned y = __shfl_up_sync(0xffffffffu, in4, o);
-      if (lane >= o) in4 += y;
-    }
-    unsigned cum = above + in4 - t4;
-    if (cum < (unsigned)B_e && (unsigned)B_e <= above + in4) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (cum < (unsigned)B_e && (unsigned)B_e <= cum + c[e]) {
-          sm.bstar = (uint32_t)(hi - e);
-          sm.need = B_e - (int)cum;
-          sm.n_bin = (int)c[e];
+      for (int j = 0; j < 8; ++j) {
+        if (cum < B_e && B_e <= cum + c[j]) {
+          sm.bstar = (uint32_t)(kScoreHistBins - 1 - 8 * tid - j);
+          sm.need = B_e - cum;
         }
-        cum += c[e];
+        cum += c[j];
       }
     }
-  }
-  __syncthreads();
-  const uint4* keys4 = reinterpret_cast<const uint4*>(keys_s);
-  if (sm.n_bin > kCandCap) {   // cluster-uniform: many keys in one bin, the general select
-    cluster_wait();
-    auto key_at = [&](int i) -> uint32_t { return keys_s[i]; };
-    cluster_radix_topk<kTopkCluster>(cluster, true, keys4, key_at, n, t0, B_e, out, sm.general, h);
-    return;
+    __syncthreads();
   }
   const uint32_t bstar = sm.bstar;
-  // keys above the bin are kept; keys inside it are candidates, pushed to CTA 0 as (key, position)
   int my_def = 0, my_cand = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint32_t d = keys_s[i] >> 20;
-    my_def += d > bstar;
-    my_cand += d == bstar;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t d = k[j] >> 20;
+    my_def += j < nv && d > bstar;
+    my_cand += j < nv && d == bstar;
   }
-  int n_def, n_cand;
-  const int packed = block_exclusive_scan((my_cand << 16) | my_def, sm.scan, &n_def);
-  n_cand = n_def >> 16;
-  n_def &= 0xFFFF;
-  cluster_wait();              // CTA 0's counter is initialised
-  if (threadIdx.x == 0) {
-    sm.cand_base = atomicAdd(cluster.map_shared_rank(&sm.n_cand, 0), n_cand);
-    cluster.map_shared_rank(&sm, 0)->def[rank] = n_def;
+  int tot_packed;
+  const int excl = block_exclusive_scan((my_cand << 16) | my_def, sm.scan, &tot_packed);
+  const int n_def = tot_packed & 0xFFFF, n_own = tot_packed >> 16;
+  if (my_cand > 0) {   // this CTA's candidates, in position order
+    int at = excl >> 16;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (j < nv && (k[j] >> 20) == bstar) {
+        if (at < kStageCap) stage[at] = make_uint2(k[j], (uint32_t)(t0 + i0 + j));
+        ++at;
+      }
+    }
+  }
+  cluster_wait();        // every CTA has started: CTA 0's counter is initialised
+  if (tid == 0) sm.cand_base = atomicAdd(cluster.map_shared_rank(&sm.n_cand, 0), n_own);
+  __syncthreads();       // the slot range and the staged list
+  const int base = sm.cand_base;
+  if (tid < kTopkCluster) {
+    FusedTopkShared* rs = cluster.map_shared_rank(&sm, tid);
+    rs->def_of[rank] = n_def;
+    rs->cand_of[rank] = n_own;
+  }
+  {
+    const int m = min(n_own, min(kStageCap, kCandCap - min(base, kCandCap)));
+#pragma unroll 1
+    for (int q = 0; q < kTopkCluster; ++q) {
+      uint2* rc = cluster.map_shared_rank(cand, q) + base;
+      for (int i = tid; i < m; i += kTopkThreads) rc[i] = stage[i];
+    }
+  }
+  cluster.sync();        // every candidate and count is in every CTA; no remote access after this
+  int nc = 0;
+  bool overflow = false;
+#pragma unroll
+  for (int q = 0; q < kTopkCluster; ++q) {
+    nc += sm.cand_of[q];
+    overflow |= sm.cand_of[q] > kStageCap;
+  }
+  if (overflow || nc > kCandCap) {   // cluster-uniform: the general select on keys re-read from L2
+    auto key_at = [&](int i) -> uint32_t { return order_key(s[i]); };
+    cluster_radix_topk<kTopkCluster>(cluster, false, nullptr, key_at, n, t0, B_e, out, sm.general, h);
+    return;
+  }
+  // theta: two 10-bit passes over the candidates' low 20 bits (the keys of one
+  // 12-bit bin spread over the sub-bins, so plain shared atomics rarely collide)
+  for (int j = tid; j < nc; j += kTopkThreads) atomicAdd(&sm.hist10[0][(cand[j].x >> 10) & 1023u], 1u);
+  __syncthreads();
+  if (warp == 0) warp_find_desc_1024(sm.hist10[0], sm.need, sm);
+  __syncthreads();
+  const uint32_t prefix22 = (bstar << 10) | (uint32_t)sm.bin;
+  const int need22 = sm.bin_need;
+  for (int j = tid; j < nc; j += kTopkThreads) {
+    const uint32_t c = cand[j].x;
+    if ((c >> 10) == prefix22) atomicAdd(&sm.hist10[1][c & 1023u], 1u);
   }
   __syncthreads();
+  if (warp == 0) warp_find_desc_1024(sm.hist10[1], need22, sm);
+  __syncthreads();
+  const uint32_t theta = (prefix22 << 10) | (uint32_t)sm.bin;
+  const int r = sm.bin_need;   // keys equal to theta to keep, lowest positions first
+  // the keys of the lower ranks above and equal to theta, and this CTA's ties:
+  // candidates at positions below t0, and inside [t0, t0 + n)
+  int offset, quota;
   {
-    uint2* dst = cluster.map_shared_rank(gath, 0);
-    int at = sm.cand_base + (packed >> 16);
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint32_t k = keys_s[i];
-      if ((k >> 20) == bstar && at < kCandCap) dst[at++] = make_uint2(k, (uint32_t)(t0 + i));
+    int gt_lo = 0, eq_lo = 0, eq_me = 0;
+    for (int j = tid; j < nc; j += kTopkThreads) {
+      const uint2 c = cand[j];
+      const bool lo = c.y < (uint32_t)t0;
+      gt_lo += lo && c.x > theta;
+      eq_lo += lo && c.x == theta;
+      eq_me += !lo && c.y < (uint32_t)(t0 + n) && c.x == theta;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gt_lo += __shfl_xor_sync(0xffffffffu, gt_lo, o);
+      eq_lo += __shfl_xor_sync(0xffffffffu, eq_lo, o);
+      eq_me += __shfl_xor_sync(0xffffffffu, eq_me, o);
+    }
+    if (lane == 0) {
+      sm.red[warp][0] = gt_lo;
+      sm.red[warp][1] = eq_lo;
+      sm.red[warp][2] = eq_me;
+    }
+    __syncthreads();
+    gt_lo = eq_lo = eq_me = 0;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) {
+      gt_lo += sm.red[w][0];
+      eq_lo += sm.red[w][1];
+      eq_me += sm.red[w][2];
+    }
+    int def_lo = 0;
+#pragma unroll
+    for (int q = 0; q < kTopkCluster; ++q) def_lo += q < rank ? sm.def_of[q] : 0;
+    offset = def_lo + gt_lo + min(eq_lo, r);
+    quota = min(eq_me, max(0, r - eq_lo));
+  }
+  // this CTA's kept positions, ascending: a key above theta goes after the keys
+  // above theta before it and the kept ties before it
+  int n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    n_gt += j < nv && k[j] > theta;
+    n_eq += j < nv && k[j] == theta;
+  }
+  int tot2;
+  const int ex2 = block_exclusive_scan((n_gt << 16) | n_eq, sm.scan, &tot2);
+  int gt_b = ex2 >> 16, eq_b = ex2 & 0xFFFF;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    if (j >= nv) continue;
+    if (k[j] > theta) {
+      const int o = offset + gt_b + min(eq_b, quota);
+      if (o < B_e) out[o] = t0 + i0 + j;
+      ++gt_b;
+    } else if (k[j] == theta) {
+      if (eq_b < quota && offset + gt_b + eq_b < B_e) out[offset + gt_b + eq_b] = t0 + i0 + j;
+      ++eq_b;
     }
   }
-  cluster.sync();   // every candidate and count is in CTA 0
-
-  if (rank == 0) {
-    const int nc = min(sm.n_cand, kCandCap);   // equals the bin's count, which the branch above bounded
-    for (int b = threadIdx.x; b < 1024; b += blockDim.x) sm.hist10[b] = 0;
-    if (threadIdx.x < kTopkCluster) sm.gt[threadIdx.x] = sm.eq[threadIdx.x] = 0;
-    __syncthreads();
-    // two 10-bit passes over the candidates' low 20 bits
-    for (int j0 = 0; j0 < nc; j0 += blockDim.x) {
-      const int j = j0 + threadIdx.x;
-      hist_add_warp(sm.hist10, j < nc ? (gath[j].x >> 10) & 1023u : 0u, j < nc);
-    }
-    __syncthreads();
-    find_desc_1024(sm.hist10, sm.need, sm);
-    const uint32_t dA = (uint32_t)sm.bin;
-    const int needA = sm.bin_need;
-    for (int b = threadIdx.x; b < 1024; b += blockDim.x) sm.hist10[b] = 0;
-    __syncthreads();
-    for (int j0 = 0; j0 < nc; j0 += blockDim.x) {
-      const int j = j0 + threadIdx.x;
-      const uint32_t k = j < nc ? gath[j].x : 0u;
-      hist_add_warp(sm.hist10, k & 1023u, j < nc && ((k >> 10) & 1023u) == dA);
-    }
-    __syncthreads();
-    find_desc_1024(sm.hist10, needA, sm);
-    const uint32_t theta = (bstar << 20) | (dA << 10) | (uint32_t)sm.bin;
-    const int r = sm.bin_need;                      // keys equal to theta to take, lowest positions first
-    // per CTA: candidates above theta and equal to it
-    for (int j0 = 0; j0 < nc; j0 += blockDim.x) {
-      const int j = j0 + threadIdx.x;
-      const uint2 c = j < nc ? gath[j] : make_uint2(0u, 0u);
-      const int q = (int)(c.y / (uint32_t)per);
-      hist_add_warp(reinterpret_cast<unsigned*>(sm.gt), (uint32_t)q, j < nc && c.x > theta);
-      hist_add_warp(reinterpret_cast<unsigned*>(sm.eq), (uint32_t)q, j < nc && c.x == theta);
-    }
-    __syncthreads();
-    if (threadIdx.x < kTopkCluster) {   // offsets and tie quotas, pushed to every CTA
-      const int q = threadIdx.x;
-      int off = 0, ties = 0;
-      for (int p = 0; p < q; ++p) {
-        off += sm.def[p] + sm.gt[p] + min(sm.eq[p], max(0, r - ties));
-        ties += sm.eq[p];
-      }
-      FusedTopkShared* rs = cluster.map_shared_rank(&sm, q);
-      rs->theta = theta;
-      rs->quota = min(sm.eq[q], max(0, r - ties));
-      rs->offset = off;
-    }
-  }
-  cluster.sync();   // theta, quota and offset are in every CTA (no remote access after this)
-  radix_compact4(keys4, n, sm.theta, sm.quota, sm.offset, 0, B_e, t0, out, sm.scan);
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
@@ -315,15 +361,20 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
     return e;
   }
   const int per = ((T_len + kTopkCluster - 1) / kTopkCluster + 3) & ~3;
-  // at least 120 KB: one CTA per SM (two sharing an SM, as they do when they take SMs while the
-  // scorer's CTAs finish, were 40% slower)
-  const size_t fused_smem = std::max<size_t>((size_t)per * 4 + (size_t)kScoreHistBins * 4 + (size_t)kCandCap * 8,
-                                             120 * 1024);
   cudaError_t e;
-  if (hist != nullptr && fused_smem <= 200 * 1024) {
-    if ((e = ensure_smem((const void*)k_topk_fused, fused_smem)) != cudaSuccess) return e;
-    e = launch_pdl(k_topk_fused, dim3(kTopkCluster, H_kv), dim3(kTopkThreads), fused_smem, st, scores, T_len, B_e,
-                   sel, per, hist);
+  if (hist != nullptr && per <= 32 * kTopkThreads) {
+    // at least 120 KB of shared memory: one CTA per SM (two sharing an SM, as they do when they take
+    // SMs while the scorer's CTAs finish, were 40% slower)
+    const size_t smem = std::max<size_t>((size_t)(kCandCap + kStageCap) * 8, 120 * 1024);
+    const int vec = T_len % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0;
+    auto launch = [&](auto kern) -> cudaError_t {
+      cudaError_t e2 = ensure_smem((const void*)kern, smem);
+      if (e2 != cudaSuccess) return e2;
+      return launch_pdl(kern, dim3(kTopkCluster, H_kv), dim3(kTopkThreads), smem, st, scores, T_len, B_e, sel, per,
+                        hist, vec);
+    };
+    e = per <= 8 * kTopkThreads ? launch(k_topk_fused<8>)
+        : per <= 16 * kTopkThreads ? launch(k_topk_fused<16>) : launch(k_topk_fused<32>);
     count_launches(1);
     return e;
   }

@@ -343,3 +343,56 @@ def test_topk_sizes_and_slices(quoka, T, B):
     got = sel.cpu().numpy()
     for g in range(H_kv):
         assert np.array_equal(got[g], qo.top_b(s[g].astype(np.float64), B))
+
+
+@pytest.mark.parametrize("T,B,n_big,n_tie", [(60_000, 3000, 1000, 59_000), (20_000, 2000, 500, 6000)])
+def test_topk_ties_inside_and_beyond_the_candidate_list(quoka, T, B, n_big, n_tie):
+    """A threshold bin with more keys than the select's candidate list (the general radix select
+    takes over) and one with fewer (resolved from the list), both ending in exact ties."""
+    H_kv = 2
+    rng = np.random.default_rng(T + B)
+    s = np.full((H_kv, T), -0.75, dtype=np.float32)
+    for g in range(H_kv):
+        perm = rng.permutation(T)
+        s[g, perm[:n_tie]] = 1.0
+        s[g, perm[n_tie:n_tie + n_big]] = 1.5 + rng.integers(0, 200, n_big).astype(np.float32) / 512
+    scores = torch.from_numpy(s).to(DEV)
+    shape = quoka.Shape(0, H_kv, H_kv, 4, T, 64, 1)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    sel = torch.empty((H_kv, B), dtype=torch.int32, device=DEV)
+    quoka.quoka_topk(shape, scores, B, sel, ws)
+    got = sel.cpu().numpy()
+    for g in range(H_kv):
+        assert np.array_equal(got[g], qo.top_b(s[g].astype(np.float64), B))
+
+
+@pytest.mark.parametrize("T,distinct", [(3000, 7), (20_000, 2), (30_000, 2)])
+def test_fused_topk_with_duplicate_keys(quoka, T, distinct):
+    """History keys repeating a few rows give exactly equal scores: the fused select (fed by the
+    scorer's histogram) keeps the lowest positions, as the oracle's top-B does on the GPU's scores;
+    with two distinct rows of 30000 the threshold bin overflows the candidate list."""
+    cfg, x = wl.small_chunk(H_q=8, H_kv=2, d=128, C=64, T=T, N_q=8, B=1500, dtype="bf16")
+    x.K_hist[:] = x.K_hist[:, torch.arange(T) % distinct]
+    r = run_stages(quoka, cfg, x, "max")
+    sc = r["scores"].cpu().numpy().astype(np.float64)
+    for g in range(cfg.H_kv):
+        want = qo.top_b(sc[g], cfg.B)
+        assert np.array_equal(r["sel"][g], want)
+        assert np.array_equal(r["sel_fused"][g], want)
+
+
+def test_fused_topk_one_slice_full_of_ties(quoka):
+    """The first eighth of every head's history repeats the head's best key: one CTA of the fused
+    select holds more candidates than it can stage, and every CTA takes the general select."""
+    cfg, x = wl.small_chunk(H_q=8, H_kv=2, d=128, C=64, T=40_000, N_q=8, B=3000, dtype="bf16")
+    r0 = run_stages(quoka, cfg, x, "max")
+    best = r0["scores"].argmax(dim=1).cpu()
+    for g in range(cfg.H_kv):
+        x.K_hist[g, :5000] = x.K_hist[g, int(best[g])]
+    r = run_stages(quoka, cfg, x, "max")
+    sc = r["scores"].cpu().numpy().astype(np.float64)
+    for g in range(cfg.H_kv):
+        want = qo.top_b(sc[g], cfg.B)
+        assert np.array_equal(want, np.arange(cfg.B))
+        assert np.array_equal(r["sel"][g], want)
+        assert np.array_equal(r["sel_fused"][g], want)
