@@ -80,13 +80,30 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Histogram of the top 12 bits of order keys (the first digit of the top-B
-// select), counted where the scores are produced: lanes of a warp with the
-// same bin add once.  `hist` may be shared or global memory.  All 32 lanes
-// call it; `valid` false skips a lane.
-__device__ __forceinline__ void hist12_add(unsigned int* hist, uint32_t key, bool valid) {
-  const uint32_t bin = valid ? key >> 20 : 0xFFFFFFFFu;
-  const unsigned peers = __match_any_sync(0xffffffffu, bin);
+// The 12-bit histogram bin of a score, counted where the scores are produced
+// so that the top-B select can start from the bin holding the B-th largest
+// score.  Cosine scores lie in [-1, 1]: a fixed-point bin of width 1/2048
+// (4096 bins over [-1, 1], the ends clamped), fine where the scores crowd
+// together.  Other scores: the top 12 bits of order_key.  Both are
+// non-decreasing in the score, with NaN in bin 0 for cosines.
+__device__ __forceinline__ uint32_t score_bin(float s, bool cosine) {
+  if (cosine) {
+    const float t = __fmul_rn(__fadd_rn(s, 1.0f), 2048.0f);
+    return t >= 0.0f ? (uint32_t)min(__float2int_rz(t), 4095) : 0u;
+  }
+  return order_key(s) >> 20;
+}
+
+// The float of an order key (inverse of order_key; -0.0 comes back as +0.0).
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// hist[bin] += 1 for every lane with `valid`; lanes of a warp with the same
+// bin add once.  `hist` may be shared or global memory.  All 32 lanes call it.
+__device__ __forceinline__ void hist_bin_add(unsigned int* hist, uint32_t bin, bool valid) {
+  const uint32_t b = valid ? bin : 0xFFFFFFFFu;
+  const unsigned peers = __match_any_sync(0xffffffffu, b);
   if (valid && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
 }
 

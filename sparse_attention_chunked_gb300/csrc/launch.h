@@ -86,8 +86,9 @@ struct KeyScale {
   int64_t k_inv_stride;
 };
 
-// The scorers can count the first digit of the top-B select: the top
-// kScoreHistBits bits of order_key(score), per KV head.
+// The scorers can count a 12-bit histogram of their scores per KV head
+// (score_bin in common.cuh: fixed-point bins for cosine scores, the top 12
+// bits of order_key otherwise), where the top-B select starts.
 constexpr int kScoreHistBits = 12;
 constexpr int kScoreHistBins = 1 << kScoreHistBits;
 
@@ -96,9 +97,9 @@ constexpr int kScoreHistBins = 1 << kScoreHistBits;
 constexpr int kScoreRowsMax = 8;
 
 // score[g, t] = max_r (r . k_t) * scale(t).  hist, if not NULL, receives
-// (adds) the histogram of the top kScoreHistBits bits of order_key(score) per
-// head, [H_kv][kScoreHistBins]; launch_build_operand with the same hist zeroes
-// it first.
+// (adds) the histogram of score_bin(score, ks.key_norm) per head,
+// [H_kv][kScoreHistBins]; launch_build_operand with the same hist zeroes it
+// first.
 cudaError_t launch_score_simt(int dtype, int d, const void* K, int64_t head_stride, int H_kv, int T_len,
                               const float* op_f32, int R, KeyScale ks, float* scores, unsigned* hist,
                               cudaStream_t st);
@@ -135,10 +136,11 @@ cudaError_t noalloc_scratch(void** base);
 // Bounded-wait self-test (see selftest.cu).
 cudaError_t launch_expire_wait(WsHeader* hdr, long long limit, cudaStream_t st);
 
-// hist: NULL, or the first-digit histogram the scorer built for these scores
-// ([H_kv][kScoreHistBins]), which replaces the select's first histogram pass.
+// hist: NULL, or the 12-bit histogram the scorer built for these scores
+// ([H_kv][kScoreHistBins], score_bin with cosine = cosine_bins), where the
+// select starts.
 cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st,
-                        const unsigned* hist = nullptr);
+                        const unsigned* hist = nullptr, bool cosine_bins = false);
 
 // Rows sel[g, j] of K and V (T_len rows per head).  An index outside
 // [0, T_len) is not read: the row is written as zeros and QUOKA_ERR_DEVICE is

@@ -98,7 +98,7 @@ int score_npass(const quoka_shape* s, int N_pad, const Params& p) {
 
 // Whether the scoring stage can run on the tensor cores: bf16 keys, at most
 // 512 scaled rows or 256 hi/lo rows, and an operand that fits shared memory
-// next to two key stages and the first-digit histogram.
+// next to two key stages and the 12-bit score histogram.
 bool score_tc_fits(const quoka_shape* s, int N_q, const Params& p) {
   if (s->dtype != QUOKA_DTYPE_BF16) return false;
   const int N_pad = score_tc_pad_rows(score_rows(s, N_q, p));
@@ -288,10 +288,11 @@ int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const
   float* scores = at<float>(ws, L.scores);
   int32_t* sel = sel_out != nullptr ? sel_out : at<int32_t>(ws, L.sel);
   QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
-  // the scorer also counts the top 12 bits of its scores, where the top-B select then starts
+  // the scorer also counts a 12-bit histogram of its scores (fixed-point bins
+  // for cosines), where the top-B select then starts
   unsigned* hist = at<unsigned>(ws, L.hist);
   QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st, kc, hist));
-  QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st, hist));
+  QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st, hist, !p.dot));
   if (use_decode(p, shape))   // the decode kernel reads the kept rows through sel: no gathered copy
     return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), sel, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,
                       st);

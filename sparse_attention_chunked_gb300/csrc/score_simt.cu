@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(128) k_score_simt(const T* __restrict__ K, int
     }
   }
   if (t < T_len) scores[(size_t)g * T_len + t] = best * rk;
-  if (hist != nullptr)   // the first digit of the top-B select, straight into the head's histogram
-    hist12_add(hist + (size_t)g * kScoreHistBins, order_key(best * rk), t < T_len);
+  if (hist != nullptr)   // the score's 12-bit bin, straight into the head's histogram
+    hist_bin_add(hist + (size_t)g * kScoreHistBins, score_bin(best * rk, ks.key_norm), t < T_len);
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(256) k_score_rows(const T* __restrict__ K, int
                                           : 1.0f / fmaxf(sqrtf(ss), kNormEps);
     const float sc = best * rk;
     if (sub == 0 && valid) scores[(size_t)g * T_len + t] = sc;
-    if (hist != nullptr) hist12_add(hist + (size_t)g * kScoreHistBins, order_key(sc), sub == 0 && valid);
+    if (hist != nullptr) hist_bin_add(hist + (size_t)g * kScoreHistBins, score_bin(sc, ks.key_norm), sub == 0 && valid);
   }
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }

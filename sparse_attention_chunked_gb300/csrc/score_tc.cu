@@ -36,8 +36,8 @@
 // shared memory (the 4 threads of a key take a quarter of its 16-byte chunks
 // each) or comes from the key-norm cache.
 //
-// With `hist` the epilogue also counts the top 12 bits of the order-preserving
-// key of every score (the first digit of the top-B select) in a shared
+// With `hist` the epilogue also counts every score's 12-bit bin (score_bin:
+// fixed-point for cosines), where the top-B select starts, in a shared
 // histogram, added to the head's global histogram at the end.  Every wait is
 // bounded; on a timeout the CTA records QUOKA_ERR_TIMEOUT, lets in-flight
 // copies and MMAs land, frees TMEM and exits.
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         else if (!ks.key_norm) rk = 1.f;
         const float val = my_m * rk;
         if (alive && t < T_len) scores[(size_t)g * T_len + t] = val;
-        if (hist != nullptr) hist12_add(hist_s, order_key(val), alive && t < T_len);
+        if (hist != nullptr) hist_bin_add(hist_s, score_bin(val, ks.key_norm), alive && t < T_len);
       }
     }
   }

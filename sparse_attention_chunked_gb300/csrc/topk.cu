@@ -68,6 +68,7 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
 
 constexpr int kCandCap = 12288;   // candidates, copied into every CTA of the cluster (96 KB)
 constexpr int kStageCap = 4096;   // one CTA's own candidates, staged before the copy (32 KB)
+constexpr int kFusedSliceCap = 16384;   // keys per CTA of the fused select (64 KB of shared memory)
 
 struct FusedTopkShared {
   ClusterTopkShared general;     // the general select, when the list would overflow
@@ -82,6 +83,8 @@ struct FusedTopkShared {
   int n_cand;                    // CTA 0: candidate slots handed out
   int cand_base;                 // this CTA's first candidate slot
   int bin, bin_need;             // digit found by a pass
+  uint32_t theta;                // the B-th largest key
+  int r;                         // keys equal to theta to keep
 };
 
 static_assert(offsetof(FusedTopkShared, hist10) % 16 == 0, "16-byte loads of the digit histograms");
@@ -128,27 +131,41 @@ __device__ __forceinline__ void warp_find_desc_1024(const unsigned* h, int need,
   }
 }
 
-// The fused select (the scorer has counted the top 12 bits of every key).
-// CTA r of the cluster owns positions [r per, (r + 1) per) of the head and
-// thread t of it the KPT consecutive positions from KPT t, held in registers.
-// Every CTA finds the bin b* of the B-th largest key from the histogram,
-// counts its keys above b* and lists its keys inside b* (the candidates, with
-// their positions) in shared memory; it takes a range of slots from an atomic
-// counter in CTA 0 and copies its list, with coalesced stores, to those slots
-// of the candidate list of EVERY CTA of the cluster.  After the one cluster
-// barrier each CTA holds the whole candidate list and every CTA's counts, and
-// finds on its own the exact threshold key theta (two 10-bit radix passes
-// over the candidates), the number r of keys equal to theta to keep (lowest
-// positions first), and its output offset: the kept keys of the lower ranks.
-// It then writes its kept positions in ascending order.  No shared memory is
-// touched remotely after the barrier.  A list that would overflow (many equal
-// scores) sends every CTA to the general select.
-template <int KPT>
+// The key a score is selected on: order_key, with NaN as -inf where the bins
+// are the fixed-point cosine bins (which count NaN in bin 0).
+__device__ __forceinline__ uint32_t select_key(float f, bool cosine) {
+  return order_key((cosine && f != f) ? -INFINITY : f);
+}
+
+constexpr int kRankMax = 128;   // candidates ranked directly (one per thread, against every other)
+
+// The fused select (the scorer has counted a 12-bit histogram of its scores,
+// score_bin).  CTA r of the cluster owns positions [r per, (r + 1) per) of the
+// head, loads their keys into shared memory, and thread t of it takes the kpt
+// consecutive positions from kpt t (kpt = per / 512 rounded up to a multiple
+// of 4).  Every CTA finds the bin b* of the B-th largest score from the
+// histogram, counts its keys above b* and lists its keys inside b* (the
+// candidates, with their positions) in shared memory; it takes a range of
+// slots from an atomic counter in CTA 0 and copies its list, with coalesced
+// stores, to those slots of the candidate list of EVERY CTA of the cluster.
+// After the one cluster barrier each CTA holds the whole candidate list and
+// every CTA's counts, and finds on its own the exact threshold key theta (up
+// to 128 candidates by ranking each against all others, else by radix passes
+// over the candidates' keys), the number r of keys equal to theta to keep
+// (lowest positions first), and its output offset: the kept keys of the lower
+// ranks.  It then writes its kept positions in ascending order.  No shared
+// memory is touched remotely after the barrier.  A list that would overflow
+// (many equal scores) sends every CTA to the general select.  The per-key
+// loops run over groups of 4 keys and are not unrolled: the kernel runs its
+// code once per launch, and straight-line code for 32 keys per thread spent
+// its time fetching instructions.
 __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThreads)
     k_topk_fused(const float* __restrict__ scores, int T_len, int B_e, int32_t* __restrict__ sel, int per,
-                 const unsigned* __restrict__ hist, int vec) {
-  extern __shared__ __align__(16) uint2 cand[];   // [kCandCap] (key, position), then [kStageCap] staged
+                 const unsigned* __restrict__ hist, int vec, int cosine) {
+  extern __shared__ __align__(16) uint2 cand[];   // [kCandCap] (key, position), [kStageCap] staged, [per] keys
   uint2* stage = cand + kCandCap;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(stage + kStageCap);
+  const uint4* keys4 = reinterpret_cast<const uint4*>(keys);
   __shared__ FusedTopkShared sm;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -158,7 +175,6 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   const int n = min(T_len, t0 + per) - t0;
   int32_t* out = sel + (size_t)g * B_e;
   sm.hist10[0][tid] = sm.hist10[0][tid + kTopkThreads] = 0u;
-  sm.hist10[1][tid] = sm.hist10[1][tid + kTopkThreads] = 0u;
   if (tid == 0) {
     sm.n_cand = 0;
     sm.bstar = 0xFFFu;   // kept only if the histogram does not sum to T (cannot happen)
@@ -168,35 +184,28 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   pdl_wait_for(scores, hist);
   const unsigned* h = hist + (size_t)g * kScoreHistBins;
   const float* s = scores + (size_t)g * T_len + t0;
-
-  // this thread's keys: positions i0 .. i0 + KPT - 1 of the slice (nv of them valid)
-  const int i0 = KPT * tid;
-  const int nv = max(0, min(KPT, n - i0));
-  uint32_t k[KPT];
-  if (vec) {   // T a multiple of 4 and 16-byte aligned rows: a float4 is wholly valid or wholly past n
-#pragma unroll
-    for (int q = 0; q < KPT / 4; ++q) {
-      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (4 * q < nv) f = *reinterpret_cast<const float4*>(s + i0 + 4 * q);
-      k[4 * q] = order_key(f.x);
-      k[4 * q + 1] = order_key(f.y);
-      k[4 * q + 2] = order_key(f.z);
-      k[4 * q + 3] = order_key(f.w);
+  const uint4 ha = reinterpret_cast<const uint4*>(h)[1023 - 2 * tid];   // bins 4095 - 8t - 3 .. 4095 - 8t
+  const uint4 hb = reinterpret_cast<const uint4*>(h)[1022 - 2 * tid];   // bins 4095 - 8t - 7 .. 4095 - 8t - 4
+  // the slice's keys into shared memory (positions past n read as key 0 and are never counted)
+  const int n4 = (n + 3) >> 2;
+  if (vec) {   // T a multiple of 4 and 16-byte aligned rows
+#pragma unroll 4
+    for (int i = tid; i < n4; i += kTopkThreads) {
+      const float4 f = reinterpret_cast<const float4*>(s)[i];
+      reinterpret_cast<uint4*>(keys)[i] =
+          make_uint4(select_key(f.x, cosine), select_key(f.y, cosine), select_key(f.z, cosine), select_key(f.w, cosine));
     }
   } else {
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) k[j] = j < nv ? order_key(s[i0 + j]) : 0u;
+    for (int i = tid; i < 4 * n4; i += kTopkThreads) keys[i] = i < n ? select_key(s[i], cosine) : 0u;
   }
   // the 12-bit bin holding the B-th largest key: 8 bins per thread, descending
   {
-    const uint4 a = reinterpret_cast<const uint4*>(h)[1023 - 2 * tid];   // bins 4095 - 8t - 3 .. 4095 - 8t
-    const uint4 b = reinterpret_cast<const uint4*>(h)[1022 - 2 * tid];   // bins 4095 - 8t - 7 .. 4095 - 8t - 4
-    const int c[8] = {(int)a.w, (int)a.z, (int)a.y, (int)a.x, (int)b.w, (int)b.z, (int)b.y, (int)b.x};
+    const int c[8] = {(int)ha.w, (int)ha.z, (int)ha.y, (int)ha.x, (int)hb.w, (int)hb.z, (int)hb.y, (int)hb.x};
     int tot = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) tot += c[j];
     int total;
-    const int above = block_exclusive_scan(tot, sm.scan, &total);
+    const int above = block_exclusive_scan(tot, sm.scan, &total);   // its barriers also publish the keys
     if (above < B_e && B_e <= above + tot) {
       int cum = above;
 #pragma unroll
@@ -211,23 +220,40 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     __syncthreads();
   }
   const uint32_t bstar = sm.bstar;
+  auto bin_of = [&](uint32_t key) -> uint32_t { return cosine ? score_bin(key_float(key), true) : key >> 20; };
+  // this thread's keys: positions i0 .. i0 + kpt - 1 of the slice, 4 at a time
+  const int kpt = ((per + kTopkThreads - 1) / kTopkThreads + 3) & ~3;
+  const int i0 = kpt * tid;
+  const int nv = max(0, min(kpt, n - i0));
+  const int ng = (nv + 3) >> 2;
   int my_def = 0, my_cand = 0;
+#pragma unroll 1
+  for (int q = 0; q < ng; ++q) {
+    const uint4 v = keys4[(i0 >> 2) + q];
+    const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const uint32_t d = k[j] >> 20;
-    my_def += j < nv && d > bstar;
-    my_cand += j < nv && d == bstar;
+    for (int e = 0; e < 4; ++e) {
+      const bool ok = 4 * q + e < nv;
+      const uint32_t d = bin_of(kk[e]);
+      my_def += ok && d > bstar;
+      my_cand += ok && d == bstar;
+    }
   }
   int tot_packed;
   const int excl = block_exclusive_scan((my_cand << 16) | my_def, sm.scan, &tot_packed);
   const int n_def = tot_packed & 0xFFFF, n_own = tot_packed >> 16;
   if (my_cand > 0) {   // this CTA's candidates, in position order
     int at = excl >> 16;
+#pragma unroll 1
+    for (int q = 0; q < ng; ++q) {
+      const uint4 v = keys4[(i0 >> 2) + q];
+      const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      if (j < nv && (k[j] >> 20) == bstar) {
-        if (at < kStageCap) stage[at] = make_uint2(k[j], (uint32_t)(t0 + i0 + j));
-        ++at;
+      for (int e = 0; e < 4; ++e) {
+        if (4 * q + e < nv && bin_of(kk[e]) == bstar) {
+          if (at < kStageCap) stage[at] = make_uint2(kk[e], (uint32_t)(t0 + i0 + 4 * q + e));
+          ++at;
+        }
       }
     }
   }
@@ -256,28 +282,60 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
     nc += sm.cand_of[q];
     overflow |= sm.cand_of[q] > kStageCap;
   }
-  if (overflow || nc > kCandCap) {   // cluster-uniform: the general select on keys re-read from L2
-    auto key_at = [&](int i) -> uint32_t { return order_key(s[i]); };
-    cluster_radix_topk<kTopkCluster>(cluster, false, nullptr, key_at, n, t0, B_e, out, sm.general, h);
+  if (overflow || nc > kCandCap) {   // cluster-uniform: the general select on the keys in shared memory
+    auto key_at = [&](int i) -> uint32_t { return keys[i]; };
+    cluster_radix_topk<kTopkCluster>(cluster, true, keys4, key_at, n, t0, B_e, out, sm.general,
+                                     cosine ? nullptr : h);
     return;
   }
-  // theta: two 10-bit passes over the candidates' low 20 bits (the keys of one
-  // 12-bit bin spread over the sub-bins, so plain shared atomics rarely collide)
-  for (int j = tid; j < nc; j += kTopkThreads) atomicAdd(&sm.hist10[0][(cand[j].x >> 10) & 1023u], 1u);
-  __syncthreads();
-  if (warp == 0) warp_find_desc_1024(sm.hist10[0], sm.need, sm);
-  __syncthreads();
-  const uint32_t prefix22 = (bstar << 10) | (uint32_t)sm.bin;
-  const int need22 = sm.bin_need;
-  for (int j = tid; j < nc; j += kTopkThreads) {
-    const uint32_t c = cand[j].x;
-    if ((c >> 10) == prefix22) atomicAdd(&sm.hist10[1][c & 1023u], 1u);
+  // theta and r
+  if (nc <= kRankMax) {
+    if (tid < nc) {   // candidate tid: keys above it and not below it
+      const uint32_t ki = cand[tid].x;
+      const int need = sm.need;
+      int gt = 0, ge = 0;
+      for (int j = 0; j < nc; ++j) {
+        const uint32_t kj = cand[j].x;
+        gt += kj > ki;
+        ge += kj >= ki;
+      }
+      if (gt < need && need <= ge) {   // written alike by every candidate equal to theta
+        sm.theta = ki;
+        sm.r = need - gt;
+      }
+    }
+    __syncthreads();
+  } else {
+    // radix passes over the candidates' keys, 10 bits at a time below the
+    // bits they share (the 12-bit bin, for order-key bins; none for cosine
+    // bins).  The keys of one bin spread over the digits, so plain shared
+    // atomics rarely collide.
+    uint32_t prefix = cosine ? 0u : bstar;
+    int pbits = cosine ? 0 : 12, need = sm.need;
+    for (int pass = 0; pbits < 32; ++pass) {
+      const int width = min(10, 32 - pbits), shift = 32 - pbits - width;
+      unsigned* hh = sm.hist10[pass & 1];
+      for (int j = tid; j < nc; j += kTopkThreads) {
+        const uint32_t c = cand[j].x;
+        if (pbits == 0 || (c >> (32 - pbits)) == prefix) atomicAdd(&hh[(c >> shift) & ((1u << width) - 1u)], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) warp_find_desc_1024(hh, need, sm);
+      // the other histogram, used by the next pass, is cleared meanwhile
+      sm.hist10[(pass + 1) & 1][tid] = sm.hist10[(pass + 1) & 1][tid + kTopkThreads] = 0u;
+      __syncthreads();
+      prefix = (prefix << width) | (uint32_t)sm.bin;
+      pbits += width;
+      need = sm.bin_need;
+    }
+    if (tid == 0) {
+      sm.theta = prefix;
+      sm.r = need;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  if (warp == 0) warp_find_desc_1024(sm.hist10[1], need22, sm);
-  __syncthreads();
-  const uint32_t theta = (prefix22 << 10) | (uint32_t)sm.bin;
-  const int r = sm.bin_need;   // keys equal to theta to keep, lowest positions first
+  const uint32_t theta = sm.theta;
+  const int r = sm.r;   // keys equal to theta to keep, lowest positions first
   // the keys of the lower ranks above and equal to theta, and this CTA's ties:
   // candidates at positions below t0, and inside [t0, t0 + n)
   int offset, quota;
@@ -318,24 +376,38 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkThre
   // this CTA's kept positions, ascending: a key above theta goes after the keys
   // above theta before it and the kept ties before it
   int n_gt = 0, n_eq = 0;
+#pragma unroll 1
+  for (int q = 0; q < ng; ++q) {
+    const uint4 v = keys4[(i0 >> 2) + q];
+    const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    n_gt += j < nv && k[j] > theta;
-    n_eq += j < nv && k[j] == theta;
+    for (int e = 0; e < 4; ++e) {
+      const bool ok = 4 * q + e < nv;
+      n_gt += ok && kk[e] > theta;
+      n_eq += ok && kk[e] == theta;
+    }
   }
   int tot2;
   const int ex2 = block_exclusive_scan((n_gt << 16) | n_eq, sm.scan, &tot2);
   int gt_b = ex2 >> 16, eq_b = ex2 & 0xFFFF;
+  if (n_gt + n_eq > 0) {
+#pragma unroll 1
+    for (int q = 0; q < ng; ++q) {
+      const uint4 v = keys4[(i0 >> 2) + q];
+      const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    if (j >= nv) continue;
-    if (k[j] > theta) {
-      const int o = offset + gt_b + min(eq_b, quota);
-      if (o < B_e) out[o] = t0 + i0 + j;
-      ++gt_b;
-    } else if (k[j] == theta) {
-      if (eq_b < quota && offset + gt_b + eq_b < B_e) out[offset + gt_b + eq_b] = t0 + i0 + j;
-      ++eq_b;
+      for (int e = 0; e < 4; ++e) {
+        if (4 * q + e >= nv) continue;
+        const int pos = t0 + i0 + 4 * q + e;
+        if (kk[e] > theta) {
+          const int o = offset + gt_b + min(eq_b, quota);
+          if (o < B_e) out[o] = pos;
+          ++gt_b;
+        } else if (kk[e] == theta) {
+          if (eq_b < quota && offset + gt_b + eq_b < B_e) out[offset + gt_b + eq_b] = pos;
+          ++eq_b;
+        }
+      }
     }
   }
   pdl_launch_dependents();   // dependents launch once this CTA is done
@@ -350,7 +422,7 @@ __global__ void k_iota_rows(int32_t* __restrict__ sel, int rows, int n) {
 }
 
 cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32_t* sel, cudaStream_t st,
-                        const unsigned* hist) {
+                        const unsigned* hist, bool cosine_bins) {
   if (B_e == 0) return cudaSuccess;
   if (B_e >= T_len) {
     const size_t total = (size_t)H_kv * T_len;
@@ -362,19 +434,14 @@ cudaError_t launch_topk(const float* scores, int H_kv, int T_len, int B_e, int32
   }
   const int per = ((T_len + kTopkCluster - 1) / kTopkCluster + 3) & ~3;
   cudaError_t e;
-  if (hist != nullptr && per <= 32 * kTopkThreads) {
+  if (hist != nullptr && per <= kFusedSliceCap) {
     // at least 120 KB of shared memory: one CTA per SM (two sharing an SM, as they do when they take
     // SMs while the scorer's CTAs finish, were 40% slower)
-    const size_t smem = std::max<size_t>((size_t)(kCandCap + kStageCap) * 8, 120 * 1024);
+    const size_t smem = std::max<size_t>((size_t)(kCandCap + kStageCap) * 8 + (size_t)per * 4, 120 * 1024);
     const int vec = T_len % 4 == 0 && reinterpret_cast<uintptr_t>(scores) % 16 == 0;
-    auto launch = [&](auto kern) -> cudaError_t {
-      cudaError_t e2 = ensure_smem((const void*)kern, smem);
-      if (e2 != cudaSuccess) return e2;
-      return launch_pdl(kern, dim3(kTopkCluster, H_kv), dim3(kTopkThreads), smem, st, scores, T_len, B_e, sel, per,
-                        hist, vec);
-    };
-    e = per <= 8 * kTopkThreads ? launch(k_topk_fused<8>)
-        : per <= 16 * kTopkThreads ? launch(k_topk_fused<16>) : launch(k_topk_fused<32>);
+    if ((e = ensure_smem((const void*)k_topk_fused, smem)) != cudaSuccess) return e;
+    e = launch_pdl(k_topk_fused, dim3(kTopkCluster, H_kv), dim3(kTopkThreads), smem, st, scores, T_len, B_e, sel, per,
+                   hist, vec, cosine_bins ? 1 : 0);
     count_launches(1);
     return e;
   }
