@@ -147,11 +147,13 @@ int quoka_select_queries(const quoka_shape* shape, const void* Q, int N_q, const
  * owned by the library, which every GPU that loads libquoka.so holds until
  * the process exits.  Same arguments, checks, layout and results as
  * quoka_select_queries, minus (ws, ws_bytes); nothing is allocated.
- * Limit: only very large groups (the clustered one-launch kernel's shared
- * memory above 160 KB, e.g. mean pooling over 64 query heads of one KV head
- * at C = 1024) use the array beyond its 256-byte error header; for them
- * 256 + 8*H_q*C + 4*H_q*ceil(C/64)*d bytes (each region rounded up to 256)
- * must fit in 4 MiB, else QUOKA_ERR_UNSUPPORTED.  The first call on a device
+ * Limit: max pooling uses only the array's 256-byte error header.  Mean
+ * pooling keeps its per-head cosines in the array (a clustered pass per query
+ * head, then a clustered select per KV group) when 256 + 4*H_q*C bytes (the
+ * cosines rounded up to 256) fit in 4 MiB; otherwise it runs one clustered
+ * launch over whole groups, whose shared memory must stay within 160 KB
+ * (about (2 + G)*C/2 + 2*G*d*4 bytes plus 64 KB of staging, G = H_q / H_kv),
+ * else the call returns QUOKA_ERR_UNSUPPORTED.  The first call on a device
  * looks up the array's device address (make that first call before any
  * stream capture).  Every call shares the one array, which keeps the last
  * call's contents: calls that overlap on the GPU (different streams or host

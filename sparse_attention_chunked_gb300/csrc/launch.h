@@ -37,15 +37,17 @@ extern std::atomic<unsigned long long> g_launch_count;
 inline void count_launches(unsigned n) { g_launch_count.fetch_add(n, std::memory_order_relaxed); }
 
 struct WsHeader;
-// Whether launch_select_queries runs the one-launch clustered kernel for this
-// problem (which keeps its intermediates in shared memory and never touches
-// qnorm / qpart / qcos) rather than the three-launch fallback.
-bool select_queries_one_launch(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel);
+// Which path launch_select_queries takes: 1 = one launch of the clustered
+// kernel over whole selection rows (intermediates in shared memory only),
+// 2 = mean pooling split into a clustered pass per query head that writes
+// qcos and a clustered group select (when split_ok), 0 = neither fits.
+int select_queries_path(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel, bool split_ok);
 
-// hdr: where device-side errors (an expired wait) are recorded; may be NULL.
+// The N_q least similar queries per selection row.  qcos: the workspace's
+// [H_q][C] floats, used by path 2.
 cudaError_t launch_select_queries(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel,
-                                  int32_t* q_idx, float* qnorm, float* qpart, float* qcos, WsHeader* hdr,
-                                  cudaStream_t st);
+                                  int32_t* q_idx, float* qcos, WsHeader* hdr, cudaStream_t st,
+                                  bool split_ok = true);
 
 // Operand of the scoring stage: which rows score a KV group's keys.
 //   mode 1 (per-head max pooling): the selected (head, token) pairs of the

@@ -3,29 +3,32 @@
 // the queries that disagree with the crowd".
 //
 // A selection row is a query head, or a KV group with the cosine averaged
-// over the group's heads.  Its N_q smallest cosines are taken by an exact
-// radix select (keys = inverted order-mapped cosines, so ties go to the lower
-// position), written in position order.
+// over the group's heads.  Its N_q smallest cosines are kept (keys =
+// inverted order-mapped cosines, so ties go to the lower position), written
+// in position order.
 //
-// One launch, k_qselect_fused: a cluster of 8 CTAs per selection row, CTA r
-// owning the r-th eighth of the chunk positions.  Each CTA copies its slice
-// of Q into shared memory with bulk copies (64-row chunks, each on its own
-// mbarrier, so the arithmetic starts as the first chunk lands), takes the row
-// norms |q| and the column sums; the cluster adds the slices' sums through
-// distributed shared memory in rank order (deterministic) for M_q; each CTA
-// then computes cos(q, M_q) for its rows from shared memory (a slice larger
-// than the 64 KB staging buffer, or a group of several heads, is staged again
-// piece by piece, from L2) into shared-memory keys.  For N_q <= 256 the
-// selection is a bitonic network (warp_topk.cuh): each warp keeps the top
-// L >= N_q of its keys, warp 0 merges its CTA's lists, CTA 0 merges the
-// cluster's lists through distributed shared memory and writes the winners'
-// positions in ascending order; larger N_q take the cluster radix select of
-// cluster_topk.cuh.  Shapes whose per-CTA shared memory would
-// not fit (very large groups) take three launches instead:
-//   k_qstats : per (head, 64-row block) row norms |q| and partial column sums
-//   k_qcos   : per (head, 64-row block) M_q from the partials (fixed order),
-//              then cos(q, M_q) for the block's rows
-//   k_qselect: per selection row, a block radix select over the cosines.
+// k_qselect_fused: a cluster of 8 CTAs per selection row, CTA r owning the
+// r-th eighth of the chunk positions.  Each CTA copies its slice of Q into
+// shared memory with bulk copies (64-row chunks, each on its own mbarrier, so
+// the arithmetic starts as the first chunk lands), takes the row norms |q|
+// and the column sums; the cluster adds the slices' sums through distributed
+// shared memory in rank order (deterministic) for M_q; each CTA then computes
+// cos(q, M_q) for its rows from shared memory (a slice larger than the 64 KB
+// staging buffer, or a group of several heads, is staged again piece by
+// piece, from L2) into shared-memory keys.  For N_q <= 256 the selection is a
+// bitonic network (warp_topk.cuh): each warp keeps the top L >= N_q of its
+// keys, warp 0 merges its CTA's lists, CTA 0 merges the cluster's lists
+// through distributed shared memory and writes the winners' positions in
+// ascending order; larger N_q take the cluster radix select of
+// cluster_topk.cuh.
+//
+// Mean pooling runs k_qselect_fused with one query head per cluster, writing
+// each head's cosines to the workspace, then k_qselect_groups sums a group's
+// cosines in head order and selects as above: the two passes over Q then run
+// on one cluster per query head instead of one per KV group (a group of four
+// heads took four times as long on a quarter of the clusters).  Where the
+// cosines have no room (the workspace-free entry point's fixed array), the
+// fused kernel takes whole groups in one launch.
 #include "common.cuh"
 #include "launch.h"
 #include <cooperative_groups.h>
@@ -47,39 +50,6 @@ template <typename T, int E>
 struct alignas(sizeof(T) * E) RowSlice {
   T v[E];
 };
-
-// Loads the warp's kRowsPerWarp rows (lane holds elements lane*E .. lane*E+E-1),
-// all loads issued before any use; rows at or beyond C read as zero.
-template <typename T, int D>
-__device__ __forceinline__ void load_rows(const T* __restrict__ Q, int h, int C, int c0, float (*x)[D / 32]) {
-  constexpr int E = D / 32;
-  const int lane = threadIdx.x & 31;
-  RowSlice<T, E> raw[kRowsPerWarp];
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int c = c0 + r;
-    if (c < C) raw[r] = *reinterpret_cast<const RowSlice<T, E>*>(Q + ((size_t)h * C + c) * D + lane * E);
-  }
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-    for (int j = 0; j < E; ++j) x[r][j] = (c0 + r < C) ? to_f32(raw[r].v[j]) : 0.f;
-}
-
-// Rows c0 .. c0 + kRowsPerWarp - 1 of `base` (row stride D), zero at or beyond n.
-template <typename T, int D>
-__device__ __forceinline__ void load_rows_n(const T* __restrict__ base, int n, int c0, float (*x)[D / 32]) {
-  constexpr int E = D / 32;
-  const int lane = threadIdx.x & 31;
-  RowSlice<T, E> raw[kRowsPerWarp];
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r)
-    if (c0 + r < n) raw[r] = *reinterpret_cast<const RowSlice<T, E>*>(base + (size_t)(c0 + r) * D + lane * E);
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-    for (int j = 0; j < E; ++j) x[r][j] = (c0 + r < n) ? to_f32(raw[r].v[j]) : 0.f;
-}
 
 constexpr int kSelCluster = 8;
 constexpr int kSelThreads = 256;
@@ -195,7 +165,7 @@ __device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* ke
 template <typename T, int D>
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
     k_qselect_fused(const T* __restrict__ Q, int C, int G_avg, int n_sel, int per, int sel_p,
-                    int32_t* __restrict__ q_idx, WsHeader* hdr) {
+                    int32_t* __restrict__ q_idx, float* __restrict__ cos_out, WsHeader* hdr) {
   constexpr int E = D / 32;
   extern __shared__ __align__(1024) uint8_t dsm_raw[];
   T* rows_s = reinterpret_cast<T*>(dsm_raw);                                 // staged rows of a piece
@@ -350,14 +320,23 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const float v = G_avg > 1 ? u_s[i] / (float)G_avg : u_s[i];
-    keys_s[i] = ~order_key(v);   // the largest key is the smallest cosine
+  if (cos_out != nullptr) {   // one head per row: its cosines, for the group select (k_qselect_groups)
+    for (int i = threadIdx.x; i < n; i += blockDim.x) cos_out[(size_t)row * C + t0 + i] = u_s[i];
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const float v = G_avg > 1 ? u_s[i] / (float)G_avg : u_s[i];
+      keys_s[i] = ~order_key(v);   // the largest key is the smallest cosine
+    }
   }
   if (threadIdx.x == 0 && *abort && round > 0) {   // let the last staged copies land before the CTA can exit
     for (int c = 0; c * kSelChunkRows < last_pn; ++c) tc::mbar_drain(&rbar[c], (round - 1) & 1);
   }
   __syncthreads();
+  if (cos_out != nullptr) {
+    cluster.sync();   // keep part_s alive until every CTA has read it
+    pdl_launch_dependents();
+    return;
+  }
 
   // 4. the n_sel least similar positions of the row
   int32_t* out = q_idx + (size_t)row * n_sel;
@@ -380,124 +359,47 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(256) k_qstats(const T* __restrict__ Q, int C, float* __restrict__ qnorm,
-                                                float* __restrict__ qpart) {
-  pdl_wait_for(Q);
-  constexpr int E = D / 32;
-  const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c0 = blk * kRowsPerBlock + warp * kRowsPerWarp;
-  float x[kRowsPerWarp][E];
-  load_rows<T, D>(Q, h, C, c0, x);
-  float part[E], ss[kRowsPerWarp];
-#pragma unroll
-  for (int j = 0; j < E; ++j) part[j] = 0.f;
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    ss[r] = 0.f;
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-      part[j] += x[r][j];
-      ss[r] = fmaf(x[r][j], x[r][j], ss[r]);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], o);
-  if (lane < kRowsPerWarp) {
-    float v = ss[0];
-#pragma unroll
-    for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? ss[r] : v;
-    if (c0 + lane < C) qnorm[(size_t)h * C + c0 + lane] = sqrtf(v);
-  }
-  __shared__ float sp[8][D];
-#pragma unroll
-  for (int j = 0; j < E; ++j) sp[warp][lane * E + j] = part[j];
-  __syncthreads();
-  if (threadIdx.x < D) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) s += sp[w][threadIdx.x];
-    qpart[((size_t)h * nblk + blk) * D + threadIdx.x] = s;
-  }
-  pdl_launch_dependents();   // dependents launch once this CTA is done
-}
-
-template <typename T, int D>
-__global__ void __launch_bounds__(256) k_qcos(const T* __restrict__ Q, int C, const float* __restrict__ qpart,
-                                              const float* __restrict__ qnorm, float* __restrict__ qcos) {
-  pdl_wait_for(Q, qpart, qnorm);
-  constexpr int E = D / 32;
-  const int h = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c0 = blk * kRowsPerBlock + warp * kRowsPerWarp;
-  float x[kRowsPerWarp][E];
-  load_rows<T, D>(Q, h, C, c0, x);                 // issued before the mean is ready
-  __shared__ float M[D];
-  __shared__ float mnorm;
-  if (threadIdx.x < D) {
-    float s = 0.f;
-    for (int b = 0; b < nblk; ++b) s += qpart[((size_t)h * nblk + b) * D + threadIdx.x];
-    M[threadIdx.x] = s / (float)C;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < E; ++j) ss = fmaf(M[lane + 32 * j], M[lane + 32 * j], ss);
-    ss = warp_sum(ss);
-    if (lane == 0) mnorm = fmaxf(sqrtf(ss), kNormEps);
-  }
-  __syncthreads();
-  float m[E];
-#pragma unroll
-  for (int j = 0; j < E; ++j) m[j] = M[lane * E + j];
-  float dot[kRowsPerWarp];
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    dot[r] = 0.f;
-#pragma unroll
-    for (int j = 0; j < E; ++j) dot[r] = fmaf(x[r][j], m[j], dot[r]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], o);
-  if (lane < kRowsPerWarp && c0 + lane < C) {
-    float v = dot[0];
-#pragma unroll
-    for (int r = 1; r < kRowsPerWarp; ++r) v = lane == r ? dot[r] : v;
-    const int c = c0 + lane;
-    qcos[(size_t)h * C + c] = v / (fmaxf(qnorm[(size_t)h * C + c], kNormEps) * mnorm);
-  }
-  pdl_launch_dependents();   // dependents launch once this CTA is done
-}
-
-__global__ void __launch_bounds__(256) k_qselect(const float* __restrict__ qcos, int C, int G_avg, int n_sel,
-                                                  int32_t* __restrict__ q_idx) {
+// The group select of mean pooling: the cosines of a KV group's query heads
+// (written by k_qselect_fused running one head per row) are summed in head
+// order and averaged, as the one-launch kernel does for a whole group, and
+// the n_sel least similar positions are kept; the cluster of 8 CTAs splits
+// the positions as k_qselect_fused does.  Splitting the selection this way
+// runs the heavy part (two passes over Q) on one cluster per query head
+// instead of one per KV group.
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
+    k_qselect_groups(const float* __restrict__ qcos, int C, int G_avg, int n_sel, int per, int sel_p,
+                     int32_t* __restrict__ q_idx) {
+  extern __shared__ __align__(16) uint8_t gsel_raw[];
+  uint32_t* keys_s = reinterpret_cast<uint32_t*>(gsel_raw);                       // [per], per % 4 == 0
+  uint64_t* lists = reinterpret_cast<uint64_t*>(gsel_raw + (size_t)per * sizeof(uint32_t));
+  __shared__ ClusterTopkShared tk;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.y;
+  const int t0 = min(C, rank * per), n = min(C, t0 + per) - t0;
   pdl_wait_for(qcos);
-  extern __shared__ __align__(16) uint32_t keys_s[];
-  __shared__ RadixSelectShared rs;
-  const int row = blockIdx.x;
-  for (int c = threadIdx.x; c < C; c += blockDim.x) {
-    float u;
-    if (G_avg == 1) {
-      u = qcos[(size_t)row * C + c];
-    } else {
-      float s = 0.f;
-      for (int k = 0; k < G_avg; ++k) s += qcos[((size_t)row * G_avg + k) * C + c];
-      u = s / (float)G_avg;
-    }
-    keys_s[c] = ~order_key(u);   // the largest key is the smallest cosine
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    float u = 0.f;
+    for (int k = 0; k < G_avg; ++k) u += qcos[((size_t)row * G_avg + k) * C + t0 + i];
+    keys_s[i] = ~order_key(u / (float)G_avg);   // the largest key is the smallest cosine
   }
   __syncthreads();
-  block_radix_topk4(reinterpret_cast<const uint4*>(keys_s), C, n_sel, q_idx + (size_t)row * n_sel, rs);
+  int32_t* out = q_idx + (size_t)row * n_sel;
+  switch (sel_p) {
+    case 1: cluster_warp_topk<1>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 2: cluster_warp_topk<2>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 4: cluster_warp_topk<4>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 8: cluster_warp_topk<8>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    default: {
+      auto key_at = [&](int i) -> uint32_t { return keys_s[i]; };
+      cluster_radix_topk<kSelCluster>(cluster, true, reinterpret_cast<const uint4*>(keys_s), key_at, n, t0, n_sel, out,
+                                      tk);
+    }
+  }
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
-// The one-launch kernel's parameters: slice length per CTA, list length
+// k_qselect_fused's parameters: slice length per CTA, list length
 // 32 * sel_p >= n_sel (0: radix select), dynamic shared memory.
 static void qselect_fused_plan(int d, int G_avg, int C, int n_sel, int* per, int* sel_p, size_t* smem) {
   *per = ((C + kSelCluster - 1) / kSelCluster + 3) & ~3;
@@ -507,52 +409,53 @@ static void qselect_fused_plan(int d, int G_avg, int C, int n_sel, int* per, int
 
 // The clustered kernel runs when its shared memory stays within 160 KB and Q
 // is 16-byte aligned (bulk copies want 16-byte aligned rows).
-bool select_queries_one_launch(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel) {
-  (void)dtype;
-  (void)H_q;
+static bool fused_fits(int d, const void* Q, int G_avg, int C, int n_sel) {
   int per, sel_p;
   size_t fsmem;
   qselect_fused_plan(d, G_avg, C, n_sel, &per, &sel_p, &fsmem);
   return fsmem <= 160 * 1024 && ((uintptr_t)Q & 15u) == 0;
 }
 
+int select_queries_path(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel, bool split_ok) {
+  (void)dtype;
+  (void)H_q;
+  if (G_avg > 1 && split_ok && fused_fits(d, Q, 1, C, n_sel)) return 2;
+  if (fused_fits(d, Q, G_avg, C, n_sel)) return 1;
+  return 0;
+}
+
 template <typename T, int D>
-static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel, int32_t* q_idx,
-                             float* qnorm, float* qpart, float* qcos, WsHeader* hdr, cudaStream_t st) {
+static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel, int32_t* q_idx, float* qcos,
+                             WsHeader* hdr, bool split_ok, cudaStream_t st) {
   const int rows = H_q / G_avg;
+  const int path = select_queries_path(0, D, Q, H_q, G_avg, C, n_sel, split_ok);
+  if (path == 0) return cudaErrorInvalidConfiguration;   // the callers check select_queries_path first
+  const int G_run = path == 2 ? 1 : G_avg;   // the split runs one head per cluster
   int per, sel_p;
   size_t fsmem;
-  qselect_fused_plan(D, G_avg, C, n_sel, &per, &sel_p, &fsmem);
-  if (select_queries_one_launch(0, D, Q, H_q, G_avg, C, n_sel)) {
-    cudaError_t e = ensure_smem((const void*)k_qselect_fused<T, D>, fsmem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(k_qselect_fused<T, D>, dim3(kSelCluster, rows), dim3(kSelThreads), fsmem, st, (const T*)Q, C, G_avg,
-                   n_sel, per, sel_p, q_idx, hdr);
-    count_launches(1);
-    return e;
-  }
-  const int nblk = (C + kRowsPerBlock - 1) / kRowsPerBlock;
-  dim3 grid(nblk, H_q);
-  cudaError_t e = launch_pdl(k_qstats<T, D>, grid, dim3(256), 0, st, (const T*)Q, C, qnorm, qpart);
+  qselect_fused_plan(D, G_run, C, n_sel, &per, &sel_p, &fsmem);
+  cudaError_t e = ensure_smem((const void*)k_qselect_fused<T, D>, fsmem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k_qcos<T, D>, grid, dim3(256), 0, st, (const T*)Q, C, (const float*)qpart, (const float*)qnorm, qcos);
-  if (e != cudaSuccess) return e;
-  const size_t smem = (size_t)((C + 3) & ~3) * sizeof(uint32_t);   // C <= 8192: at most 32 KB
-  e = launch_pdl(k_qselect, dim3(rows), dim3(256), smem, st, (const float*)qcos, C, G_avg, n_sel, q_idx);
-  if (e != cudaSuccess) return e;
-  count_launches(3);
-  return cudaGetLastError();
+  e = launch_pdl(k_qselect_fused<T, D>, dim3(kSelCluster, H_q / G_run), dim3(kSelThreads), fsmem, st, (const T*)Q, C,
+                 G_run, n_sel, per, sel_p, q_idx, path == 2 ? qcos : (float*)nullptr, hdr);
+  count_launches(1);
+  if (e != cudaSuccess || path == 1) return e;
+  const size_t gsmem = (size_t)per * sizeof(uint32_t) + (size_t)(kSelWarps + 1) * 32 * sel_p * sizeof(uint64_t);
+  if ((e = ensure_smem((const void*)k_qselect_groups, gsmem)) != cudaSuccess) return e;
+  e = launch_pdl(k_qselect_groups, dim3(kSelCluster, rows), dim3(kSelThreads), gsmem, st, (const float*)qcos, C, G_avg,
+                 n_sel, per, sel_p, q_idx);
+  count_launches(1);
+  return e;
 }
 
 cudaError_t launch_select_queries(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel,
-                                  int32_t* q_idx, float* qnorm, float* qpart, float* qcos, WsHeader* hdr,
-                                  cudaStream_t st) {
+                                  int32_t* q_idx, float* qcos, WsHeader* hdr, cudaStream_t st, bool split_ok) {
   if (dtype == 0) {
-    return d == 64 ? qsel_impl<__nv_bfloat16, 64>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, hdr, st)
-                   : qsel_impl<__nv_bfloat16, 128>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, hdr, st);
+    return d == 64 ? qsel_impl<__nv_bfloat16, 64>(Q, H_q, G_avg, C, n_sel, q_idx, qcos, hdr, split_ok, st)
+                   : qsel_impl<__nv_bfloat16, 128>(Q, H_q, G_avg, C, n_sel, q_idx, qcos, hdr, split_ok, st);
   }
-  return d == 64 ? qsel_impl<float, 64>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, hdr, st)
-                 : qsel_impl<float, 128>(Q, H_q, G_avg, C, n_sel, q_idx, qnorm, qpart, qcos, hdr, st);
+  return d == 64 ? qsel_impl<float, 64>(Q, H_q, G_avg, C, n_sel, q_idx, qcos, hdr, split_ok, st)
+                 : qsel_impl<float, 128>(Q, H_q, G_avg, C, n_sel, q_idx, qcos, hdr, split_ok, st);
 }
 
 }  // namespace quoka

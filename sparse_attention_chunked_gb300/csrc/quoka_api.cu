@@ -122,7 +122,7 @@ bool use_tensor_cores(const Params& p, const quoka_shape* s, int stage, int N_q 
 // Workspace regions, in order; each stage only touches the prefix it needs:
 //   [header][select scratch][score scratch][chunk intermediates]
 struct Layout {
-  size_t qnorm, qpart, qcos, select_end;
+  size_t qcos, select_end;
   size_t op_f32, op_bf, op_scale, score_end;
   size_t q_idx, scores, hist, sel, ksel, vsel, dec, total;
 };
@@ -133,11 +133,8 @@ struct Layout {
 Layout make_layout(const quoka_shape* s, int N_q, int B, const Params& p, size_t start = sizeof(WsHeader)) {
   Layout L;
   const size_t H_q = s->H_q, H_kv = s->H_kv, C = s->C, d = s->d, T = s->T;
-  const size_t nblk = (C + 63) / 64;
   size_t o = start;
-  L.qnorm = o;  o = align_up(o + H_q * C * 4);
-  L.qpart = o;  o = align_up(o + H_q * nblk * d * 4);
-  L.qcos = o;   o = align_up(o + H_q * C * 4);
+  L.qcos = o;   o = align_up(o + H_q * C * 4);   // per-head cosines of the split mean-pooling select
   L.select_end = o;
   const size_t R = (size_t)score_rows(s, N_q > 0 ? N_q : 1, p);
   const size_t N_pad = (size_t)score_tc_pad_rows((int)R);
@@ -182,14 +179,15 @@ template <typename P> P* at(void* ws, size_t off) { return reinterpret_cast<P*>(
 #define QUOKA_CUDA(x) QUOKA_TRY(cuda_status(x))
 
 int run_select(const quoka_shape* s, const void* Q, int n, const Params& p, int32_t* q_idx, void* ws,
-               const Layout& L, cudaStream_t st) {
+               const Layout& L, cudaStream_t st, bool split_ok = true) {
   const int G = s->H_q / s->H_kv;
   const int G_avg = p.gqa == QUOKA_GQA_MAX ? 1 : G;
   // N_q >= C keeps every query (a decode step's one token, say): the ascending
   // positions 0..C-1, with no cosines to compute
   if (n >= s->C) return cuda_status(launch_topk(nullptr, s->H_q / G_avg, s->C, s->C, q_idx, st));
-  return cuda_status(launch_select_queries(s->dtype, s->d, Q, s->H_q, G_avg, s->C, n, q_idx, at<float>(ws, L.qnorm),
-                                           at<float>(ws, L.qpart), at<float>(ws, L.qcos), at<WsHeader>(ws, 0), st));
+  if (select_queries_path(s->dtype, s->d, Q, s->H_q, G_avg, s->C, n, split_ok) == 0) return QUOKA_ERR_UNSUPPORTED;
+  return cuda_status(launch_select_queries(s->dtype, s->d, Q, s->H_q, G_avg, s->C, n, q_idx, at<float>(ws, L.qcos),
+                                           at<WsHeader>(ws, 0), st, split_ok));
 }
 
 // An optional cache of 1 / max(|k_t|, eps) for the history keys ([H_kv] rows
@@ -466,18 +464,19 @@ int quoka_select_queries_noalloc(const quoka_shape* shape, const void* Q, int N_
   if (N_q < 1 || Q == nullptr || q_idx == nullptr) return QUOKA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(q_idx)) return QUOKA_ERR_ALIGNMENT;
   // The library's scratch array stands in for the workspace, laid out the same
-  // way (error header first).  Only the three-launch fallback of very large
-  // groups reads and writes the regions after the header, so the size limit
-  // applies to that path alone.
+  // way (error header first).  Only the split of mean pooling reads and writes
+  // the region after the header (the per-head cosines), and only when the
+  // layout fits the array; otherwise mean pooling runs the one-launch kernel
+  // over whole groups where its shared memory allows.
   const Layout L = make_layout(shape, N_q, 1, p);
   const int n = n_sel_of(shape, N_q);
   const int G_avg = p.gqa == QUOKA_GQA_MAX ? 1 : shape->H_q / shape->H_kv;
-  const bool fallback =
-      n < shape->C && !select_queries_one_launch(shape->dtype, shape->d, Q, shape->H_q, G_avg, shape->C, n);
-  if (fallback && L.select_end > kNoAllocScratchBytes) return QUOKA_ERR_UNSUPPORTED;
+  const bool fits = L.select_end <= kNoAllocScratchBytes;
+  if (n < shape->C && select_queries_path(shape->dtype, shape->d, Q, shape->H_q, G_avg, shape->C, n, fits) == 0)
+    return QUOKA_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   QUOKA_CUDA(noalloc_scratch(&scratch));
-  return run_select(shape, Q, n, p, q_idx, scratch, L, (cudaStream_t)stream);
+  return run_select(shape, Q, n, p, q_idx, scratch, L, (cudaStream_t)stream, fits);
 }
 
 int quoka_score_keys(const quoka_shape* shape, const void* Q, const int32_t* q_idx, int N_q, const void* K_hist,

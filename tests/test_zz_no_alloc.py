@@ -4,10 +4,11 @@ the workspace entry point on the same inputs, over two calls in a row.
 Some callers cannot give the library any device scratch memory (engine
 plugins whose enqueue path may not allocate, runtimes that plan all device
 memory up front); this entry point keeps the selection kernels' scratch in a
-library-owned device array.  The cases cover both launch paths: the
+library-owned device array.  The cases cover every launch path: the
 one-launch clustered kernel (which needs no scratch beyond the error header)
-and the three-launch fallback of very large groups, which reads and writes
-the array, so a wrong array address or layout offset fails here.
+and the split of mean pooling, which writes the per-head cosines into the
+array and reads them back, so a wrong array address or layout offset fails
+here.
 
 Collected last on purpose (file name), so that a run stopping at the first
 failure has already run every other test."""
@@ -53,20 +54,24 @@ def _check_two_calls(quoka, cases, gqa, launches_expected):
 
 
 @pytest.mark.parametrize("gqa", ["max", "mean"])
-def test_noalloc_matches_workspace_entry_one_launch(quoka, gqa):
-    """Groups small enough for the clustered kernel: one launch, no scratch regions used."""
-    cases = [wl.small_chunk(H_q=8, H_kv=2, d=128, C=300, T=64, N_q=20, B=8, dtype="bf16", seed=1),
-             wl.small_chunk(H_q=4, H_kv=4, d=64, C=97, T=64, N_q=9, B=8, dtype="fp32", seed=2)]
-    _check_two_calls(quoka, cases, gqa, launches_expected=1)
+def test_noalloc_matches_workspace_entry_clustered(quoka, gqa):
+    """Chunks small enough for the clustered kernel.  Max pooling, and mean pooling with one query head
+    per KV head: one launch, no scratch region used.  Mean pooling over several heads: a clustered pass
+    per query head writes its cosines into the array, then the clustered group select reads them."""
+    cases = [(wl.small_chunk(H_q=8, H_kv=2, d=128, C=300, T=64, N_q=20, B=8, dtype="bf16", seed=1), 1, 2),
+             (wl.small_chunk(H_q=4, H_kv=4, d=64, C=97, T=64, N_q=9, B=8, dtype="fp32", seed=2), 1, 1),
+             (wl.small_chunk(H_q=64, H_kv=1, d=128, C=1024, T=64, N_q=64, B=8, dtype="bf16", seed=3), 1, 2),
+             (wl.small_chunk(H_q=32, H_kv=1, d=128, C=4096, T=64, N_q=64, B=8, dtype="bf16", seed=4), 1, 2)]
+    for (cfg, x), n_max, n_mean in cases:
+        _check_two_calls(quoka, [(cfg, x)], gqa, launches_expected=n_max if gqa == "max" else n_mean)
 
 
-def test_noalloc_matches_workspace_entry_three_launch_fallback(quoka):
-    """Mean pooling over 64 or 32 query heads of one KV head: the clustered kernel's shared memory is
-    above its 160 KB limit, so the statistics / cosine / select launches run on the library's array
-    (about 1 and 2 MiB of it)."""
-    cases = [wl.small_chunk(H_q=64, H_kv=1, d=128, C=1024, T=64, N_q=64, B=8, dtype="bf16", seed=3),
-             wl.small_chunk(H_q=32, H_kv=1, d=128, C=4096, T=64, N_q=64, B=8, dtype="bf16", seed=4)]
-    _check_two_calls(quoka, cases, "mean", launches_expected=3)
+def test_noalloc_mean_pooling_beyond_the_array(quoka):
+    """Mean pooling whose cosines would not fit the 4 MiB array (128 query heads x 8192 queries: 4 MiB
+    plus the header) runs the one-launch kernel over whole groups of 8 heads, and matches the workspace
+    entry point (which splits)."""
+    cases = [wl.small_chunk(H_q=128, H_kv=16, d=64, C=8192, T=64, N_q=64, B=8, dtype="bf16", seed=7)]
+    _check_two_calls(quoka, cases, "mean", launches_expected=1)
 
 
 def test_noalloc_keeps_every_query_when_n_q_reaches_c(quoka):
@@ -81,9 +86,9 @@ def test_noalloc_keeps_every_query_when_n_q_reaches_c(quoka):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(quoka):
-    """A fallback-sized problem whose scratch exceeds the 4 MiB array is refused before anything is
-    enqueued (the pointers are never dereferenced): mean pooling over 128 query heads of one KV head
-    at C = 8192 needs about 16 MiB."""
+    """Mean pooling over 128 query heads of one KV head at C = 8192: the per-head cosines need 4 MiB
+    plus the header (more than the array) and the whole-group kernel's shared memory is far above its
+    limit, so the call is refused before anything is enqueued (the pointers are never dereferenced)."""
     shape = quoka.Shape(0, 128, 1, 8192, 0, 128, 0)
     rc = quoka.load().quoka_select_queries_noalloc(ctypes.byref(shape), ctypes.c_void_p(1 << 20), 8,
                                                    ctypes.byref(quoka.params_of("mean")), ctypes.c_void_p(1 << 20),
