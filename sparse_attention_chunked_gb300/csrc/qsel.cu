@@ -23,8 +23,8 @@
 // cluster_topk.cuh.
 //
 // Mean pooling runs k_qselect_fused with one query head per cluster, writing
-// each head's cosines to the workspace, then k_qselect_groups sums a group's
-// cosines in head order and selects as above: the two passes over Q then run
+// each head's cosines to the workspace, then k_qselect_groups (one CTA per KV
+// group) sums a group's cosines in head order and selects by a histogram: the two passes over Q then run
 // on one cluster per query head instead of one per KV group (a group of four
 // heads took four times as long on a quarter of the clusters).  Where the
 // cosines have no room (the workspace-free entry point's fixed array), the
@@ -33,6 +33,7 @@
 #include "launch.h"
 #include <cooperative_groups.h>
 
+#include "block_select.cuh"
 #include "cluster_topk.cuh"
 #include "tc_common.cuh"
 #include "radix_select.cuh"
@@ -359,43 +360,33 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
-// The group select of mean pooling: the cosines of a KV group's query heads
-// (written by k_qselect_fused running one head per row) are summed in head
-// order and averaged, as the one-launch kernel does for a whole group, and
-// the n_sel least similar positions are kept; the cluster of 8 CTAs splits
-// the positions as k_qselect_fused does.  Splitting the selection this way
-// runs the heavy part (two passes over Q) on one cluster per query head
-// instead of one per KV group.
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
-    k_qselect_groups(const float* __restrict__ qcos, int C, int G_avg, int n_sel, int per, int sel_p,
-                     int32_t* __restrict__ q_idx) {
-  extern __shared__ __align__(16) uint8_t gsel_raw[];
-  uint32_t* keys_s = reinterpret_cast<uint32_t*>(gsel_raw);                       // [per], per % 4 == 0
-  uint64_t* lists = reinterpret_cast<uint64_t*>(gsel_raw + (size_t)per * sizeof(uint32_t));
-  __shared__ ClusterTopkShared tk;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
-  const int row = blockIdx.y;
-  const int t0 = min(C, rank * per), n = min(C, t0 + per) - t0;
+// The group select of mean pooling: one CTA per KV group sums the cosines of
+// the group's query heads (written by k_qselect_fused running one head per
+// cluster) in head order and averages them, as the one-launch kernel does for
+// a whole group, then keeps the n_sel least similar positions by the
+// histogram select of block_select.cuh: the keys are inverted order keys of
+// the averaged cosine, binned by the fixed-point bin of its negation (4096
+// bins of width 1/2048 over [-1, 1], non-decreasing in the key).  Splitting
+// the selection this way runs the heavy part (two passes over Q) on one
+// cluster per query head instead of one per KV group.
+constexpr int kRowSelThreads = 1024;
+
+__global__ void __launch_bounds__(kRowSelThreads)
+    k_qselect_groups(const float* __restrict__ qcos, int C, int G_avg, int n_sel, int32_t* __restrict__ q_idx) {
+  extern __shared__ __align__(16) uint8_t rsel_raw[];
+  uint2* cand = reinterpret_cast<uint2*>(rsel_raw);                // [C] (key, position)
+  uint32_t* keys = reinterpret_cast<uint32_t*>(cand + C);          // [C]
+  __shared__ BlockSelectShared bs;
+  const int row = blockIdx.x;
   pdl_wait_for(qcos);
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
     float u = 0.f;
-    for (int k = 0; k < G_avg; ++k) u += qcos[((size_t)row * G_avg + k) * C + t0 + i];
-    keys_s[i] = ~order_key(u / (float)G_avg);   // the largest key is the smallest cosine
+    for (int k = 0; k < G_avg; ++k) u += qcos[((size_t)row * G_avg + k) * C + c];
+    keys[c] = ~order_key(G_avg > 1 ? u / (float)G_avg : u);   // the largest key is the smallest cosine
   }
   __syncthreads();
-  int32_t* out = q_idx + (size_t)row * n_sel;
-  switch (sel_p) {
-    case 1: cluster_warp_topk<1>(cluster, keys_s, n, t0, n_sel, lists, out); return;
-    case 2: cluster_warp_topk<2>(cluster, keys_s, n, t0, n_sel, lists, out); return;
-    case 4: cluster_warp_topk<4>(cluster, keys_s, n, t0, n_sel, lists, out); return;
-    case 8: cluster_warp_topk<8>(cluster, keys_s, n, t0, n_sel, lists, out); return;
-    default: {
-      auto key_at = [&](int i) -> uint32_t { return keys_s[i]; };
-      cluster_radix_topk<kSelCluster>(cluster, true, reinterpret_cast<const uint4*>(keys_s), key_at, n, t0, n_sel, out,
-                                      tk);
-    }
-  }
+  auto bin_of = [](uint32_t key) -> uint32_t { return score_bin(-key_float(~key), true); };
+  block_select_top(keys, C, n_sel, q_idx + (size_t)row * n_sel, 0, cand, bs, bin_of);
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
@@ -440,10 +431,10 @@ static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel
                  G_run, n_sel, per, sel_p, q_idx, path == 2 ? qcos : (float*)nullptr, hdr);
   count_launches(1);
   if (e != cudaSuccess || path == 1) return e;
-  const size_t gsmem = (size_t)per * sizeof(uint32_t) + (size_t)(kSelWarps + 1) * 32 * sel_p * sizeof(uint64_t);
+  const size_t gsmem = (size_t)C * (sizeof(uint2) + sizeof(uint32_t));
   if ((e = ensure_smem((const void*)k_qselect_groups, gsmem)) != cudaSuccess) return e;
-  e = launch_pdl(k_qselect_groups, dim3(kSelCluster, rows), dim3(kSelThreads), gsmem, st, (const float*)qcos, C, G_avg,
-                 n_sel, per, sel_p, q_idx);
+  e = launch_pdl(k_qselect_groups, dim3(rows), dim3(kRowSelThreads), gsmem, st, (const float*)qcos, C, G_avg, n_sel,
+                 q_idx);
   count_launches(1);
   return e;
 }
