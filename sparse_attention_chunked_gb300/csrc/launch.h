@@ -74,7 +74,7 @@ struct OperandSpec {
 //                     unit).
 // Padding rows R..N_pad-1 of op_bf (and their scales) repeat row 0, so they
 // never change a maximum.  hist (NULL or [H_kv][kScoreHistBins]) is zeroed
-// for the scorer that follows.
+// for the scorer that follows.  q_idx NULL selects every position (n = C).
 cudaError_t launch_build_operand(int dtype, int d, const void* Q, const int32_t* q_idx, int H_kv, int C, int G,
                                  int n, OperandSpec spec, int N_pad, float* op_f32, __nv_bfloat16* op_bf,
                                  float* op_scale, unsigned* hist, cudaStream_t st);

@@ -285,11 +285,14 @@ int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const
   int32_t* q_idx = at<int32_t>(ws, L.q_idx);
   float* scores = at<float>(ws, L.scores);
   int32_t* sel = sel_out != nullptr ? sel_out : at<int32_t>(ws, L.sel);
-  QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
+  // N_q >= C keeps every query (a decode step): the operand kernel takes them
+  // all directly, with no index list to write first
+  const bool all_queries = n >= shape->C;
+  if (!all_queries) QUOKA_TRY(run_select(shape, Q, n, p, q_idx, ws, L, st));
   // the scorer also counts a 12-bit histogram of its scores (fixed-point bins
   // for cosines), where the top-B select then starts
   unsigned* hist = at<unsigned>(ws, L.hist);
-  QUOKA_TRY(run_score(shape, Q, q_idx, n, K_hist, p, scores, ws, L, st, kc, hist));
+  QUOKA_TRY(run_score(shape, Q, all_queries ? nullptr : q_idx, n, K_hist, p, scores, ws, L, st, kc, hist));
   QUOKA_CUDA(launch_topk(scores, shape->H_kv, T, B, sel, st, hist, !p.dot));
   if (use_decode(p, shape))   // the decode kernel reads the kept rows through sel: no gathered copy
     return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), sel, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(32 * kOpWarps) k_build_operand(const T* __rest
   float x[E], inv = 1.f;
   for (int p = warp; p < pairs; p += nwarps) {
     const int h = g * G + k0 + p / ni, i = i0 + p % ni;
-    const int c = q_idx[(size_t)(spec.mode == 1 ? h : g) * n + i];
+    const int c = q_idx != nullptr ? q_idx[(size_t)(spec.mode == 1 ? h : g) * n + i] : i;   // NULL: every position
     const T* q = Q + ((size_t)h * C + c) * D;
     float ss = 0.f;
 #pragma unroll
