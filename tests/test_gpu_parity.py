@@ -93,6 +93,9 @@ SMALL = [
     ("iid_recipe_bf16", dict(H_q=4, H_kv=4, d=64, C=128, T=1024, N_q=16, B=256, dtype="bf16", recipe="iid_outliers")),
     # max pooling with 320 scoring rows: two accumulator chunks, the second 64 wide
     ("gqa5_bf16_320_rows", dict(H_q=10, H_kv=2, d=128, C=256, T=2000, N_q=64, B=300, dtype="bf16")),
+    # max pooling with 384 and 512 scoring rows: two accumulator chunks of 192 and 256 columns
+    ("gqa4_bf16_384_rows", dict(H_q=8, H_kv=2, d=128, C=256, T=1500, N_q=96, B=200, dtype="bf16")),
+    ("gqa4_bf16_512_rows", dict(H_q=8, H_kv=2, d=64, C=300, T=2100, N_q=128, B=333, dtype="bf16")),
     # max pooling with 576 scoring rows: wider than TMEM, the CUDA-core scorer takes it
     ("gqa8_bf16_576_rows", dict(H_q=16, H_kv=2, d=64, C=100, T=900, N_q=72, B=111, dtype="bf16")),
     # decode-size chunks (G * C <= 32): the split-key attention, 64-key blocks with ragged tails
