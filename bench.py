@@ -1043,6 +1043,8 @@ def run_suite(args, rank, world, local_rank):
         sub = copy.copy(args)
         sub.workload, sub.gqa = workload, gqa
         sub.steps = max(10, args.steps // 2)
+        if workload == "decode32k":   # a ~45 us step: more steps for a stable mean at no real cost
+            sub.steps = max(100, args.steps)
         if workload == "sweep64k":
             r = run_sweep(sub, rank, world, local_rank)
         elif workload in RAGGED:
