@@ -247,9 +247,12 @@ typedef struct {
   int32_t reserved;        /* must be 0 */
 } quoka_varlen_shape;
 
-/* Workspace bytes for quoka_chunk_attend_varlen: the 256-byte error header
- * plus one slice per stream lane (one lane per sequence with C_s > 0, at most
- * 8), each slice the largest single-sequence requirement of the batch.
+/* Workspace bytes for quoka_chunk_attend_varlen: the 256-byte error header,
+ * then the kept K and V rows of every sequence that attends in the joint
+ * launch and selects keys (0 < B < T_s; 2 * H_kv * B * d elements each,
+ * every block rounded up to 256 bytes), then one slice per stream lane (one
+ * lane per sequence with C_s > 0, at most 8), each slice the largest
+ * single-sequence requirement of the batch without those rows.
  * cu_T, cu_C as for quoka_chunk_attend_varlen. */
 int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
                                 int N_q, int B, const quoka_params* params, size_t* bytes);
@@ -278,12 +281,40 @@ int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* 
  * everything enqueued on `stream` so far; `stream` then waits for every lane,
  * so the call behaves as one unit of work on `stream` (and stream capture
  * records the fork and the join).  Each lane uses its own slice of ws; the
- * error header is shared.  Concurrent calls from several host threads are
- * serialised on the lane streams. */
+ * error header is shared.  Sequences whose attention runs on the tensor cores
+ * (bf16, G * C_s > 32 or the tensor engine forced) stop on their lane after
+ * the gather: after the join, one persistent attention launch per 16 such
+ * sequences, on `stream`, attends for all of them, its work items (query
+ * tile x head pair) ordered longest first over the whole batch.  The results
+ * are those of quoka_chunk_attend on each sequence, bit for bit.  Concurrent
+ * calls from several host threads are serialised on the lane streams. */
 int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
                               const void* Q, const void* K_hist, const void* V_hist, const void* K_chunk,
                               const void* V_chunk, int N_q, int B, const quoka_params* params, void* O, float* lse,
                               int32_t* sel_out, void* ws, size_t ws_bytes, void* stream);
+
+/* quoka_sparse_attend over a ragged batch ([P1] "Chunked Prefill with QUOKA":
+ * each sequence attends to its own kept rows and its causal chunk): one
+ * persistent tensor-core launch per 16 sequences spreads the work items
+ * (query tile x head pair) of every sequence, longest first over the whole
+ * batch, over one CTA per SM.  cu_B and cu_C are HOST int64 arrays of
+ * nseq + 1 prefix sums (cu[0] = 0, non-decreasing): sequence s has
+ * B_s = cu_B[s+1] - cu_B[s] kept rows (0 allowed) and C_s = cu_C[s+1] - cu_C[s]
+ * queries (0: the sequence is skipped; each C_s <= 8192).  Packed tensors,
+ * sequence-major:
+ *   Q, O          start at element H_q  * d * cu_C[s]   ([H_q,  C_s, d])
+ *   K_sel, V_sel  start at element H_kv * d * cu_B[s]   ([H_kv, B_s, d])
+ *   K/V_chunk     start at element H_kv * d * cu_C[s]   ([H_kv, C_s, d])
+ *   lse           starts at H_q * cu_C[s]               (fp32 [H_q, C_s]; may be NULL)
+ * lse needs 4-byte alignment, the other tensors 16 bytes.  bf16 only, and
+ * not with QUOKA_ENGINE_SIMT (QUOKA_ERR_UNSUPPORTED); of params only
+ * softmax_scale is read.  ws: the 256-byte error header.  Each sequence's
+ * O and lse are those of quoka_sparse_attend with QUOKA_ENGINE_TENSOR on that
+ * sequence, bit for bit. */
+int quoka_sparse_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu_B, const int64_t* cu_C,
+                               const void* Q, const void* K_sel, const void* V_sel, const void* K_chunk,
+                               const void* V_chunk, const quoka_params* params, void* O, float* lse, void* ws,
+                               size_t ws_bytes, void* stream);
 
 /* quoka_chunk_attend with the history's key norms from the cache (as
  * quoka_score_keys_cached). */

@@ -31,6 +31,10 @@
 // the other keeps the pipe fed.  Every wait is bounded;
 // on a timeout the CTA records QUOKA_ERR_TIMEOUT, drains what it has in
 // flight, frees TMEM and exits.
+#include <string.h>
+
+#include <algorithm>
+
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -104,27 +108,52 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Work item i (0 = most key blocks): query tile qt = n_qt - 1 - i / (H_kv * pairs)
-// of KV group g and head pair hp.  CTA c of P runs items c, 2P - 1 - c, 2P + c,
+// What one launch attends: NS sequences (1 for a single chunk, up to
+// kAttVarSeqs for a ragged batch), each with its own tensor maps, chunk length,
+// kept history rows and output.  A "run" is one query tile of one sequence;
+// every run holds H_kv * pairs work items of the same length.
+template <int NS>
+struct AttArgs {
+  CUtensorMap q[NS], kh[NS], vh[NS], kc[NS], vc[NS];
+  __nv_bfloat16* O[NS];
+  float* lse[NS];
+  int C[NS], n_hist[NS];
+  int n_items;
+  int n_qt;                         // NS == 1: the query tiles of the one sequence, longest (last) first
+  uint16_t run[NS == 1 ? 2 : NS * 64];   // NS > 1: sequence << 8 | query tile, longest first
+};
+
+// Work item i (0 = most key blocks) is head pair hp of KV group g in run
+// i / (H_kv * pairs).  CTA c of P runs items c, 2P - 1 - c, 2P + c,
 // 4P - 1 - c, ...: a serpentine over the longest-first list, so the CTAs that
 // drew the longest first items draw the shortest second ones.
 struct AttItem {
-  int qt, g, h0, n_slots, n_blocks;
+  int seq, qt, g, h0, n_slots, nh, n_blocks;
 };
 
 __device__ __forceinline__ int att_item_index(int c, int round, int P) {
   return (round & 1) ? (round + 1) * P - 1 - c : round * P + c;
 }
 
-__device__ __forceinline__ AttItem att_item(int i, int n_qt, int H_kv_pairs, int pairs, int G, int nh) {
+template <int NS>
+__device__ __forceinline__ AttItem att_item(const AttArgs<NS>& a, int i, int H_kv_pairs, int pairs, int G) {
   AttItem it;
-  it.qt = n_qt - 1 - i / H_kv_pairs;
-  const int rem = i % H_kv_pairs;
+  const int run = i / H_kv_pairs;
+  if constexpr (NS == 1) {
+    it.seq = 0;
+    it.qt = a.n_qt - 1 - run;
+  } else {
+    const unsigned v = a.run[run];
+    it.seq = (int)(v >> 8);
+    it.qt = (int)(v & 255u);
+  }
+  const int rem = i - run * H_kv_pairs;
   it.g = rem / pairs;
-  const int hp = rem % pairs;
+  const int hp = rem - it.g * pairs;
   it.h0 = it.g * G + 2 * hp;
   it.n_slots = (2 * hp + 1 < G) ? 2 : 1;
-  it.n_blocks = nh + it.qt + 1;
+  it.nh = (a.n_hist[it.seq] + 127) >> 7;
+  it.n_blocks = it.nh + it.qt + 1;
   return it;
 }
 
@@ -242,12 +271,9 @@ __device__ __noinline__ bool softmax_item(AttSmem* sm, uint8_t* p_row, int s, in
   return true;
 }
 
-template <int D>
+template <int D, int NS>
 __global__ void __launch_bounds__(kAttThreads, 1)
-    k_attend_tc(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap khmap,
-                const __grid_constant__ CUtensorMap vhmap, const __grid_constant__ CUtensorMap kcmap,
-                const __grid_constant__ CUtensorMap vcmap, int n_hist, int C, int G, int H_kv, float scale_log2,
-                __nv_bfloat16* __restrict__ O, float* __restrict__ lse, WsHeader* hdr) {
+    k_attend_tc(const __grid_constant__ AttArgs<NS> a, int G, int H_kv, float scale_log2, WsHeader* hdr) {
   constexpr int HALVES = D / 64;
   constexpr uint32_t kHalfBytes = 128 * 128;            // 128 rows x 128 bytes
   constexpr uint32_t kTileBytes = HALVES * kHalfBytes;  // one Q, K or V tile of 128 rows
@@ -260,11 +286,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   AttSmem* sm = reinterpret_cast<AttSmem*>(kv_s + kKvStages * kTileBytes);
 
   const int pairs = (G + 1) / 2;
-  const int n_qt = (C + 127) / 128;
   const int H_kv_pairs = H_kv * pairs;
-  const int n_items = n_qt * H_kv_pairs;
+  const int n_items = a.n_items;
   const int P = gridDim.x, cta = blockIdx.x;
-  const int nh = (n_hist + 127) / 128;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -293,10 +317,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   if (threadIdx.x == 0 && cta < n_items) {
     // The first item's query tiles do not come from the previous kernel (the
     // kept K/V rows do): start them towards L2 while that kernel finishes.
-    const AttItem it0 = att_item(att_item_index(cta, 0, P), n_qt, H_kv_pairs, pairs, G, nh);
-    tc::tma_prefetch_desc(&qmap);
+    const AttItem it0 = att_item(a, att_item_index(cta, 0, P), H_kv_pairs, pairs, G);
+    const CUtensorMap* qm = &a.q[it0.seq];
+    tc::tma_prefetch_desc(qm);
     for (int s = 0; s < it0.n_slots; ++s)
-      for (int hf = 0; hf < HALVES; ++hf) tc::tma_prefetch_l2_3d(&qmap, hf * 64, it0.qt * 128, it0.h0 + s);
+      for (int hf = 0; hf < HALVES; ++hf) tc::tma_prefetch_l2_3d(qm, hf * 64, it0.qt * 128, it0.h0 + s);
   }
   pdl_wait();                                   // inputs may come from the previous kernel
   tc::tc_fence_before();
@@ -308,33 +333,39 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer: per work item Q, then K_j, V_j, ...
     if (lane == 0) {
-      tc::tma_prefetch_desc(&qmap);
-      tc::tma_prefetch_desc(&kcmap);
-      tc::tma_prefetch_desc(&vcmap);
-      if (nh > 0) {
-        tc::tma_prefetch_desc(&khmap);
-        tc::tma_prefetch_desc(&vhmap);
-      }
       int k = 0, n_done = 0;                    // ring items issued; work items started
+      int seq_maps = -1;                         // the sequence whose maps were last prefetched
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int i = att_item_index(cta, round, P);
         if (i >= n_items) break;
-        const AttItem it = att_item(i, n_qt, H_kv_pairs, pairs, G, nh);
+        const AttItem it = att_item(a, i, H_kv_pairs, pairs, G);
+        const CUtensorMap* qm = &a.q[it.seq];
+        if (it.seq != seq_maps) {
+          seq_maps = it.seq;
+          tc::tma_prefetch_desc(qm);
+          tc::tma_prefetch_desc(&a.kc[it.seq]);
+          tc::tma_prefetch_desc(&a.vc[it.seq]);
+          if (it.nh > 0) {
+            tc::tma_prefetch_desc(&a.kh[it.seq]);
+            tc::tma_prefetch_desc(&a.vh[it.seq]);
+          }
+        }
         // Q of this item, once every S MMA of the previous one has read the old Q
         if (n_done > 0 && !(ok = tc::mbar_wait(&sm->q_free, (n_done - 1) & 1, abort, hdr, 0x20a))) break;
         tc::mbar_arrive_expect_tx(&sm->q_full, it.n_slots * kTileBytes);
         for (int s = 0; s < it.n_slots; ++s)
           for (int hf = 0; hf < HALVES; ++hf)
-            tc::tma_load_3d(q_s + s * kTileBytes + hf * kHalfBytes, &qmap, &sm->q_full, hf * 64, it.qt * 128,
+            tc::tma_load_3d(q_s + s * kTileBytes + hf * kHalfBytes, qm, &sm->q_full, hf * 64, it.qt * 128,
                             it.h0 + s);
         ++n_done;
         // the next item's query tiles towards L2, so that its Q load after this item is a short one
         const int i_next = att_item_index(cta, round + 1, P);
         if (i_next < n_items) {
-          const AttItem nx = att_item(i_next, n_qt, H_kv_pairs, pairs, G, nh);
+          const AttItem nx = att_item(a, i_next, H_kv_pairs, pairs, G);
+          const CUtensorMap* nqm = &a.q[nx.seq];
           for (int s = 0; s < nx.n_slots; ++s)
-            for (int hf = 0; hf < HALVES; ++hf) tc::tma_prefetch_l2_3d(&qmap, hf * 64, nx.qt * 128, nx.h0 + s);
+            for (int hf = 0; hf < HALVES; ++hf) tc::tma_prefetch_l2_3d(nqm, hf * 64, nx.qt * 128, nx.h0 + s);
         }
         // Ring items in the order the MMA warps consume them: K_0, then for every
         // block j: K_{j+1} (used early, by S of the next block) and V_j (used late).
@@ -342,9 +373,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           const int s = k % kKvStages;
           if (k >= kKvStages && !tc::mbar_wait(&sm->kv_empty[s], ((k / kKvStages) - 1) & 1, abort, hdr, 0x201))
             return false;
-          const bool hist = jb < nh;
-          const int row = hist ? jb * 128 : (jb - nh) * 128;
-          const CUtensorMap* map = hist ? (which == 0 ? &khmap : &vhmap) : (which == 0 ? &kcmap : &vcmap);
+          const bool hist = jb < it.nh;
+          const int row = hist ? jb * 128 : (jb - it.nh) * 128;
+          const CUtensorMap* map = hist ? (which == 0 ? &a.kh[it.seq] : &a.vh[it.seq])
+                                        : (which == 0 ? &a.kc[it.seq] : &a.vc[it.seq]);
           tc::mbar_arrive_expect_tx(&sm->kv_full[s], kTileBytes);
           for (int hf = 0; hf < HALVES; ++hf)
             tc::tma_load_3d(kv_s + s * kTileBytes + hf * kHalfBytes, map, &sm->kv_full[s], hf * 64, row, it.g);
@@ -381,7 +413,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       for (int round = 0, n_done = 0; ok; ++round, ++n_done) {
         const int i = att_item_index(cta, round, P);
         if (i >= n_items) break;
-        const AttItem it = att_item(i, n_qt, H_kv_pairs, pairs, G, nh);
+        const AttItem it = att_item(a, i, H_kv_pairs, pairs, G);
         if (s_issuer) {
           auto issue_s = [&](int s, int stage) {   // S_s = Q_s K^T, K in `stage`
             const uint32_t qb = qb0 + s * kTileBytes, kb = kvb + stage * kTileBytes;
@@ -460,10 +492,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     for (int round = 0;; ++round) {
       const int i = att_item_index(cta, round, P);
       if (i >= n_items) break;
-      const AttItem it = att_item(i, n_qt, H_kv_pairs, pairs, G, nh);
+      const AttItem it = att_item(a, i, H_kv_pairs, pairs, G);
       if (s >= it.n_slots) continue;
-      if (!softmax_item<D>(sm, p_row, s, lane, r, s_addr, nb, it.n_blocks, nh, n_hist, it.qt, C, it.h0 + s, scale_log2,
-                           O, lse, hdr))
+      if (!softmax_item<D>(sm, p_row, s, lane, r, s_addr, nb, it.n_blocks, it.nh, a.n_hist[it.seq], it.qt,
+                           a.C[it.seq], it.h0 + s, scale_log2, a.O[it.seq], a.lse[it.seq], hdr))
         break;
       nb += it.n_blocks;
     }
@@ -483,44 +515,98 @@ size_t attend_tc_smem(int d) {
   return 1024 + (size_t)(2 + kKvStages) * (d / 64) * 128 * 128 + 2 * (size_t)kPBytes + sizeof(AttSmem);
 }
 
-cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
-                             const void* Kc, const void* Vc, int H_q, int H_kv, int C, float scale, void* O,
-                             float* lse, WsHeader* hdr, cudaStream_t st) {
-  const int G = H_q / H_kv;
-  CUtensorMap qmap, khmap, vhmap, kcmap, vcmap;
+namespace {
+
+// The five tensor maps of sequence slot k: Q [H_q, C, d], history K/V
+// [H_kv, n_hist, d] with heads h_stride elements apart, chunk K/V [H_kv, C, d].
+template <int NS>
+cudaError_t fill_att_seq(AttArgs<NS>& a, int k, int d, const AttSeq& q, int H_q, int H_kv) {
   cudaError_t e;
-  if ((e = make_tmap_bf16_3d(&qmap, Q, d, C, H_q, (uint64_t)d * 2, (uint64_t)C * d * 2, 64, 128)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_3d(&kcmap, Kc, d, C, H_kv, (uint64_t)d * 2, (uint64_t)C * d * 2, 64, 128)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_3d(&vcmap, Vc, d, C, H_kv, (uint64_t)d * 2, (uint64_t)C * d * 2, 64, 128)) != cudaSuccess) return e;
-  if (n_hist > 0) {
-    if ((e = make_tmap_bf16_3d(&khmap, Kh, d, n_hist, H_kv, (uint64_t)d * 2, (uint64_t)h_stride * 2, 64, 128)) != cudaSuccess) return e;
-    if ((e = make_tmap_bf16_3d(&vhmap, Vh, d, n_hist, H_kv, (uint64_t)d * 2, (uint64_t)h_stride * 2, 64, 128)) != cudaSuccess) return e;
+  const uint64_t row = (uint64_t)d * 2, chunk_head = (uint64_t)q.C * d * 2;
+  if ((e = make_tmap_bf16_3d(&a.q[k], q.Q, d, q.C, H_q, row, chunk_head, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_3d(&a.kc[k], q.Kc, d, q.C, H_kv, row, chunk_head, 64, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_3d(&a.vc[k], q.Vc, d, q.C, H_kv, row, chunk_head, 64, 128)) != cudaSuccess) return e;
+  if (q.n_hist > 0) {
+    const uint64_t hs = (uint64_t)q.h_stride * 2;
+    if ((e = make_tmap_bf16_3d(&a.kh[k], q.Kh, d, q.n_hist, H_kv, row, hs, 64, 128)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16_3d(&a.vh[k], q.Vh, d, q.n_hist, H_kv, row, hs, 64, 128)) != cudaSuccess) return e;
   } else {   // never read: no history blocks
-    khmap = kcmap;
-    vhmap = vcmap;
+    a.kh[k] = a.kc[k];
+    a.vh[k] = a.vc[k];
   }
-  const int n_qt = (C + 127) / 128;
-  const int pairs = (G + 1) / 2;
-  const int n_items = n_qt * H_kv * pairs;
+  a.O[k] = (__nv_bfloat16*)q.O;
+  a.lse[k] = q.lse;
+  a.C[k] = q.C;
+  a.n_hist[k] = q.n_hist;
+  return cudaSuccess;
+}
+
+template <int NS>
+cudaError_t launch_att(int d, const AttArgs<NS>& a, int G, int H_kv, float scale, WsHeader* hdr, cudaStream_t st) {
   int dev = 0, sms = 0;
+  cudaError_t e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  dim3 grid(n_items < sms ? n_items : sms);     // persistent: one CTA per SM, looping over work items
+  const dim3 grid(a.n_items < sms ? a.n_items : sms);   // persistent: one CTA per SM, looping over work items
   const size_t smem = attend_tc_smem(d);
   const float scale_log2 = scale * 1.4426950408889634f;
   if (d == 64) {
-    if ((e = ensure_smem((const void*)k_attend_tc<64>, smem)) != cudaSuccess) return e;
-    if ((e = launch_pdl(k_attend_tc<64>, grid, dim3(kAttThreads), smem, st, qmap, khmap, vhmap, kcmap, vcmap, n_hist, C,
-                        G, H_kv, scale_log2, (__nv_bfloat16*)O, lse, hdr)) != cudaSuccess)
-      return e;
+    if ((e = ensure_smem((const void*)k_attend_tc<64, NS>, smem)) != cudaSuccess) return e;
+    e = launch_pdl(k_attend_tc<64, NS>, grid, dim3(kAttThreads), smem, st, a, G, H_kv, scale_log2, hdr);
   } else {
-    if ((e = ensure_smem((const void*)k_attend_tc<128>, smem)) != cudaSuccess) return e;
-    if ((e = launch_pdl(k_attend_tc<128>, grid, dim3(kAttThreads), smem, st, qmap, khmap, vhmap, kcmap, vcmap, n_hist,
-                        C, G, H_kv, scale_log2, (__nv_bfloat16*)O, lse, hdr)) != cudaSuccess)
-      return e;
+    if ((e = ensure_smem((const void*)k_attend_tc<128, NS>, smem)) != cudaSuccess) return e;
+    e = launch_pdl(k_attend_tc<128, NS>, grid, dim3(kAttThreads), smem, st, a, G, H_kv, scale_log2, hdr);
   }
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* Vh, int64_t h_stride, int n_hist,
+                             const void* Kc, const void* Vc, int H_q, int H_kv, int C, float scale, void* O,
+                             float* lse, WsHeader* hdr, cudaStream_t st) {
+  AttArgs<1> a;
+  memset(&a, 0, sizeof(a));
+  const AttSeq q{Q, Kh, Vh, Kc, Vc, h_stride, n_hist, C, O, lse};
+  cudaError_t e = fill_att_seq(a, 0, d, q, H_q, H_kv);
+  if (e != cudaSuccess) return e;
+  const int G = H_q / H_kv;
+  a.n_qt = (C + 127) / 128;
+  a.n_items = a.n_qt * H_kv * ((G + 1) / 2);
+  return launch_att(d, a, G, H_kv, scale, hdr, st);
+}
+
+cudaError_t launch_attend_tc_varlen(int d, const AttSeq* seqs, int nseq, int H_q, int H_kv, float scale, WsHeader* hdr,
+                                    cudaStream_t st) {
+  const int G = H_q / H_kv, pairs = (G + 1) / 2;
+  for (int s0 = 0; s0 < nseq; s0 += kAttVarSeqs) {
+    const int n = nseq - s0 < kAttVarSeqs ? nseq - s0 : kAttVarSeqs;
+    static thread_local AttArgs<kAttVarSeqs> a;   // 13 KB: kept off the stack
+    memset(&a, 0, sizeof(a));
+    // runs (sequence, query tile) longest first; equal lengths keep batch order
+    struct Run {
+      int len;
+      uint16_t code;
+    };
+    Run runs[kAttVarSeqs * 64];
+    int n_runs = 0;
+    for (int k = 0; k < n; ++k) {
+      const AttSeq& q = seqs[s0 + k];
+      if (q.C < 1 || q.C > 64 * 128 || q.n_hist < 0) return cudaErrorInvalidValue;
+      cudaError_t e = fill_att_seq(a, k, d, q, H_q, H_kv);
+      if (e != cudaSuccess) return e;
+      const int nh = (q.n_hist + 127) / 128;
+      for (int qt = 0; qt < (q.C + 127) / 128; ++qt) runs[n_runs++] = Run{nh + qt + 1, (uint16_t)((k << 8) | qt)};
+    }
+    std::stable_sort(runs, runs + n_runs, [](const Run& x, const Run& y) { return x.len > y.len; });
+    for (int r = 0; r < n_runs; ++r) a.run[r] = runs[r].code;
+    a.n_items = n_runs * H_kv * pairs;
+    cudaError_t e = launch_att(d, a, G, H_kv, scale, hdr, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace quoka

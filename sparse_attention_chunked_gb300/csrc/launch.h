@@ -130,6 +130,22 @@ cudaError_t launch_attend_tc(int d, const void* Q, const void* Kh, const void* V
                              const void* Kc, const void* Vc, int H_q, int H_kv, int C, float scale, void* O,
                              float* lse, WsHeader* hdr, cudaStream_t st);
 
+// One sequence of a ragged tensor-core attention launch: arguments as
+// launch_attend_tc's (C in [1, 8192], O and lse this sequence's own).
+struct AttSeq {
+  const void *Q, *Kh, *Vh, *Kc, *Vc;
+  int64_t h_stride;
+  int n_hist, C;
+  void* O;
+  float* lse;
+};
+// Sequences per ragged launch; a longer list is covered by consecutive launches.
+constexpr int kAttVarSeqs = 16;
+// Every sequence's work items (query tile x head pair) in one persistent
+// launch per kAttVarSeqs sequences, longest first over the whole batch.
+cudaError_t launch_attend_tc_varlen(int d, const AttSeq* seqs, int nseq, int H_q, int H_kv, float scale, WsHeader* hdr,
+                                    cudaStream_t st);
+
 // The library-owned scratch of quoka_select_queries_noalloc: its device
 // address on the current device (looked up on the first call per device).
 constexpr size_t kNoAllocScratchBytes = 4u << 20;

@@ -129,8 +129,10 @@ struct Layout {
 
 // Regions start at `start` (just past the header for a single call; a lane's
 // slice for the ragged entry point).  The header is always the workspace's
-// first 256 bytes, shared by every lane.
-Layout make_layout(const quoka_shape* s, int N_q, int B, const Params& p, size_t start = sizeof(WsHeader)) {
+// first 256 bytes, shared by every lane.  gather = false leaves out the
+// gathered K/V rows (the ragged entry point keeps them outside the lanes).
+Layout make_layout(const quoka_shape* s, int N_q, int B, const Params& p, size_t start = sizeof(WsHeader),
+                   bool gather = true) {
   Layout L;
   const size_t H_q = s->H_q, H_kv = s->H_kv, C = s->C, d = s->d, T = s->T;
   size_t o = start;
@@ -148,8 +150,9 @@ Layout make_layout(const quoka_shape* s, int N_q, int B, const Params& p, size_t
   L.scores = o; o = align_up(o + H_kv * T * 4);
   L.hist = o;   o = align_up(o + H_kv * kScoreHistBins * 4);
   L.sel = o;    o = align_up(o + H_kv * B_e * 4);
-  L.ksel = o;   o = align_up(o + H_kv * B_e * d * elt_bytes(s->dtype));
-  L.vsel = o;   o = align_up(o + H_kv * B_e * d * elt_bytes(s->dtype));
+  const size_t kept = gather ? H_kv * B_e * d * elt_bytes(s->dtype) : 0;
+  L.ksel = o;   o = align_up(o + kept);
+  L.vsel = o;   o = align_up(o + kept);
   L.dec = o;    o = align_up(o + (use_decode(p, s) ? attend_decode_ws_bytes(s->d, s->H_q, s->C, s->T) : 0));
   L.total = o;
   return L;
@@ -269,15 +272,24 @@ int check_chunk_args(const quoka_shape* shape, const void* Q, const void* K_hist
   return QUOKA_OK;
 }
 
+// Where the ragged entry point wants a chunk's kept K/V rows ([H_kv, B, d]
+// each): that chunk's attention runs later, in one launch over the batch.
+struct KeepOnly {
+  void* K;
+  void* V;
+};
+
 // One chunk, arguments already checked: select queries, score the history,
 // keep the top-B keys, gather them and attend.  T = 0 or B >= T attends to the
-// whole history instead.
+// whole history instead.  With `keep`, the chunk stops after the gather (into
+// keep's rows; nothing to gather when every history key is kept).
 int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const void* V_hist, const void* K_chunk,
               const void* V_chunk, int N_q, int B, const Params& p, void* O, float* lse, int32_t* sel_out, void* ws,
-              const Layout& L, cudaStream_t st, KeyCache kc = KeyCache()) {
+              const Layout& L, cudaStream_t st, KeyCache kc = KeyCache(), const KeepOnly* keep = nullptr) {
   const int T = shape->T;
   if (T == 0 || B >= T) {   // every history key is kept: dense chunked-prefill attention
     if (sel_out != nullptr && T > 0) QUOKA_CUDA(launch_topk(nullptr, shape->H_kv, T, T, sel_out, st));
+    if (keep != nullptr) return QUOKA_OK;
     return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), nullptr, T, K_chunk, V_chunk, p, O, lse, ws,
                       L.dec, st);
   }
@@ -297,10 +309,11 @@ int run_chunk(const quoka_shape* shape, const void* Q, const void* K_hist, const
   if (use_decode(p, shape))   // the decode kernel reads the kept rows through sel: no gathered copy
     return run_attend(shape, Q, K_hist, V_hist, head_stride(shape), sel, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,
                       st);
-  void* ksel = at<void>(ws, L.ksel);
-  void* vsel = at<void>(ws, L.vsel);
+  void* ksel = keep != nullptr ? keep->K : at<void>(ws, L.ksel);
+  void* vsel = keep != nullptr ? keep->V : at<void>(ws, L.vsel);
   QUOKA_CUDA(launch_gather(elt_bytes(shape->dtype), shape->d, K_hist, V_hist, head_stride(shape), sel, shape->H_kv, B,
                            T, ksel, vsel, at<WsHeader>(ws, 0), st));
+  if (keep != nullptr) return QUOKA_OK;
   return run_attend(shape, Q, ksel, vsel, (int64_t)B * shape->d, nullptr, B, K_chunk, V_chunk, p, O, lse, ws, L.dec,
                     st);
 }
@@ -339,8 +352,23 @@ struct SeqArgs {
   int32_t* sel_out;
   Params p;
   Layout L;
+  bool joint;        // attends in the batch's joint tensor-core launch
+  size_t kept;       // joint and selecting: offset of its gathered K rows (V rows follow)
   double work;
 };
+
+// A ragged batch's sequences whose attention runs on the tensor cores (bf16,
+// more than decode size) attend in one joint launch over the whole batch, so
+// that its work items balance across the SMs; the lanes run their selection
+// only.  The rest (decode-size chunks, fp32) run whole on the lanes.
+bool joint_attention(const quoka_shape& sh, const Params& p) { return use_tensor_cores(p, &sh, 1); }
+
+// Bytes of one joint sequence's gathered K and V rows (both), 0 when it keeps
+// every history key (attended in place) or has none.
+size_t joint_kept_bytes(const quoka_shape& sh, int B) {
+  if (sh.T == 0 || B >= sh.T) return 0;
+  return 2 * align_up((size_t)sh.H_kv * B * sh.d * elt_bytes(sh.dtype));
+}
 
 // Streams the ragged entry point runs sequences on: sequences of one batch
 // share nothing, so their launches may overlap on the GPU.
@@ -352,26 +380,32 @@ int varlen_lanes(const quoka_varlen_shape* v, const int64_t* cu_C) {
   return std::max(1, std::min(busy, kMaxLanes));
 }
 
-// Workspace of one lane: room for the largest sequence's regions.
+// Workspace of one lane: room for the largest sequence's regions (without
+// the gathered rows of joint sequences); *kept: the joint sequences' gathered
+// rows, which sit between the header and the lanes.
 int varlen_lane_bytes(const quoka_varlen_shape* v, const int64_t* cu_T, const int64_t* cu_C, int N_q, int B,
-                      const quoka_params* params, size_t* out) {
-  size_t lane = 0;
+                      const quoka_params* params, size_t* out, size_t* kept) {
+  size_t lane = 0, rows = 0;
   for (int s = 0; s < v->nseq; ++s) {
     const quoka_shape sh = seq_shape(v, cu_T, cu_C, s);
     if (sh.C == 0) continue;
     Params p;
     QUOKA_TRY(read_params(params, &sh, &p));
-    lane = std::max(lane, make_layout(&sh, N_q, B, p).total - sizeof(WsHeader));
+    const bool joint = joint_attention(sh, p);
+    lane = std::max(lane, make_layout(&sh, N_q, B, p, sizeof(WsHeader), !joint).total - sizeof(WsHeader));
+    if (joint) rows += joint_kept_bytes(sh, B);
   }
   *out = align_up(lane);
+  *kept = rows;
   return QUOKA_OK;
 }
 
 // Relative cost of a sequence, for balancing lanes: the history it scores and
-// the keys each query attends to.
-double seq_work(const quoka_shape& s, int B) {
+// (unless it attends in the joint launch) the keys each query attends to.
+double seq_work(const quoka_shape& s, int B, bool attends) {
   const double Be = std::min(B, s.T);
-  return (double)s.H_kv * s.T * s.d * 2.0 / 8.0 + (double)s.H_q * s.C * (Be + 0.5 * s.C) * s.d * 4.0 / 1000.0;
+  return (double)s.H_kv * s.T * s.d * 2.0 / 8.0 +
+         (attends ? (double)s.H_q * s.C * (Be + 0.5 * s.C) * s.d * 4.0 / 1000.0 : 0.0);
 }
 
 struct LaneStreams {
@@ -617,9 +651,9 @@ int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* 
                                 int N_q, int B, const quoka_params* params, size_t* bytes) {
   if (bytes == nullptr || N_q < 1 || B < 1) return QUOKA_ERR_INVALID_ARG;
   QUOKA_TRY(check_varlen(shape, cu_T, cu_C));
-  size_t lane = 0;
-  QUOKA_TRY(varlen_lane_bytes(shape, cu_T, cu_C, N_q, B, params, &lane));
-  *bytes = sizeof(WsHeader) + (size_t)varlen_lanes(shape, cu_C) * lane;
+  size_t lane = 0, kept = 0;
+  QUOKA_TRY(varlen_lane_bytes(shape, cu_T, cu_C, N_q, B, params, &lane, &kept));
+  *bytes = sizeof(WsHeader) + kept + (size_t)varlen_lanes(shape, cu_C) * lane;
   return QUOKA_OK;
 }
 
@@ -631,9 +665,10 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
   if (N_q < 1 || B < 1) return QUOKA_ERR_INVALID_ARG;
   const int nseq = shape->nseq;
   const size_t eb = elt_bytes(shape->dtype), d = shape->d;
-  size_t lane_bytes = 0;
-  QUOKA_TRY(varlen_lane_bytes(shape, cu_T, cu_C, N_q, B, params, &lane_bytes));
+  size_t lane_bytes = 0, kept_bytes = 0;
+  QUOKA_TRY(varlen_lane_bytes(shape, cu_T, cu_C, N_q, B, params, &lane_bytes, &kept_bytes));
   const int lanes = varlen_lanes(shape, cu_C);
+  const size_t lane0 = sizeof(WsHeader) + kept_bytes;   // the lanes' slices follow the joint gathered rows
   // Every sequence is checked before the first one is enqueued.
   std::vector<SeqArgs> seqs;
   seqs.reserve(nseq);
@@ -659,10 +694,29 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
     QUOKA_TRY(read_params(params, &a.shape, &a.p));
     QUOKA_TRY(check_chunk_args(&a.shape, a.Q, a.K_hist, a.V_hist, a.K_chunk, a.V_chunk, N_q, B, a.O, a.lse,
                                a.sel_out));
-    a.work = seq_work(a.shape, B);
+    a.joint = joint_attention(a.shape, a.p);
+    a.kept = 0;
+    a.work = seq_work(a.shape, B, !a.joint);
     seqs.push_back(a);
   }
-  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader) + (size_t)lanes * lane_bytes));
+  QUOKA_TRY(check_ws(ws, ws_bytes, lane0 + (size_t)lanes * lane_bytes));
+  // the joint sequences' gathered rows, in batch order after the header
+  size_t kept_at = sizeof(WsHeader);
+  std::vector<AttSeq> joint;
+  for (SeqArgs& a : seqs) {
+    if (!a.joint) continue;
+    const quoka_shape& sh = a.shape;
+    AttSeq q{a.Q, a.K_hist, a.V_hist, a.K_chunk, a.V_chunk, head_stride(&sh), sh.T, sh.C, a.O, a.lse};
+    if (joint_kept_bytes(sh, B) > 0) {
+      a.kept = kept_at;
+      q.Kh = at<void>(ws, kept_at);
+      q.Vh = at<void>(ws, kept_at + joint_kept_bytes(sh, B) / 2);
+      q.h_stride = (int64_t)B * sh.d;
+      q.n_hist = B;
+      kept_at += joint_kept_bytes(sh, B);
+    }
+    joint.push_back(q);
+  }
   cudaStream_t st = (cudaStream_t)stream;
   if (seqs.empty()) return QUOKA_OK;
   // Longest first onto the least-loaded lane; each lane owns a workspace slice.
@@ -678,13 +732,23 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
   }
   for (int l = 0; l < lanes; ++l)
     for (int i : plan[l])
-      seqs[i].L = make_layout(&seqs[i].shape, N_q, B, seqs[i].p, sizeof(WsHeader) + (size_t)l * lane_bytes);
+      seqs[i].L = make_layout(&seqs[i].shape, N_q, B, seqs[i].p, lane0 + (size_t)l * lane_bytes, !seqs[i].joint);
+  // a sequence on its lane: the whole chunk, or (joint) its selection and gather
+  auto run_seq = [&](const SeqArgs& a, cudaStream_t lst) -> int {
+    KeepOnly keep{a.kept ? at<void>(ws, a.kept) : nullptr,
+                  a.kept ? at<void>(ws, a.kept + joint_kept_bytes(a.shape, B) / 2) : nullptr};
+    return run_chunk(&a.shape, a.Q, a.K_hist, a.V_hist, a.K_chunk, a.V_chunk, N_q, B, a.p, a.O, a.lse, a.sel_out,
+                     ws, a.L, lst, KeyCache(), a.joint ? &keep : nullptr);
+  };
+  const float scale = seqs[0].p.scale;   // d and the params are the batch's
+  auto run_joint = [&]() -> int {
+    if (joint.empty()) return QUOKA_OK;
+    return cuda_status(launch_attend_tc_varlen(shape->d, joint.data(), (int)joint.size(), shape->H_q, shape->H_kv,
+                                               scale, at<WsHeader>(ws, 0), st));
+  };
   if (lanes == 1) {
-    for (int i : plan[0])
-      QUOKA_TRY(run_chunk(&seqs[i].shape, seqs[i].Q, seqs[i].K_hist, seqs[i].V_hist, seqs[i].K_chunk,
-                          seqs[i].V_chunk, N_q, B, seqs[i].p, seqs[i].O, seqs[i].lse, seqs[i].sel_out, ws, seqs[i].L,
-                          st));
-    return QUOKA_OK;
+    for (int i : plan[0]) QUOKA_TRY(run_seq(seqs[i], st));
+    return run_joint();
   }
   // Fork: lane l > 0 runs on a library stream that first waits for everything
   // enqueued on `stream` so far; lane 0 runs on `stream` itself.  Join: `stream`
@@ -698,8 +762,7 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
     cudaStream_t lst = l == 0 ? st : ls->stream[l - 1];
     if (l > 0 && (rc = cuda_status(cudaStreamWaitEvent(lst, ls->fork, 0))) != QUOKA_OK) break;
     for (int i : plan[l]) {
-      rc = run_chunk(&seqs[i].shape, seqs[i].Q, seqs[i].K_hist, seqs[i].V_hist, seqs[i].K_chunk, seqs[i].V_chunk,
-                     N_q, B, seqs[i].p, seqs[i].O, seqs[i].lse, seqs[i].sel_out, ws, seqs[i].L, lst);
+      rc = run_seq(seqs[i], lst);
       if (rc != QUOKA_OK) break;
     }
   }
@@ -709,7 +772,52 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
     const int w = j == QUOKA_OK ? cuda_status(cudaStreamWaitEvent(st, ls->join[l - 1], 0)) : j;
     if (rc == QUOKA_OK) rc = w;
   }
-  return rc;
+  if (rc != QUOKA_OK) return rc;
+  return run_joint();   // after the join: every lane's gathered rows are in
+}
+
+int quoka_sparse_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu_B, const int64_t* cu_C,
+                               const void* Q, const void* K_sel, const void* V_sel, const void* K_chunk,
+                               const void* V_chunk, const quoka_params* params, void* O, float* lse, void* ws,
+                               size_t ws_bytes, void* stream) {
+  QUOKA_TRY(check_varlen(shape, cu_B, cu_C));
+  if (Q == nullptr || K_chunk == nullptr || V_chunk == nullptr || O == nullptr) return QUOKA_ERR_INVALID_ARG;
+  const int nseq = shape->nseq;
+  if (cu_B[nseq] > 0 && (K_sel == nullptr || V_sel == nullptr)) return QUOKA_ERR_INVALID_ARG;
+  const quoka_shape sh0 = seq_shape(shape, cu_B, cu_C, 0);
+  Params p;
+  QUOKA_TRY(read_params(params, &sh0, &p));
+  if (shape->dtype != QUOKA_DTYPE_BF16 || p.engine == QUOKA_ENGINE_SIMT || attend_tc_smem(shape->d) > 227 * 1024)
+    return QUOKA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K_sel) || !aligned16(V_sel) || !aligned16(K_chunk) || !aligned16(V_chunk) ||
+      !aligned16(O) || !aligned4(lse))
+    return QUOKA_ERR_ALIGNMENT;
+  QUOKA_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
+  const size_t d = shape->d, eb = 2;
+  auto off = [&](const void* base, size_t elems) -> const void* {
+    return base == nullptr ? nullptr : static_cast<const char*>(base) + elems * eb;
+  };
+  std::vector<AttSeq> seqs;
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t c0 = cu_C[s], b0 = cu_B[s];
+    const int C = (int)(cu_C[s + 1] - c0), B_s = (int)(cu_B[s + 1] - b0);
+    if (C == 0) continue;
+    AttSeq q;
+    q.Q = off(Q, (size_t)shape->H_q * d * c0);
+    q.O = const_cast<void*>(off(O, (size_t)shape->H_q * d * c0));
+    q.Kc = off(K_chunk, (size_t)shape->H_kv * d * c0);
+    q.Vc = off(V_chunk, (size_t)shape->H_kv * d * c0);
+    q.Kh = B_s > 0 ? off(K_sel, (size_t)shape->H_kv * d * b0) : nullptr;
+    q.Vh = B_s > 0 ? off(V_sel, (size_t)shape->H_kv * d * b0) : nullptr;
+    q.h_stride = (int64_t)B_s * shape->d;
+    q.n_hist = B_s;
+    q.C = C;
+    q.lse = lse == nullptr ? nullptr : lse + (size_t)shape->H_q * c0;
+    seqs.push_back(q);
+  }
+  if (seqs.empty()) return QUOKA_OK;
+  return cuda_status(launch_attend_tc_varlen(shape->d, seqs.data(), (int)seqs.size(), shape->H_q, shape->H_kv,
+                                             p.scale, at<WsHeader>(ws, 0), (cudaStream_t)stream));
 }
 
 int quoka_append_kv(const quoka_shape* shape, void* K_hist, void* V_hist, const void* K_chunk, const void* V_chunk,

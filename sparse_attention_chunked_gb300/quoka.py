@@ -71,6 +71,8 @@ _SIG = {
     "quoka_chunk_attend_varlen": (ctypes.c_int, [ctypes.POINTER(VarlenShape), _I64P, _I64P, _P, _P, _P, _P, _P,
                                                  ctypes.c_int, ctypes.c_int, ctypes.POINTER(Params), _P, _P, _P, _P,
                                                  ctypes.c_size_t, _P]),
+    "quoka_sparse_attend_varlen": (ctypes.c_int, [ctypes.POINTER(VarlenShape), _I64P, _I64P, _P, _P, _P, _P, _P,
+                                                  ctypes.POINTER(Params), _P, _P, _P, ctypes.c_size_t, _P]),
     "quoka_key_inv_norms": (ctypes.c_int, [ctypes.POINTER(Shape), _P, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int64,
                                            _P]),
     "quoka_score_keys_cached": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, ctypes.c_int, _P, _P, ctypes.c_int64,
@@ -235,6 +237,14 @@ def quoka_chunk_attend_varlen(vshape, cu_T, cu_C, Q, K_hist, V_hist, K_chunk, V_
         ctypes.byref(vshape), _cu(cu_T), _cu(cu_C), _ptr(Q), _ptr(K_hist), _ptr(V_hist), _ptr(K_chunk),
         _ptr(V_chunk), N_q, B, ctypes.byref(params), _ptr(O), _ptr(lse), _ptr(sel_out), _ptr(ws),
         ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def quoka_sparse_attend_varlen(vshape, cu_B, cu_C, Q, K_sel, V_sel, K_chunk, V_chunk, params, O, lse, ws,
+                               stream=None):
+    """cu_B, cu_C: host sequences of nseq + 1 prefix sums; tensors packed sequence-major (see quoka.h)."""
+    _check("quoka_sparse_attend_varlen", load().quoka_sparse_attend_varlen(
+        ctypes.byref(vshape), _cu(cu_B), _cu(cu_C), _ptr(Q), _ptr(K_sel), _ptr(V_sel), _ptr(K_chunk), _ptr(V_chunk),
+        ctypes.byref(params), _ptr(O), _ptr(lse), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def quoka_dense_attend(shape, Q, K_hist, V_hist, K_chunk, V_chunk, params, O, lse, ws, stream=None):

@@ -141,17 +141,31 @@ def _ws_varlen(q, vshape, cu_T, cu_C, N_q=16, B=64, gqa="max"):
     return rc, n.value
 
 
-def test_varlen_workspace_is_one_slice_per_lane(quoka):
-    """Header + one slice per stream lane (up to 8, one per non-empty sequence), each for the largest sequence."""
+def test_varlen_workspace_layout(quoka):
+    """Header, then the kept K/V rows of the sequences that attend in the joint tensor-core
+    launch and select keys, then one slice per stream lane (up to 8, one per non-empty
+    sequence), each for the largest sequence without the joint sequences' kept rows."""
+    al = lambda x: (x + 255) // 256 * 256
+    H_kv, d, G, B = 2, 128, 4, 64
     for cu_T, cu_C, lanes in (([0, 1000, 1000, 41000], [0, 128, 200, 201], 3),
                               ([0, 1000, 1000, 41000], [0, 128, 128, 201], 2),
+                              ([0, 50, 1050], [0, 40, 80], 2),
                               ([0, 5, 9, 13, 17, 21, 25], [0, 1, 2, 3, 4, 5, 6], 6),
                               (list(range(0, 55, 5)), list(range(0, 11)), 8)):
-        rc, n = _ws_varlen(quoka, _vshape(quoka, nseq=len(cu_T) - 1), cu_T, cu_C)
+        rc, n = _ws_varlen(quoka, _vshape(quoka, nseq=len(cu_T) - 1), cu_T, cu_C, B=B)
         assert rc == 0
-        per_seq = [quoka.workspace_size(_shape(quoka, C=c1 - c0, T=t1 - t0), 16, 64, quoka.params_of("max"))
-                   for (c0, c1, t0, t1) in zip(cu_C, cu_C[1:], cu_T, cu_T[1:]) if c1 > c0]
-        assert n == 256 + lanes * (max(per_seq) - 256)
+        per_lane, kept = [], 0
+        for (c0, c1, t0, t1) in zip(cu_C, cu_C[1:], cu_T, cu_T[1:]):
+            C, T = c1 - c0, t1 - t0
+            if C == 0:
+                continue
+            single = quoka.workspace_size(_shape(quoka, C=C, T=T), 16, B, quoka.params_of("max"))
+            joint = G * C > 32                       # bf16 above decode size: the joint attention launch
+            rows = 2 * al(H_kv * min(B, T) * d * 2)  # the gathered K and V rows of a single call
+            per_lane.append(single - 256 - (rows if joint else 0))
+            if joint and 0 < B < T:
+                kept += rows
+        assert n == 256 + kept + lanes * max(per_lane)
 
 
 @pytest.mark.parametrize("cu_T,cu_C,kw,code", [
@@ -218,3 +232,27 @@ def test_key_norm_cache_argument_errors(quoka):
     # appending C = 128 keys needs room for T + C norms per row
     assert lib.quoka_append_kv_norms(ctypes.byref(_shape(q, kv_head_stride=2000 * 128)), *([P(FAKE)] * 4), P(FAKE),
                                      1100, None) == 1
+
+
+def test_sparse_attend_varlen_checks(quoka):
+    """The ragged attention entry point: prefix sums, element type, engine, alignment, workspace."""
+    q = quoka
+    P = ctypes.c_void_p
+    fn = q.load().quoka_sparse_attend_varlen
+    cu_B, cu_C = [0, 100, 100], [0, 64, 200]
+
+    def call(vs, cuB=cu_B, cuC=cu_C, params=None, lse=None, ws_bytes=256, ksel=P(FAKE)):
+        return fn(ctypes.byref(vs), q._cu(cuB), q._cu(cuC), P(FAKE), ksel, ksel, P(FAKE), P(FAKE),
+                  ctypes.byref(params or q.params_of("max")), P(FAKE), lse, P(FAKE), ws_bytes, None)
+
+    vs = _vshape(q, nseq=2)
+    assert call(vs, cuB=[1, 100, 100]) == 1                     # prefix sums must start at 0
+    assert call(vs, cuC=[0, 64, 9000]) == 2                     # a chunk longer than 8192
+    assert call(_vshape(q, nseq=2, dtype=1)) == 2               # fp32: no tensor-core attention
+    simt = q.params_of("max")
+    simt.engine = 1
+    assert call(vs, params=simt) == 2                           # the CUDA-core engine is not offered
+    assert call(vs, ksel=None) == 1                             # kept rows but no K_sel / V_sel
+    assert call(vs, lse=P(FAKE + 2)) == 4                       # lse needs 4-byte alignment
+    assert call(vs, ws_bytes=255) == 3                          # the error header
+

@@ -124,6 +124,75 @@ def test_varlen_ragged8_full_size(quoka, gqa):
             check_against_oracle(quoka, x, cfg.H_q, cfg.H_kv, cfg.d, cfg.N_q, cfg.B, gqa, cfg.dtype, got[s])
 
 
+def test_varlen_more_sequences_than_one_joint_launch(quoka):
+    """Twenty-five sequences: the bf16 chunks above decode size (G * C_s > 32) attend in joint
+    launches of at most 16 sequences each; decode-size chunks, histories within the budget and
+    empty histories mixed in.  Every sequence must match its single-sequence call bit for bit."""
+    H_q, H_kv, d, N_q, B = 8, 2, 128, 9, 40
+    Cs = [130, 1, 77, 9, 256, 8, 33, 200, 2, 129, 64]
+    Ts = [300, 1000, 0, 50, 2100, 129, 40, 777, 0, 128]
+    shapes = [(Cs[i % len(Cs)], Ts[i % len(Ts)]) for i in range(25)]
+    assert sum(4 * C > 32 for C, _ in shapes) > 16
+    seqs = [wl.small_chunk(H_q=H_q, H_kv=H_kv, d=d, C=C, T=T, N_q=N_q, B=B, dtype="bf16", seed=60 + i)[1]
+            for i, (C, T) in enumerate(shapes)]
+    for gqa in ("max", "mean"):
+        got = run_varlen(quoka, seqs, H_q, H_kv, d, N_q, B, gqa, "bf16")
+        for s, x in enumerate(seqs):
+            ref = single(quoka, x, N_q, B, gqa)
+            assert torch.equal(got[s]["O"], ref["O"]), f"{gqa}: sequence {s} {shapes[s]}: O differs"
+            assert torch.equal(got[s]["lse"], ref["lse"]), f"{gqa}: sequence {s}: lse differs"
+            if ref["sel"].numel():
+                assert torch.equal(got[s]["sel"], ref["sel"]), f"{gqa}: sequence {s}: sel differs"
+            if s in (4, 17, 20):
+                check_against_oracle(quoka, x, H_q, H_kv, d, N_q, B, gqa, "bf16", got[s])
+
+
+def test_sparse_attend_varlen_matches_single_calls(quoka):
+    """quoka_sparse_attend_varlen on packed kept rows: every sequence's O and lse equal
+    quoka_sparse_attend (tensor-core engine) on that sequence bit for bit, and the oracle's
+    attention within the bf16 tolerance.  Kept-row counts include 0 and ragged tails; one
+    chunk is empty; twenty sequences take two launches."""
+    q = quoka
+    H_q, H_kv, d = 8, 2, 128
+    shapes = [(130, 40), (1, 0), (77, 300), (0, 50), (256, 129), (33, 128), (200, 7), (5, 2048), (129, 1000),
+              (64, 64)] * 2
+    g = torch.Generator().manual_seed(7)
+    mk = lambda h, n: (torch.randn((h, n, d), generator=g) * 0.5).to(torch.bfloat16)
+    seqs = [(mk(H_q, C), mk(H_kv, B), mk(H_kv, B), mk(H_kv, C), mk(H_kv, C)) for C, B in shapes]
+    cu_C = [0] + list(np.cumsum([C for C, _ in shapes]))
+    cu_B = [0] + list(np.cumsum([B for _, B in shapes]))
+    cat = lambda i: torch.cat([x[i].reshape(-1) for x in seqs]).to(DEV)
+    Q, Ks, Vs, Kc, Vc = (cat(i) for i in range(5))
+    O = torch.full_like(Q, float("nan"))
+    lse = torch.full((H_q * cu_C[-1],), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    vs = q.varlen_shape_of(len(shapes), H_q, H_kv, d, torch.bfloat16)
+    params = q.params_of("max")
+    q.quoka_sparse_attend_varlen(vs, cu_B, cu_C, Q, Ks, Vs, Kc, Vc, params, O, lse, ws)
+    torch.cuda.synchronize()
+    assert q.quoka_get_last_device_error(ws) == 0
+    tensor = q.params_of("max")
+    tensor.engine = 2
+    for s, (C, B) in enumerate(shapes):
+        if C == 0:
+            continue
+        x = [t.to(DEV) for t in seqs[s]]
+        shape = q.shape_of(x[0], x[1], H_kv=H_kv)
+        O1 = torch.empty_like(x[0])
+        lse1 = torch.empty((H_q, C), dtype=torch.float32, device=DEV)
+        ws1 = q.make_workspace(shape, 1, max(B, 1), tensor)
+        q.quoka_sparse_attend(shape, x[0], x[1] if B else None, x[2] if B else None, B, x[3], x[4], tensor, O1,
+                              lse1, ws1)
+        torch.cuda.synchronize()
+        c0, c1 = cu_C[s], cu_C[s + 1]
+        Ov = O[H_q * d * c0:H_q * d * c1].view(H_q, C, d)
+        assert torch.equal(Ov, O1), f"sequence {s} {shapes[s]}: O differs from quoka_sparse_attend"
+        assert torch.equal(lse[H_q * c0:H_q * c1].view(H_q, C), lse1), f"sequence {s}: lse differs"
+        if s in (0, 4, 8):
+            O_ref, _ = qo.attend(*(f64(t) for t in seqs[s]))
+            check_output(Ov, O_ref, f"O (sequence {s})")
+
+
 def test_varlen_decode_batch(quoka):
     """Batched decode: twelve sequences of one new token each over histories of 1 to 3000 keys."""
     H_q, H_kv, d, N_q, B = 8, 2, 128, 1, 64
