@@ -43,9 +43,9 @@ FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x FP32 lanes x 2 fl
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one tensor-core attention launch per
 # workload, from one ncu capture, and a digest of the kernel sources that capture ran on: once the
 # sources change the figure no longer describes the kernel and the bench reports null.
-ATTEND_TRAFFIC = {"gqa32k": 33_625_344}
+ATTEND_TRAFFIC = {"gqa32k": 33_622_272, "ragged8": 337_428_224}
 ATTEND_TRAFFIC_SOURCES = ("attend_tc.cu", "tc_common.cuh")   # the attention kernel and its tcgen05/TMA wrappers
-ATTEND_TRAFFIC_SHA256 = "5b45875a61fc5e55f20e8154c9b9ad0227cbe0017b75a30dac40c8405e29be6b"
+ATTEND_TRAFFIC_SHA256 = "764c4a01c7ebc4af15c9419bfcf06cf8a6f6dd868437799e090c2de03af2a572"
 
 
 def attend_sources_sha256() -> str:
@@ -758,7 +758,7 @@ def run_quoka_ragged(args, rank, world, local_rank, light=False):
                      "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": round(peaks["bf16_tflops"], 1), "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4), "peak_source": peaks["source"],
-                     "traffic": None, "traffic_unit": "bytes/launch"},
+                     "traffic": attend_traffic(args.workload) if joint else None, "traffic_unit": "bytes/launch"},
         "attend_ms_per_batch": round(att_ms, 5),
         "dense": None if dense_ms is None else {"ms_per_step": round(dense_ms, 4),
                                                 "speedup": round(dense_ms / step_ms, 2)},

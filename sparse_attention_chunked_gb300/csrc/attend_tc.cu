@@ -111,7 +111,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // What one launch attends: NS sequences (1 for a single chunk, up to
 // kAttVarSeqs for a ragged batch), each with its own tensor maps, chunk length,
 // kept history rows and output.  A "run" is one query tile of one sequence;
-// every run holds H_kv * pairs work items of the same length.
+// every run holds H_kv * pairs work items of the same length.  The items are
+// dealt to the CTAs in run order.
 template <int NS>
 struct AttArgs {
   CUtensorMap q[NS], kh[NS], vh[NS], kc[NS], vc[NS];
@@ -120,13 +121,13 @@ struct AttArgs {
   int C[NS], n_hist[NS];
   int n_items;
   int n_qt;                         // NS == 1: the query tiles of the one sequence, longest (last) first
-  uint16_t run[NS == 1 ? 2 : NS * 64];   // NS > 1: sequence << 8 | query tile, longest first
+  uint16_t run[NS == 1 ? 2 : NS * 64];   // NS > 1: sequence << 8 | query tile, in work order
 };
 
-// Work item i (0 = most key blocks) is head pair hp of KV group g in run
-// i / (H_kv * pairs).  CTA c of P runs items c, 2P - 1 - c, 2P + c,
-// 4P - 1 - c, ...: a serpentine over the longest-first list, so the CTAs that
-// drew the longest first items draw the shortest second ones.
+// Work item i is head pair hp of KV group g in run i / (H_kv * pairs); the
+// runs of a sequence come longest (last query tile) first.  CTA c of P runs
+// items c, 2P - 1 - c, 2P + c, 4P - 1 - c, ...: a serpentine over the list, so
+// the CTAs that drew the longest first items draw the shortest second ones.
 struct AttItem {
   int seq, qt, g, h0, n_slots, nh, n_blocks;
 };
@@ -585,23 +586,27 @@ cudaError_t launch_attend_tc_varlen(int d, const AttSeq* seqs, int nseq, int H_q
     const int n = nseq - s0 < kAttVarSeqs ? nseq - s0 : kAttVarSeqs;
     static thread_local AttArgs<kAttVarSeqs> a;   // 13 KB: kept off the stack
     memset(&a, 0, sizeof(a));
-    // runs (sequence, query tile) longest first; equal lengths keep batch order
-    struct Run {
-      int len;
-      uint16_t code;
-    };
-    Run runs[kAttVarSeqs * 64];
-    int n_runs = 0;
+    // Runs (sequence, query tile) sequence by sequence, the sequences with the
+    // longest items first and each sequence's query tiles longest (last) first.
+    // The CTAs work on neighbouring items at any time, so one sequence's kept
+    // and chunk K/V rows are read from HBM once and then served from L2 (a
+    // batch-wide longest-first order interleaves every sequence's runs, and
+    // the rows are evicted between one query tile and the next).
+    int order[kAttVarSeqs], longest[kAttVarSeqs];
     for (int k = 0; k < n; ++k) {
       const AttSeq& q = seqs[s0 + k];
       if (q.C < 1 || q.C > 64 * 128 || q.n_hist < 0) return cudaErrorInvalidValue;
       cudaError_t e = fill_att_seq(a, k, d, q, H_q, H_kv);
       if (e != cudaSuccess) return e;
-      const int nh = (q.n_hist + 127) / 128;
-      for (int qt = 0; qt < (q.C + 127) / 128; ++qt) runs[n_runs++] = Run{nh + qt + 1, (uint16_t)((k << 8) | qt)};
+      order[k] = k;
+      longest[k] = (q.n_hist + 127) / 128 + (q.C + 127) / 128;
     }
-    std::stable_sort(runs, runs + n_runs, [](const Run& x, const Run& y) { return x.len > y.len; });
-    for (int r = 0; r < n_runs; ++r) a.run[r] = runs[r].code;
+    std::stable_sort(order, order + n, [&](int x, int y) { return longest[x] > longest[y]; });
+    int n_runs = 0;
+    for (int o = 0; o < n; ++o) {
+      const int k = order[o];
+      for (int qt = (seqs[s0 + k].C + 127) / 128 - 1; qt >= 0; --qt) a.run[n_runs++] = (uint16_t)((k << 8) | qt);
+    }
     a.n_items = n_runs * H_kv * pairs;
     cudaError_t e = launch_att(d, a, G, H_kv, scale, hdr, st);
     if (e != cudaSuccess) return e;
