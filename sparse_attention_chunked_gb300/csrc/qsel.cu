@@ -7,8 +7,10 @@
 // inverted order-mapped cosines, so ties go to the lower position), written
 // in position order.
 //
-// k_qselect_fused: a cluster of 8 CTAs per selection row, CTA r owning the
-// r-th eighth of the chunk positions.  Each CTA copies its slice of Q into
+// k_qselect_fused: a cluster of CL CTAs per selection row (8; 4 when a
+// quarter of the chunk fits one staging piece, so that short chunks do not
+// spread thin over twice the CTAs), CTA r owning the r-th CL-th of the chunk
+// positions.  Each CTA copies its slice of Q into
 // shared memory with bulk copies (64-row chunks, each on its own mbarrier, so
 // the arithmetic starts as the first chunk lands), takes the row norms |q|
 // and the column sums; the cluster adds the slices' sums through distributed
@@ -52,10 +54,10 @@ struct alignas(sizeof(T) * E) RowSlice {
   T v[E];
 };
 
-constexpr int kSelCluster = 8;
+constexpr int kSelCluster = 8;                      // the largest cluster
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
-static_assert(kSelWarps == kSelCluster, "warp q of CTA 0 fetches the list of CTA q");
+static_assert(kSelWarps >= kSelCluster, "warp q of CTA 0 fetches the list of CTA q");
 static_assert(kRowsPerWarp == 8, "the reduce-scatter below is written for 8 rows");
 
 // Warp sums of 8 rows at once: v[r] is this lane's part of row r; afterwards
@@ -102,7 +104,7 @@ static size_t qselect_fused_smem(int per, int G_avg, int D, int sel_p) {
 // merged as a tree, then CTA 0's warps fetch the CTAs' lists (one each) and
 // merge those as a tree.  Every CTA passes the same two cluster barriers; CTA
 // 0 alone continues after the second.
-template <int P>
+template <int P, int CL>
 __device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* keys_s, int n, int t0, int n_sel,
                                   uint64_t* lists, int32_t* __restrict__ out) {
   constexpr int L = 32 * P;
@@ -144,10 +146,15 @@ __device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* ke
     for (int p = 0; p < P; ++p) lists[kSelWarps * L + p * 32 + lane] = run[p];
   cluster.sync();                                 // every CTA's list is ready
   const bool leader = cluster.block_rank() == 0;
-  if (leader) {                                   // warp q of CTA 0 fetches CTA q's list
-    const uint64_t* rl = cluster.map_shared_rank(lists + kSelWarps * L, warp);
+  if (leader) {                                   // warp q of CTA 0 fetches CTA q's list (q < CL)
+    if (warp < CL) {
+      const uint64_t* rl = cluster.map_shared_rank(lists + kSelWarps * L, warp);
 #pragma unroll
-    for (int p = 0; p < P; ++p) run[p] = rl[p * 32 + lane];
+      for (int p = 0; p < P; ++p) run[p] = rl[p * 32 + lane];
+    } else {
+#pragma unroll
+      for (int p = 0; p < P; ++p) run[p] = 0ull;
+    }
   }
   cluster.sync();                                 // every remote read is done: the other CTAs may finish
   if (!leader) return;
@@ -163,8 +170,8 @@ __device__ void cluster_warp_topk(cg::cluster_group& cluster, const uint32_t* ke
   }
 }
 
-template <typename T, int D>
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads, 2)
+template <typename T, int D, int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kSelThreads, 2)
     k_qselect_fused(const T* __restrict__ Q, int C, int G_avg, int n_sel, int per, int sel_p,
                     int32_t* __restrict__ q_idx, float* __restrict__ cos_out, WsHeader* hdr) {
   constexpr int E = D / 32;
@@ -276,7 +283,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   for (int i = threadIdx.x; i < G_avg * D; i += blockDim.x) {
     float acc = 0.f;
 #pragma unroll
-    for (int q = 0; q < kSelCluster; ++q) acc += cluster.map_shared_rank(part_s, q)[i];
+    for (int q = 0; q < CL; ++q) acc += cluster.map_shared_rank(part_s, q)[i];
     mean_s[i] = acc / (float)C;
   }
   __syncthreads();
@@ -347,13 +354,13 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     return;
   }
   switch (sel_p) {
-    case 1: cluster_warp_topk<1>(cluster, keys_s, n, t0, n_sel, lists, out); return;
-    case 2: cluster_warp_topk<2>(cluster, keys_s, n, t0, n_sel, lists, out); return;
-    case 4: cluster_warp_topk<4>(cluster, keys_s, n, t0, n_sel, lists, out); return;
-    case 8: cluster_warp_topk<8>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 1: cluster_warp_topk<1, CL>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 2: cluster_warp_topk<2, CL>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 4: cluster_warp_topk<4, CL>(cluster, keys_s, n, t0, n_sel, lists, out); return;
+    case 8: cluster_warp_topk<8, CL>(cluster, keys_s, n, t0, n_sel, lists, out); return;
     default: {
       auto key_at = [&](int i) -> uint32_t { return keys_s[i]; };
-      cluster_radix_topk<kSelCluster>(cluster, true, reinterpret_cast<const uint4*>(keys_s), key_at, n, t0, n_sel, out,
+      cluster_radix_topk<CL>(cluster, true, reinterpret_cast<const uint4*>(keys_s), key_at, n, t0, n_sel, out,
                                       tk);
     }
   }
@@ -390,45 +397,63 @@ __global__ void __launch_bounds__(kRowSelThreads)
   pdl_launch_dependents();   // dependents launch once this CTA is done
 }
 
+// CTAs per selection row: 4 when a quarter of the chunk fits one staging
+// piece, else 8.
+static int qselect_cluster(int d, int elt, int C) {
+  return (C + 3) / 4 <= qselect_piece_rows(d, elt) ? 4 : kSelCluster;
+}
+
 // k_qselect_fused's parameters: slice length per CTA, list length
 // 32 * sel_p >= n_sel (0: radix select), dynamic shared memory.
-static void qselect_fused_plan(int d, int G_avg, int C, int n_sel, int* per, int* sel_p, size_t* smem) {
-  *per = ((C + kSelCluster - 1) / kSelCluster + 3) & ~3;
+static void qselect_fused_plan(int d, int elt, int G_avg, int C, int n_sel, int* per, int* sel_p, size_t* smem) {
+  const int cl = qselect_cluster(d, elt, C);
+  *per = ((C + cl - 1) / cl + 3) & ~3;
   *sel_p = n_sel <= 32 ? 1 : n_sel <= 64 ? 2 : n_sel <= 128 ? 4 : n_sel <= 256 ? 8 : 0;
   *smem = qselect_fused_smem(*per, G_avg, d, *sel_p);
 }
 
 // The clustered kernel runs when its shared memory stays within 160 KB and Q
 // is 16-byte aligned (bulk copies want 16-byte aligned rows).
-static bool fused_fits(int d, const void* Q, int G_avg, int C, int n_sel) {
+static bool fused_fits(int d, int elt, const void* Q, int G_avg, int C, int n_sel) {
   int per, sel_p;
   size_t fsmem;
-  qselect_fused_plan(d, G_avg, C, n_sel, &per, &sel_p, &fsmem);
+  qselect_fused_plan(d, elt, G_avg, C, n_sel, &per, &sel_p, &fsmem);
   return fsmem <= 160 * 1024 && ((uintptr_t)Q & 15u) == 0;
 }
 
 int select_queries_path(int dtype, int d, const void* Q, int H_q, int G_avg, int C, int n_sel, bool split_ok) {
-  (void)dtype;
   (void)H_q;
-  if (G_avg > 1 && split_ok && fused_fits(d, Q, 1, C, n_sel)) return 2;
-  if (fused_fits(d, Q, G_avg, C, n_sel)) return 1;
+  const int elt = dtype == 0 ? 2 : 4;
+  if (G_avg > 1 && split_ok && fused_fits(d, elt, Q, 1, C, n_sel)) return 2;
+  if (fused_fits(d, elt, Q, G_avg, C, n_sel)) return 1;
   return 0;
+}
+
+template <typename T, int D, int CL>
+static cudaError_t qsel_launch(dim3 grid, size_t smem, cudaStream_t st, const void* Q, int C, int G_run, int n_sel,
+                               int per, int sel_p, int32_t* q_idx, float* cos_out, WsHeader* hdr) {
+  cudaError_t e = ensure_smem((const void*)k_qselect_fused<T, D, CL>, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_qselect_fused<T, D, CL>, grid, dim3(kSelThreads), smem, st, (const T*)Q, C, G_run, n_sel, per,
+                    sel_p, q_idx, cos_out, hdr);
 }
 
 template <typename T, int D>
 static cudaError_t qsel_impl(const void* Q, int H_q, int G_avg, int C, int n_sel, int32_t* q_idx, float* qcos,
                              WsHeader* hdr, bool split_ok, cudaStream_t st) {
   const int rows = H_q / G_avg;
-  const int path = select_queries_path(0, D, Q, H_q, G_avg, C, n_sel, split_ok);
+  const int path = select_queries_path(sizeof(T) == 2 ? 0 : 1, D, Q, H_q, G_avg, C, n_sel, split_ok);
   if (path == 0) return cudaErrorInvalidConfiguration;   // the callers check select_queries_path first
   const int G_run = path == 2 ? 1 : G_avg;   // the split runs one head per cluster
   int per, sel_p;
   size_t fsmem;
-  qselect_fused_plan(D, G_run, C, n_sel, &per, &sel_p, &fsmem);
-  cudaError_t e = ensure_smem((const void*)k_qselect_fused<T, D>, fsmem);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(k_qselect_fused<T, D>, dim3(kSelCluster, H_q / G_run), dim3(kSelThreads), fsmem, st, (const T*)Q, C,
-                 G_run, n_sel, per, sel_p, q_idx, path == 2 ? qcos : (float*)nullptr, hdr);
+  qselect_fused_plan(D, (int)sizeof(T), G_run, C, n_sel, &per, &sel_p, &fsmem);
+  const int cl = qselect_cluster(D, (int)sizeof(T), C);
+  float* cos_out = path == 2 ? qcos : (float*)nullptr;
+  const dim3 grid(cl, H_q / G_run);
+  cudaError_t e = cl == 4 ? qsel_launch<T, D, 4>(grid, fsmem, st, Q, C, G_run, n_sel, per, sel_p, q_idx, cos_out, hdr)
+                          : qsel_launch<T, D, kSelCluster>(grid, fsmem, st, Q, C, G_run, n_sel, per, sel_p, q_idx,
+                                                           cos_out, hdr);
   count_launches(1);
   if (e != cudaSuccess || path == 1) return e;
   const size_t gsmem = (size_t)C * (sizeof(uint2) + sizeof(uint32_t));
