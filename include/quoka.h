@@ -285,9 +285,9 @@ int quoka_workspace_size_varlen(const quoka_varlen_shape* shape, const int64_t* 
  * (bf16, G * C_s > 32 or the tensor engine forced) stop on their lane after
  * the gather: after the join, one persistent attention launch per 16 such
  * sequences, on `stream`, attends for all of them (as
- * quoka_sparse_attend_varlen).  The results
- * are those of quoka_chunk_attend on each sequence, bit for bit.  Concurrent
- * calls from several host threads are serialised on the lane streams. */
+ * quoka_sparse_attend_varlen does).  The results are those of
+ * quoka_chunk_attend on each sequence, bit for bit.  Concurrent calls from
+ * several host threads are serialised on the lane streams. */
 int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu_T, const int64_t* cu_C,
                               const void* Q, const void* K_hist, const void* V_hist, const void* K_chunk,
                               const void* V_chunk, int N_q, int B, const quoka_params* params, void* O, float* lse,
@@ -299,8 +299,8 @@ int quoka_chunk_attend_varlen(const quoka_varlen_shape* shape, const int64_t* cu
  * tile x head pair) of every sequence to one CTA per SM, sequence by
  * sequence (the sequences with the longest items first, each sequence's
  * longest items first), so that a sequence's K/V rows stay in L2 while its
- * items run.  cu_B and cu_C are HOST int64 arrays of
- * nseq + 1 prefix sums (cu[0] = 0, non-decreasing): sequence s has
+ * items run.  cu_B and cu_C are HOST int64 arrays of nseq + 1 prefix sums
+ * (cu[0] = 0, non-decreasing): sequence s has
  * B_s = cu_B[s+1] - cu_B[s] kept rows (0 allowed) and C_s = cu_C[s+1] - cu_C[s]
  * queries (0: the sequence is skipped; each C_s <= 8192).  Packed tensors,
  * sequence-major:
