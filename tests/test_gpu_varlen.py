@@ -147,6 +147,23 @@ def test_varlen_more_sequences_than_one_joint_launch(quoka):
                 check_against_oracle(quoka, x, H_q, H_kv, d, N_q, B, gqa, "bf16", got[s])
 
 
+@pytest.mark.parametrize("H_q,H_kv", [(4, 4), (10, 2)], ids=["mha", "gqa5"])
+def test_varlen_joint_attention_head_layouts(quoka, H_q, H_kv):
+    """One query head per KV group, and an odd group size (the last head pair of a group is a
+    single slot): the joint attention launch against per-sequence calls, bit for bit."""
+    d, N_q, B = 128, 9, 40
+    shapes = [(77, 300), (200, 1000), (130, 0), (33, 20)]
+    seqs = [wl.small_chunk(H_q=H_q, H_kv=H_kv, d=d, C=C, T=T, N_q=N_q, B=B, dtype="bf16", seed=90 + i)[1]
+            for i, (C, T) in enumerate(shapes)]
+    for gqa in ("max", "mean"):
+        got = run_varlen(quoka, seqs, H_q, H_kv, d, N_q, B, gqa, "bf16")
+        for s, x in enumerate(seqs):
+            ref = single(quoka, x, N_q, B, gqa)
+            assert torch.equal(got[s]["O"], ref["O"]), f"{gqa}: sequence {s} {shapes[s]}: O differs"
+            assert torch.equal(got[s]["lse"], ref["lse"]), f"{gqa}: sequence {s}: lse differs"
+        check_against_oracle(quoka, seqs[1], H_q, H_kv, d, N_q, B, gqa, "bf16", got[1])
+
+
 def test_sparse_attend_varlen_matches_single_calls(quoka):
     """quoka_sparse_attend_varlen on packed kept rows: every sequence's O and lse equal
     quoka_sparse_attend (tensor-core engine) on that sequence bit for bit, and the oracle's
